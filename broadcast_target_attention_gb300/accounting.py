@@ -1,0 +1,54 @@
+"""Work and traffic accounting for IKBO target attention (host arithmetic only).
+
+FLOPs count the two contractions (Q·Kᵀ and P·V), 2 FLOPs per multiply-add,
+softmax excluded -- the convention of "In-Kernel Broadcast Optimization:
+Co-Designing Kernels for RecSys Inference", Appendix 9 (roofline of standard
+vs IKBO flash attention) and Appendix 2 (arithmetic intensity = FLOPs over
+bytes moved to and from HBM).
+
+Algorithmic bytes are what an ideal IKBO kernel must move: every user K/V row
+read once, every query read once, every output written once, plus the index
+tensors.  The explicit-broadcast comparison path additionally writes the
+per-candidate K/V copy and reads it back.
+"""
+from __future__ import annotations
+
+BF16 = 2
+
+
+def flops(H: int, D: int, Lq: int, S: int) -> int:
+    """4·H·D·Lq·S, with S = Σ_c L_{u(c)} keys visited over all candidates."""
+    return 4 * H * D * Lq * S
+
+
+def alg_bytes(H: int, D: int, Lq: int, T: int, n_cand: int, n_user: int) -> int:
+    """K and V read once per user, q read and out written once, int32 indices."""
+    kv = 2 * T * H * D * BF16
+    q_out = 2 * n_cand * H * Lq * D * BF16
+    idx = 4 * (n_cand + n_user + 1)
+    return kv + q_out + idx
+
+
+def broadcast_extra_bytes(H: int, D: int, S_tokens: int) -> int:
+    """Extra traffic of the explicit broadcast: write the K/V copy, read it back."""
+    return 2 * (2 * S_tokens * H * D * BF16)
+
+
+def ai_per_user_head(r: int, Lq: int, L: int) -> float:
+    """Arithmetic intensity (FLOP/B) of one user-head with r candidates.
+
+    FLOPs 4·D·r·Lq·L over bytes 2·D·(2L + 2·r·Lq): K/V of the user read once,
+    each candidate's queries read and outputs written once.  r = 1 is the
+    standard (broadcast) kernel, whose K/V are re-read for every candidate.
+    """
+    return r * Lq * L / (L + r * Lq)
+
+
+def workload_numbers(wl) -> dict:
+    """FLOPs, algorithmic bytes and the broadcast path's extra bytes of a workload."""
+    c = wl.cfg
+    return {
+        "flops": flops(c.H, c.D, c.Lq, wl.S),
+        "alg_bytes": alg_bytes(c.H, c.D, c.Lq, wl.T, wl.n_cand, wl.n_user),
+        "broadcast_extra_bytes": broadcast_extra_bytes(c.H, c.D, wl.S),
+    }

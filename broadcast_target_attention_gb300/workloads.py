@@ -1,0 +1,262 @@
+"""Seeded synthetic workloads for IKBO target attention.
+
+This module draws inputs and nothing else: the candidate count of each user,
+the user sequence lengths, the ``cand_to_user`` map, the jagged
+``user_offsets`` and the bf16 bits of q, k and v.  It holds none of the
+attention arithmetic, so the CUDA path's tests and bench and the CPU oracle
+can both take their inputs from it.
+
+Shapes (the layout the library's C ABI documents):
+
+* ``q``            bf16 bits ``uint16[n_cand, H, Lq, D]``
+* ``k``, ``v``     bf16 bits ``uint16[T, H, D]``, user sequences packed back to
+                   back (jagged, no padding tokens), ``T = user_offsets[-1]``
+* ``user_offsets`` ``int32[n_user + 1]``, ``user_offsets[0] = 0``, non-decreasing
+* ``cand_to_user`` ``int32[n_cand]``, values in ``[0, n_user)``
+
+The named configurations follow the workload shapes of "In-Kernel Broadcast
+Optimization: Co-Designing Kernels for RecSys Inference" (§1.1: about 15
+users behind 1024 candidates, a ~70x replication; §3: target attention over
+the user history) with the jagged packing of "Optimizing Jagged Flash
+Attention with TLX" (introduction: sequences packed with an offsets tensor).
+The pages name no public dataset; these seeded draws stand in for their
+production traffic.
+
+Every draw uses numpy's PCG64 generator, whose output is the same on x86_64
+and aarch64 (structure from one stream seeded by the config's seed, values
+from per-chunk streams), and floats are rounded to bf16 with integer arithmetic
+(round-to-nearest-even), so the bits are identical on every machine.
+"""
+from __future__ import annotations
+
+import os
+from concurrent.futures import ThreadPoolExecutor
+
+from dataclasses import dataclass, field
+from typing import Optional, Sequence
+
+import numpy as np
+
+# Values are drawn in chunks of this many elements so that very large tensors
+# never need a float32 temporary of their full size.
+_CHUNK = 1 << 24
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to bf16 (nearest, ties to even); returns uint16 bits.
+
+    Finite inputs only (the generators below never produce inf or NaN).
+    """
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    lsb = (u >> np.uint32(16)) & np.uint32(1)
+    return ((u + np.uint32(0x7FFF) + lsb) >> np.uint32(16)).astype(np.uint16)
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    """Exact widening of bf16 bits to float32."""
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def _normal_bf16(seed: int, tensor_id: int, shape, std: float) -> np.ndarray:
+    """N(0, std^2) values rounded to bf16.
+
+    Chunk ``i`` of tensor ``tensor_id`` is drawn from its own PCG64 stream
+    seeded by ``SeedSequence([seed, tensor_id, i])``, so chunks can be drawn
+    on several threads and the result does not depend on the thread count.
+    """
+    n = int(np.prod(shape, dtype=np.int64))
+    out = np.empty(n, dtype=np.uint16)
+
+    def fill(i: int) -> None:
+        s = i * _CHUNK
+        e = min(n, s + _CHUNK)
+        g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, tensor_id, i])))
+        x = g.standard_normal(e - s, dtype=np.float32)
+        if std != 1.0:
+            x *= np.float32(std)
+        out[s:e] = f32_to_bf16_bits(x)
+
+    n_chunks = (n + _CHUNK - 1) // _CHUNK
+    if n_chunks <= 1:
+        for i in range(n_chunks):
+            fill(i)
+    else:
+        workers = min(n_chunks, os.cpu_count() or 1)
+        with ThreadPoolExecutor(workers) as ex:
+            list(ex.map(fill, range(n_chunks)))
+    return out.reshape(shape)
+
+
+@dataclass(frozen=True)
+class Config:
+    """A workload recipe.  ``counts``/``lens`` pick how the structure is drawn.
+
+    counts: "multinomial" -> every user gets 1 + Multinomial(n_cand - n_user, uniform)
+            "zipf"        -> Zipf(s) weights, with the last users forced to ``forced_counts``
+            a tuple       -> explicit per-user counts
+    lens:   "uniform"     -> integers uniform in [len_lo, len_hi]
+            "loguniform"  -> round(exp(U[ln len_lo, ln len_hi]))
+            a tuple       -> explicit per-user lengths
+    """
+
+    name: str
+    n_cand: int
+    n_user: int
+    H: int
+    D: int
+    Lq: int
+    seed: int
+    std: float = 1.0
+    counts: object = "multinomial"
+    lens: object = "uniform"
+    len_lo: int = 0
+    len_hi: int = 0
+    zipf_s: float = 1.1
+    forced_counts: Sequence[int] = ()
+    shuffle: bool = False
+    description: str = ""
+
+
+@dataclass
+class Workload:
+    cfg: Config
+    q: np.ndarray
+    k: np.ndarray
+    v: np.ndarray
+    user_offsets: np.ndarray
+    cand_to_user: np.ndarray
+    scale: float
+    counts: np.ndarray = field(repr=False, default=None)
+    lens: np.ndarray = field(repr=False, default=None)
+
+    @property
+    def n_cand(self) -> int:
+        return int(self.cand_to_user.shape[0])
+
+    @property
+    def n_user(self) -> int:
+        return int(self.user_offsets.shape[0] - 1)
+
+    @property
+    def T(self) -> int:
+        return int(self.user_offsets[-1])
+
+    @property
+    def S(self) -> int:
+        """Total keys visited: sum over candidates of their user's length."""
+        L = np.diff(self.user_offsets.astype(np.int64))
+        return int(L[self.cand_to_user.astype(np.int64)].sum())
+
+
+def _draw_counts(cfg: Config, rng: np.random.Generator) -> np.ndarray:
+    if isinstance(cfg.counts, (tuple, list)):
+        c = np.asarray(cfg.counts, dtype=np.int64)
+        assert c.shape == (cfg.n_user,) and int(c.sum()) == cfg.n_cand
+        return c
+    if cfg.counts == "multinomial":
+        extra = rng.multinomial(cfg.n_cand - cfg.n_user, [1.0 / cfg.n_user] * cfg.n_user)
+        return 1 + extra.astype(np.int64)
+    if cfg.counts == "zipf":
+        forced = np.asarray(cfg.forced_counts, dtype=np.int64)
+        n_free = cfg.n_user - forced.size
+        w = (np.arange(1, n_free + 1, dtype=np.float64)) ** (-cfg.zipf_s)
+        w /= w.sum()
+        extra = rng.multinomial(cfg.n_cand - int(forced.sum()) - n_free, w)
+        return np.concatenate([1 + extra.astype(np.int64), forced])
+    raise ValueError(f"unknown counts recipe {cfg.counts!r}")
+
+
+def _draw_lens(cfg: Config, rng: np.random.Generator) -> np.ndarray:
+    if isinstance(cfg.lens, (tuple, list)):
+        L = np.asarray(cfg.lens, dtype=np.int64)
+        assert L.shape == (cfg.n_user,)
+        return L
+    if cfg.lens == "uniform":
+        return rng.integers(cfg.len_lo, cfg.len_hi + 1, size=cfg.n_user).astype(np.int64)
+    if cfg.lens == "loguniform":
+        x = rng.uniform(np.log(cfg.len_lo), np.log(cfg.len_hi), size=cfg.n_user)
+        return np.clip(np.round(np.exp(x)), cfg.len_lo, cfg.len_hi).astype(np.int64)
+    raise ValueError(f"unknown lens recipe {cfg.lens!r}")
+
+
+def generate(cfg: Config) -> Workload:
+    """Draw one workload.  The same ``cfg`` always gives the same bits."""
+    rng = np.random.Generator(np.random.PCG64(cfg.seed))
+    counts = _draw_counts(cfg, rng)
+    lens = _draw_lens(cfg, rng)
+    c2u = np.repeat(np.arange(cfg.n_user, dtype=np.int32), counts)
+    if cfg.shuffle:
+        c2u = c2u[rng.permutation(c2u.shape[0])]
+    offsets = np.zeros(cfg.n_user + 1, dtype=np.int64)
+    np.cumsum(lens, out=offsets[1:])
+    assert offsets[-1] < 2**31
+    T = int(offsets[-1])
+    q = _normal_bf16(cfg.seed, 0, (cfg.n_cand, cfg.H, cfg.Lq, cfg.D), cfg.std)
+    k = _normal_bf16(cfg.seed, 1, (T, cfg.H, cfg.D), cfg.std)
+    v = _normal_bf16(cfg.seed, 2, (T, cfg.H, cfg.D), cfg.std)
+    return Workload(cfg=cfg, q=q, k=k, v=v,
+                    user_offsets=offsets.astype(np.int32),
+                    cand_to_user=c2u.astype(np.int32),
+                    scale=float(1.0 / np.sqrt(cfg.D)),
+                    counts=counts, lens=lens)
+
+
+def custom(n_user: int, counts: Sequence[int], lens: Sequence[int], H: int, D: int, Lq: int,
+           seed: int = 0, std: float = 1.0, shuffle: bool = False, name: str = "custom") -> Workload:
+    """A workload with explicit per-user candidate counts and sequence lengths."""
+    cfg = Config(name=name, n_cand=int(sum(counts)), n_user=n_user, H=H, D=D, Lq=Lq, seed=seed,
+                 std=std, counts=tuple(int(c) for c in counts), lens=tuple(int(x) for x in lens),
+                 shuffle=shuffle)
+    return generate(cfg)
+
+
+def sample_candidates(wl: Workload, max_count: int) -> np.ndarray:
+    """A deterministic subset of candidate indices for large workloads.
+
+    Every user's first and last candidate, plus an even stride over all
+    candidates, capped near ``max_count``; sorted, unique, int64.
+    """
+    n = wl.n_cand
+    if n <= max_count:
+        return np.arange(n, dtype=np.int64)
+    c2u = wl.cand_to_user.astype(np.int64)
+    picks = set(np.linspace(0, n - 1, num=max_count, dtype=np.int64).tolist())
+    first = {}
+    last = {}
+    for i, u in enumerate(c2u.tolist()):
+        first.setdefault(u, i)
+        last[u] = i
+    picks.update(first.values())
+    picks.update(last.values())
+    return np.asarray(sorted(picks), dtype=np.int64)
+
+
+CONFIGS = {
+    "tiny_8x2": Config(
+        name="tiny_8x2", n_cand=8, n_user=2, H=2, D=64, Lq=1, seed=0,
+        counts=(5, 3), lens=(16, 24),
+        description="2 users, 8 candidates (cand_to_user 0,0,0,0,0,1,1,1), L=16/24, H=2 D=64 Lq=1"),
+    "ratio_1024x15": Config(
+        name="ratio_1024x15", n_cand=1024, n_user=15, H=4, D=128, Lq=1, seed=1,
+        counts="multinomial", lens="uniform", len_lo=256, len_hi=1024,
+        description="1024 candidates over 15 users (~70:1), sorted, L~U[256,1024], H=4 D=128 Lq=1"),
+    "odd_groups_2048x16": Config(
+        name="odd_groups_2048x16", n_cand=2048, n_user=16, H=8, D=128, Lq=4, seed=2,
+        counts="zipf", zipf_s=1.1, forced_counts=(1, 1, 3), lens="uniform", len_lo=64, len_hi=4096,
+        description="2048 candidates over 16 users, Zipf(1.1) counts with users at 1,1,3, "
+                    "L~U[64,4096], H=8 D=128 Lq=4"),
+    "extreme_4096x4": Config(
+        name="extreme_4096x4", n_cand=4096, n_user=4, H=8, D=128, Lq=8, seed=3, std=0.5,
+        counts="multinomial", lens="uniform", len_lo=1024, len_hi=2048,
+        description="4096 candidates over 4 users (~1000:1), L~U[1024,2048], H=8 D=128 Lq=8, N(0,0.5)"),
+}
+for _D in (64, 128):
+    for _Lq in (1, 4):
+        _n = f"sweep_16384x64_d{_D}_lq{_Lq}"
+        CONFIGS[_n] = Config(
+            name=_n, n_cand=16384, n_user=64, H=16, D=_D, Lq=_Lq, seed=4,
+            counts="multinomial", lens="loguniform", len_lo=128, len_hi=8192,
+            description=f"16384 candidates over 64 users, L log-uniform [128,8192], H=16 D={_D} Lq={_Lq}")
+
+# The configuration the headline metric is quoted on (1024 candidates / 15 users).
+HEADLINE = "ratio_1024x15"

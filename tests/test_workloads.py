@@ -1,0 +1,58 @@
+"""The seeded input generators: determinism, bf16 rounding and the configs' structure."""
+import numpy as np
+import torch
+
+from broadcast_target_attention_gb300 import workloads as W
+
+
+def test_bf16_rounding_matches_torch():
+    rng = np.random.Generator(np.random.PCG64(0))
+    x = (rng.standard_normal(100000) * np.exp(rng.uniform(-20, 20, 100000))).astype(np.float32)
+    x[:4] = [1.00390625, 1.01171875, -1.00390625, 3.0]   # ties and exact values
+    ours = W.f32_to_bf16_bits(x)
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, ref)
+    assert np.array_equal(W.bf16_bits_to_f32(ours),
+                          torch.from_numpy(x).to(torch.bfloat16).float().numpy())
+
+
+def test_generation_is_deterministic():
+    a = W.generate(W.CONFIGS["ratio_1024x15"])
+    b = W.generate(W.CONFIGS["ratio_1024x15"])
+    for name in ("q", "k", "v", "user_offsets", "cand_to_user"):
+        assert np.array_equal(getattr(a, name), getattr(b, name))
+
+
+def test_headline_structure():
+    wl = W.generate(W.CONFIGS["ratio_1024x15"])
+    assert wl.n_cand == 1024 and wl.n_user == 15
+    assert np.all(wl.counts >= 1) and wl.counts.sum() == 1024
+    assert np.all(np.diff(wl.cand_to_user) >= 0)          # sorted
+    assert wl.lens.min() >= 256 and wl.lens.max() <= 1024
+    assert wl.q.shape == (1024, 4, 1, 128) and wl.k.shape == (wl.T, 4, 128)
+    x = W.bf16_bits_to_f32(wl.k)
+    assert abs(float(x.std()) - 1.0) < 0.01
+
+
+def test_odd_group_structure():
+    wl = W.generate(W.CONFIGS["odd_groups_2048x16"])
+    assert wl.counts.sum() == 2048 and list(wl.counts[-3:]) == [1, 1, 3]
+    assert int((wl.counts % 2 == 1).sum()) >= 2
+    assert wl.lens.min() >= 64 and wl.lens.max() <= 4096
+
+
+def test_extreme_and_sweep_structure():
+    wl = W.generate(W.CONFIGS["extreme_4096x4"])
+    assert wl.counts.sum() == 4096 and wl.n_user == 4
+    assert abs(float(W.bf16_bits_to_f32(wl.q).std()) - 0.5) < 0.01
+    cfg = W.CONFIGS["sweep_16384x64_d64_lq1"]
+    rng = np.random.Generator(np.random.PCG64(cfg.seed))
+    counts = W._draw_counts(cfg, rng)
+    lens = W._draw_lens(cfg, rng)
+    assert counts.sum() == 16384 and lens.min() >= 128 and lens.max() <= 8192
+
+
+def test_shuffled_mapping_is_a_permutation():
+    wl = W.custom(n_user=3, counts=[4, 2, 5], lens=[3, 4, 5], H=1, D=8, Lq=1, shuffle=True, seed=3)
+    assert sorted(wl.cand_to_user.tolist()) == [0] * 4 + [1] * 2 + [2] * 5
+    assert np.any(np.diff(wl.cand_to_user) < 0)
