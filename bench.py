@@ -1,0 +1,386 @@
+"""Benchmark of IKBO target attention on GB300 -- prints ONE JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ikbo|reference]
+
+A step is one pass of the whole hot path (planning kernel + tcgen05 attention
+kernel) over one batch of the headline workload: 1024 candidates over 15
+users (~70:1), user sequences of 256-1024 keys, H=4, D=128, Lq=1, bf16,
+seeded synthetic inputs already resident in HBM.  L2 is flushed (a write
+larger than L2) before every timed step.  `value` is whole-job TFLOP/s
+(4*H*D*Lq*S FLOPs, S = keys visited over all candidates); `e2e` is the same
+metric through the host-buffer entry point with the copies inside the timed
+region.  Under torchrun every rank runs its own replica (users shard with no
+exchange); the time is the max over ranks.
+
+--impl reference times the CPU fp64 oracle on the host cores on the same
+workload (bounded samples), the in-run baseline of this build.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from broadcast_target_attention_gb300 import accounting as A  # noqa: E402
+from broadcast_target_attention_gb300 import workloads as W  # noqa: E402
+
+METRIC = "IKBO target-attn BF16 TFLOP/s & candidates/s (1024 cand/15 users); % of peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "source": "measured"}
+    return dict(FALLBACK_PEAKS)
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def workload_for_rank(name: str, rank: int):
+    cfg = W.CONFIGS[name]
+    if rank:
+        cfg = W.Config(**{**cfg.__dict__, "seed": cfg.seed + 1000 * rank})
+    return W.generate(cfg)
+
+
+def config_block(wl, extra=None):
+    c = wl.cfg
+    d = {"workload": f"{c.name}: {c.description}", "n_cand": wl.n_cand, "n_user": wl.n_user,
+         "H": c.H, "D": c.D, "Lq": c.Lq, "T_keys": wl.T, "S_keys_visited": wl.S,
+         "l2": "flushed before every timed step (write of 2x L2 size)"}
+    if extra:
+        d.update(extra)
+    return d
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling while the GPU is busy."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, val in zip(names, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        busy = [x for x in sm if x > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(smax),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def kernel_traffic(kernel_name: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel_name, {}).get(workload)
+    if not e:
+        return None
+    src = os.path.join(ROOT, "broadcast_target_attention_gb300", "csrc")
+    h = hashlib.sha256()
+    for fn in sorted(os.listdir(src)):
+        with open(os.path.join(src, fn), "rb") as f:
+            h.update(f.read())
+    if e.get("source_sha256") != h.hexdigest():
+        return None
+    return float(e["dram_bytes_per_launch"])
+
+
+def run_reference(args):
+    """The oracle, as it stands, on the host cores: bounded samples of the workload."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    wl = workload_for_rank(args.config, 0)
+    c = wl.cfg
+    L = np.diff(wl.user_offsets.astype(np.int64))
+    cores = oracle.num_threads()
+    # size each step's sample so the whole run stays within ~2 minutes
+    t0 = time.perf_counter()
+    probe = W.sample_candidates(wl, 64)
+    oracle.attention_wl(wl, probe)
+    per_cand = (time.perf_counter() - t0) / len(probe)
+    budget_s = 120.0 / max(1, args.steps + args.warmup)
+    n_sel = int(max(16, min(wl.n_cand, budget_s / max(per_cand, 1e-9))))
+    sel = W.sample_candidates(wl, n_sel)
+    flops = A.flops(c.H, c.D, c.Lq, int(L[wl.cand_to_user[sel]].sum()))
+    for _ in range(args.warmup):
+        oracle.attention_wl(wl, sel)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.attention_wl(wl, sel)
+        times.append(time.perf_counter() - t0)
+    t = statistics.mean(times)
+    value = flops / t / 1e12
+    sample = f"{len(sel)} of {wl.n_cand} candidates per step (all heads, all users represented)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_block(wl, {"reference": "CPU fp64 oracle (broadcast, then softmax attention)"}),
+        "candidates_per_s": len(sel) / t,
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(wl, seconds: float = 10.0):
+    """The oracle timed on the host cores: whole-workload passes until ~`seconds` elapse."""
+    import oracle
+    c = wl.cfg
+    cores = oracle.num_threads()
+    sel = None
+    L = np.diff(wl.user_offsets.astype(np.int64))
+    t0 = time.perf_counter()
+    probe = W.sample_candidates(wl, 64)
+    oracle.attention_wl(wl, probe)
+    per_cand = (time.perf_counter() - t0) / len(probe)
+    if per_cand * wl.n_cand > seconds:
+        sel = W.sample_candidates(wl, int(max(16, seconds / per_cand)))
+    S = int(L[wl.cand_to_user[sel]].sum()) if sel is not None else wl.S
+    flops = A.flops(c.H, c.D, c.Lq, S)
+    runs, t_total = 0, 0.0
+    while t_total < seconds and runs < 1000:
+        t0 = time.perf_counter()
+        oracle.attention_wl(wl, sel)
+        t_total += time.perf_counter() - t0
+        runs += 1
+    n = wl.n_cand if sel is None else len(sel)
+    return {"value": flops * runs / t_total / 1e12, "unit": "TFLOP/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{runs} passes over {n} of {wl.n_cand} candidates ({t_total:.1f} s of CPU work)"}
+
+
+def run_ikbo(args):
+    import torch
+    import torch.distributed as dist
+
+    import broadcast_target_attention_gb300 as ikbo
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ikbo.load()
+    wl = workload_for_rank(args.config, rank)
+    c = wl.cfg
+    nums = A.workload_numbers(wl)
+    flops, alg_bytes = nums["flops"], nums["alg_bytes"]
+
+    def t(a, dt):
+        return torch.from_numpy(np.ascontiguousarray(a)).view(dt).to(dev)
+
+    q = t(wl.q.view(np.int16), torch.bfloat16)
+    k = t(wl.k.view(np.int16), torch.bfloat16)
+    v = t(wl.v.view(np.int16), torch.bfloat16)
+    off = t(wl.user_offsets, torch.int32)
+    c2u = t(wl.cand_to_user, torch.int32)
+    out = torch.empty_like(q)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.int32, device=dev)
+
+    def step():
+        ikbo.attn_fwd(q, k, v, off, c2u, wl.scale, out=out)
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    with ClockSampler(local) as clk:
+        for _ in range(args.warmup):
+            flush.fill_(1)
+            step()
+        assert ikbo.get_device_error() == 0
+        # 1. timed steps: flush, then the hot path between two events, back to back
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        barrier()
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            starts[i].record()
+            step()
+            ends[i].record()
+        barrier()
+        step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        # 2. per-kernel durations (events recorded by the library around each kernel)
+        ikbo.set_timing(True)
+        plan_ms, attn_ms = [], []
+        for i in range(min(args.steps, 200)):
+            flush.fill_(i & 0xFF)
+            step()
+            a, b = ikbo.get_timing()
+            plan_ms.append(a)
+            attn_ms.append(b)
+        ikbo.set_timing(False)
+        # 3. end to end through the host-buffer entry point
+        hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
+        hoff, hc2u = off.cpu().pin_memory(), c2u.cpu().pin_memory()
+        hout = torch.empty_like(hq).pin_memory()
+        for _ in range(3):
+            ikbo.attn_fwd_host(hq, hk, hv, hoff, hc2u, wl.scale, out=hout)
+        e2e_ms = []
+        n_e2e = min(args.steps, 50)
+        for _ in range(n_e2e):
+            t0 = time.perf_counter()
+            ikbo.attn_fwd_host(hq, hk, hv, hoff, hc2u, wl.scale, out=hout)
+            e2e_ms.append((time.perf_counter() - t0) * 1e3)
+        # 4. the explicit-broadcast comparison path
+        bout = torch.empty_like(q)
+        ikbo.broadcast_attn_fwd(q, k, v, off, c2u, wl.scale, out=bout)
+        ikbo.set_timing(True)
+        bc_ms = []
+        for i in range(min(args.steps, 20)):
+            flush.fill_(i & 0xFF)
+            ikbo.broadcast_attn_fwd(q, k, v, off, c2u, wl.scale, out=bout)
+            bc_ms.append(ikbo.get_timing()[1])
+        ikbo.set_timing(False)
+    assert ikbo.get_device_error() == 0
+    clocks = clk.summary()
+
+    ms = statistics.mean(step_ms)
+    if ws > 1:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    total_flops = flops * ws
+    value = total_flops / (ms * 1e-3) / 1e12
+    pk = peaks()
+    attn = statistics.mean(attn_ms)
+    achieved_gbs = alg_bytes / (attn * 1e-3) / 1e9
+    traffic = kernel_traffic(f"ikbo_attn_tc_kernel<{c.D}>", c.name)
+    ai = flops / alg_bytes
+    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    if ai < ridge:
+        roof = {"bound": "hbm", "achieved": achieved_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved_gbs / pk["hbm_gbs"], "traffic": traffic,
+                "kernel": f"ikbo_attn_tc_kernel<{c.D}>", "alg_bytes_per_launch": alg_bytes,
+                "peak_source": pk["source"] + " (burst copy)"}
+    else:
+        tf = flops / (attn * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": tf, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": tf / pk["bf16_tflops"], "traffic": traffic,
+                "kernel": f"ikbo_attn_tc_kernel<{c.D}>", "flops_per_launch": flops,
+                "peak_source": pk["source"] + " (burst cuBLAS bf16)"}
+    qb = wl.q.nbytes
+    h2d = qb + wl.k.nbytes + wl.v.nbytes + wl.user_offsets.nbytes + wl.cand_to_user.nbytes
+    e2e = statistics.mean(e2e_ms)
+    bc = statistics.mean(bc_ms)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_block(wl, {"parallelism": f"{ws} independent replica(s), users sharded, no exchange"}),
+        "candidates_per_s": wl.n_cand * ws / (ms * 1e-3),
+        "pct_of_peak": {"bf16_tensor": value / ws / pk["bf16_tflops"],
+                        "hbm_roofline_attn_kernel": achieved_gbs / pk["hbm_gbs"]},
+        "kernel_ms": {"plan": statistics.mean(plan_ms), "attn": attn,
+                      "step_min": min(step_ms), "step_median": statistics.median(step_ms)},
+        "roofline": roof,
+        "e2e": {"value": total_flops / (e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": qb, "ms_per_step": e2e},
+        "broadcast_path": {"ms_per_step": bc, "value": flops / (bc * 1e-3) / 1e12, "unit": "TFLOP/s",
+                           "ikbo_speedup": bc / ms,
+                           "extra_bytes": nums["broadcast_extra_bytes"]},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0:
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds) if not args.no_cpu_baseline else None
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ikbo", choices=["ikbo", "reference"])
+    ap.add_argument("--config", default=W.HEADLINE, choices=sorted(W.CONFIGS))
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ikbo(args)
+
+
+if __name__ == "__main__":
+    main()

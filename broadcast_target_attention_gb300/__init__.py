@@ -1,0 +1,167 @@
+"""IKBO target attention on GB300 (sm_103a): Python binding of the C ABI.
+
+Every function here only checks and marshals arguments (tensor pointers,
+sizes, the current CUDA stream) and calls ``libikbo.so``; all arithmetic runs
+in the library's CUDA kernels.  There is no CPU or PyTorch fallback: if the
+library is missing the call raises.
+
+Layouts (see include/ikbo.h): q/out bf16 [n_cand, H, Lq, D]; k/v bf16
+[T, H, D] packed by user; user_offsets int32 [n_user+1]; cand_to_user int32
+[n_cand].
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Tuple
+
+from . import _lib
+from ._lib import STATUS
+
+__all__ = ["attn_fwd", "broadcast_attn_fwd", "attn_fwd_host", "get_device_error", "set_timing",
+           "get_timing", "set_kernel", "set_debug", "version", "load", "IkboError", "STATUS"]
+
+
+class IkboError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        msg = _lib.lib().ikbo_strerror(status).decode()
+        super().__init__(f"{STATUS.get(status, status)}: {msg}" + (f" ({what})" if what else ""))
+
+
+def load():
+    """Load the CUDA library (raises if it was not built)."""
+    return _lib.lib()
+
+
+def _check(rc: int, what: str = "") -> None:
+    if rc != 0:
+        raise IkboError(rc, what)
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream_handle(stream) -> Optional[int]:
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _shape(q, k):
+    if q.dim() != 4 or k.dim() != 3:
+        raise ValueError("q must be [n_cand, H, Lq, D] and k/v [T, H, D]")
+    n_cand, H, Lq, D = q.shape
+    if k.shape[1] != H or k.shape[2] != D:
+        raise ValueError(f"k shape {tuple(k.shape)} does not match q heads/dim ({H}, {D})")
+    return int(n_cand), int(H), int(Lq), int(D)
+
+
+def _validate(q, k, v, user_offsets, cand_to_user, device: bool):
+    import torch
+    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16), ("v", v, torch.bfloat16),
+                        ("user_offsets", user_offsets, torch.int32),
+                        ("cand_to_user", cand_to_user, torch.int32)):
+        if t.dtype != dt:
+            raise TypeError(f"{name} must be {dt}, got {t.dtype}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if device and not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not device and t.is_cuda:
+            raise ValueError(f"{name} must be a host tensor")
+    if v.shape != k.shape:
+        raise ValueError("k and v must have the same shape")
+
+
+def attn_fwd(q, k, v, user_offsets, cand_to_user, scale: Optional[float] = None, out=None,
+             stream=None):
+    """IKBO target attention on device tensors; returns ``out`` (bf16, like q).
+
+    Asynchronous on ``stream`` (default: torch's current stream).  Index
+    errors found on the GPU are reported by :func:`get_device_error`.
+    """
+    import torch
+    _validate(q, k, v, user_offsets, cand_to_user, device=True)
+    n_cand, H, Lq, D = _shape(q, k)
+    n_user = int(user_offsets.shape[0]) - 1
+    if scale is None:
+        scale = D ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    rc = _lib.lib().ikbo_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(user_offsets), _ptr(cand_to_user),
+                                  n_cand, n_user, H, Lq, D, float(scale), _ptr(out),
+                                  _stream_handle(stream))
+    _check(rc, "ikbo_attn_fwd")
+    return out
+
+
+def broadcast_attn_fwd(q, k, v, user_offsets, cand_to_user, scale: Optional[float] = None,
+                       out=None, mem_budget_bytes: int = 16 << 30, stream=None):
+    """The explicit-broadcast comparison path (copies K/V per candidate first)."""
+    import torch
+    _validate(q, k, v, user_offsets, cand_to_user, device=True)
+    n_cand, H, Lq, D = _shape(q, k)
+    n_user = int(user_offsets.shape[0]) - 1
+    if scale is None:
+        scale = D ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    rc = _lib.lib().ikbo_broadcast_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(user_offsets),
+                                            _ptr(cand_to_user), n_cand, n_user, H, Lq, D,
+                                            float(scale), _ptr(out), int(mem_budget_bytes),
+                                            _stream_handle(stream))
+    _check(rc, "ikbo_broadcast_attn_fwd")
+    return out
+
+
+def attn_fwd_host(q, k, v, user_offsets, cand_to_user, scale: Optional[float] = None, out=None,
+                  stream=None):
+    """IKBO target attention on HOST tensors (pinned recommended); synchronous.
+
+    The library copies the inputs to the GPU, runs, and copies ``out`` back.
+    """
+    import torch
+    _validate(q, k, v, user_offsets, cand_to_user, device=False)
+    n_cand, H, Lq, D = _shape(q, k)
+    n_user = int(user_offsets.shape[0]) - 1
+    if scale is None:
+        scale = D ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    rc = _lib.lib().ikbo_attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(user_offsets),
+                                       _ptr(cand_to_user), n_cand, n_user, H, Lq, D, float(scale),
+                                       _ptr(out), _stream_handle(stream))
+    _check(rc, "ikbo_attn_fwd_host")
+    return out
+
+
+def get_device_error(stream=None) -> int:
+    """Synchronise the stream; return and clear the device error word (0 = none)."""
+    return int(_lib.lib().ikbo_get_device_error(_stream_handle(stream)))
+
+
+def set_timing(enable: bool) -> None:
+    _check(_lib.lib().ikbo_set_timing(1 if enable else 0))
+
+
+def get_timing() -> Tuple[float, float]:
+    """(planning kernel ms, attention kernel ms) of the last timed call."""
+    a = ctypes.c_float()
+    b = ctypes.c_float()
+    _check(_lib.lib().ikbo_get_timing(ctypes.byref(a), ctypes.byref(b)), "ikbo_get_timing")
+    return a.value, b.value
+
+
+def set_kernel(which: int) -> int:
+    """0 = tcgen05 kernel (default), 1 = SIMT cross-check kernel; returns the previous choice."""
+    return int(_lib.lib().ikbo_set_kernel(int(which)))
+
+
+def set_debug(flags: int = 0, timeout_ns: int = 0) -> None:
+    """Test hook of the library (see ikbo_set_debug in include/ikbo.h)."""
+    _check(_lib.lib().ikbo_set_debug(int(flags), int(timeout_ns)))
+
+
+def version() -> int:
+    return int(_lib.lib().ikbo_version())

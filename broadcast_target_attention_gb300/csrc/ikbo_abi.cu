@@ -1,0 +1,603 @@
+// C ABI of the IKBO target-attention library: host-side checks, scratch
+// space, tensor-map templates and kernel launches.  See include/ikbo.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/ikbo.h"
+#include "ikbo_attn_simt.cuh"
+#include "ikbo_attn_tc.cuh"
+#include "ikbo_broadcast.cuh"
+#include "ikbo_common.cuh"
+#include "ikbo_plan.cuh"
+
+namespace ikbo {
+
+// Per-device error word (bits kErrIndex, kErrOffsets, kErrTimeout).
+__device__ int g_ikbo_error_word;
+
+namespace {
+
+constexpr int kVersion = 10000;  // 1.0.0
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;   // 2 s bound on any in-kernel wait
+
+struct DeviceState {
+  bool ready = false;
+  int num_sms = 0;
+  int* err_word = nullptr;
+  cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
+  bool ev_ready = false;
+};
+
+std::mutex g_mutex;
+DeviceState g_dev[kMaxDevices];
+bool g_timing = false;
+int g_timing_dev = -1;
+int g_debug_flags = 0;
+uint64_t g_timeout_ns = kDefaultTimeoutNs;
+thread_local int t_kernel = 0;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+int cuda_fail(cudaError_t e) {
+  (void)e;
+  return IKBO_ERR_CUDA;
+}
+
+// Current device's state, initialised on first use.
+int device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return IKBO_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return IKBO_ERR_DEVICE;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState& s = g_dev[dev];
+  if (!s.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return IKBO_ERR_CUDA;
+    if (major != 10 || minor != 3) return IKBO_ERR_DEVICE;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_ikbo_error_word) != cudaSuccess) return IKBO_ERR_CUDA;
+    // Keep freed scratch in the stream-ordered pool instead of returning it
+    // to the driver after every call.
+    cudaMemPool_t pool;
+    if (cudaDeviceGetDefaultMemPool(&pool, dev) == cudaSuccess) {
+      uint64_t thr = UINT64_MAX;
+      cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &thr);
+    }
+    if (!g_encode) {
+      cudaDriverEntryPointQueryResult q;
+      void* fn = nullptr;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return IKBO_ERR_CUDA;
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    s.num_sms = sms;
+    s.err_word = static_cast<int*>(p);
+    s.ready = true;
+  }
+  *out = &s;
+  return IKBO_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_args(const void* q, const void* k, const void* v, const int32_t* off, const int32_t* c2u,
+               int64_t n_cand, int64_t n_user, int32_t H, int32_t Lq, int32_t D, float scale,
+               const void* out) {
+  if (n_cand < 0 || n_user < 0 || H < 1 || Lq < 1 || Lq > kTileM || (D != 64 && D != 128))
+    return IKBO_ERR_SHAPE;
+  if (n_cand >= (int64_t(1) << 31) || n_user >= (int64_t(1) << 31) - 1) return IKBO_ERR_SHAPE;
+  if (!std::isfinite(scale)) return IKBO_ERR_SCALE;
+  if (n_cand == 0) return IKBO_OK;
+  if (!q || !k || !v || !off || !c2u || !out) return IKBO_ERR_NULL;
+  if (n_user == 0) return IKBO_ERR_INDEX;  // every candidate would point outside [0, 0)
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(off) & 3u) || (reinterpret_cast<uintptr_t>(c2u) & 3u))
+    return IKBO_ERR_ALIGN;
+  const uintptr_t ob = reinterpret_cast<uintptr_t>(out);
+  const uintptr_t oe = ob + uintptr_t(n_cand) * H * Lq * D * 2;
+  const uintptr_t qb = reinterpret_cast<uintptr_t>(q);
+  const uintptr_t qe = qb + uintptr_t(n_cand) * H * Lq * D * 2;
+  if (ob < qe && qb < oe) return IKBO_ERR_ALIAS;
+  const uintptr_t kb = reinterpret_cast<uintptr_t>(k), vb = reinterpret_cast<uintptr_t>(v);
+  if ((kb >= ob && kb < oe) || (vb >= ob && vb < oe)) return IKBO_ERR_ALIAS;
+  return IKBO_OK;
+}
+
+// Candidates per query tile: floor(128 / Lq), rounded down to a whole number
+// of Q boxes (a box holds `qbox_cands(Lq)` candidates).
+int qbox_cands(int Lq) {
+  if (Lq >= 8) return 1;
+  int nb = 1;
+  while (nb * 2 * Lq <= 8) nb *= 2;
+  return nb;
+}
+int cands_per_tile(int Lq) {
+  const int nb = qbox_cands(Lq);
+  return (kTileM / Lq) / nb * nb;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Layout of the per-call scratch space.
+struct Workspace {
+  size_t header, kmap, vmap, items, units, perm, cand_start, scratch, partial_o, partial_ml, total;
+  int max_items, max_split_items, max_units;
+};
+
+Workspace plan_workspace(int64_t n_cand, int64_t n_user, int H, int Lq, int D, int num_sms) {
+  Workspace w;
+  const int cpt = cands_per_tile(Lq);
+  const int64_t units_bound =
+      int64_t(H) * ((n_cand + cpt - 1) / cpt + (n_user < n_cand ? n_user : n_cand));
+  w.max_items = int(num_sms + units_bound);
+  w.max_split_items = 3 * num_sms;
+  w.max_units = w.max_split_items;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = o;
+    o = align_up(o + bytes, 256);
+    return at;
+  };
+  w.header = take(sizeof(PlanHeader));
+  w.kmap = take(sizeof(CUtensorMap));
+  w.vmap = take(sizeof(CUtensorMap));
+  w.items = take(sizeof(WorkItem) * size_t(w.max_items));
+  w.units = take(sizeof(UnitInfo) * size_t(w.max_units));
+  w.perm = take(sizeof(int32_t) * size_t(n_cand));
+  w.cand_start = take(sizeof(int32_t) * size_t(n_user + 1));
+  w.scratch = take(sizeof(int32_t) * size_t(3 * n_user + 2));
+  w.partial_o = take(sizeof(float) * size_t(w.max_split_items) * kTileM * D);
+  w.partial_ml = take(sizeof(float2) * size_t(w.max_split_items) * kTileM);
+  w.total = o;
+  return w;
+}
+
+int encode_kv_map(CUtensorMap* m, const void* base, int H, int D, int block_n) {
+  // 2-D view of k (or v): rows = tokens, columns = H * D; the row count is a
+  // placeholder that the planner replaces with T on the device.
+  cuuint64_t dims[2] = {cuuint64_t(H) * D, cuuint64_t(block_n)};
+  cuuint64_t strides[1] = {cuuint64_t(H) * D * 2};
+  cuuint32_t box[2] = {64, cuuint32_t(block_n)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? IKBO_OK : IKBO_ERR_CUDA;
+}
+
+int encode_q_map(CUtensorMap* m, const void* q, int64_t n_cand, int H, int Lq, int D, int nb) {
+  // 4-D view {D, Lq, H, n_cand}; one box = nb candidates x Lq tokens x 64
+  // columns of one head, as 128-byte swizzled rows.
+  cuuint64_t dims[4] = {cuuint64_t(D), cuuint64_t(Lq), cuuint64_t(H), cuuint64_t(n_cand)};
+  cuuint64_t strides[3] = {cuuint64_t(D) * 2, cuuint64_t(Lq) * D * 2, cuuint64_t(H) * Lq * D * 2};
+  cuuint32_t box[4] = {64, cuuint32_t(Lq), 1, cuuint32_t(nb)};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(q), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? IKBO_OK : IKBO_ERR_CUDA;
+}
+
+template <typename Kern, typename... Args>
+cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+template <int D>
+cudaError_t launch_attn_tc(const AttnParams& ap, const CUtensorMap& qmap, const CUtensorMap& qmap1,
+                           int grid, cudaStream_t st) {
+  constexpr int smem = TcConfig<D>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(ikbo_attn_tc_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(ikbo_attn_tc_kernel<D>, dim3(grid), dim3(kTcThreads), smem, st, ap, qmap, qmap1);
+}
+
+// Plan + attention on device buffers, scratch from `ws` (>= plan_workspace().total).
+int run_ikbo(DeviceState* ds, const void* q, const void* k, const void* v, const int32_t* off,
+             const int32_t* c2u, int64_t n_cand, int64_t n_user, int H, int Lq, int D, float scale,
+             void* out, char* ws, const Workspace& L, cudaStream_t st) {
+  const int kernel = t_kernel;
+  PlanParams pp = {};
+  pp.cand_to_user = c2u;
+  pp.user_offsets = off;
+  pp.n_cand = n_cand;
+  pp.n_user = n_user;
+  pp.H = H;
+  pp.cands_per_tile = cands_per_tile(Lq);
+  pp.block_n = kBlockN;
+  pp.num_sms = ds->num_sms;
+  pp.max_items = L.max_items;
+  pp.max_split_items = L.max_split_items;
+  pp.max_units = L.max_units;
+  pp.header = reinterpret_cast<PlanHeader*>(ws + L.header);
+  pp.items = reinterpret_cast<WorkItem*>(ws + L.items);
+  pp.units = reinterpret_cast<UnitInfo*>(ws + L.units);
+  pp.perm = reinterpret_cast<int32_t*>(ws + L.perm);
+  pp.cand_start = reinterpret_cast<int32_t*>(ws + L.cand_start);
+  pp.scratch = reinterpret_cast<int32_t*>(ws + L.scratch);
+  pp.err_word = ds->err_word;
+
+  PlanExtra px;
+  std::memset(&px, 0, sizeof px);
+  px.out = out;
+  px.Lq = Lq;
+  px.D = D;
+  px.patch_maps = kernel == 0 ? 1 : 0;
+  px.kmap_dst = reinterpret_cast<CUtensorMap*>(ws + L.kmap);
+  px.vmap_dst = reinterpret_cast<CUtensorMap*>(ws + L.vmap);
+  CUtensorMap qmap, qmap1;
+  std::memset(&qmap, 0, sizeof qmap);
+  std::memset(&qmap1, 0, sizeof qmap1);
+  if (kernel == 0) {
+    if (encode_kv_map(&px.kmap_tmpl, k, H, D, kBlockN) != IKBO_OK ||
+        encode_kv_map(&px.vmap_tmpl, v, H, D, kBlockN) != IKBO_OK ||
+        encode_q_map(&qmap, q, n_cand, H, Lq, D, qbox_cands(Lq)) != IKBO_OK ||
+        encode_q_map(&qmap1, q, n_cand, H, Lq, D, 1) != IKBO_OK)
+      return IKBO_ERR_CUDA;
+  }
+
+  AttnParams ap = {};
+  ap.q = static_cast<const uint16_t*>(q);
+  ap.k = static_cast<const uint16_t*>(k);
+  ap.v = static_cast<const uint16_t*>(v);
+  ap.out = static_cast<uint16_t*>(out);
+  ap.n_cand = n_cand;
+  ap.H = H;
+  ap.Lq = Lq;
+  ap.scale_log2 = scale * 1.4426950408889634f;
+  ap.max_items = L.max_items;
+  ap.header = pp.header;
+  ap.items = pp.items;
+  ap.units = pp.units;
+  ap.perm = pp.perm;
+  ap.partial_o = reinterpret_cast<float*>(ws + L.partial_o);
+  ap.partial_ml = reinterpret_cast<float2*>(ws + L.partial_ml);
+  ap.err_word = ds->err_word;
+  ap.kmap = px.kmap_dst;
+  ap.vmap = px.vmap_dst;
+  ap.timeout_ns = g_timeout_ns;
+  ap.qbox = qbox_cands(Lq);
+  ap.debug_flags = g_debug_flags;
+
+  const bool timed = g_timing;
+  if (timed) cudaEventRecord(ds->ev[0], st);
+  ikbo_plan_kernel<<<1, kPlanThreads, 0, st>>>(pp, px);
+  if (cudaGetLastError() != cudaSuccess) return IKBO_ERR_CUDA;
+  if (timed) cudaEventRecord(ds->ev[1], st);
+  cudaError_t e;
+  if (kernel == 1) {
+    const int grid = L.max_items < ds->num_sms * 8 ? L.max_items : ds->num_sms * 8;
+    if (D == 64)
+      e = launch_pdl(ikbo_attn_simt_kernel<64>, dim3(grid), dim3(kSimtThreads), 0, st, ap);
+    else
+      e = launch_pdl(ikbo_attn_simt_kernel<128>, dim3(grid), dim3(kSimtThreads), 0, st, ap);
+  } else {
+    const int grid = L.max_items < ds->num_sms ? L.max_items : ds->num_sms;
+    if (D == 64)
+      e = launch_attn_tc<64>(ap, qmap, qmap1, grid, st);
+    else
+      e = launch_attn_tc<128>(ap, qmap, qmap1, grid, st);
+  }
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (timed) {
+    cudaEventRecord(ds->ev[2], st);
+    int dev = 0;
+    cudaGetDevice(&dev);
+    g_timing_dev = dev;
+  }
+  return IKBO_OK;
+}
+
+int ensure_events(DeviceState* ds) {
+  if (ds->ev_ready) return IKBO_OK;
+  for (auto& e : ds->ev)
+    if (cudaEventCreate(&e) != cudaSuccess) return IKBO_ERR_CUDA;
+  ds->ev_ready = true;
+  return IKBO_OK;
+}
+
+}  // namespace
+}  // namespace ikbo
+
+using namespace ikbo;
+
+extern "C" {
+
+int ikbo_attn_fwd(const void* q, const void* k_user, const void* v_user,
+                  const int32_t* user_offsets, const int32_t* cand_to_user, int64_t n_cand,
+                  int64_t n_user, int32_t H, int32_t Lq, int32_t D, float scale, void* out,
+                  ikbo_stream_t stream) {
+  int rc = check_args(q, k_user, v_user, user_offsets, cand_to_user, n_cand, n_user, H, Lq, D,
+                      scale, out);
+  if (rc != IKBO_OK || n_cand == 0) return rc;
+  DeviceState* ds = nullptr;
+  if ((rc = device_state(&ds)) != IKBO_OK) return rc;
+  if (g_timing && (rc = ensure_events(ds)) != IKBO_OK) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const Workspace L = plan_workspace(n_cand, n_user, H, Lq, D, ds->num_sms);
+  void* ws = nullptr;
+  if (cudaMallocAsync(&ws, L.total, st) != cudaSuccess) return IKBO_ERR_CUDA;
+  rc = run_ikbo(ds, q, k_user, v_user, user_offsets, cand_to_user, n_cand, n_user, H, Lq, D, scale,
+                out, static_cast<char*>(ws), L, st);
+  if (cudaFreeAsync(ws, st) != cudaSuccess && rc == IKBO_OK) rc = IKBO_ERR_CUDA;
+  return rc;
+}
+
+int ikbo_attn_fwd_host(const void* q, const void* k_user, const void* v_user,
+                       const int32_t* user_offsets, const int32_t* cand_to_user, int64_t n_cand,
+                       int64_t n_user, int32_t H, int32_t Lq, int32_t D, float scale, void* out,
+                       ikbo_stream_t stream) {
+  int rc = check_args(q, k_user, v_user, user_offsets, cand_to_user, n_cand, n_user, H, Lq, D,
+                      scale, out);
+  if (rc != IKBO_OK || n_cand == 0) return rc;
+  if (user_offsets[0] != 0) return IKBO_ERR_OFFSETS;
+  const int64_t T = user_offsets[n_user];
+  if (T < 0) return IKBO_ERR_OFFSETS;
+  DeviceState* ds = nullptr;
+  if ((rc = device_state(&ds)) != IKBO_OK) return rc;
+  if (g_timing && (rc = ensure_events(ds)) != IKBO_OK) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const Workspace L = plan_workspace(n_cand, n_user, H, Lq, D, ds->num_sms);
+  const size_t qbytes = size_t(n_cand) * H * Lq * D * 2;
+  const size_t kvbytes = size_t(T) * H * D * 2;
+  const size_t o_q = 0, o_k = align_up(o_q + qbytes, 256), o_v = align_up(o_k + kvbytes, 256);
+  const size_t o_off = align_up(o_v + kvbytes, 256);
+  const size_t o_c2u = align_up(o_off + size_t(n_user + 1) * 4, 256);
+  const size_t o_out = align_up(o_c2u + size_t(n_cand) * 4, 256);
+  const size_t o_ws = align_up(o_out + qbytes, 256);
+  char* buf = nullptr;
+  if (cudaMallocAsync(reinterpret_cast<void**>(&buf), o_ws + L.total, st) != cudaSuccess)
+    return IKBO_ERR_CUDA;
+  cudaError_t e = cudaSuccess;
+  if (e == cudaSuccess) e = cudaMemcpyAsync(buf + o_q, q, qbytes, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess && kvbytes) e = cudaMemcpyAsync(buf + o_k, k_user, kvbytes, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess && kvbytes) e = cudaMemcpyAsync(buf + o_v, v_user, kvbytes, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(buf + o_off, user_offsets, size_t(n_user + 1) * 4, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(buf + o_c2u, cand_to_user, size_t(n_cand) * 4, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) {
+    rc = run_ikbo(ds, buf + o_q, buf + o_k, buf + o_v, reinterpret_cast<int32_t*>(buf + o_off),
+                  reinterpret_cast<int32_t*>(buf + o_c2u), n_cand, n_user, H, Lq, D, scale,
+                  buf + o_out, buf + o_ws, L, st);
+    if (rc == IKBO_OK) e = cudaMemcpyAsync(out, buf + o_out, qbytes, cudaMemcpyDeviceToHost, st);
+  }
+  cudaFreeAsync(buf, st);
+  if (cudaStreamSynchronize(st) != cudaSuccess || e != cudaSuccess) return IKBO_ERR_CUDA;
+  if (rc != IKBO_OK) return rc;
+  return ikbo_get_device_error(stream);
+}
+
+int ikbo_broadcast_attn_fwd(const void* q, const void* k_user, const void* v_user,
+                            const int32_t* user_offsets, const int32_t* cand_to_user,
+                            int64_t n_cand, int64_t n_user, int32_t H, int32_t Lq, int32_t D,
+                            float scale, void* out, size_t mem_budget_bytes,
+                            ikbo_stream_t stream) {
+  int rc = check_args(q, k_user, v_user, user_offsets, cand_to_user, n_cand, n_user, H, Lq, D,
+                      scale, out);
+  if (rc != IKBO_OK || n_cand == 0) return rc;
+  DeviceState* ds = nullptr;
+  if ((rc = device_state(&ds)) != IKBO_OK) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // Read the index tensors back to size the copies.
+  std::vector<int32_t> off(static_cast<size_t>(n_user + 1));
+  std::vector<int32_t> c2u(static_cast<size_t>(n_cand));
+  if (cudaMemcpyAsync(off.data(), user_offsets, off.size() * 4, cudaMemcpyDeviceToHost, st) !=
+          cudaSuccess ||
+      cudaMemcpyAsync(c2u.data(), cand_to_user, c2u.size() * 4, cudaMemcpyDeviceToHost, st) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return IKBO_ERR_CUDA;
+  if (off[0] != 0) return IKBO_ERR_OFFSETS;
+  for (int64_t u = 0; u < n_user; ++u)
+    if (off[u + 1] < off[u]) return IKBO_ERR_OFFSETS;
+  for (int64_t c = 0; c < n_cand; ++c)
+    if (c2u[c] < 0 || c2u[c] >= n_user) return IKBO_ERR_INDEX;
+  const size_t row_bytes = size_t(H) * D * 2;
+  const size_t qrow = size_t(H) * Lq * D * 2;
+  // Chunks [c0, c1) whose K+V copy fits the budget.
+  std::vector<int64_t> cuts(1, 0);
+  std::vector<int64_t> chunk_rows;
+  {
+    int64_t rows = 0;
+    for (int64_t c = 0; c < n_cand; ++c) {
+      const int64_t L = off[c2u[c] + 1] - off[c2u[c]];
+      if (size_t(L) * row_bytes * 2 > mem_budget_bytes) return IKBO_ERR_BUDGET;
+      if (size_t(rows + L) * row_bytes * 2 > mem_budget_bytes) {
+        cuts.push_back(c);
+        chunk_rows.push_back(rows);
+        rows = 0;
+      }
+      rows += L;
+    }
+    cuts.push_back(n_cand);
+    chunk_rows.push_back(rows);
+  }
+  // Per candidate: source row, destination offset (int64, copy kernel) and
+  // the per-chunk jagged offsets / identity map (int32, attention), all
+  // copied to the device once.
+  std::vector<int32_t> src(static_cast<size_t>(n_cand));
+  std::vector<int32_t> offb(static_cast<size_t>(n_cand) + cuts.size());
+  std::vector<int32_t> id(static_cast<size_t>(n_cand));
+  std::vector<int64_t> dst(static_cast<size_t>(n_cand) + cuts.size());
+  {
+    size_t ob = 0;
+    for (size_t ch = 0; ch + 1 < cuts.size(); ++ch) {
+      int64_t acc = 0;
+      for (int64_t c = cuts[ch]; c < cuts[ch + 1]; ++c) {
+        const int32_t u = c2u[c];
+        src[c] = off[u];
+        dst[ob] = acc;
+        offb[ob] = int32_t(acc);
+        id[c] = int32_t(c - cuts[ch]);
+        acc += off[u + 1] - off[u];
+        ++ob;
+      }
+      dst[ob] = acc;
+      offb[ob] = int32_t(acc);
+      ++ob;
+    }
+  }
+  const size_t m_src = 0, m_dst = align_up(src.size() * 4, 256);
+  const size_t m_offb = align_up(m_dst + dst.size() * 8, 256);
+  const size_t m_id = align_up(m_offb + offb.size() * 4, 256);
+  const size_t m_total = align_up(m_id + id.size() * 4, 256);
+  char* meta = nullptr;
+  if (cudaMallocAsync(reinterpret_cast<void**>(&meta), m_total, st) != cudaSuccess)
+    return IKBO_ERR_CUDA;
+  cudaError_t e = cudaMemcpyAsync(meta + m_src, src.data(), src.size() * 4, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(meta + m_dst, dst.data(), dst.size() * 8, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(meta + m_offb, offb.data(), offb.size() * 4, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(meta + m_id, id.data(), id.size() * 4, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);   // host vectors die at return
+  if (e != cudaSuccess) {
+    cudaFreeAsync(meta, st);
+    return IKBO_ERR_CUDA;
+  }
+  const bool timed = g_timing;
+  if (timed) {
+    if ((rc = ensure_events(ds)) != IKBO_OK) {
+      cudaFreeAsync(meta, st);
+      return rc;
+    }
+    cudaEventRecord(ds->ev[0], st);
+    cudaEventRecord(ds->ev[1], st);
+  }
+  g_timing = false;   // the inner attention calls must not move the events
+  size_t ob = 0;
+  for (size_t ch = 0; ch + 1 < cuts.size() && rc == IKBO_OK; ++ch) {
+    const int64_t c0 = cuts[ch], n = cuts[ch + 1] - c0, rows = chunk_rows[ch];
+    const Workspace L = plan_workspace(n, n, H, Lq, D, ds->num_sms);
+    const size_t o_kb = 0, o_vb = align_up(size_t(rows) * row_bytes, 256);
+    const size_t o_ws = align_up(o_vb + size_t(rows) * row_bytes, 256);
+    char* buf = nullptr;
+    if (cudaMallocAsync(reinterpret_cast<void**>(&buf), o_ws + L.total, st) != cudaSuccess) {
+      rc = IKBO_ERR_CUDA;
+      break;
+    }
+    const int grid = int(n < 4 * ds->num_sms ? n : 4 * ds->num_sms);
+    ikbo_broadcast_copy_kernel<<<grid, 256, 0, st>>>(
+        static_cast<const uint4*>(k_user), static_cast<const uint4*>(v_user),
+        reinterpret_cast<uint4*>(buf + o_kb), reinterpret_cast<uint4*>(buf + o_vb),
+        reinterpret_cast<const int32_t*>(meta + m_src) + c0,
+        reinterpret_cast<const int64_t*>(meta + m_dst) + ob, int32_t(n), int32_t(row_bytes / 16));
+    if (cudaGetLastError() != cudaSuccess) rc = IKBO_ERR_CUDA;
+    if (rc == IKBO_OK)
+      rc = run_ikbo(ds, static_cast<const char*>(q) + size_t(c0) * qrow, buf + o_kb, buf + o_vb,
+                    reinterpret_cast<int32_t*>(meta + m_offb) + ob,
+                    reinterpret_cast<int32_t*>(meta + m_id) + c0, n, n, H, Lq, D, scale,
+                    static_cast<char*>(out) + size_t(c0) * qrow, buf + o_ws, L, st);
+    cudaFreeAsync(buf, st);
+    ob += size_t(n) + 1;
+  }
+  g_timing = timed;
+  if (timed) {
+    cudaEventRecord(ds->ev[2], st);
+    int dev = 0;
+    cudaGetDevice(&dev);
+    g_timing_dev = dev;
+  }
+  cudaFreeAsync(meta, st);
+  return rc;
+}
+
+int ikbo_get_device_error(ikbo_stream_t stream) {
+  DeviceState* ds = nullptr;
+  int rc = device_state(&ds);
+  if (rc != IKBO_OK) return rc;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return IKBO_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_ikbo_error_word, sizeof word) != cudaSuccess)
+    return IKBO_ERR_CUDA;
+  const int zero = 0;
+  if (word && cudaMemcpyToSymbol(g_ikbo_error_word, &zero, sizeof zero) != cudaSuccess)
+    return IKBO_ERR_CUDA;
+  if (word & kErrIndex) return IKBO_ERR_INDEX;
+  if (word & kErrOffsets) return IKBO_ERR_OFFSETS;
+  if (word & kErrTimeout) return IKBO_ERR_TIMEOUT;
+  return IKBO_OK;
+}
+
+const char* ikbo_strerror(int status) {
+  switch (status) {
+    case IKBO_OK: return "ok";
+    case IKBO_ERR_NULL: return "a required pointer is NULL";
+    case IKBO_ERR_SHAPE: return "unsupported shape (D must be 64 or 128, 1 <= Lq <= 128, H >= 1)";
+    case IKBO_ERR_ALIGN: return "a tensor pointer is not 16-byte aligned";
+    case IKBO_ERR_SCALE: return "scale is not finite";
+    case IKBO_ERR_CUDA: return "a CUDA call failed";
+    case IKBO_ERR_INDEX: return "cand_to_user has a value outside [0, n_user)";
+    case IKBO_ERR_OFFSETS: return "user_offsets is not a jagged index (offsets[0] != 0 or decreasing)";
+    case IKBO_ERR_TIMEOUT: return "a bounded wait on the GPU ran out";
+    case IKBO_ERR_ALIAS: return "out overlaps an input";
+    case IKBO_ERR_DEVICE: return "the current device is not a compute capability 10.3 GPU";
+    case IKBO_ERR_BUDGET: return "memory budget too small for one candidate's K/V copy";
+    default: return "unknown status";
+  }
+}
+
+int ikbo_version(void) { return kVersion; }
+
+int ikbo_set_timing(int enable) {
+  g_timing = enable != 0;
+  return IKBO_OK;
+}
+
+int ikbo_get_timing(float* plan_ms, float* attn_ms) {
+  if (g_timing_dev < 0) return IKBO_ERR_CUDA;
+  DeviceState& s = g_dev[g_timing_dev];
+  if (!s.ev_ready) return IKBO_ERR_CUDA;
+  if (cudaEventSynchronize(s.ev[2]) != cudaSuccess) return IKBO_ERR_CUDA;
+  float a = 0.f, b = 0.f;
+  if (cudaEventElapsedTime(&a, s.ev[0], s.ev[1]) != cudaSuccess ||
+      cudaEventElapsedTime(&b, s.ev[1], s.ev[2]) != cudaSuccess)
+    return IKBO_ERR_CUDA;
+  if (plan_ms) *plan_ms = a;
+  if (attn_ms) *attn_ms = b;
+  return IKBO_OK;
+}
+
+int ikbo_set_debug(int flags, uint64_t timeout_ns) {
+  g_debug_flags = flags;
+  g_timeout_ns = timeout_ns ? timeout_ns : kDefaultTimeoutNs;
+  return IKBO_OK;
+}
+
+int ikbo_set_kernel(int which) {
+  const int prev = t_kernel;
+  t_kernel = which == 1 ? 1 : 0;
+  return prev;
+}
+
+}  // extern "C"

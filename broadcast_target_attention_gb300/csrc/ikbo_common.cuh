@@ -1,0 +1,115 @@
+// Shared definitions of the IKBO target-attention kernels (sm_103a).
+#pragma once
+
+#include <cstdint>
+
+namespace ikbo {
+
+// Rows of one query tile: the M extent of the tcgen05 MMA.  A tile holds the
+// query tokens of up to floor(128 / Lq) candidates of ONE user, so that all
+// of them share every K/V tile the CTA streams ("In-Kernel Broadcast
+// Optimization", §3.2: one CTA issues several candidates of the same user
+// to fill the MMA M extent).
+constexpr int kTileM = 128;
+
+// Bits of the per-device error word.
+constexpr int kErrIndex = 1;    // cand_to_user value outside [0, n_user)
+constexpr int kErrOffsets = 2;  // user_offsets[0] != 0, or decreasing
+constexpr int kErrTimeout = 4;  // a bounded wait ran out
+
+// One unit of work of the attention kernel: a query tile of one user and one
+// head, against one contiguous range of that user's keys.
+struct WorkItem {
+  int32_t user;        // user index
+  int32_t head;        // head index
+  int32_t cand_begin;  // first position in the grouped candidate order
+  int32_t n_cand;      // candidates in this tile (<= cands per tile)
+  int32_t kv_begin;    // first key row in k/v (absolute, = user_offsets[u] + split start)
+  int32_t kv_len;      // keys in this item (> 0)
+  int32_t unit;        // split-combine unit, or -1 when the item covers all keys
+  int32_t unit_first;  // first item index of the unit (its n_split items are consecutive)
+};
+static_assert(sizeof(WorkItem) == 32, "WorkItem layout");
+
+struct PlanHeader {
+  int32_t n_items;       // work items written
+  int32_t sorted;        // 1: cand_to_user non-decreasing, grouped order == candidate order
+  int32_t total_keys;    // T = user_offsets[n_user]
+  int32_t split_tiles;   // key tiles per split item (0 = no splitting)
+  int32_t work_counter;  // dynamic scheduler: next item to take
+  int32_t n_units;       // split-combine units
+  int32_t error;         // error bits found by the planner (0 = ok)
+  int32_t pad;
+};
+
+// Per-unit record of a split (user, head, query tile): how many items, and
+// the arrival counter the last-arriving CTA detects itself with.
+struct UnitInfo {
+  int32_t n_split;
+  int32_t arrived;
+};
+
+// Planner parameters (host -> planning kernel).
+struct PlanParams {
+  const int32_t* cand_to_user;
+  const int32_t* user_offsets;
+  int64_t n_cand;
+  int64_t n_user;
+  int32_t H;
+  int32_t cands_per_tile;   // floor(128 / Lq), rounded down to the Q-box granularity
+  int32_t block_n;          // keys per K/V tile
+  int32_t num_sms;          // SMs of the device
+  int32_t max_items;        // capacity of the work list
+  int32_t max_split_items;  // capacity of the split partial buffers
+  int32_t max_units;        // capacity of UnitInfo
+  // outputs (workspace)
+  PlanHeader* header;
+  WorkItem* items;
+  UnitInfo* units;
+  int32_t* perm;            // [n_cand] grouped order -> candidate (only when unsorted)
+  int32_t* cand_start;      // [n_user + 1] first grouped position of each user
+  int32_t* scratch;         // [3 * n_user + 2] per-user counters, order and prefixes
+  int* err_word;            // per-device error word
+};
+
+// Parameters shared by the attention kernels (host -> device).
+struct AttnParams {
+  const uint16_t* q;        // bf16 [n_cand, H, Lq, D]
+  const uint16_t* k;        // bf16 [T, H, D]
+  const uint16_t* v;        // bf16 [T, H, D]
+  uint16_t* out;            // bf16 [n_cand, H, Lq, D]
+  int64_t n_cand;
+  int32_t H;
+  int32_t Lq;
+  float scale_log2;         // scale * log2(e): scores are kept in base 2
+  int32_t max_items;        // grid-stride bound (items beyond header->n_items are skipped)
+  const PlanHeader* header;
+  const WorkItem* items;
+  UnitInfo* units;
+  const int32_t* perm;      // grouped position -> candidate, used when header->sorted == 0
+  float* partial_o;         // [max_split_items, 128, D] unnormalised O of split items
+  float2* partial_ml;       // [max_split_items, 128] (running max m in base 2, row sum l)
+  int* err_word;
+  const void* kmap;         // K/V tensor maps (device copies patched by the planner)
+  const void* vmap;
+  uint64_t timeout_ns;      // bound of every wait on another warp or the TMA/MMA units
+  int32_t qbox;             // candidates per Q box of the sorted-order tensor map
+  int32_t debug_flags;      // test hook: 1 = never arm the Q barrier (exercises the timeout path)
+};
+
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
+  // round to nearest even; inputs here are finite
+  uint32_t u = __float_as_uint(f);
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+}  // namespace ikbo

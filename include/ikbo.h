@@ -1,0 +1,172 @@
+/*
+ * ikbo.h -- C ABI of the GB300 (sm_103a) IKBO target-attention library.
+ *
+ * IKBO ("In-Kernel Broadcast Optimization: Co-Designing Kernels for RecSys
+ * Inference", §1.1-§1.3 and §3.1 with Fig. 10): a request carries a few users
+ * and many candidates.  Each candidate's query tokens attend to its own
+ * user's history sequence (target attention, full/non-causal, §3), chosen
+ * through a candidate-to-user map handed over by the inference runtime
+ * (§1.3 item 3).  The kernels index the user's K/V through that map; no
+ * per-candidate copy of a user tensor is ever materialised.
+ *
+ * Result, for every candidate c, head h and query token t
+ * (u = cand_to_user[c], L_u = user_offsets[u+1] - user_offsets[u]):
+ *
+ *   s_j = scale * <q[c,h,t,:], k[user_offsets[u] + j, h, :]>      j < L_u
+ *   out[c,h,t,:] = sum_j softmax(s)_j * v[user_offsets[u] + j, h, :]
+ *
+ * and an all-zero row when L_u == 0.
+ *
+ * Layouts (row-major, contiguous, bf16 = IEEE bfloat16):
+ *   q, out        bf16 [n_cand, H, Lq, D]
+ *   k_user, v_user bf16 [T, H, D], the users' sequences packed back to back
+ *                 with no padding ("Optimizing Jagged Flash Attention with
+ *                 TLX", introduction: jagged tensors plus an offsets tensor),
+ *                 T = user_offsets[n_user]
+ *   user_offsets  int32 [n_user + 1], user_offsets[0] = 0, non-decreasing
+ *   cand_to_user  int32 [n_cand], values in [0, n_user); any order (sorted
+ *                 input skips the internal grouping pass)
+ *
+ * Ownership: every pointer argument is owned by the caller and never freed
+ * by the library.  Device-pointer entry points are asynchronous on `stream`
+ * (a cudaStream_t; NULL = legacy default stream) and never synchronise the
+ * host unless stated.  The library owns its scratch space (schedule, split
+ * partials, tensor maps) and takes it from the device's stream-ordered
+ * memory pool on `stream`, releasing it on the same stream.
+ *
+ * Errors: a negative status is returned at once, with nothing enqueued, for
+ * anything the host can see (IKBO_ERR_NULL, _SHAPE, _ALIGN, _SCALE, _ALIAS,
+ * _DEVICE).  Bad contents of the index tensors (a candidate mapped outside
+ * [0, n_user), offsets that are not a jagged index) and bounded waits that
+ * ran out can only be seen on the GPU: the kernels then skip all work (out
+ * is left unchanged), never trap, and record the error in a per-device error
+ * word that ikbo_get_device_error() returns.  k/v must be finite: a key tile
+ * can read rows of the neighbouring user, which are masked out with weight
+ * zero, and 0 * inf is NaN.
+ */
+#ifndef IKBO_H
+#define IKBO_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t. */
+typedef struct CUstream_st* ikbo_stream_t;
+
+enum ikbo_status {
+  IKBO_OK = 0,
+  IKBO_ERR_NULL = -1,    /* a required pointer is NULL */
+  IKBO_ERR_SHAPE = -2,   /* D not 64/128, H < 1, Lq not in [1,128], n_cand < 0, n_user < 0 ... */
+  IKBO_ERR_ALIGN = -3,   /* a tensor pointer is not 16-byte aligned */
+  IKBO_ERR_SCALE = -4,   /* scale is not finite */
+  IKBO_ERR_CUDA = -5,    /* a CUDA runtime/driver call failed (launch, pool allocation) */
+  IKBO_ERR_INDEX = -6,   /* device: cand_to_user value outside [0, n_user) */
+  IKBO_ERR_OFFSETS = -7, /* device: user_offsets[0] != 0 or decreasing */
+  IKBO_ERR_TIMEOUT = -8, /* device: a bounded wait ran out */
+  IKBO_ERR_ALIAS = -9,   /* out overlaps an input */
+  IKBO_ERR_DEVICE = -10, /* current device is not a compute capability 10.3 GPU */
+  IKBO_ERR_BUDGET = -11  /* broadcast path: mem_budget_bytes too small for one candidate */
+};
+
+/*
+ * IKBO target attention, forward (the hot path).
+ * "In-Kernel Broadcast Optimization: Co-Designing Kernels for RecSys
+ * Inference", §3.1 (Fig. 10, right): candidates index their user's K/V at
+ * run time instead of receiving a broadcast copy.
+ *
+ * Enqueues on `stream`: (1) a planning kernel that validates the index
+ * tensors, groups candidates by user and writes the work list; (2) the
+ * persistent tcgen05 attention kernel, which packs a user's candidates into
+ * 128-row query tiles, streams that user's K/V tiles through shared memory
+ * once per tile and, where a user-head is split across CTAs, merges the
+ * partial results in the CTA that finishes last.
+ * All pointers are device pointers; q, k_user, v_user and out must be 16-byte
+ * aligned; out must not overlap q, k_user or v_user.  n_cand == 0 is a no-op.
+ */
+int ikbo_attn_fwd(const void* q, const void* k_user, const void* v_user,
+                  const int32_t* user_offsets, const int32_t* cand_to_user,
+                  int64_t n_cand, int64_t n_user, int32_t H, int32_t Lq, int32_t D,
+                  float scale, void* out, ikbo_stream_t stream);
+
+/*
+ * The explicit-broadcast comparison path the IKBO pages argue against
+ * ("In-Kernel Broadcast Optimization", §1.4 item 1 and §3.1, Fig. 10 left):
+ * K and V are first copied once per candidate into a [S_chunk, H, D] buffer
+ * (S_chunk = sum of L_{u(c)} over a chunk of candidates), then the same
+ * attention kernel runs with every candidate as its own "user".
+ * Candidates are processed in chunks whose copies fit in mem_budget_bytes.
+ * Same arguments and layouts as ikbo_attn_fwd.  This path reads
+ * user_offsets and cand_to_user back to the host to size its chunks, so it
+ * synchronises `stream` once per call.  Returns IKBO_ERR_BUDGET if one
+ * candidate's copy does not fit the budget.
+ */
+int ikbo_broadcast_attn_fwd(const void* q, const void* k_user, const void* v_user,
+                            const int32_t* user_offsets, const int32_t* cand_to_user,
+                            int64_t n_cand, int64_t n_user, int32_t H, int32_t Lq, int32_t D,
+                            float scale, void* out, size_t mem_budget_bytes,
+                            ikbo_stream_t stream);
+
+/*
+ * ikbo_attn_fwd on HOST buffers (pinned memory recommended).  Copies the
+ * inputs to device memory taken from the stream-ordered pool, runs the same
+ * two kernels, copies out back and synchronises `stream` before returning.
+ * The result is in `out` when the call returns IKBO_OK; device-side index
+ * errors are returned directly (no separate ikbo_get_device_error needed).
+ * user_offsets is read on the host (T = user_offsets[n_user]).
+ */
+int ikbo_attn_fwd_host(const void* q, const void* k_user, const void* v_user,
+                       const int32_t* user_offsets, const int32_t* cand_to_user,
+                       int64_t n_cand, int64_t n_user, int32_t H, int32_t Lq, int32_t D,
+                       float scale, void* out, ikbo_stream_t stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the current device's error
+ * word: IKBO_OK, or IKBO_ERR_INDEX / _OFFSETS / _TIMEOUT for the first kind
+ * of error recorded since the last call.  The word is shared by all streams
+ * of the device.
+ */
+int ikbo_get_device_error(ikbo_stream_t stream);
+
+/* Static description of a status code. */
+const char* ikbo_strerror(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int ikbo_version(void);
+
+/*
+ * Kernel timing, for measurement.  When enabled, every ikbo_attn_fwd call
+ * records CUDA events on its stream around its planning kernel and its
+ * attention kernel; ikbo_get_timing() synchronises on the last call's events
+ * and returns both durations in milliseconds.  After ikbo_broadcast_attn_fwd,
+ * attn_ms is the whole GPU part of that path (copies, planning and attention
+ * of every chunk) and plan_ms is 0.  Off by default.
+ */
+int ikbo_set_timing(int enable);
+int ikbo_get_timing(float* plan_ms, float* attn_ms);
+
+/*
+ * Test hook.  flags = 1 makes the TMA producer of the attention kernel skip
+ * arming the query-tile barrier, so the MMA and softmax warps wait until the
+ * bound runs out: the kernel then records IKBO_ERR_TIMEOUT, skips all work
+ * and exits normally (nothing traps, the context stays usable).
+ * timeout_ns bounds every in-kernel wait (0 = the default of 2 s).
+ * flags = 0 restores normal operation.
+ */
+int ikbo_set_debug(int flags, uint64_t timeout_ns);
+
+/*
+ * Selects the attention kernel for later calls on this thread: 0 = the
+ * tcgen05/TMEM/TMA kernel (default), 1 = the SIMT kernel kept as an
+ * independent GPU cross-check.  Returns the previous value.
+ */
+int ikbo_set_kernel(int which);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* IKBO_H */

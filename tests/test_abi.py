@@ -1,0 +1,87 @@
+"""The C ABI without a GPU: the library loads, exports what include/ikbo.h
+declares, and rejects bad host-visible arguments before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import broadcast_target_attention_gb300 as ikbo
+from broadcast_target_attention_gb300 import _lib
+from broadcast_target_attention_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return _lib.lib()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "ikbo.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ikbo_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("ikbo_attn_fwd", "ikbo_broadcast_attn_fwd", "ikbo_attn_fwd_host",
+                     "ikbo_get_device_error", "ikbo_strerror", "ikbo_version"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in _lib.SIGNATURES, f"{name} has no ctypes signature"
+
+
+def test_version_and_strerror(lib):
+    assert lib.ikbo_version() >= 10000
+    for code in _lib.STATUS:
+        assert lib.ikbo_strerror(code)
+    assert lib.ikbo_strerror(12345) == b"unknown status"
+
+
+A = 1 << 20   # a fake, 16-byte aligned "device" address; never dereferenced
+
+
+def call(lib, q=A, k=2 * A, v=3 * A, off=4 * A, c2u=5 * A, n_cand=8, n_user=2, H=2, Lq=1, D=64,
+         scale=0.125, out=6 * A):
+    return lib.ikbo_attn_fwd(q, k, v, off, c2u, n_cand, n_user, H, Lq, D, scale, out, None)
+
+
+def test_host_detectable_errors_return_before_any_cuda_call(lib):
+    assert call(lib, D=96) == _lib.IKBO_ERR_SHAPE
+    assert call(lib, Lq=0) == _lib.IKBO_ERR_SHAPE
+    assert call(lib, Lq=129) == _lib.IKBO_ERR_SHAPE
+    assert call(lib, H=0) == _lib.IKBO_ERR_SHAPE
+    assert call(lib, n_cand=-1) == _lib.IKBO_ERR_SHAPE
+    assert call(lib, n_user=-1) == _lib.IKBO_ERR_SHAPE
+    assert call(lib, scale=float("inf")) == _lib.IKBO_ERR_SCALE
+    assert call(lib, scale=float("nan")) == _lib.IKBO_ERR_SCALE
+    assert call(lib, q=None) == _lib.IKBO_ERR_NULL
+    assert call(lib, out=None) == _lib.IKBO_ERR_NULL
+    assert call(lib, c2u=None) == _lib.IKBO_ERR_NULL
+    assert call(lib, k=2 * A + 8) == _lib.IKBO_ERR_ALIGN
+    assert call(lib, off=4 * A + 2) == _lib.IKBO_ERR_ALIGN
+    assert call(lib, out=A + 64) == _lib.IKBO_ERR_ALIAS      # overlaps q
+    assert call(lib, n_user=0) == _lib.IKBO_ERR_INDEX         # nothing to map candidates to
+    assert call(lib, n_cand=0, q=None, out=None) == _lib.IKBO_OK   # empty batch: no-op
+
+
+def test_broadcast_and_host_paths_check_arguments_too(lib):
+    rc = lib.ikbo_broadcast_attn_fwd(A, 2 * A, 3 * A, 4 * A, 5 * A, 8, 2, 2, 1, 80, 0.1, 6 * A,
+                                     1 << 30, None)
+    assert rc == _lib.IKBO_ERR_SHAPE
+    rc = lib.ikbo_attn_fwd_host(A, 2 * A, 3 * A, 4 * A, 5 * A, 8, 2, 2, 1, 64, float("inf"), 6 * A,
+                                None)
+    assert rc == _lib.IKBO_ERR_SCALE
+
+
+def test_python_binding_raises_on_bad_status(lib):
+    with pytest.raises(ikbo.IkboError) as e:
+        ikbo._check(_lib.IKBO_ERR_SHAPE, "x")
+    assert "IKBO_ERR_SHAPE" in str(e.value)

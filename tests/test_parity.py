@@ -1,0 +1,144 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle.
+
+Every configuration of the workload table, plus edge cases: ragged tails,
+odd and single-candidate groups, empty sequences, users without candidates,
+an unsorted candidate map, Lq from 1 to 128, D = 64 and 128, split-KV units.
+Tolerance: max-abs 2e-2 and mean-abs 2e-3 for bf16 inputs with fp32
+accumulation.  Both GPU kernels are checked: the tcgen05 kernel (0, the
+default) and the SIMT kernel (1).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from broadcast_target_attention_gb300 import workloads as W
+from _helpers import assert_close, out_f64, to_device
+
+pytestmark = pytest.mark.gpu
+
+KERNELS = [0, 1]
+# (config, number of candidates checked against the oracle; None = all)
+CONFIG_SAMPLES = [
+    ("tiny_8x2", None),
+    ("ratio_1024x15", None),
+    ("odd_groups_2048x16", 160),
+    ("extreme_4096x4", 96),
+    ("sweep_16384x64_d64_lq1", 160),
+    ("sweep_16384x64_d64_lq4", 96),
+    ("sweep_16384x64_d128_lq1", 160),
+    ("sweep_16384x64_d128_lq4", 96),
+]
+
+_cache = {}
+
+
+def workload(name):
+    if name not in _cache:
+        wl = W.generate(W.CONFIGS[name])
+        _cache.clear()
+        _cache[name] = wl
+    return _cache[name]
+
+
+def run(ikbo, wl, kernel, **kw):
+    prev = ikbo.set_kernel(kernel)
+    try:
+        d = to_device(wl)
+        out = ikbo.attn_fwd(d["q"], d["k"], d["v"], d["user_offsets"], d["cand_to_user"], wl.scale, **kw)
+        rc = ikbo.get_device_error()
+    finally:
+        ikbo.set_kernel(prev)
+    assert rc == 0, f"device error {rc}"
+    return out
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("name,n_sample", CONFIG_SAMPLES)
+def test_config_matches_oracle(gpu_lib, name, n_sample, kernel):
+    wl = workload(name)
+    cands = None if n_sample is None else W.sample_candidates(wl, n_sample)
+    out = run(gpu_lib, wl, kernel)
+    ref = oracle.attention_wl(wl, cands)
+    assert_close(out_f64(out, cands), ref, f"{name} kernel={kernel}")
+    # properties that hold for every row, checked at full size
+    assert torch.isfinite(out.float()).all()
+
+
+EDGE = {
+    # ragged tails around the 128-key tile, a length-1 user, an empty user,
+    # a user without candidates, odd groups
+    "ragged": dict(n_user=7, counts=[3, 1, 0, 5, 2, 1, 4], lens=[129, 1, 300, 0, 127, 128, 257]),
+    # one user, one candidate, long sequence: split across CTAs
+    "single_long": dict(n_user=1, counts=[1], lens=[5000]),
+    # few units, long sequences: the split-KV merge path
+    "split": dict(n_user=2, counts=[3, 2], lens=[3001, 1800]),
+    # many users with one candidate each (many small units)
+    "many_users": dict(n_user=300, counts=[1] * 300, lens=list(range(1, 301))),
+    # more candidates than one query tile holds
+    "multi_tile": dict(n_user=2, counts=[300, 7], lens=[200, 64]),
+}
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("Lq", [1, 3, 8])
+@pytest.mark.parametrize("case", sorted(EDGE))
+def test_edge_cases(gpu_lib, case, Lq, D, kernel):
+    spec = EDGE[case]
+    wl = W.custom(H=2, D=D, Lq=Lq, seed=100 + Lq, **spec)
+    out = run(gpu_lib, wl, kernel)
+    assert_close(out_f64(out), oracle.attention_wl(wl), f"{case} Lq={Lq} D={D} kernel={kernel}")
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("Lq", [5, 64, 128])
+def test_large_query_groups(gpu_lib, Lq, kernel):
+    wl = W.custom(n_user=3, counts=[5, 2, 9], lens=[140, 70, 390], H=3, D=128, Lq=Lq, seed=7)
+    out = run(gpu_lib, wl, kernel)
+    assert_close(out_f64(out), oracle.attention_wl(wl), f"Lq={Lq} kernel={kernel}")
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("D", [64, 128])
+def test_unsorted_mapping(gpu_lib, D, kernel):
+    wl = W.custom(n_user=5, counts=[40, 3, 1, 90, 17], lens=[333, 20, 1, 700, 129], H=4, D=D, Lq=2,
+                  seed=9, shuffle=True)
+    assert np.any(np.diff(wl.cand_to_user) < 0)
+    out = run(gpu_lib, wl, kernel)
+    assert_close(out_f64(out), oracle.attention_wl(wl), f"unsorted D={D} kernel={kernel}")
+
+
+def test_kernels_agree_at_full_size(gpu_lib):
+    wl = workload("odd_groups_2048x16")
+    a = run(gpu_lib, wl, 0).float()
+    b = run(gpu_lib, wl, 1).float()
+    assert (a - b).abs().max().item() <= 2e-2
+
+
+def test_identical_queries_give_identical_rows(gpu_lib):
+    """A property at any size: candidates of one user with the same queries get the same rows."""
+    wl = workload("ratio_1024x15")
+    q = wl.q.copy()
+    first = np.nonzero(wl.cand_to_user == 3)[0]
+    q[first[1:]] = q[first[0]]
+    wl2 = W.Workload(cfg=wl.cfg, q=q, k=wl.k, v=wl.v, user_offsets=wl.user_offsets,
+                     cand_to_user=wl.cand_to_user, scale=wl.scale)
+    out = run(gpu_lib, wl2, 0)
+    rows = out[torch.as_tensor(first, device=out.device)]
+    assert torch.equal(rows, rows[:1].expand_as(rows))
+
+
+def test_empty_batch_is_a_noop(gpu_lib):
+    wl = W.custom(n_user=2, counts=[1, 1], lens=[3, 3], H=1, D=64, Lq=1)
+    d = to_device(wl)
+    q = d["q"][:0]
+    out = gpu_lib.attn_fwd(q, d["k"], d["v"], d["user_offsets"], d["cand_to_user"][:0], 0.1)
+    assert out.shape[0] == 0
+
+
+def test_repeated_calls_are_deterministic(gpu_lib):
+    wl = workload("ratio_1024x15")
+    a = run(gpu_lib, wl, 0)
+    b = run(gpu_lib, wl, 0)
+    assert torch.equal(a, b)
