@@ -17,7 +17,7 @@ from typing import Optional, Tuple
 from . import _lib
 from ._lib import STATUS
 
-__all__ = ["attn_fwd", "broadcast_attn_fwd", "attn_fwd_host", "get_device_error", "set_timing",
+__all__ = ["attn_fwd", "broadcast_attn_fwd", "attn_fwd_host", "attn_fwd_noalloc", "get_device_error", "set_timing",
            "get_timing", "set_kernel", "set_debug", "version", "load", "IkboError", "STATUS"]
 
 
@@ -133,6 +133,27 @@ def attn_fwd_host(q, k, v, user_offsets, cand_to_user, scale: Optional[float] = 
                                        _ptr(cand_to_user), n_cand, n_user, H, Lq, D, float(scale),
                                        _ptr(out), _stream_handle(stream))
     _check(rc, "ikbo_attn_fwd_host")
+    return out
+
+
+def attn_fwd_noalloc(q, k, v, user_offsets, cand_to_user, scale: Optional[float] = None, out=None,
+                     stream=None):
+    """attn_fwd whose scratch comes from the library's fixed device array, not
+    from an allocation (for callers whose memory manager forbids the library
+    to allocate); see ikbo_attn_fwd_noalloc in include/ikbo.h.  ``out`` must
+    be passed in by such callers to avoid the allocation of a new tensor."""
+    import torch
+    _validate(q, k, v, user_offsets, cand_to_user, device=True)
+    n_cand, H, Lq, D = _shape(q, k)
+    n_user = int(user_offsets.shape[0]) - 1
+    if scale is None:
+        scale = D ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    rc = _lib.lib().ikbo_attn_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(user_offsets),
+                                          _ptr(cand_to_user), n_cand, n_user, H, Lq, D,
+                                          float(scale), _ptr(out), _stream_handle(stream))
+    _check(rc, "ikbo_attn_fwd_noalloc")
     return out
 
 

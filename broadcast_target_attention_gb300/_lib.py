@@ -14,6 +14,7 @@ STATUS = {
     0: "IKBO_OK", -1: "IKBO_ERR_NULL", -2: "IKBO_ERR_SHAPE", -3: "IKBO_ERR_ALIGN",
     -4: "IKBO_ERR_SCALE", -5: "IKBO_ERR_CUDA", -6: "IKBO_ERR_INDEX", -7: "IKBO_ERR_OFFSETS",
     -8: "IKBO_ERR_TIMEOUT", -9: "IKBO_ERR_ALIAS", -10: "IKBO_ERR_DEVICE", -11: "IKBO_ERR_BUDGET",
+    -12: "IKBO_ERR_SCRATCH",
 }
 globals().update({name: code for code, name in STATUS.items()})
 
@@ -34,6 +35,8 @@ SIGNATURES = {
     "ikbo_get_timing": (ctypes.c_int, [ctypes.POINTER(_F), ctypes.POINTER(_F)]),
     "ikbo_set_debug": (ctypes.c_int, [ctypes.c_int, ctypes.c_uint64]),
     "ikbo_set_kernel": (ctypes.c_int, [ctypes.c_int]),
+    "ikbo_attn_fwd_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I32, _I32, _I32, _F,
+                                              _P, _P]),
 }
 
 

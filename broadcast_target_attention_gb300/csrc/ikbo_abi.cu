@@ -563,6 +563,8 @@ const char* ikbo_strerror(int status) {
     case IKBO_ERR_ALIAS: return "out overlaps an input";
     case IKBO_ERR_DEVICE: return "the current device is not a compute capability 10.3 GPU";
     case IKBO_ERR_BUDGET: return "memory budget too small for one candidate's K/V copy";
+    case IKBO_ERR_SCRATCH:
+      return "the call needs more scratch than ikbo_attn_fwd_noalloc's fixed 40 MiB array";
     default: return "unknown status";
   }
 }
@@ -601,3 +603,59 @@ int ikbo_set_kernel(int which) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of ikbo_attn_fwd.
+//
+// For callers that must not see the library allocate device memory (a memory
+// manager that owns the whole device, or no stream-ordered pools), the
+// scratch of the planning and attention kernels lives in this fixed array
+// instead of the pool.  Host code only ever passes its device address, which
+// is looked up once per device; the array's host-side name is a stand-in, not
+// a device pointer.  Concurrent calls on the same device share it and race.
+namespace ikbo {
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[IKBO_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mutex;
+char* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (looked up on the
+// first call there, with that device current).
+int noalloc_scratch(char** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return IKBO_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return IKBO_ERR_DEVICE;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return IKBO_ERR_CUDA;
+    g_noalloc_ptr[dev] = static_cast<char*>(ptr);
+  }
+  *out = g_noalloc_ptr[dev];
+  return IKBO_OK;
+}
+
+}  // namespace
+}  // namespace ikbo
+
+extern "C" int ikbo_attn_fwd_noalloc(const void* q, const void* k_user, const void* v_user,
+                                     const int32_t* user_offsets, const int32_t* cand_to_user,
+                                     int64_t n_cand, int64_t n_user, int32_t H, int32_t Lq,
+                                     int32_t D, float scale, void* out, ikbo_stream_t stream) {
+  using namespace ikbo;
+  int rc = check_args(q, k_user, v_user, user_offsets, cand_to_user, n_cand, n_user, H, Lq, D,
+                      scale, out);
+  if (rc != IKBO_OK || n_cand == 0) return rc;
+  DeviceState* ds = nullptr;
+  if ((rc = device_state(&ds)) != IKBO_OK) return rc;
+  if (g_timing && (rc = ensure_events(ds)) != IKBO_OK) return rc;
+  const Workspace L = plan_workspace(n_cand, n_user, H, Lq, D, ds->num_sms);
+  if (L.total > size_t(IKBO_NOALLOC_SCRATCH_BYTES)) return IKBO_ERR_SCRATCH;
+  char* ws = nullptr;
+  if ((rc = noalloc_scratch(&ws)) != IKBO_OK) return rc;
+  return run_ikbo(ds, q, k_user, v_user, user_offsets, cand_to_user, n_cand, n_user, H, Lq, D,
+                  scale, out, ws, L, reinterpret_cast<cudaStream_t>(stream));
+}
+

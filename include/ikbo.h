@@ -69,7 +69,8 @@ enum ikbo_status {
   IKBO_ERR_TIMEOUT = -8, /* device: a bounded wait ran out */
   IKBO_ERR_ALIAS = -9,   /* out overlaps an input */
   IKBO_ERR_DEVICE = -10, /* current device is not a compute capability 10.3 GPU */
-  IKBO_ERR_BUDGET = -11  /* broadcast path: mem_budget_bytes too small for one candidate */
+  IKBO_ERR_BUDGET = -11, /* broadcast path: mem_budget_bytes too small for one candidate */
+  IKBO_ERR_SCRATCH = -12 /* ikbo_attn_fwd_noalloc: the call needs more than its fixed scratch */
 };
 
 /*
@@ -164,6 +165,40 @@ int ikbo_set_debug(int flags, uint64_t timeout_ns);
  * independent GPU cross-check.  Returns the previous value.
  */
 int ikbo_set_kernel(int which);
+
+/*
+ * ikbo_attn_fwd without any memory allocation.  (The IKBO pages have no
+ * counterpart to this entry point; it exists for deployment.)
+ *
+ * Some callers cannot let a library allocate GPU memory: a serving process
+ * whose memory manager reserves the device memory up front and forbids any
+ * later driver allocation, or a platform where stream-ordered memory pools
+ * are unavailable.  ikbo_attn_fwd takes its scratch (work list, split
+ * partials, tensor maps) from the stream-ordered pool on every call; this
+ * variant takes it instead from one fixed array in device memory that is
+ * part of the library (IKBO_NOALLOC_SCRATCH_BYTES = 40 MiB, held on every
+ * GPU where the library is loaded until the process exits).  It never calls
+ * cudaMalloc, cudaMallocAsync, cudaFree or any other allocating routine.
+ *
+ * Arguments, layouts, results and errors are those of ikbo_attn_fwd.  In
+ * addition it returns IKBO_ERR_SCRATCH, with nothing enqueued, when the call
+ * would need more scratch than the array holds (the need grows with n_cand,
+ * n_user, H and D; every configuration in workloads.py needs under 30 MiB).
+ *
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  Every
+ * call on a device uses the same array, and the planning kernel
+ * re-initialises everything the attention kernel reads, so a call never
+ * depends on what an earlier call left there.  Two calls whose kernels
+ * overlap on the GPU (different streams, no ordering between them) race on
+ * the array and give wrong results: order them on one stream, or use
+ * ikbo_attn_fwd.
+ */
+#define IKBO_NOALLOC_SCRATCH_BYTES (40u * 1024u * 1024u)
+int ikbo_attn_fwd_noalloc(const void* q, const void* k_user, const void* v_user,
+                          const int32_t* user_offsets, const int32_t* cand_to_user,
+                          int64_t n_cand, int64_t n_user, int32_t H, int32_t Lq, int32_t D,
+                          float scale, void* out, ikbo_stream_t stream);
 
 #ifdef __cplusplus
 }
