@@ -184,5 +184,11 @@ def set_debug(flags: int = 0, timeout_ns: int = 0) -> None:
     _check(_lib.lib().ikbo_set_debug(int(flags), int(timeout_ns)))
 
 
+def set_trace(buffer) -> None:
+    """Trace the tcgen05 kernel into ``buffer`` (a CUDA uint64/int64 tensor of
+    at least SMs*4*16 entries), or stop tracing with None."""
+    _check(_lib.lib().ikbo_set_trace(None if buffer is None else buffer.data_ptr()))
+
+
 def version() -> int:
     return int(_lib.lib().ikbo_version())

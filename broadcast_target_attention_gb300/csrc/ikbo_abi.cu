@@ -30,6 +30,7 @@ constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;   // 2 s bound on any in-k
 struct DeviceState {
   bool ready = false;
   int num_sms = 0;
+  int tc_grid[2] = {0, 0};   // CTAs of the tcgen05 kernel (clusters of 2), D = 64 / 128
   int* err_word = nullptr;
   cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
   bool ev_ready = false;
@@ -40,6 +41,7 @@ DeviceState g_dev[kMaxDevices];
 bool g_timing = false;
 int g_timing_dev = -1;
 int g_debug_flags = 0;
+uint64_t* g_trace = nullptr;
 uint64_t g_timeout_ns = kDefaultTimeoutNs;
 thread_local int t_kernel = 0;
 
@@ -136,18 +138,27 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Layout of the per-call scratch space.
 struct Workspace {
-  size_t header, kmap, vmap, items, units, perm, cand_start, scratch, partial_o, partial_ml, total;
-  int max_items, max_split_items, max_units;
+  size_t header, kmap, vmap, items, units, perm, cand_start, scratch, partial_o, partial_ml,
+      cta_items, map_slots, total;
+  int max_items, max_split_items, max_units, max_cta_items, grid;
+  bool fused;
 };
 
-Workspace plan_workspace(int64_t n_cand, int64_t n_user, int H, int Lq, int D, int num_sms) {
-  Workspace w;
+// kernel: 0 = tcgen05 (plans in-kernel when the inputs fit its shared memory,
+// otherwise reads the planning kernel's list; never splits a unit through
+// global memory), 1 = SIMT (planning kernel, may split).
+Workspace plan_workspace(int64_t n_cand, int64_t n_user, int H, int Lq, int D, int num_sms,
+                         int grid, int kernel) {
+  Workspace w = {};
   const int cpt = cands_per_tile(Lq);
   const int64_t units_bound =
       int64_t(H) * ((n_cand + cpt - 1) / cpt + (n_user < n_cand ? n_user : n_cand));
+  w.grid = grid;
+  w.fused = kernel == 0 && n_cand <= kFusedMaxCand && n_user <= kFusedMaxUser;
   w.max_items = int(num_sms + units_bound);
-  w.max_split_items = 3 * num_sms;
+  w.max_split_items = kernel == 1 ? 3 * num_sms : 0;
   w.max_units = w.max_split_items;
+  w.max_cta_items = int((units_bound + grid - 1) / grid) + 1;
   size_t o = 0;
   auto take = [&](size_t bytes) {
     size_t at = o;
@@ -155,15 +166,22 @@ Workspace plan_workspace(int64_t n_cand, int64_t n_user, int H, int Lq, int D, i
     return at;
   };
   w.header = take(sizeof(PlanHeader));
-  w.kmap = take(sizeof(CUtensorMap));
-  w.vmap = take(sizeof(CUtensorMap));
-  w.items = take(sizeof(WorkItem) * size_t(w.max_items));
-  w.units = take(sizeof(UnitInfo) * size_t(w.max_units));
   w.perm = take(sizeof(int32_t) * size_t(n_cand));
-  w.cand_start = take(sizeof(int32_t) * size_t(n_user + 1));
-  w.scratch = take(sizeof(int32_t) * size_t(3 * n_user + 2));
-  w.partial_o = take(sizeof(float) * size_t(w.max_split_items) * kTileM * D);
-  w.partial_ml = take(sizeof(float2) * size_t(w.max_split_items) * kTileM);
+  if (w.fused) {
+    w.cta_items = take(sizeof(WorkItem) * size_t(grid) * size_t(w.max_cta_items));
+    w.map_slots = take(sizeof(CUtensorMap) * size_t(grid) * 2);
+  } else {
+    w.kmap = take(sizeof(CUtensorMap));
+    w.vmap = take(sizeof(CUtensorMap));
+    w.items = take(sizeof(WorkItem) * size_t(w.max_items));
+    w.units = take(sizeof(UnitInfo) * size_t(w.max_units > 0 ? w.max_units : 1));
+    w.cand_start = take(sizeof(int32_t) * size_t(n_user + 1));
+    w.scratch = take(sizeof(int32_t) * size_t(3 * n_user + 2));
+    if (w.max_split_items) {
+      w.partial_o = take(sizeof(float) * size_t(w.max_split_items) * kTileM * D);
+      w.partial_ml = take(sizeof(float2) * size_t(w.max_split_items) * kTileM);
+    }
+  }
   w.total = o;
   return w;
 }
@@ -197,29 +215,75 @@ int encode_q_map(CUtensorMap* m, const void* q, int64_t n_cand, int H, int Lq, i
 }
 
 template <typename Kern, typename... Args>
-cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                       Args... args) {
+cudaError_t launch_ex(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
+                      int cluster, Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  if (cluster > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = cluster;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+template <typename Kern, typename... Args>
+cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args... args) {
+  return launch_ex(kern, grid, block, smem, st, true, 1, args...);
+}
+
+// CTAs of the tcgen05 kernel: two per cluster, as many clusters as fit at once.
+template <int D>
+int tc_grid(DeviceState* ds) {
+  int& g = ds->tc_grid[D == 128 ? 1 : 0];
+  if (g) return g;
+  if (cudaFuncSetAttribute(ikbo_attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kTcSmemBytes) != cudaSuccess ||
+      cudaFuncSetAttribute(ikbo_attn_tc_kernel<D>, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                           0) != cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ds->num_sms & ~1);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = kTcSmemBytes;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, args...);
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, ikbo_attn_tc_kernel<D>, &cfg) != cudaSuccess ||
+      clusters <= 0) {
+    cudaGetLastError();
+    clusters = ds->num_sms / 2;
+  }
+  g = 2 * clusters;
+  return g;
 }
 
 template <int D>
 cudaError_t launch_attn_tc(const AttnParams& ap, const CUtensorMap& qmap, const CUtensorMap& qmap1,
-                           int grid, cudaStream_t st) {
-  constexpr int smem = TcConfig<D>::kSmemBytes;
-  cudaError_t e = cudaFuncSetAttribute(ikbo_attn_tc_kernel<D>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(ikbo_attn_tc_kernel<D>, dim3(grid), dim3(kTcThreads), smem, st, ap, qmap, qmap1);
+                           const CUtensorMap& kt, const CUtensorMap& vt, int grid, bool pdl,
+                           cudaStream_t st) {
+  return launch_ex(ikbo_attn_tc_kernel<D>, dim3(grid), dim3(kTcThreads), kTcSmemBytes, st, pdl, 2,
+                   ap, qmap, qmap1, kt, vt);
 }
 
 // Plan + attention on device buffers, scratch from `ws` (>= plan_workspace().total).
@@ -239,6 +303,7 @@ int run_ikbo(DeviceState* ds, const void* q, const void* k, const void* v, const
   pp.max_items = L.max_items;
   pp.max_split_items = L.max_split_items;
   pp.max_units = L.max_units;
+  pp.allow_split = kernel == 1 ? 1 : 0;
   pp.header = reinterpret_cast<PlanHeader*>(ws + L.header);
   pp.items = reinterpret_cast<WorkItem*>(ws + L.items);
   pp.units = reinterpret_cast<UnitInfo*>(ws + L.units);
@@ -280,19 +345,31 @@ int run_ikbo(DeviceState* ds, const void* q, const void* k, const void* v, const
   ap.items = pp.items;
   ap.units = pp.units;
   ap.perm = pp.perm;
-  ap.partial_o = reinterpret_cast<float*>(ws + L.partial_o);
-  ap.partial_ml = reinterpret_cast<float2*>(ws + L.partial_ml);
+  ap.partial_o = L.max_split_items ? reinterpret_cast<float*>(ws + L.partial_o) : nullptr;
+  ap.partial_ml = L.max_split_items ? reinterpret_cast<float2*>(ws + L.partial_ml) : nullptr;
   ap.err_word = ds->err_word;
   ap.kmap = px.kmap_dst;
   ap.vmap = px.vmap_dst;
   ap.timeout_ns = g_timeout_ns;
   ap.qbox = qbox_cands(Lq);
   ap.debug_flags = g_debug_flags;
+  ap.trace = g_trace;
+  ap.fused = L.fused ? 1 : 0;
+  ap.cands_per_tile = pp.cands_per_tile;
+  ap.user_offsets = off;
+  ap.cand_to_user = c2u;
+  ap.n_user = n_user;
+  ap.cta_items = reinterpret_cast<WorkItem*>(ws + L.cta_items);
+  ap.max_cta_items = L.max_cta_items;
+  ap.perm_ws = pp.perm;
+  ap.map_slots = reinterpret_cast<CUtensorMap*>(ws + L.map_slots);
 
   const bool timed = g_timing;
   if (timed) cudaEventRecord(ds->ev[0], st);
-  ikbo_plan_kernel<<<1, kPlanThreads, 0, st>>>(pp, px);
-  if (cudaGetLastError() != cudaSuccess) return IKBO_ERR_CUDA;
+  if (!L.fused) {
+    ikbo_plan_kernel<<<1, kPlanThreads, 0, st>>>(pp, px);
+    if (cudaGetLastError() != cudaSuccess) return IKBO_ERR_CUDA;
+  }
   if (timed) cudaEventRecord(ds->ev[1], st);
   cudaError_t e;
   if (kernel == 1) {
@@ -302,11 +379,11 @@ int run_ikbo(DeviceState* ds, const void* q, const void* k, const void* v, const
     else
       e = launch_pdl(ikbo_attn_simt_kernel<128>, dim3(grid), dim3(kSimtThreads), 0, st, ap);
   } else {
-    const int grid = L.max_items < ds->num_sms ? L.max_items : ds->num_sms;
+    // the planning kernel (listed mode) is followed with programmatic dependent launch
     if (D == 64)
-      e = launch_attn_tc<64>(ap, qmap, qmap1, grid, st);
+      e = launch_attn_tc<64>(ap, qmap, qmap1, px.kmap_tmpl, px.vmap_tmpl, L.grid, !L.fused, st);
     else
-      e = launch_attn_tc<128>(ap, qmap, qmap1, grid, st);
+      e = launch_attn_tc<128>(ap, qmap, qmap1, px.kmap_tmpl, px.vmap_tmpl, L.grid, !L.fused, st);
   }
   if (e != cudaSuccess) return cuda_fail(e);
   if (timed) {
@@ -315,6 +392,19 @@ int run_ikbo(DeviceState* ds, const void* q, const void* k, const void* v, const
     cudaGetDevice(&dev);
     g_timing_dev = dev;
   }
+  return IKBO_OK;
+}
+
+// Workspace for a call on this device with the current kernel choice.
+int call_workspace(DeviceState* ds, int64_t n_cand, int64_t n_user, int H, int Lq, int D,
+                   Workspace* out) {
+  int grid = 0;
+  if (t_kernel == 0) {
+    grid = D == 64 ? tc_grid<64>(ds) : tc_grid<128>(ds);
+    if (grid <= 0) return IKBO_ERR_CUDA;
+  }
+  *out = plan_workspace(n_cand, n_user, H, Lq, D, ds->num_sms, grid > 0 ? grid : ds->num_sms,
+                        t_kernel);
   return IKBO_OK;
 }
 
@@ -344,7 +434,8 @@ int ikbo_attn_fwd(const void* q, const void* k_user, const void* v_user,
   if ((rc = device_state(&ds)) != IKBO_OK) return rc;
   if (g_timing && (rc = ensure_events(ds)) != IKBO_OK) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const Workspace L = plan_workspace(n_cand, n_user, H, Lq, D, ds->num_sms);
+  Workspace L;
+  if ((rc = call_workspace(ds, n_cand, n_user, H, Lq, D, &L)) != IKBO_OK) return rc;
   void* ws = nullptr;
   if (cudaMallocAsync(&ws, L.total, st) != cudaSuccess) return IKBO_ERR_CUDA;
   rc = run_ikbo(ds, q, k_user, v_user, user_offsets, cand_to_user, n_cand, n_user, H, Lq, D, scale,
@@ -367,7 +458,8 @@ int ikbo_attn_fwd_host(const void* q, const void* k_user, const void* v_user,
   if ((rc = device_state(&ds)) != IKBO_OK) return rc;
   if (g_timing && (rc = ensure_events(ds)) != IKBO_OK) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const Workspace L = plan_workspace(n_cand, n_user, H, Lq, D, ds->num_sms);
+  Workspace L;
+  if ((rc = call_workspace(ds, n_cand, n_user, H, Lq, D, &L)) != IKBO_OK) return rc;
   const size_t qbytes = size_t(n_cand) * H * Lq * D * 2;
   const size_t kvbytes = size_t(T) * H * D * 2;
   const size_t o_q = 0, o_k = align_up(o_q + qbytes, 256), o_v = align_up(o_k + kvbytes, 256);
@@ -497,7 +589,8 @@ int ikbo_broadcast_attn_fwd(const void* q, const void* k_user, const void* v_use
   size_t ob = 0;
   for (size_t ch = 0; ch + 1 < cuts.size() && rc == IKBO_OK; ++ch) {
     const int64_t c0 = cuts[ch], n = cuts[ch + 1] - c0, rows = chunk_rows[ch];
-    const Workspace L = plan_workspace(n, n, H, Lq, D, ds->num_sms);
+    Workspace L;
+    if ((rc = call_workspace(ds, n, n, H, Lq, D, &L)) != IKBO_OK) break;
     const size_t o_kb = 0, o_vb = align_up(size_t(rows) * row_bytes, 256);
     const size_t o_ws = align_up(o_vb + size_t(rows) * row_bytes, 256);
     char* buf = nullptr;
@@ -596,6 +689,11 @@ int ikbo_set_debug(int flags, uint64_t timeout_ns) {
   return IKBO_OK;
 }
 
+int ikbo_set_trace(uint64_t* device_buffer) {
+  g_trace = device_buffer;
+  return IKBO_OK;
+}
+
 int ikbo_set_kernel(int which) {
   const int prev = t_kernel;
   t_kernel = which == 1 ? 1 : 0;
@@ -651,7 +749,8 @@ extern "C" int ikbo_attn_fwd_noalloc(const void* q, const void* k_user, const vo
   DeviceState* ds = nullptr;
   if ((rc = device_state(&ds)) != IKBO_OK) return rc;
   if (g_timing && (rc = ensure_events(ds)) != IKBO_OK) return rc;
-  const Workspace L = plan_workspace(n_cand, n_user, H, Lq, D, ds->num_sms);
+  Workspace L;
+  if ((rc = call_workspace(ds, n_cand, n_user, H, Lq, D, &L)) != IKBO_OK) return rc;
   if (L.total > size_t(IKBO_NOALLOC_SCRATCH_BYTES)) return IKBO_ERR_SCRATCH;
   char* ws = nullptr;
   if ((rc = noalloc_scratch(&ws)) != IKBO_OK) return rc;

@@ -1,5 +1,6 @@
 // IKBO target attention on the 5th-generation tensor cores (sm_103a):
-// persistent, warp-specialised, TMA-fed, accumulators in tensor memory.
+// persistent, warp-specialised, TMA-fed, accumulators in tensor memory,
+// launched as clusters of two CTAs.
 //
 // What it computes: for every work item (one user, one head, a query tile of
 // up to 128 rows = that user's candidates x Lq tokens, one range of the
@@ -10,22 +11,41 @@
 // Where IKBO enters ("In-Kernel Broadcast Optimization", §3.1-§3.2): the
 // rows of a query tile are the queries of several candidates of ONE user, so
 // every K/V tile that the TMA brings into shared memory serves all of them;
-// the user's sequence is found through the work item (user_offsets), never
-// through a per-candidate copy.  A tile that is only partly filled (odd or
-// short groups, §3.2 "generalised" kernel) simply carries unused rows: the
-// MMA computes them, the epilogue does not store them, and no warp waits for
-// a partner that does not exist.
+// the user's sequence is found through user_offsets, never through a
+// per-candidate copy.  A tile that is only partly filled (odd or short
+// groups, §3.2 "generalised" kernel) simply carries unused rows: the MMA
+// computes them, the epilogue does not store them, and no warp waits for a
+// partner that does not exist.
 //
-// Warp roles (one CTA per SM, 256 threads), after the Blackwell design of
-// "Optimizing Jagged Flash Attention with TLX", §2.1 (dedicated load, MMA and
-// softmax warps; explicit SMEM/TMEM buffers; S/P sharing one TMEM buffer, the
-// PV accumulator its own; persistent CTAs):
-//   warp 0      TMA producer: Q tile (double-buffered), then K_0, K_1, V_0,
-//               K_2, V_1, ... into a ring of shared-memory slots;
+// Planning.  For inputs of moderate size every CTA plans in its prologue,
+// from the index tensors, with its shared memory as scratch: it validates
+// cand_to_user and user_offsets, groups candidates by user (a stable counting
+// sort when the map is unsorted), orders users longest first and derives its
+// own work items, so the whole forward is ONE launch.  Larger inputs use the
+// separate planning kernel's work list.  Items are handed to CTAs in
+// boustrophedon order over the longest-first list ("Optimizing Jagged Flash
+// Attention with TLX", §2.2: tiles sorted by K/V work, even passes left to
+// right, odd passes right to left); the items of one (user, head) are
+// adjacent so CTAs sharing a user's K/V run together ("In-Kernel Broadcast
+// Optimization", §3.1, Table 1).
+//
+// Pair mode.  When there are no more (user, head, query tile) units than
+// clusters, the two CTAs of a cluster split one unit's keys in half.  The
+// second CTA sends its un-normalised O and (m, l) through distributed shared
+// memory into the first, which merges them with the log-sum-exp rule of
+// "Chapter 4", §4.6.4 (Flash-Decoding): M = max(m0, m1),
+// out = (2^(m0-M) O0 + 2^(m1-M) O1) / (2^(m0-M) l0 + 2^(m1-M) l1).
+//
+// Warp roles (256 threads), after the Blackwell design of "Optimizing Jagged
+// Flash Attention with TLX", §2.1 (dedicated load, MMA and softmax warps;
+// explicit SMEM/TMEM buffers; S/P sharing one TMEM buffer, the PV
+// accumulator its own; persistent CTAs):
+//   warp 0      TMA producer: Q tile, then K_0, K_1, V_0, K_2, V_1, ... into a
+//               ring of shared-memory slots;
 //   warp 1      TMEM allocator and single-thread tcgen05.mma issuer:
-//               S_j = Q K_j^T (SS form, both operands in SMEM) into one of
-//               two S buffers, then O += P_{j-1} V_{j-1} (TS form, P read
-//               from TMEM), so S_j overlaps the softmax of tile j-1;
+//               S_j = Q K_j^T (SS form) into one of two S buffers, then
+//               O += P_{j-1} V_{j-1} (TS form, P read from TMEM), so S_j
+//               overlaps the softmax of tile j-1;
 //   warps 4-7   softmax, O correction and epilogue; thread i owns TMEM lane
 //               (= query row) i.
 // Every wait is bounded: a wait that runs out sets the device error word,
@@ -46,24 +66,58 @@ constexpr int kTcThreads = 256;
 // than this (base-2 units), so un-normalised weights stay <= 2^8 and the
 // O correction is skipped on most tiles; the final O / l is exact either way.
 constexpr float kLazyRescale = 8.0f;
+constexpr int kDataBytes = 229376;   // 224 KB: operands (and planning scratch in the prologue)
+constexpr int kCtrlBytes = 2048;     // barriers, flags, plan results, partner (m, l)
+constexpr int kTcSmemBytes = kCtrlBytes + 1024 + kDataBytes;   // = 227 KB, the per-CTA maximum
+constexpr int kMaxSlots = 14;
+// In-kernel planning keeps off/cand_start/order/prefix (n_user), the per-warp
+// counters of the counting sort (8 x n_user) and cand_to_user/perm (n_cand)
+// in the operand area.
+constexpr int kFusedMaxUser = 1024;
+constexpr int kFusedMaxCand = 20480;
+constexpr int kLptMaxUsersFused = 256;
+
+enum TcMode { kModeSkip = -1, kModeListed = 0, kModeIndep = 1, kModePair = 2 };
 
 template <int D>
 struct TcConfig {
   static constexpr int kCB = D / 64;                   // 128-byte column blocks per row
   static constexpr int kQBytes = kCB * kTileM * 128;    // one Q tile
   static constexpr int kKVBytes = kCB * kBlockN * 128;  // one K or V tile
-  static constexpr int kNQ = 2;                         // Q buffers
-  static constexpr int kNS = D == 128 ? 5 : 12;         // K/V ring slots
-  static constexpr int kData = kNQ * kQBytes + kNS * kKVBytes;
-  static constexpr int kNumBars = 2 * kNQ + 2 * kNS + 2 + 2 + 1 + 1;   // + tmem slot and flags
-  static constexpr int kSmemBytes = kData + kNumBars * 8 + 64 + 1024;   // + flags, alignment
+  static constexpr int kSlotsIndep = (kDataBytes - 2 * kQBytes) / kKVBytes;   // 2 Q buffers
+  static constexpr int kSlotsPair = (kDataBytes - kQBytes) / kKVBytes;        // 1 Q buffer
+  static constexpr int kRecvBytes = kTileM * D * 4;     // partner's O, received in the ring
   // tensor-memory columns: two S/P buffers and the O accumulator
   static constexpr int kSCol = 0;
   static constexpr int kOCol = 2 * kBlockN;
   static constexpr int kTmemCols = 512;
   static_assert(kOCol + D <= kTmemCols, "TMEM budget");
-  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(kSlotsPair <= kMaxSlots && kSlotsIndep >= 3, "ring size");
+  static_assert(kRecvBytes <= kSlotsPair * kKVBytes, "receive area");
 };
+
+static_assert(kTcSmemBytes <= 232448, "shared memory budget");
+static_assert(4 * (4 * (kFusedMaxUser + 1) + 8 * kFusedMaxUser + 2 * kFusedMaxCand) <= kDataBytes,
+              "planning scratch");
+
+// Control block at the start of dynamic shared memory.
+struct TcCtrl {
+  uint64_t q_full[2], q_empty[2];
+  uint64_t kv_full[kMaxSlots], kv_empty[kMaxSlots];
+  uint64_t s_full[2], p_full[2];
+  uint64_t pv_done, drain, pair_go, pair_recv;
+  uint32_t tmem_base;
+  int abort_flag;
+  int wg_count;
+  int mode;
+  int n_my_items;
+  int sorted;
+  int n_slots;
+  int pad;
+  int red_i[32];
+  float2 partner_ml[kTileM];
+};
+static_assert(sizeof(TcCtrl) <= kCtrlBytes, "control block");
 
 // Bounded mbarrier wait shared by all roles of a CTA.
 struct Waiter {
@@ -71,12 +125,15 @@ struct Waiter {
   int* err_word;
   uint64_t timeout_ns;
 
-  __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity) const {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+  __device__ __forceinline__ bool poll(uint32_t bar, uint32_t parity, bool cluster) const {
+    return cluster ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
+  }
+  __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, bool cluster = false) const {
+    if (poll(bar, parity, cluster)) return true;
     uint64_t t_end = 0;
     for (uint32_t spin = 1;; ++spin) {
       if (*abort) return false;
-      if (ptx::mbar_try_wait(bar, parity)) return true;
+      if (poll(bar, parity, cluster)) return true;
       if ((spin & 63u) == 0) {
         const uint64_t now = ptx::globaltimer();
         if (t_end == 0) {
@@ -107,194 +164,386 @@ struct Waiter {
     }
   }
   // One lane polls, the warp follows its verdict.
-  __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) const {
+  __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, bool cluster = false) const {
     int ok = 0;
-    if ((threadIdx.x & 31) == 0) ok = wait(bar, parity) ? 1 : 0;
+    if ((threadIdx.x & 31) == 0) ok = wait(bar, parity, cluster) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
     return ok != 0;
   }
 };
+
+__device__ __forceinline__ void trace(const AttnParams& p, int ord, int point) {
+  if (p.trace && ord < kTraceItems)
+    p.trace[(size_t(blockIdx.x) * kTraceItems + ord) * kTracePoints + point] = ptx::globaltimer();
+}
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Barrier of the four softmax warps built on a shared counter, bounded like
-// every other wait (a hardware named barrier cannot time out, and a warp that
-// aborted would leave the others stuck on it).  `target` grows by 4 per use.
-__device__ __forceinline__ bool wg_sync(int* count, int target, const Waiter& W) {
-  int ok = 1;
-  __syncwarp();
-  if ((threadIdx.x & 31) == 0) {
-    __threadfence_block();
-    atomicAdd(count, 1);
-    uint64_t t_end = 0;
-    for (uint32_t spin = 0; *reinterpret_cast<volatile int*>(count) < target; ++spin) {
-      if (*W.abort) {
-        ok = 0;
-        break;
-      }
-      if ((spin & 63u) == 63u) {
-        const uint64_t now = ptx::globaltimer();
-        if (t_end == 0) {
-          t_end = now + W.timeout_ns;
-        } else if (now > t_end) {
-          *W.abort = 1;
-          atomicOr(W.err_word, kErrTimeout);
-          ok = 0;
-          break;
-        }
-      }
-    }
-    __threadfence_block();
+__device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Block-wide exclusive scan of one int per thread (all threads call it).
+__device__ __forceinline__ int block_scan_excl(int x, int* red, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int v = x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += y;
   }
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  return ok != 0;
+  if (lane == 31) red[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < nw ? red[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    red[lane] = w;
+  }
+  __syncthreads();
+  const int pre = warp == 0 ? 0 : red[warp - 1];
+  *total = red[nw - 1];
+  __syncthreads();
+  return pre + v - x;
 }
 
-// Split-KV merge of one query row by the CTA that finished the unit last
-// (thread per row): M = max_s m_s, l = sum_s 2^(m_s - M) l_s,
-// out = sum_s 2^(m_s - M) O_s / l  ("Chapter 4: High-performance Kernels",
-// §4.6.4, log-sum-exp merge of Flash-Decoding).
-template <int D>
-__device__ __forceinline__ void merge_row(const AttnParams& p, const WorkItem& w, int row, int ci,
-                                          int t, bool sorted) {
-  const int ns = p.units[w.unit].n_split;
-  const int64_t slot0 = (int64_t)w.unit_first * kTileM + row;
-  float M = -INFINITY;
-  for (int s = 0; s < ns; ++s) M = fmaxf(M, __ldcg(&p.partial_ml[slot0 + (int64_t)s * kTileM]).x);
-  float L = 0.f;
-  for (int s = 0; s < ns; ++s) {
-    const float2 ml = __ldcg(&p.partial_ml[slot0 + (int64_t)s * kTileM]);
-    L += fast_exp2(ml.x - M) * ml.y;
+// ---------------------------------------------------------------------------
+// In-kernel planning.  All threads of the CTA; `scratch` is the operand area.
+// Every CTA computes the same plan (the inputs are small) and keeps only its
+// own items.  The K/V tensor maps get their row count T here, in a per-CTA
+// slot in global memory.
+// ---------------------------------------------------------------------------
+__device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch,
+                            const CUtensorMap& kt, const CUtensorMap& vt, int D) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int grid = gridDim.x, b = blockIdx.x;
+  const int n_cand = (int)p.n_cand, n_user = (int)p.n_user;
+  int32_t* off = reinterpret_cast<int32_t*>(scratch);   // n_user + 1
+  int32_t* cs = off + (n_user + 1);                     // cand_start, n_user + 1
+  int32_t* order = cs + (n_user + 1);                   // n_user
+  int32_t* ubefore = order + n_user;                    // n_user + 1
+  int32_t* wcnt = ubefore + (n_user + 1);               // 8 x n_user (unsorted only)
+  int32_t* c2u = wcnt + 8 * n_user;                     // n_cand
+  int32_t* perm = c2u + n_cand;                         // n_cand
+
+  for (int u = tid; u <= n_user; u += nt) off[u] = p.user_offsets[u];
+  for (int c = tid; c < n_cand; c += nt) c2u[c] = p.cand_to_user[c];
+  __syncthreads();
+  // K/V tensor maps: row count T, into this CTA's global slots
+  if (tid == 0) {
+    const int T = off[n_user];
+    const int rows = T > 0 ? T : 1;
+#pragma unroll
+    for (int mi = 0; mi < 2; ++mi) {
+      CUtensorMap* dst = p.map_slots + 2 * b + mi;
+      const uint4* s4 = reinterpret_cast<const uint4*>(mi == 0 ? &kt : &vt);
+      uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+      for (int i = 0; i < (int)(sizeof(CUtensorMap) / 16); ++i) d4[i] = s4[i];
+      asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 1, %1;" ::"l"(dst),
+                   "r"(rows)
+                   : "memory");
+    }
+    asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
   }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-  const int32_t gpos = w.cand_begin + ci;
-  const int64_t c = sorted ? gpos : p.perm[gpos];
-  uint16_t* dst = p.out + (((c * p.H + w.head) * (int64_t)p.Lq + t) * D);
-#pragma unroll 1
-  for (int cc = 0; cc < D / 32; ++cc) {
-    float acc[32];
-#pragma unroll
-    for (int e = 0; e < 32; ++e) acc[e] = 0.f;
-#pragma unroll 1
-    for (int s0 = 0; s0 < ns; s0 += 2) {
-      float a[2];
-      float4 x[2][8];
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int s = s0 + u;
-        if (s < ns) {
-          const int64_t slot = slot0 + (int64_t)s * kTileM;
-          a[u] = fast_exp2(__ldcg(&p.partial_ml[slot]).x - M);
-          const float4* src = reinterpret_cast<const float4*>(p.partial_o + slot * D + cc * 32);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) x[u][q] = __ldcg(src + q);
-        } else {
-          a[u] = 0.f;
-#pragma unroll
-          for (int q = 0; q < 8; ++q) x[u][q] = make_float4(0.f, 0.f, 0.f, 0.f);
+  // validation
+  int e_off = 0, e_idx = 0, unsorted = 0;
+  if (tid == 0 && off[0] != 0) e_off = 1;
+  for (int u = tid; u < n_user; u += nt)
+    if (off[u + 1] < off[u]) e_off = 1;
+  for (int c = tid; c < n_cand; c += nt) {
+    const int x = c2u[c];
+    if (x < 0 || x >= n_user) e_idx = 1;
+    if (c > 0 && c2u[c - 1] > x) unsorted = 1;
+  }
+  const int any_off = __syncthreads_or(e_off);
+  const int any_idx = __syncthreads_or(e_idx);
+  const int any_uns = __syncthreads_or(unsorted);
+  if (any_off || any_idx) {
+    if (tid == 0) {
+      ctl->mode = kModeSkip;
+      ctl->n_my_items = 0;
+      ctl->sorted = 1;
+      if (b == 0) atomicOr(p.err_word, (any_off ? kErrOffsets : 0) | (any_idx ? kErrIndex : 0));
+    }
+    __syncthreads();
+    return;
+  }
+  // group candidates by user
+  if (!any_uns) {
+    for (int c = tid; c < n_cand; c += nt) {
+      const int x = c2u[c];
+      const int prev = c == 0 ? -1 : c2u[c - 1];
+      for (int uu = prev + 1; uu <= x; ++uu) cs[uu] = c;
+    }
+    for (int uu = c2u[n_cand - 1] + 1 + tid; uu <= n_user; uu += nt) cs[uu] = n_cand;
+    __syncthreads();
+  } else {
+    // stable counting sort: warp w owns a contiguous segment of candidates
+    const int warp = tid >> 5, lane = tid & 31, nw = nt >> 5;
+    const int seg = (n_cand + nw - 1) / nw;
+    const int seg_end = min(n_cand, (warp + 1) * seg);
+    for (int i = tid; i < nw * n_user; i += nt) wcnt[i] = 0;
+    __syncthreads();
+    for (int c = warp * seg + lane; c < seg_end; c += 32) atomicAdd(&wcnt[warp * n_user + c2u[c]], 1);
+    __syncthreads();
+    // per-user totals -> cand_start (exclusive scan over users)
+    int carry = 0;
+    for (int base = 0; base < n_user; base += nt) {
+      const int u = base + tid;
+      int tot_u = 0;
+      if (u < n_user)
+        for (int w = 0; w < nw; ++w) tot_u += wcnt[w * n_user + u];
+      int tot;
+      const int ex = block_scan_excl(tot_u, ctl->red_i, &tot);
+      if (u < n_user) cs[u] = carry + ex;
+      carry += tot;
+    }
+    if (tid == 0) cs[n_user] = n_cand;
+    __syncthreads();
+    // per-warp cursors: cand_start + counts of the earlier warps
+    for (int u = tid; u < n_user; u += nt) {
+      int acc = cs[u];
+      for (int w = 0; w < nw; ++w) {
+        const int cnt = wcnt[w * n_user + u];
+        wcnt[w * n_user + u] = acc;
+        acc += cnt;
+      }
+    }
+    __syncthreads();
+    const unsigned lt = (1u << lane) - 1u;
+    for (int base = warp * seg; base < seg_end; base += 32) {
+      const int c = base + lane;
+      const bool valid = c < seg_end;
+      const int x = valid ? c2u[c] : -1;
+      const unsigned same = __match_any_sync(0xffffffffu, x);
+      int pos = 0;
+      if (valid) pos = wcnt[warp * n_user + x] + __popc(same & lt);
+      __syncwarp();
+      if (valid && (same & lt) == 0) wcnt[warp * n_user + x] += __popc(same);
+      if (valid) perm[pos] = c;
+      __syncwarp();
+    }
+    __syncthreads();
+    // every CTA writes the same permutation; each reads back only its own writes
+    for (int i = tid; i < n_cand; i += nt) p.perm_ws[i] = perm[i];
+  }
+  // rows of candidates whose user has an empty sequence are zero
+  {
+    const int64_t elems = (int64_t)p.H * p.Lq * D;
+    for (int c = b * nt + tid; c < n_cand; c += grid * nt) {
+      const int x = c2u[c];
+      if (off[x + 1] == off[x]) {
+        uint4* dst = reinterpret_cast<uint4*>(p.out + (int64_t)c * elems);
+        for (int64_t i = 0; i < elems / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+      }
+    }
+  }
+  // users, longest first (index order beyond kLptMaxUsersFused users)
+  for (int u = tid; u < n_user; u += nt) {
+    if (n_user <= kLptMaxUsersFused) {
+      const int Lu = off[u + 1] - off[u];
+      int rank = 0;
+      for (int w = 0; w < n_user; ++w) {
+        const int Lw = off[w + 1] - off[w];
+        rank += (Lw > Lu) || (Lw == Lu && w < u);
+      }
+      order[rank] = u;
+    } else {
+      order[u] = u;
+    }
+  }
+  __syncthreads();
+  // units per rank: H x query tiles of users with candidates and keys
+  const int cpt = p.cands_per_tile;
+  {
+    int carry = 0;
+    for (int base = 0; base < n_user; base += nt) {
+      const int rk = base + tid;
+      int nu = 0;
+      if (rk < n_user) {
+        const int u = order[rk];
+        const int r = cs[u + 1] - cs[u], L = off[u + 1] - off[u];
+        if (r > 0 && L > 0) nu = p.H * ceil_div(r, cpt);
+      }
+      int tot;
+      const int ex = block_scan_excl(nu, ctl->red_i, &tot);
+      if (rk < n_user) ubefore[rk] = carry + ex;
+      carry += tot;
+    }
+    if (tid == 0) ubefore[n_user] = carry;
+    __syncthreads();
+  }
+  const int N = ubefore[n_user];
+  const bool pair = N > 0 && 2 * N <= grid;
+  // decode unit i into a work item
+  auto decode = [&](int i, WorkItem& w) {
+    int lo = 0, hi = n_user - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (ubefore[mid] <= i) lo = mid; else hi = mid - 1;
+    }
+    const int u = order[lo];
+    const int r = cs[u + 1] - cs[u];
+    const int nmt = ceil_div(r, cpt);
+    const int local = i - ubefore[lo];
+    const int h = local / nmt, mt = local - h * nmt;
+    w.user = u;
+    w.head = h;
+    w.cand_begin = cs[u] + mt * cpt;
+    w.n_cand = min(cpt, r - mt * cpt);
+    w.kv_begin = off[u];
+    w.kv_len = off[u + 1] - off[u];
+    w.unit = -1;
+    w.unit_first = 0;
+  };
+  WorkItem* mine = p.cta_items + (size_t)b * p.max_cta_items;
+  if (pair) {
+    if (tid == 0) {
+      const int c = b >> 1, rank = b & 1;
+      int count = 0;
+      if (c < N) {
+        WorkItem w;
+        decode(c, w);
+        const int kt = ceil_div(w.kv_len, kBlockN);
+        if (kt >= 2) {
+          const int first = ceil_div(kt, 2) * kBlockN;   // keys of the leader
+          if (rank == 0) {
+            w.kv_len = first;
+            w.unit = 0;
+            w.unit_first = 1;
+          } else {
+            w.kv_begin += first;
+            w.kv_len -= first;
+            w.unit = 1;
+          }
+          mine[0] = w;
+          count = 1;
+        } else if (rank == 0) {
+          mine[0] = w;
+          count = 1;
         }
       }
-#pragma unroll
-      for (int u = 0; u < 2; ++u)
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          acc[q * 4 + 0] += a[u] * x[u][q].x;
-          acc[q * 4 + 1] += a[u] * x[u][q].y;
-          acc[q * 4 + 2] += a[u] * x[u][q].z;
-          acc[q * 4 + 3] += a[u] * x[u][q].w;
-        }
+      ctl->n_my_items = count;
     }
-    uint4* d4 = reinterpret_cast<uint4*>(dst + cc * 32);
-#pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {
-      uint4 v;
-      v.x = pack_bf16(acc[q4 * 8 + 0] * inv, acc[q4 * 8 + 1] * inv);
-      v.y = pack_bf16(acc[q4 * 8 + 2] * inv, acc[q4 * 8 + 3] * inv);
-      v.z = pack_bf16(acc[q4 * 8 + 4] * inv, acc[q4 * 8 + 5] * inv);
-      v.w = pack_bf16(acc[q4 * 8 + 6] * inv, acc[q4 * 8 + 7] * inv);
-      d4[q4] = v;
+  } else {
+    const int full = N / grid, rem = N - full * grid;
+    const int pos_last = (full & 1) ? grid - 1 - b : b;
+    int count = full + (pos_last < rem ? 1 : 0);
+    count = min(count, p.max_cta_items);
+    for (int k = tid; k < count; k += nt) {
+      const int i = k * grid + ((k & 1) ? grid - 1 - b : b);
+      WorkItem w;
+      decode(i, w);
+      mine[k] = w;
     }
+    if (tid == 0) ctl->n_my_items = count;
   }
+  if (tid == 0) {
+    ctl->mode = pair ? kModePair : kModeIndep;
+    ctl->sorted = any_uns ? 0 : 1;
+  }
+  __syncthreads();
 }
 
+// ---------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
 ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap qmap,
-                    const __grid_constant__ CUtensorMap qmap1) {
+                    const __grid_constant__ CUtensorMap qmap1,
+                    const __grid_constant__ CUtensorMap kmap_tmpl,
+                    const __grid_constant__ CUtensorMap vmap_tmpl) {
   using C = TcConfig<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
-  uint8_t* q_smem = smem;
-  uint8_t* kv_smem = smem + C::kNQ * C::kQBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kData);
-  uint64_t* q_full = bars;
-  uint64_t* q_empty = q_full + C::kNQ;
-  uint64_t* kv_full = q_empty + C::kNQ;
-  uint64_t* kv_empty = kv_full + C::kNS;
-  uint64_t* s_full = kv_empty + C::kNS;
-  uint64_t* p_full = s_full + 2;
-  uint64_t* pv_done = p_full + 2;
-  uint64_t* drain_bar = pv_done + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  volatile int* s_last = abort_flag + 1;
-  int* wg_count = const_cast<int*>(s_last + 1);
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  TcCtrl* ctl = reinterpret_cast<TcCtrl*>(smem_raw);
+  uint8_t* data = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + kCtrlBytes + 1023) & ~uintptr_t(1023));
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t cta_rank = ptx::cluster_ctarank();
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::kNQ; ++i) {
-      ptx::mbar_init(ptx::smem_addr(&q_full[i]), 1);
-      ptx::mbar_init(ptx::smem_addr(&q_empty[i]), 1);
-    }
-    for (int i = 0; i < C::kNS; ++i) {
-      ptx::mbar_init(ptx::smem_addr(&kv_full[i]), 1);
-      ptx::mbar_init(ptx::smem_addr(&kv_empty[i]), 1);
-    }
     for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(ptx::smem_addr(&s_full[i]), 1);
-      ptx::mbar_init(ptx::smem_addr(&p_full[i]), 4);
+      ptx::mbar_init(ptx::smem_addr(&ctl->q_full[i]), 1);
+      ptx::mbar_init(ptx::smem_addr(&ctl->q_empty[i]), 1);
+      ptx::mbar_init(ptx::smem_addr(&ctl->s_full[i]), 1);
+      ptx::mbar_init(ptx::smem_addr(&ctl->p_full[i]), 4);
     }
-    ptx::mbar_init(ptx::smem_addr(pv_done), 1);
-    ptx::mbar_init(ptx::smem_addr(drain_bar), 1);
-    *abort_flag = 0;
-    *s_last = 0;
-    *wg_count = 0;
+    for (int i = 0; i < kMaxSlots; ++i) {
+      ptx::mbar_init(ptx::smem_addr(&ctl->kv_full[i]), 1);
+      ptx::mbar_init(ptx::smem_addr(&ctl->kv_empty[i]), 1);
+    }
+    ptx::mbar_init(ptx::smem_addr(&ctl->pv_done), 1);
+    ptx::mbar_init(ptx::smem_addr(&ctl->drain), 1);
+    ptx::mbar_init(ptx::smem_addr(&ctl->pair_go), 1);
+    ptx::mbar_init(ptx::smem_addr(&ctl->pair_recv), 4);
+    ctl->abort_flag = 0;
+    ctl->wg_count = 0;
     ptx::fence_mbar_init();
   }
   if (warp == 1) {
-    ptx::tmem_alloc(ptx::smem_addr(tmem_slot), C::kTmemCols);
+    ptx::tmem_alloc(ptx::smem_addr(&ctl->tmem_base), C::kTmemCols);
     ptx::tmem_relinquish();
   }
-  // Programmatic dependent launch: the planner may still be running; its
-  // results (work list, patched tensor maps) are visible after this wait.
+  // A planning kernel may precede this one (programmatic dependent launch):
+  // its work list is visible after this wait.  Without one it returns at once.
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (p.fused) {
+    __syncthreads();
+    plan_in_cta(p, ctl, data, kmap_tmpl, vmap_tmpl, D);
+    // the planning scratch is overwritten by TMA (async proxy) from here on
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  } else if (threadIdx.x == 0) {
+    ctl->mode = kModeListed;
+    ctl->sorted = p.header->sorted != 0;
+    const int n = p.header->n_items;
+    ctl->n_my_items =
+        n > (int)blockIdx.x ? (n - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+  }
+  if (threadIdx.x == 0) {
+    ctl->n_slots = ctl->mode == kModePair ? C::kSlotsPair : C::kSlotsIndep;
+    trace(p, 0, kTrCtaStart);
+  }
   ptx::tc_fence_before();
   __syncthreads();
+  // the partner's barriers are initialised before any remote arrive
+  ptx::cluster_sync();
   ptx::tc_fence_after();
 
-  const uint32_t tmem = *tmem_slot;
-  const int n_items = p.header->n_items;
-  const bool sorted = p.header->sorted != 0;
-  const Waiter W{abort_flag, p.err_word, p.timeout_ns};
+  const uint32_t tmem = ctl->tmem_base;
+  const int mode = ctl->mode;
+  const int n_my = ctl->n_my_items;
+  const bool sorted = ctl->sorted != 0;
+  const int NS = ctl->n_slots;
+  const int NQ = mode == kModePair ? 1 : 2;
+  uint8_t* q_smem = data;
+  uint8_t* kv_smem = data + NQ * C::kQBytes;
+  const int32_t* perm = p.fused ? p.perm_ws : p.perm;
+  const void* kmap = p.fused ? (const void*)(p.map_slots + 2 * blockIdx.x) : p.kmap;
+  const void* vmap = p.fused ? (const void*)(p.map_slots + 2 * blockIdx.x + 1) : p.vmap;
+  const Waiter W{&ctl->abort_flag, p.err_word, p.timeout_ns};
   const int Lq = p.Lq;
+  auto item_at = [&](int k) -> WorkItem {
+    return p.fused ? p.cta_items[(size_t)blockIdx.x * p.max_cta_items + k]
+                   : p.items[blockIdx.x + (size_t)k * gridDim.x];
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      ptx::tensormap_acquire(p.kmap);
-      ptx::tensormap_acquire(p.vmap);
+    if (lane == 0 && mode != kModeSkip) {
+      ptx::tensormap_acquire(kmap);
+      ptx::tensormap_acquire(vmap);
       uint32_t kv_it = 0, q_it = 0;
       bool ok = true;
       auto load_tile = [&](const void* map, int head, int32_t row) -> bool {
-        const uint32_t slot = kv_it % C::kNS;
-        if (!W.wait(ptx::smem_addr(&kv_empty[slot]), ((kv_it / C::kNS) & 1u) ^ 1u)) return false;
-        const uint32_t bar = ptx::smem_addr(&kv_full[slot]);
+        const uint32_t slot = kv_it % NS;
+        if (!W.wait(ptx::smem_addr(&ctl->kv_empty[slot]), ((kv_it / NS) & 1u) ^ 1u)) return false;
+        const uint32_t bar = ptx::smem_addr(&ctl->kv_full[slot]);
         const uint32_t dst = ptx::smem_addr(kv_smem + slot * C::kKVBytes);
         ptx::mbar_arrive_expect_tx(bar, C::kKVBytes);
 #pragma unroll
@@ -303,26 +552,28 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
         ++kv_it;
         return true;
       };
-      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-        const WorkItem w = p.items[it];
-        const int n = (w.kv_len + kBlockN - 1) / kBlockN;
-        const uint32_t qb = q_it & 1u;
-        if (!W.wait(ptx::smem_addr(&q_empty[qb]), ((q_it >> 1) & 1u) ^ 1u)) break;
-        const uint32_t qbar = ptx::smem_addr(&q_full[qb]);
+      for (int k = 0; k < n_my && ok; ++k) {
+        const WorkItem w = item_at(k);
+        const int n = ceil_div(w.kv_len, kBlockN);
+        const uint32_t qb = q_it % NQ;
+        const uint32_t qpar = ((q_it / NQ) & 1u) ^ 1u;
+        trace(p, k, kTrProdItem);
+        if (!W.wait(ptx::smem_addr(&ctl->q_empty[qb]), qpar)) break;
+        const uint32_t qbar = ptx::smem_addr(&ctl->q_full[qb]);
         const uint32_t qdst = ptx::smem_addr(q_smem + qb * C::kQBytes);
         if (!(p.debug_flags & 1)) {
           if (sorted) {
             const int nb = p.qbox;
-            const int nbox = (w.n_cand + nb - 1) / nb;
+            const int nbox = ceil_div(w.n_cand, nb);
             ptx::mbar_arrive_expect_tx(qbar, uint32_t(nbox * nb * Lq * 128 * C::kCB));
             for (int cb = 0; cb < C::kCB; ++cb)
-              for (int b = 0; b < nbox; ++b)
-                ptx::tma_load_4d(qdst + cb * kTileM * 128 + b * nb * Lq * 128, &qmap, qbar,
-                                 cb * 64, 0, w.head, w.cand_begin + b * nb);
+              for (int bx = 0; bx < nbox; ++bx)
+                ptx::tma_load_4d(qdst + cb * kTileM * 128 + bx * nb * Lq * 128, &qmap, qbar,
+                                 cb * 64, 0, w.head, w.cand_begin + bx * nb);
           } else {
             ptx::mbar_arrive_expect_tx(qbar, uint32_t(w.n_cand * Lq * 128 * C::kCB));
             for (int i = 0; i < w.n_cand; ++i) {
-              const int32_t c = p.perm[w.cand_begin + i];
+              const int32_t c = perm[w.cand_begin + i];
               for (int cb = 0; cb < C::kCB; ++cb)
                 ptx::tma_load_4d(qdst + cb * kTileM * 128 + i * Lq * 128, &qmap1, qbar, cb * 64, 0,
                                  w.head, c);
@@ -332,39 +583,42 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
         ++q_it;
         // K/V tiles in the order the MMA warp consumes them: K0, K1, V0, K2, V1, ...
         for (int j = 0; j <= n && ok; ++j) {
-          if (j < n) ok = load_tile(p.kmap, w.head, w.kv_begin + j * kBlockN);
-          if (ok && j >= 1) ok = load_tile(p.vmap, w.head, w.kv_begin + (j - 1) * kBlockN);
+          if (j < n) ok = load_tile(kmap, w.head, w.kv_begin + j * kBlockN);
+          if (ok && j >= 1) ok = load_tile(vmap, w.head, w.kv_begin + (j - 1) * kBlockN);
         }
+        trace(p, k, kTrProdIssued);
       }
       // Drain: every armed barrier phase must complete before the CTA exits.
-      for (uint32_t s = 0; s < C::kNS && s < kv_it; ++s) {
-        const uint32_t uses = (kv_it - s + C::kNS - 1) / C::kNS;
-        W.drain(ptx::smem_addr(&kv_full[s]), (uses - 1) & 1u);
+      for (uint32_t s = 0; s < (uint32_t)NS && s < kv_it; ++s) {
+        const uint32_t uses = (kv_it - s + NS - 1) / NS;
+        W.drain(ptx::smem_addr(&ctl->kv_full[s]), (uses - 1) & 1u);
       }
       if (!(p.debug_flags & 1))
-        for (uint32_t b = 0; b < C::kNQ && b < q_it; ++b) {
-          const uint32_t uses = (q_it - b + 1) / 2;
-          W.drain(ptx::smem_addr(&q_full[b]), (uses - 1) & 1u);
+        for (uint32_t qb = 0; qb < (uint32_t)NQ && qb < q_it; ++qb) {
+          const uint32_t uses = (q_it - qb + NQ - 1) / NQ;
+          W.drain(ptx::smem_addr(&ctl->q_full[qb]), (uses - 1) & 1u);
         }
     }
+    __syncwarp();
   } else if (warp == 1) {
     // -------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && mode != kModeSkip) {
       constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(kTileM, kBlockN, 0);
       constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(kTileM, 64, 1);
       uint32_t kv_it = 0, q_it = 0, g = 0;
       bool ok = true;
-      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-        const WorkItem w = p.items[it];
-        const int n = (w.kv_len + kBlockN - 1) / kBlockN;
-        const uint32_t qb = q_it & 1u;
-        if (!W.wait(ptx::smem_addr(&q_full[qb]), (q_it >> 1) & 1u)) break;
+      for (int k = 0; k < n_my && ok; ++k) {
+        const WorkItem w = item_at(k);
+        const int n = ceil_div(w.kv_len, kBlockN);
+        const uint32_t qb = q_it % NQ;
+        if (!W.wait(ptx::smem_addr(&ctl->q_full[qb]), (q_it / NQ) & 1u)) break;
         ptx::tc_fence_after();
+        trace(p, k, kTrMmaQ);
         const uint32_t q_base = ptx::smem_addr(q_smem + qb * C::kQBytes);
         for (int j = 0; j <= n; ++j) {
           if (j < n) {
-            const uint32_t slot = kv_it % C::kNS;
-            if (!W.wait(ptx::smem_addr(&kv_full[slot]), (kv_it / C::kNS) & 1u)) {
+            const uint32_t slot = kv_it % NS;
+            if (!W.wait(ptx::smem_addr(&ctl->kv_full[slot]), (kv_it / NS) & 1u)) {
               ok = false;
               break;
             }
@@ -377,24 +631,25 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
               const int cb = kk >> 2;
               const uint32_t koff = (kk & 3) * 32;
               const uint64_t a = ptx::smem_desc_sw128(q_base + cb * kTileM * 128 + koff, 16, 1024);
-              const uint64_t b = ptx::smem_desc_sw128(k_base + cb * kBlockN * 128 + koff, 16, 1024);
-              ptx::mma_ss(d_tmem, a, b, kIdescQK, kk > 0 ? 1u : 0u);
+              const uint64_t bdesc = ptx::smem_desc_sw128(k_base + cb * kBlockN * 128 + koff, 16, 1024);
+              ptx::mma_ss(d_tmem, a, bdesc, kIdescQK, kk > 0 ? 1u : 0u);
             }
-            ptx::mma_commit(ptx::smem_addr(&kv_empty[slot]));
-            ptx::mma_commit(ptx::smem_addr(&s_full[sb]));
-            if (j == n - 1) ptx::mma_commit(ptx::smem_addr(&q_empty[qb]));
+            if (j == 0) trace(p, k, kTrMmaFirstS);
+            ptx::mma_commit(ptx::smem_addr(&ctl->kv_empty[slot]));
+            ptx::mma_commit(ptx::smem_addr(&ctl->s_full[sb]));
+            if (j == n - 1) ptx::mma_commit(ptx::smem_addr(&ctl->q_empty[qb]));
             ++kv_it;
           }
           if (j >= 1) {
             const uint32_t pj = g + j - 1;
             const uint32_t pb = pj & 1u;
-            if (!W.wait(ptx::smem_addr(&p_full[pb]), (pj >> 1) & 1u)) {
+            if (!W.wait(ptx::smem_addr(&ctl->p_full[pb]), (pj >> 1) & 1u)) {
               ok = false;
               break;
             }
             ptx::tc_fence_after();
-            const uint32_t slot = kv_it % C::kNS;
-            if (!W.wait(ptx::smem_addr(&kv_full[slot]), (kv_it / C::kNS) & 1u)) {
+            const uint32_t slot = kv_it % NS;
+            if (!W.wait(ptx::smem_addr(&ctl->kv_full[slot]), (kv_it / NS) & 1u)) {
               ok = false;
               break;
             }
@@ -405,14 +660,15 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
             for (int kk = 0; kk < kBlockN / 16; ++kk) {
 #pragma unroll
               for (int cb = 0; cb < C::kCB; ++cb) {
-                const uint64_t b = ptx::smem_desc_sw128(v_base + cb * kBlockN * 128 + kk * 16 * 128,
-                                                        kBlockN * 128, 1024);
-                ptx::mma_ts(tmem + C::kOCol + cb * 64, a_tmem + kk * 8, b, kIdescPV,
+                const uint64_t bdesc = ptx::smem_desc_sw128(
+                    v_base + cb * kBlockN * 128 + kk * 16 * 128, kBlockN * 128, 1024);
+                ptx::mma_ts(tmem + C::kOCol + cb * 64, a_tmem + kk * 8, bdesc, kIdescPV,
                             (j > 1 || kk > 0) ? 1u : 0u);
               }
             }
-            ptx::mma_commit(ptx::smem_addr(&kv_empty[slot]));
-            ptx::mma_commit(ptx::smem_addr(pv_done));
+            ptx::mma_commit(ptx::smem_addr(&ctl->kv_empty[slot]));
+            ptx::mma_commit(ptx::smem_addr(&ctl->pv_done));
+            if (j == n) trace(p, k, kTrMmaLastPV);
             ++kv_it;
           }
         }
@@ -420,30 +676,31 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
         ++q_it;
       }
       // All issued MMAs must finish before tensor memory is released.
-      ptx::mma_commit(ptx::smem_addr(drain_bar));
-      W.drain(ptx::smem_addr(drain_bar), 0);
+      ptx::mma_commit(ptx::smem_addr(&ctl->drain));
+      W.drain(ptx::smem_addr(&ctl->drain), 0);
     }
-  } else if (warp >= 4) {
+    __syncwarp();
+  } else if (warp >= 4 && mode != kModeSkip) {
     // ------------------------------------------- softmax / correction / epilogue
     const int row = threadIdx.x - 128;                       // TMEM lane == tile row
     const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
     const float sl2 = p.scale_log2;
     uint32_t g = 0, pv_it = 0;
-    int wg_target = 0;
-    for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-      const WorkItem w = p.items[it];
-      const int n = (w.kv_len + kBlockN - 1) / kBlockN;
+    for (int k = 0; k < n_my; ++k) {
+      const WorkItem w = item_at(k);
+      const int n = ceil_div(w.kv_len, kBlockN);
       const int rows = w.n_cand * Lq;
       float m = -INFINITY, l = 0.f;
       bool ok = true;
       for (int j = 0; j < n; ++j) {
         const uint32_t gj = g + j;
         const uint32_t sb = gj & 1u;
-        if (!W.warp_wait(ptx::smem_addr(&s_full[sb]), (gj >> 1) & 1u)) {
+        if (!W.warp_wait(ptx::smem_addr(&ctl->s_full[sb]), (gj >> 1) & 1u)) {
           ok = false;
           break;
         }
         ptx::tc_fence_after();
+        if (j == 0 && row == 0) trace(p, k, kTrSmS0);
         const uint32_t scol = tmem + lane_off + C::kSCol + sb * kBlockN;
         uint32_t sr[4][32];
 #pragma unroll
@@ -491,7 +748,7 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
         ptx::tmem_st_wait();
         if (j > 0) {
           // O holds P_0..P_{j-1} V: wait for PV_{j-1}, then rescale if m moved.
-          if (!W.warp_wait(ptx::smem_addr(pv_done), pv_it & 1u)) {
+          if (!W.warp_wait(ptx::smem_addr(&ctl->pv_done), pv_it & 1u)) {
             ok = false;
             break;
           }
@@ -514,70 +771,102 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
         m = m_new;
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&p_full[sb]));
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&ctl->p_full[sb]));
       }
       if (!ok) break;
-      // ---- epilogue: O / l
-      if (!W.warp_wait(ptx::smem_addr(pv_done), pv_it & 1u)) break;
+      if (row == 0) trace(p, k, kTrSmLastP);
+      // ---- epilogue
+      if (!W.warp_wait(ptx::smem_addr(&ctl->pv_done), pv_it & 1u)) break;
       ++pv_it;
       ptx::tc_fence_after();
+      if (row == 0) trace(p, k, kTrEpiO);
       const uint32_t ocol = tmem + lane_off + C::kOCol;
       const bool live = row < rows;
       const int ci = live ? row / Lq : 0;
       const int t = live ? row - ci * Lq : 0;
-      if (w.unit < 0) {
-        const int32_t gpos = w.cand_begin + ci;
-        const int64_t c = live ? (sorted ? gpos : p.perm[gpos]) : 0;
-        uint16_t* dst = p.out + (((c * p.H + w.head) * (int64_t)Lq + t) * D);
-        const float inv = l > 0.f ? 1.f / l : 0.f;
+      if (w.unit == 1) {
+        // pair sender: once the leader's ring is free, write O and (m, l) into it
+        if (!W.warp_wait(ptx::smem_addr(&ctl->pair_go), 0, true)) break;
+        const uint32_t recv = ptx::map_to_cta(ptx::smem_addr(kv_smem), cta_rank ^ 1u);
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t o[32];
           ptx::tmem_ld32(ocol + cc * 32, o);
           ptx::tmem_ld_wait();
           if (live) {
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {
+              const int vec = cc * 8 + q4;                     // 16-byte vector of the row
+              const uint32_t addr = recv + row * (D * 4) + ((vec ^ (row & 7)) * 16);
+              ptx::st_cluster_v4(addr, o[q4 * 4 + 0], o[q4 * 4 + 1], o[q4 * 4 + 2], o[q4 * 4 + 3]);
+            }
+          }
+        }
+        if (live) {
+          const uint32_t mla = ptx::map_to_cta(ptx::smem_addr(&ctl->partner_ml[row]), cta_rank ^ 1u);
+          ptx::st_cluster_v2(mla, __float_as_uint(m), __float_as_uint(l));
+        }
+        __syncwarp();
+        if (lane == 0)
+          ptx::mbar_arrive_cluster(ptx::map_to_cta(ptx::smem_addr(&ctl->pair_recv), cta_rank ^ 1u));
+        if (row == 0) trace(p, k, kTrEpiStored);
+      } else {
+        const int32_t gpos = w.cand_begin + ci;
+        const int64_t cidx = live ? (sorted ? gpos : perm[gpos]) : 0;
+        uint16_t* dst = p.out + (((cidx * p.H + w.head) * (int64_t)Lq + t) * D);
+        float mp = -INFINITY, lp = 0.f;
+        const bool merge = w.unit == 0 && w.unit_first != 0;
+        if (merge) {
+          // pair leader: its ring is drained (all MMAs done): let the sender write
+          if (row == 0)
+            ptx::mbar_arrive_cluster(ptx::map_to_cta(ptx::smem_addr(&ctl->pair_go), cta_rank ^ 1u));
+          if (!W.warp_wait(ptx::smem_addr(&ctl->pair_recv), 0, true)) break;
+          if (row == 0) trace(p, k, kTrArrived);
+          if (live) {
+            const float2 ml = ctl->partner_ml[row];
+            mp = ml.x;
+            lp = ml.y;
+          }
+        }
+        const float M = fmaxf(m, mp);
+        const float a0 = fast_exp2(m - M), a1 = merge ? fast_exp2(mp - M) : 0.f;
+        const float L = a0 * l + a1 * lp;
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        const float w0 = a0 * inv, w1 = a1 * inv;
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          ptx::tmem_ld32(ocol + cc * 32, o);
+          ptx::tmem_ld_wait();
+          if (live) {
+            float x[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(o[e]) * w0;
+            if (merge) {
+#pragma unroll
+              for (int q4 = 0; q4 < 8; ++q4) {
+                const int vec = cc * 8 + q4;
+                const float4 y = *reinterpret_cast<const float4*>(
+                    kv_smem + row * (D * 4) + ((vec ^ (row & 7)) * 16));
+                x[q4 * 4 + 0] += y.x * w1;
+                x[q4 * 4 + 1] += y.y * w1;
+                x[q4 * 4 + 2] += y.z * w1;
+                x[q4 * 4 + 3] += y.w * w1;
+              }
+            }
             uint4* d4 = reinterpret_cast<uint4*>(dst + cc * 32);
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
               uint4 v;
-              v.x = pack_bf16(__uint_as_float(o[q4 * 8 + 0]) * inv, __uint_as_float(o[q4 * 8 + 1]) * inv);
-              v.y = pack_bf16(__uint_as_float(o[q4 * 8 + 2]) * inv, __uint_as_float(o[q4 * 8 + 3]) * inv);
-              v.z = pack_bf16(__uint_as_float(o[q4 * 8 + 4]) * inv, __uint_as_float(o[q4 * 8 + 5]) * inv);
-              v.w = pack_bf16(__uint_as_float(o[q4 * 8 + 6]) * inv, __uint_as_float(o[q4 * 8 + 7]) * inv);
+              v.x = pack_bf16(x[q4 * 8 + 0], x[q4 * 8 + 1]);
+              v.y = pack_bf16(x[q4 * 8 + 2], x[q4 * 8 + 3]);
+              v.z = pack_bf16(x[q4 * 8 + 4], x[q4 * 8 + 5]);
+              v.w = pack_bf16(x[q4 * 8 + 6], x[q4 * 8 + 7]);
               d4[q4] = v;
             }
           }
         }
-      } else {
-        const int64_t slot = (int64_t)it * kTileM + row;
-        float* po = p.partial_o + slot * D;
-#pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t o[32];
-          ptx::tmem_ld32(ocol + cc * 32, o);
-          ptx::tmem_ld_wait();
-          if (live) {
-            float4* d4 = reinterpret_cast<float4*>(po + cc * 32);
-#pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4)
-              __stcg(d4 + q4, make_float4(__uint_as_float(o[q4 * 4 + 0]), __uint_as_float(o[q4 * 4 + 1]),
-                                          __uint_as_float(o[q4 * 4 + 2]), __uint_as_float(o[q4 * 4 + 3])));
-          }
-        }
-        if (live) __stcg(&p.partial_ml[slot], make_float2(m, l));
-        __threadfence();
-        if (!wg_sync(wg_count, wg_target += 4, W)) break;
-        if (row == 0) {
-          const int prev = atomicAdd(&p.units[w.unit].arrived, 1);
-          *s_last = prev == p.units[w.unit].n_split - 1 ? 1 : 0;
-        }
-        if (!wg_sync(wg_count, wg_target += 4, W)) break;
-        const bool last = *s_last != 0;
-        if (!wg_sync(wg_count, wg_target += 4, W)) break;   // s_last may be reused after this
-        if (last) {
-          __threadfence();
-          if (live) merge_row<D>(p, w, row, ci, t, sorted);
-        }
+        if (row == 0) trace(p, k, merge ? kTrMerged : kTrEpiStored);
       }
       g += n;
     }
@@ -585,6 +874,9 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
 
   ptx::tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) trace(p, 0, kTrCtaEnd);
+  // neither CTA of a pair may exit while the other can still touch its memory
+  ptx::cluster_sync();
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, C::kTmemCols);

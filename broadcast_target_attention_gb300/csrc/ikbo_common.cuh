@@ -62,6 +62,7 @@ struct PlanParams {
   int32_t max_items;        // capacity of the work list
   int32_t max_split_items;  // capacity of the split partial buffers
   int32_t max_units;        // capacity of UnitInfo
+  int32_t allow_split;      // 1: split key ranges when units are few (SIMT kernel); 0: never
   // outputs (workspace)
   PlanHeader* header;
   WorkItem* items;
@@ -95,6 +96,37 @@ struct AttnParams {
   uint64_t timeout_ns;      // bound of every wait on another warp or the TMA/MMA units
   int32_t qbox;             // candidates per Q box of the sorted-order tensor map
   int32_t debug_flags;      // test hook: 1 = never arm the Q barrier (exercises the timeout path)
+  uint64_t* trace;          // optional %globaltimer stamps [grid][kTraceItems][kTracePoints], or null
+  // in-kernel planning (tcgen05 kernel, "fused" mode)
+  int32_t fused;            // 1: every CTA plans from the index tensors itself; 0: read `items`
+  int32_t cands_per_tile;
+  const int32_t* user_offsets;
+  const int32_t* cand_to_user;
+  int64_t n_user;
+  WorkItem* cta_items;      // fused: [grid][max_cta_items] this CTA's items
+  int32_t max_cta_items;
+  int32_t* perm_ws;         // fused, unsorted input: grouped position -> candidate
+  CUtensorMap* map_slots;   // fused: [grid][2] K/V tensor maps with the row count set on the device
+};
+
+// In-kernel timeline tracing (ikbo_set_trace): the first kTraceItems items of
+// every CTA record %globaltimer (ns) at these points.
+constexpr int kTraceItems = 4;
+constexpr int kTracePoints = 16;
+enum TracePoint {
+  kTrCtaStart = 0,      // after the prologue (item slot 0 only)
+  kTrProdItem = 1,      // producer starts the item
+  kTrProdIssued = 2,    // producer issued every load of the item
+  kTrMmaQ = 3,          // MMA warp saw the Q tile
+  kTrMmaFirstS = 4,     // first S MMA issued
+  kTrMmaLastPV = 5,     // last PV MMA issued
+  kTrSmS0 = 6,          // softmax saw the first S
+  kTrSmLastP = 7,       // softmax handed over the last P
+  kTrEpiO = 8,          // epilogue: O complete in TMEM
+  kTrEpiStored = 9,     // epilogue: output / partial stored
+  kTrArrived = 10,      // split: arrival counted
+  kTrMerged = 11,       // split: merge done (last arriver)
+  kTrCtaEnd = 12        // before teardown (item slot 0 only)
 };
 
 __device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {

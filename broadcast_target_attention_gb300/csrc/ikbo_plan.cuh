@@ -212,7 +212,7 @@ ikbo_plan_kernel(const __grid_constant__ PlanParams p, const __grid_constant__ P
   __syncthreads();
   const int64_t base_units = s_sum_units;
   int64_t split_tiles = 0;
-  if (base_units > 0 && base_units < 2 * (int64_t)p.num_sms) {
+  if (p.allow_split && base_units > 0 && base_units < 2 * (int64_t)p.num_sms) {
     split_tiles = ceil_div64(s_sum_tiles, p.num_sms);
     if (split_tiles < 1) split_tiles = 1;
   }

@@ -160,6 +160,17 @@ int ikbo_get_timing(float* plan_ms, float* attn_ms);
 int ikbo_set_debug(int flags, uint64_t timeout_ns);
 
 /*
+ * In-kernel timeline tracing, for profiling.  With a non-NULL device buffer
+ * of at least (number of SMs) x 4 x 16 uint64 entries, later calls of the
+ * tcgen05 kernel write %globaltimer stamps (ns) into it: entry
+ * [(cta * 4 + item) * 16 + point] for the first 4 work items of every CTA,
+ * at the points listed in csrc/ikbo_common.cuh (TracePoint).  Entries that
+ * are not reached keep their old contents.  NULL switches tracing off (the
+ * default).  The caller owns the buffer.
+ */
+int ikbo_set_trace(uint64_t* device_buffer);
+
+/*
  * Selects the attention kernel for later calls on this thread: 0 = the
  * tcgen05/TMEM/TMA kernel (default), 1 = the SIMT kernel kept as an
  * independent GPU cross-check.  Returns the previous value.
