@@ -78,22 +78,25 @@ constexpr int kFusedMaxCand = 20480;
 constexpr int kLptMaxUsersFused = 256;
 
 enum TcMode { kModeSkip = -1, kModeListed = 0, kModeIndep = 1, kModePair = 2 };
+constexpr int kCtlItems = 4;
 
 template <int D>
 struct TcConfig {
   static constexpr int kCB = D / 64;                   // 128-byte column blocks per row
   static constexpr int kQBytes = kCB * kTileM * 128;    // one Q tile
   static constexpr int kKVBytes = kCB * kBlockN * 128;  // one K or V tile
-  static constexpr int kSlotsIndep = (kDataBytes - 2 * kQBytes) / kKVBytes;   // 2 Q buffers
-  static constexpr int kSlotsPair = (kDataBytes - kQBytes) / kKVBytes;        // 1 Q buffer
-  static constexpr int kRecvBytes = kTileM * D * 4;     // partner's O, received in the ring
+  // Operand area: two Q buffers, then the K/V ring.  In pair mode only the
+  // first Q buffer is used and both together receive the partner's O.
+  static constexpr int kSlots = (kDataBytes - 2 * kQBytes) / kKVBytes;
+  static constexpr int kRecvBytes = kTileM * D * 4;
   // tensor-memory columns: two S/P buffers and the O accumulator
   static constexpr int kSCol = 0;
   static constexpr int kOCol = 2 * kBlockN;
   static constexpr int kTmemCols = 512;
   static_assert(kOCol + D <= kTmemCols, "TMEM budget");
-  static_assert(kSlotsPair <= kMaxSlots && kSlotsIndep >= 3, "ring size");
-  static_assert(kRecvBytes <= kSlotsPair * kKVBytes, "receive area");
+  static_assert(kSlots <= kMaxSlots && kSlots >= 3, "ring size");
+  static_assert(kRecvBytes == 2 * kQBytes, "receive area = both Q buffers");
+  static_assert(kRecvBytes + 16 * kTileM <= kSlots * kKVBytes, "staging area");
 };
 
 static_assert(kTcSmemBytes <= 232448, "shared memory budget");
@@ -105,7 +108,7 @@ struct TcCtrl {
   uint64_t q_full[2], q_empty[2];
   uint64_t kv_full[kMaxSlots], kv_empty[kMaxSlots];
   uint64_t s_full[2], p_full[2];
-  uint64_t pv_done, drain, pair_go, pair_recv;
+  uint64_t pv_done, drain, pair_go, pair_recv, stage_done;
   uint32_t tmem_base;
   int abort_flag;
   int wg_count;
@@ -113,9 +116,10 @@ struct TcCtrl {
   int n_my_items;
   int sorted;
   int n_slots;
-  int pad;
+  int go_sent;
   int red_i[32];
-  float2 partner_ml[kTileM];
+  WorkItem items[kCtlItems];            // the first items of this CTA (the rest in global memory)
+  alignas(16) float2 partner_ml[kTileM];
 };
 static_assert(sizeof(TcCtrl) <= kCtrlBytes, "control block");
 
@@ -422,9 +426,11 @@ __device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch,
             w.unit = 1;
           }
           mine[0] = w;
+          ctl->items[0] = w;
           count = 1;
         } else if (rank == 0) {
           mine[0] = w;
+          ctl->items[0] = w;
           count = 1;
         }
       }
@@ -440,6 +446,7 @@ __device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch,
       WorkItem w;
       decode(i, w);
       mine[k] = w;
+      if (k < kCtlItems) ctl->items[k] = w;
     }
     if (tid == 0) ctl->n_my_items = count;
   }
@@ -481,7 +488,9 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
     ptx::mbar_init(ptx::smem_addr(&ctl->pv_done), 1);
     ptx::mbar_init(ptx::smem_addr(&ctl->drain), 1);
     ptx::mbar_init(ptx::smem_addr(&ctl->pair_go), 1);
-    ptx::mbar_init(ptx::smem_addr(&ctl->pair_recv), 4);
+    ptx::mbar_init(ptx::smem_addr(&ctl->pair_recv), 1);
+    ptx::mbar_init(ptx::smem_addr(&ctl->stage_done), 4);
+    ctl->go_sent = 0;
     ctl->abort_flag = 0;
     ctl->wg_count = 0;
     ptx::fence_mbar_init();
@@ -506,7 +515,7 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
         n > (int)blockIdx.x ? (n - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
   }
   if (threadIdx.x == 0) {
-    ctl->n_slots = ctl->mode == kModePair ? C::kSlotsPair : C::kSlotsIndep;
+    ctl->n_slots = C::kSlots;
     trace(p, 0, kTrCtaStart);
   }
   ptx::tc_fence_before();
@@ -522,15 +531,15 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
   const int NS = ctl->n_slots;
   const int NQ = mode == kModePair ? 1 : 2;
   uint8_t* q_smem = data;
-  uint8_t* kv_smem = data + NQ * C::kQBytes;
+  uint8_t* kv_smem = data + 2 * C::kQBytes;
   const int32_t* perm = p.fused ? p.perm_ws : p.perm;
   const void* kmap = p.fused ? (const void*)(p.map_slots + 2 * blockIdx.x) : p.kmap;
   const void* vmap = p.fused ? (const void*)(p.map_slots + 2 * blockIdx.x + 1) : p.vmap;
   const Waiter W{&ctl->abort_flag, p.err_word, p.timeout_ns};
   const int Lq = p.Lq;
   auto item_at = [&](int k) -> WorkItem {
-    return p.fused ? p.cta_items[(size_t)blockIdx.x * p.max_cta_items + k]
-                   : p.items[blockIdx.x + (size_t)k * gridDim.x];
+    if (p.fused) return k < kCtlItems ? ctl->items[k] : p.cta_items[(size_t)blockIdx.x * p.max_cta_items + k];
+    return p.items[blockIdx.x + (size_t)k * gridDim.x];
   };
 
   if (warp == 0) {
@@ -587,6 +596,16 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
           if (ok && j >= 1) ok = load_tile(vmap, w.head, w.kv_begin + (j - 1) * kBlockN);
         }
         trace(p, k, kTrProdIssued);
+        if (ok && w.unit == 0 && w.unit_first) {
+          // pair leader: once the last S has read Q, both Q buffers can receive
+          // the partner's O and (m, l); tell the partner so
+          if (!W.wait(ptx::smem_addr(&ctl->q_empty[0]), 0)) break;
+          const int rows = w.n_cand * Lq;
+          const uint32_t bytes = uint32_t(rows * D * 4 + ((rows + 1) & ~1) * 8);
+          ptx::mbar_arrive_expect_tx(ptx::smem_addr(&ctl->pair_recv), bytes);
+          ctl->go_sent = 1;
+          ptx::mbar_arrive_cluster(ptx::map_to_cta(ptx::smem_addr(&ctl->pair_go), cta_rank ^ 1u));
+        }
       }
       // Drain: every armed barrier phase must complete before the CTA exits.
       for (uint32_t s = 0; s < (uint32_t)NS && s < kv_it; ++s) {
@@ -709,23 +728,29 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
         const int valid = min(kBlockN, w.kv_len - j * kBlockN);
         // row maximum of the scaled scores (of the raw minimum when scale < 0)
         const float sgn = sl2 < 0.f ? -1.f : 1.f;
-        float mx = -INFINITY;
+        float mxv[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mxv[e] = -INFINITY;
         if (valid == kBlockN) {
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
-            for (int e = 0; e < 32; ++e) mx = fmaxf(mx, sgn * __uint_as_float(sr[c][e]));
+            for (int e = 0; e < 32; ++e) mxv[e & 7] = fmaxf(mxv[e & 7], sgn * __uint_as_float(sr[c][e]));
         } else {
 #pragma unroll
           for (int c = 0; c < 4; ++c)
 #pragma unroll
             for (int e = 0; e < 32; ++e)
-              if (c * 32 + e < valid) mx = fmaxf(mx, sgn * __uint_as_float(sr[c][e]));
+              if (c * 32 + e < valid) mxv[e & 7] = fmaxf(mxv[e & 7], sgn * __uint_as_float(sr[c][e]));
         }
+        float mx = fmaxf(fmaxf(fmaxf(mxv[0], mxv[1]), fmaxf(mxv[2], mxv[3])),
+                         fmaxf(fmaxf(mxv[4], mxv[5]), fmaxf(mxv[6], mxv[7])));
         mx *= sgn * sl2;
         const float m_new = (m == -INFINITY || mx > m + kLazyRescale) ? fmaxf(m, mx) : m;
         const float alpha = fast_exp2(m - m_new);   // 0 on the first tile, 1 when m stays
-        float sum = 0.f;
+        float sumv[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) sumv[e] = 0.f;
         uint32_t pk[2][32];
 #pragma unroll
         for (int c = 0; c < 4; ++c)
@@ -738,9 +763,11 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
               p0 = col < valid ? p0 : 0.f;
               p1 = col + 1 < valid ? p1 : 0.f;
             }
-            sum += p0 + p1;
+            sumv[(e >> 1) & 7] += p0 + p1;
             pk[c >> 1][(c & 1) * 16 + (e >> 1)] = pack_bf16(p0, p1);
           }
+        const float sum = ((sumv[0] + sumv[1]) + (sumv[2] + sumv[3])) +
+                          ((sumv[4] + sumv[5]) + (sumv[6] + sumv[7]));
         l = l * alpha + sum;
         // P (bf16 pairs) overwrites the first half of this S buffer.
         ptx::tmem_st32(scol, pk[0]);
@@ -785,9 +812,10 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
       const int ci = live ? row / Lq : 0;
       const int t = live ? row - ci * Lq : 0;
       if (w.unit == 1) {
-        // pair sender: once the leader's ring is free, write O and (m, l) into it
-        if (!W.warp_wait(ptx::smem_addr(&ctl->pair_go), 0, true)) break;
-        const uint32_t recv = ptx::map_to_cta(ptx::smem_addr(kv_smem), cta_rank ^ 1u);
+        // pair sender: stage O (swizzled rows) and (m, l) in this CTA's ring,
+        // which no MMA reads any more, then one bulk copy into the leader
+        uint8_t* stage = kv_smem;
+        float2* stage_ml = reinterpret_cast<float2*>(kv_smem + C::kRecvBytes);
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t o[32];
@@ -797,19 +825,28 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
 #pragma unroll
             for (int q4 = 0; q4 < 8; ++q4) {
               const int vec = cc * 8 + q4;                     // 16-byte vector of the row
-              const uint32_t addr = recv + row * (D * 4) + ((vec ^ (row & 7)) * 16);
-              ptx::st_cluster_v4(addr, o[q4 * 4 + 0], o[q4 * 4 + 1], o[q4 * 4 + 2], o[q4 * 4 + 3]);
+              *reinterpret_cast<uint4*>(stage + row * (D * 4) + ((vec ^ (row & 7)) * 16)) =
+                  make_uint4(o[q4 * 4 + 0], o[q4 * 4 + 1], o[q4 * 4 + 2], o[q4 * 4 + 3]);
             }
           }
         }
-        if (live) {
-          const uint32_t mla = ptx::map_to_cta(ptx::smem_addr(&ctl->partner_ml[row]), cta_rank ^ 1u);
-          ptx::st_cluster_v2(mla, __float_as_uint(m), __float_as_uint(l));
+        if (live) stage_ml[row] = make_float2(m, l);
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&ctl->stage_done));
+        if (row == 0) {
+          if (W.wait(ptx::smem_addr(&ctl->stage_done), 0) &&
+              W.wait(ptx::smem_addr(&ctl->pair_go), 0, true)) {
+            const uint32_t peer = cta_rank ^ 1u;
+            const uint32_t rbar = ptx::map_to_cta(ptx::smem_addr(&ctl->pair_recv), peer);
+            ptx::bulk_copy_to_cta(ptx::map_to_cta(ptx::smem_addr(data), peer), ptx::smem_addr(stage),
+                                  uint32_t(rows * D * 4), rbar);
+            ptx::bulk_copy_to_cta(ptx::map_to_cta(ptx::smem_addr(ctl->partner_ml), peer),
+                                  ptx::smem_addr(stage_ml), uint32_t(((rows + 1) & ~1) * 8), rbar);
+            trace(p, k, kTrEpiStored);
+          }
         }
         __syncwarp();
-        if (lane == 0)
-          ptx::mbar_arrive_cluster(ptx::map_to_cta(ptx::smem_addr(&ctl->pair_recv), cta_rank ^ 1u));
-        if (row == 0) trace(p, k, kTrEpiStored);
       } else {
         const int32_t gpos = w.cand_begin + ci;
         const int64_t cidx = live ? (sorted ? gpos : perm[gpos]) : 0;
@@ -817,9 +854,7 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
         float mp = -INFINITY, lp = 0.f;
         const bool merge = w.unit == 0 && w.unit_first != 0;
         if (merge) {
-          // pair leader: its ring is drained (all MMAs done): let the sender write
-          if (row == 0)
-            ptx::mbar_arrive_cluster(ptx::map_to_cta(ptx::smem_addr(&ctl->pair_go), cta_rank ^ 1u));
+          // pair leader: the partner's O and (m, l) arrive in the Q buffers
           if (!W.warp_wait(ptx::smem_addr(&ctl->pair_recv), 0, true)) break;
           if (row == 0) trace(p, k, kTrArrived);
           if (live) {
@@ -847,7 +882,7 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
               for (int q4 = 0; q4 < 8; ++q4) {
                 const int vec = cc * 8 + q4;
                 const float4 y = *reinterpret_cast<const float4*>(
-                    kv_smem + row * (D * 4) + ((vec ^ (row & 7)) * 16));
+                    data + row * (D * 4) + ((vec ^ (row & 7)) * 16));
                 x[q4 * 4 + 0] += y.x * w1;
                 x[q4 * 4 + 1] += y.y * w1;
                 x[q4 * 4 + 2] += y.z * w1;
@@ -874,7 +909,11 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
 
   ptx::tc_fence_before();
   __syncthreads();
+  // a leader that invited its partner's copy waits for it (bounded) before
+  // its shared memory can go away, even if it gave up on the merge
+  if (threadIdx.x == 0 && ctl->go_sent) W.drain(ptx::smem_addr(&ctl->pair_recv), 0);
   if (threadIdx.x == 0) trace(p, 0, kTrCtaEnd);
+  __syncwarp();
   // neither CTA of a pair may exit while the other can still touch its memory
   ptx::cluster_sync();
   if (warp == 1) {

@@ -101,7 +101,7 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t remote_bar) {
 
 __device__ __forceinline__ uint64_t globaltimer() {
   uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t)::"memory");
   return t;
 }
 
@@ -123,6 +123,23 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* map, uint3
       " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
       "l"(map), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
       : "memory");
+}
+
+// Bulk copy (no tensor map) from this CTA's shared memory into the shared
+// memory of another CTA of the cluster; completes `bytes` on the mbarrier
+// `remote_bar` (a shared::cluster address in the destination CTA).  Both
+// addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_copy_to_cta(uint32_t remote_dst, uint32_t local_src,
+                                                 uint32_t bytes, uint32_t remote_bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(remote_dst), "r"(local_src), "r"(bytes), "r"(remote_bar)
+      : "memory");
+}
+
+// Generic-proxy writes to shared memory become visible to the async proxy.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const void* map) {
