@@ -33,6 +33,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from broadcast_target_attention_gb300 import accounting as A  # noqa: E402
+from broadcast_target_attention_gb300 import replicas as R  # noqa: E402
 from broadcast_target_attention_gb300 import workloads as W  # noqa: E402
 
 METRIC = "IKBO target-attn BF16 TFLOP/s & candidates/s (1024 cand/15 users); % of peak"
@@ -49,18 +50,8 @@ def peaks():
     return dict(FALLBACK_PEAKS)
 
 
-def dist_env():
-    ws = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return ws, rank, local
-
-
 def workload_for_rank(name: str, rank: int):
-    cfg = W.CONFIGS[name]
-    if rank:
-        cfg = W.Config(**{**cfg.__dict__, "seed": cfg.seed + 1000 * rank})
-    return W.generate(cfg)
+    return W.generate(R.rank_config(name, rank))
 
 
 def config_block(wl, extra=None):
@@ -131,6 +122,19 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
+# the files the tcgen05 attention kernel is compiled from
+KERNEL_SOURCES = ("ikbo_attn_tc.cuh", "ikbo_common.cuh", "ikbo_ptx.cuh")
+
+
+def kernel_source_sha256() -> str:
+    src = os.path.join(ROOT, "broadcast_target_attention_gb300", "csrc")
+    h = hashlib.sha256()
+    for fn in KERNEL_SOURCES:
+        with open(os.path.join(src, fn), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def kernel_traffic(kernel_name: str, workload: str):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
     the current kernel source; else None."""
@@ -142,19 +146,14 @@ def kernel_traffic(kernel_name: str, workload: str):
     e = d.get(kernel_name, {}).get(workload)
     if not e:
         return None
-    src = os.path.join(ROOT, "broadcast_target_attention_gb300", "csrc")
-    h = hashlib.sha256()
-    for fn in sorted(os.listdir(src)):
-        with open(os.path.join(src, fn), "rb") as f:
-            h.update(f.read())
-    if e.get("source_sha256") != h.hexdigest():
+    if e.get("source_sha256") != kernel_source_sha256():
         return None
     return float(e["dram_bytes_per_launch"])
 
 
 def run_reference(args):
     """The oracle, as it stands, on the host cores: bounded samples of the workload."""
-    ws, rank, _ = dist_env()
+    ws, rank, _ = R.dist_env()
     if rank != 0:
         return
     import oracle
@@ -228,7 +227,7 @@ def run_ikbo(args):
 
     import broadcast_target_attention_gb300 as ikbo
 
-    ws, rank, local = dist_env()
+    ws, rank, local = R.dist_env()
     if ws > 1:
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     torch.cuda.set_device(local)
@@ -310,13 +309,9 @@ def run_ikbo(args):
     assert ikbo.get_device_error() == 0
     clocks = clk.summary()
 
-    ms = statistics.mean(step_ms)
-    if ws > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = R.max_over_ranks(statistics.mean(step_ms), dev)
     total_flops = flops * ws
-    value = total_flops / (ms * 1e-3) / 1e12
+    value = R.job_throughput(flops, ws, ms) / 1e12
     pk = peaks()
     attn = statistics.mean(attn_ms)
     achieved_gbs = alg_bytes / (attn * 1e-3) / 1e9
@@ -336,14 +331,14 @@ def run_ikbo(args):
                 "peak_source": pk["source"] + " (burst cuBLAS bf16)"}
     qb = wl.q.nbytes
     h2d = qb + wl.k.nbytes + wl.v.nbytes + wl.user_offsets.nbytes + wl.cand_to_user.nbytes
-    e2e = statistics.mean(e2e_ms)
+    e2e = R.max_over_ranks(statistics.mean(e2e_ms), dev)
     bc = statistics.mean(bc_ms)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": config_block(wl, {"parallelism": f"{ws} independent replica(s), users sharded, no exchange"}),
-        "candidates_per_s": wl.n_cand * ws / (ms * 1e-3),
+        "candidates_per_s": R.job_throughput(wl.n_cand, ws, ms),
         "pct_of_peak": {"bf16_tensor": value / ws / pk["bf16_tflops"],
                         "hbm_roofline_attn_kernel": achieved_gbs / pk["hbm_gbs"]},
         "kernel_ms": {"plan": statistics.mean(plan_ms), "attn": attn,
@@ -354,7 +349,7 @@ def run_ikbo(args):
         "broadcast_path": {"ms_per_step": bc, "value": flops / (bc * 1e-3) / 1e12, "unit": "TFLOP/s",
                            "ikbo_speedup": bc / ms,
                            "extra_bytes": nums["broadcast_extra_bytes"]},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": ikbo.launches_per_call(wl.n_cand, wl.n_user) * args.steps,
         "clocks": clocks,
     }
     if rank == 0:

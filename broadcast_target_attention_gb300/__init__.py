@@ -18,7 +18,7 @@ from . import _lib
 from ._lib import STATUS
 
 __all__ = ["attn_fwd", "broadcast_attn_fwd", "attn_fwd_host", "attn_fwd_noalloc", "get_device_error", "set_timing",
-           "get_timing", "set_kernel", "set_debug", "version", "load", "IkboError", "STATUS"]
+           "get_timing", "set_kernel", "set_debug", "launches_per_call", "version", "load", "IkboError", "STATUS"]
 
 
 class IkboError(RuntimeError):
@@ -177,6 +177,13 @@ def get_timing() -> Tuple[float, float]:
 def set_kernel(which: int) -> int:
     """0 = tcgen05 kernel (default), 1 = SIMT cross-check kernel; returns the previous choice."""
     return int(_lib.lib().ikbo_set_kernel(int(which)))
+
+
+def launches_per_call(n_cand: int, n_user: int) -> int:
+    """Kernel launches one attn_fwd call makes for this batch size (host arithmetic only)."""
+    n = int(_lib.lib().ikbo_launches_per_call(int(n_cand), int(n_user)))
+    _check(min(n, 0), "launches_per_call")
+    return n
 
 
 def set_debug(flags: int = 0, timeout_ns: int = 0) -> None:

@@ -36,6 +36,7 @@ SIGNATURES = {
     "ikbo_set_debug": (ctypes.c_int, [ctypes.c_int, ctypes.c_uint64]),
     "ikbo_set_kernel": (ctypes.c_int, [ctypes.c_int]),
     "ikbo_set_trace": (ctypes.c_int, [_P]),
+    "ikbo_launches_per_call": (ctypes.c_int, [_I64, _I64]),
     "ikbo_attn_fwd_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I32, _I32, _I32, _F,
                                               _P, _P]),
 }

@@ -154,6 +154,7 @@ Workspace plan_workspace(int64_t n_cand, int64_t n_user, int H, int Lq, int D, i
   const int64_t units_bound =
       int64_t(H) * ((n_cand + cpt - 1) / cpt + (n_user < n_cand ? n_user : n_cand));
   w.grid = grid;
+  // keep in step with ikbo_launches_per_call
   w.fused = kernel == 0 && n_cand <= kFusedMaxCand && n_user <= kFusedMaxUser;
   w.max_items = int(num_sms + units_bound);
   w.max_split_items = kernel == 1 ? 3 * num_sms : 0;
@@ -698,6 +699,12 @@ int ikbo_set_kernel(int which) {
   const int prev = t_kernel;
   t_kernel = which == 1 ? 1 : 0;
   return prev;
+}
+
+int ikbo_launches_per_call(int64_t n_cand, int64_t n_user) {
+  if (n_cand < 0 || n_user < 0) return IKBO_ERR_SHAPE;
+  if (n_cand == 0) return 0;
+  return (t_kernel == 0 && n_cand <= kFusedMaxCand && n_user <= kFusedMaxUser) ? 1 : 2;
 }
 
 }  // extern "C"

@@ -178,6 +178,17 @@ int ikbo_set_trace(uint64_t* device_buffer);
 int ikbo_set_kernel(int which);
 
 /*
+ * Number of kernel launches that ikbo_attn_fwd (and ikbo_attn_fwd_host,
+ * ikbo_attn_fwd_noalloc) makes for a batch of n_cand candidates over n_user
+ * users with the current kernel choice of this thread: 0 for an empty batch,
+ * 1 when the tcgen05 kernel plans in-kernel (n_cand <= 20480 and
+ * n_user <= 1024), else 2 (a planning kernel, then the attention kernel).
+ * Host arithmetic only: it touches no GPU.  Negative sizes return
+ * IKBO_ERR_SHAPE.
+ */
+int ikbo_launches_per_call(int64_t n_cand, int64_t n_user);
+
+/*
  * ikbo_attn_fwd without any memory allocation.  (The IKBO pages have no
  * counterpart to this entry point; it exists for deployment.)
  *

@@ -45,6 +45,20 @@ def test_version_and_strerror(lib):
     assert lib.ikbo_strerror(12345) == b"unknown status"
 
 
+def test_launches_per_call(lib):
+    assert lib.ikbo_launches_per_call(0, 5) == 0
+    assert lib.ikbo_launches_per_call(1024, 15) == 1         # planning fused into the kernel
+    assert lib.ikbo_launches_per_call(20480, 1024) == 1
+    assert lib.ikbo_launches_per_call(20481, 15) == 2        # separate planning launch
+    assert lib.ikbo_launches_per_call(1024, 1025) == 2
+    assert lib.ikbo_launches_per_call(-1, 2) == _lib.IKBO_ERR_SHAPE
+    prev = lib.ikbo_set_kernel(1)
+    try:
+        assert lib.ikbo_launches_per_call(1024, 15) == 2     # SIMT kernel: always planned apart
+    finally:
+        lib.ikbo_set_kernel(prev)
+
+
 A = 1 << 20   # a fake, 16-byte aligned "device" address; never dereferenced
 
 
