@@ -187,10 +187,16 @@ Workspace plan_workspace(int64_t n_cand, int64_t n_user, int H, int Lq, int D, i
   return w;
 }
 
-int encode_kv_map(CUtensorMap* m, const void* base, int H, int D, int block_n) {
-  // 2-D view of k (or v): rows = tokens, columns = H * D; the row count is a
-  // placeholder that the planner replaces with T on the device.
-  cuuint64_t dims[2] = {cuuint64_t(H) * D, cuuint64_t(block_n)};
+// Row count of the K/V maps that the tcgen05 kernel loads through directly
+// when it plans in-kernel: open, since T is only known on the device.  Every
+// tile it loads this way lies inside rows [0, T); a tile that reaches past T
+// goes through a device-side copy with the row count set to T.
+constexpr cuuint64_t kOpenRows = 0x7fffffff;
+
+int encode_kv_map(CUtensorMap* m, const void* base, int H, int D, int block_n, cuuint64_t rows) {
+  // 2-D view of k (or v): rows = tokens, columns = H * D.  `rows` is either
+  // open (above) or a placeholder that the planning kernel replaces with T.
+  cuuint64_t dims[2] = {cuuint64_t(H) * D, rows};
   cuuint64_t strides[1] = {cuuint64_t(H) * D * 2};
   cuuint32_t box[2] = {64, cuuint32_t(block_n)};
   cuuint32_t estr[2] = {1, 1};
@@ -325,8 +331,9 @@ int run_ikbo(DeviceState* ds, const void* q, const void* k, const void* v, const
   std::memset(&qmap, 0, sizeof qmap);
   std::memset(&qmap1, 0, sizeof qmap1);
   if (kernel == 0) {
-    if (encode_kv_map(&px.kmap_tmpl, k, H, D, kBlockN) != IKBO_OK ||
-        encode_kv_map(&px.vmap_tmpl, v, H, D, kBlockN) != IKBO_OK ||
+    const cuuint64_t rows = L.fused ? kOpenRows : cuuint64_t(kBlockN);
+    if (encode_kv_map(&px.kmap_tmpl, k, H, D, kBlockN, rows) != IKBO_OK ||
+        encode_kv_map(&px.vmap_tmpl, v, H, D, kBlockN, rows) != IKBO_OK ||
         encode_q_map(&qmap, q, n_cand, H, Lq, D, qbox_cands(Lq)) != IKBO_OK ||
         encode_q_map(&qmap1, q, n_cand, H, Lq, D, 1) != IKBO_OK)
       return IKBO_ERR_CUDA;
@@ -640,6 +647,7 @@ int ikbo_get_device_error(ikbo_stream_t stream) {
   if (word & kErrIndex) return IKBO_ERR_INDEX;
   if (word & kErrOffsets) return IKBO_ERR_OFFSETS;
   if (word & kErrTimeout) return IKBO_ERR_TIMEOUT;
+  if (word & kErrLayout) return IKBO_ERR_CUDA;
   return IKBO_OK;
 }
 

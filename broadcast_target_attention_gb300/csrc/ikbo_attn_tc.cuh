@@ -19,15 +19,21 @@
 //
 // Planning.  For inputs of moderate size every CTA plans in its prologue,
 // from the index tensors, with its shared memory as scratch: it validates
-// cand_to_user and user_offsets, groups candidates by user (a stable counting
-// sort when the map is unsorted), orders users longest first and derives its
-// own work items, so the whole forward is ONE launch.  Larger inputs use the
-// separate planning kernel's work list.  Items are handed to CTAs in
-// boustrophedon order over the longest-first list ("Optimizing Jagged Flash
-// Attention with TLX", §2.2: tiles sorted by K/V work, even passes left to
-// right, odd passes right to left); the items of one (user, head) are
-// adjacent so CTAs sharing a user's K/V run together ("In-Kernel Broadcast
-// Optimization", §3.1, Table 1).
+// cand_to_user and user_offsets, groups candidates by user (in the same pass
+// for a sorted map, by a stable counting sort otherwise) and derives its own
+// work items, so the whole forward is ONE launch.  Larger inputs use the
+// separate planning kernel's work list.  When there are more units than
+// clusters, items are handed to CTAs in boustrophedon order over the users
+// sorted longest first ("Optimizing Jagged Flash Attention with TLX", §2.2:
+// tiles sorted by K/V work, even passes left to right, odd passes right to
+// left); the items of one (user, head) are adjacent so CTAs sharing a user's
+// K/V run together ("In-Kernel Broadcast Optimization", §3.1, Table 1).
+//
+// K/V are read through tensor maps whose row count is left open, because T
+// is only known on the device; the one tile that may reach past row T (the
+// tail of the last user) goes through a copy of the map with the row count
+// set to T, made by the producer when it first needs it, so the TMA
+// zero-fills the missing rows.
 //
 // Pair mode.  When there are no more (user, head, query tile) units than
 // clusters, the two CTAs of a cluster split one unit's keys in half.  The
@@ -36,7 +42,7 @@
 // "Chapter 4", §4.6.4 (Flash-Decoding): M = max(m0, m1),
 // out = (2^(m0-M) O0 + 2^(m1-M) O1) / (2^(m0-M) l0 + 2^(m1-M) l1).
 //
-// Warp roles (256 threads), after the Blackwell design of "Optimizing Jagged
+// Warp roles (384 threads), after the Blackwell design of "Optimizing Jagged
 // Flash Attention with TLX", §2.1 (dedicated load, MMA and softmax warps;
 // explicit SMEM/TMEM buffers; S/P sharing one TMEM buffer, the PV
 // accumulator its own; persistent CTAs):
@@ -44,10 +50,13 @@
 //               ring of shared-memory slots;
 //   warp 1      TMEM allocator and single-thread tcgen05.mma issuer:
 //               S_j = Q K_j^T (SS form) into one of two S buffers, then
-//               O += P_{j-1} V_{j-1} (TS form, P read from TMEM), so S_j
-//               overlaps the softmax of tile j-1;
-//   warps 4-7   softmax, O correction and epilogue; thread i owns TMEM lane
-//               (= query row) i.
+//               O += P_{j-1} V_{j-1} (TS form, P read from TMEM, one MMA of
+//               N = D per 16 keys), so S_j overlaps the softmax of tile j-1;
+//   warps 4-11  softmax, O correction and epilogue.  Query row r lives in TMEM
+//               lane r; warps 4-7 take key columns 0-63 of every tile and
+//               output columns 0..D/2-1, warps 8-11 the other halves, so each
+//               row is worked on by two threads that agree on its running
+//               maximum through shared memory once per tile.
 // Every wait is bounded: a wait that runs out sets the device error word,
 // raises an abort flag that ends all roles, and the CTA drains its
 // outstanding copies and MMAs before freeing tensor memory.
@@ -60,25 +69,33 @@
 
 namespace ikbo {
 
+
 constexpr int kBlockN = 128;      // keys per K/V tile
-constexpr int kTcThreads = 256;
+constexpr int kTcThreads = 384;
+constexpr int kSoftmaxWarp0 = 4;  // warps 4..11 run the softmax
 // The running maximum is moved only when a tile's maximum exceeds it by more
 // than this (base-2 units), so un-normalised weights stay <= 2^8 and the
 // O correction is skipped on most tiles; the final O / l is exact either way.
 constexpr float kLazyRescale = 8.0f;
-constexpr int kDataBytes = 229376;   // 224 KB: operands (and planning scratch in the prologue)
-constexpr int kCtrlBytes = 2048;     // barriers, flags, plan results, partner (m, l)
-constexpr int kTcSmemBytes = kCtrlBytes + 1024 + kDataBytes;   // = 227 KB, the per-CTA maximum
-constexpr int kMaxSlots = 14;
+// Dynamic shared memory: the operand area first (1 KB aligned: 128-byte
+// swizzle atoms), the control block after it; 227 KB, the per-CTA maximum.
+constexpr int kDataBytes = 229376;
+constexpr int kCtrlBytes = 3072;
+constexpr int kTcSmemBytes = kDataBytes + kCtrlBytes;
+constexpr int kMaxSlots = 11;
 // In-kernel planning keeps off/cand_start/order/prefix (n_user), the per-warp
-// counters of the counting sort (8 x n_user) and cand_to_user/perm (n_cand)
-// in the operand area.
+// counters of the counting sort (kSortWarps x n_user) and cand_to_user/perm
+// (n_cand) in the operand area.
 constexpr int kFusedMaxUser = 1024;
 constexpr int kFusedMaxCand = 20480;
 constexpr int kLptMaxUsersFused = 256;
+constexpr int kSortWarps = 8;
+// Sorted grouping fills cand_start while validating; gaps between
+// consecutive users wider than this are filled in a second pass.
+constexpr int kSmallGap = 64;
 
 enum TcMode { kModeSkip = -1, kModeListed = 0, kModeIndep = 1, kModePair = 2 };
-constexpr int kCtlItems = 4;
+constexpr int kCtlItems = 2;
 
 template <int D>
 struct TcConfig {
@@ -87,39 +104,45 @@ struct TcConfig {
   static constexpr int kKVBytes = kCB * kBlockN * 128;  // one K or V tile
   // Operand area: two Q buffers, then the K/V ring.  In pair mode only the
   // first Q buffer is used and both together receive the partner's O.
-  static constexpr int kSlots = (kDataBytes - 2 * kQBytes) / kKVBytes;
+  static constexpr int kFit = (kDataBytes - 2 * kQBytes) / kKVBytes;
+  static constexpr int kSlots = kFit < kMaxSlots ? kFit : kMaxSlots;
   static constexpr int kRecvBytes = kTileM * D * 4;
+  static constexpr int kHalf = D / 2;                   // output columns per softmax thread
+  static constexpr int kChunks = kHalf / 32;            // 32-column TMEM loads per half row
   // tensor-memory columns: two S/P buffers and the O accumulator
   static constexpr int kSCol = 0;
   static constexpr int kOCol = 2 * kBlockN;
   static constexpr int kTmemCols = 512;
   static_assert(kOCol + D <= kTmemCols, "TMEM budget");
-  static_assert(kSlots <= kMaxSlots && kSlots >= 3, "ring size");
+  static_assert(kSlots >= 3, "ring size");
   static_assert(kRecvBytes == 2 * kQBytes, "receive area = both Q buffers");
-  static_assert(kRecvBytes + 16 * kTileM <= kSlots * kKVBytes, "staging area");
+  static_assert(kRecvBytes + 4 * kTileM <= kSlots * kKVBytes, "staging area");
 };
 
 static_assert(kTcSmemBytes <= 232448, "shared memory budget");
-static_assert(4 * (4 * (kFusedMaxUser + 1) + 8 * kFusedMaxUser + 2 * kFusedMaxCand) <= kDataBytes,
+static_assert(4 * (4 * (kFusedMaxUser + 1) + kSortWarps * kFusedMaxUser + 2 * kFusedMaxCand) <=
+                  kDataBytes,
               "planning scratch");
 
-// Control block at the start of dynamic shared memory.
+// Control block, after the operand area.
 struct TcCtrl {
   uint64_t q_full[2], q_empty[2];
   uint64_t kv_full[kMaxSlots], kv_empty[kMaxSlots];
   uint64_t s_full[2], p_full[2];
   uint64_t pv_done, drain, pair_go, pair_recv, stage_done;
+  uint64_t xbar[4][2];                  // row-maximum / row-sum exchange, [row quarter][parity]
   uint32_t tmem_base;
   int abort_flag;
-  int wg_count;
   int mode;
   int n_my_items;
   int sorted;
-  int n_slots;
   int go_sent;
-  int red_i[32];
+  int total_keys;
+  int flags;
+  int red[12];
   WorkItem items[kCtlItems];            // the first items of this CTA (the rest in global memory)
-  alignas(16) float2 partner_ml[kTileM];
+  alignas(16) float partner_lse[kTileM];
+  float xchg[2][2][kTileM];             // [parity][half][row]
 };
 static_assert(sizeof(TcCtrl) <= kCtrlBytes, "control block");
 
@@ -181,6 +204,11 @@ __device__ __forceinline__ void trace(const AttnParams& p, int ord, int point) {
     p.trace[(size_t(blockIdx.x) * kTraceItems + ord) * kTracePoints + point] = ptx::globaltimer();
 }
 
+// Prologue timeline (debug_flags bit 4): item slot 3, points 0..10.
+__device__ __forceinline__ void trace_pro(const AttnParams& p, int point) {
+  if ((p.debug_flags & 4) && threadIdx.x == 0) trace(p, 3, point);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -206,7 +234,7 @@ __device__ __forceinline__ int block_scan_excl(int x, int* red, int* total) {
       const int y = __shfl_up_sync(0xffffffffu, w, o);
       if (lane >= o) w += y;
     }
-    red[lane] = w;
+    if (lane < nw) red[lane] = w;
   }
   __syncthreads();
   const int pre = warp == 0 ? 0 : red[warp - 1];
@@ -216,84 +244,114 @@ __device__ __forceinline__ int block_scan_excl(int x, int* red, int* total) {
 }
 
 // ---------------------------------------------------------------------------
-// In-kernel planning.  All threads of the CTA; `scratch` is the operand area.
-// Every CTA computes the same plan (the inputs are small) and keeps only its
-// own items.  The K/V tensor maps get their row count T here, in a per-CTA
-// slot in global memory.
+// In-kernel planning.  All threads of the CTA; `scratch` is the operand area,
+// already holding user_offsets and cand_to_user (plan_load).  Every CTA
+// computes the same plan (the inputs are small) and keeps only its own items.
+// Few phases, few barriers: on a kernel that runs for microseconds every
+// phase costs a barrier and fresh instruction fetches.
 // ---------------------------------------------------------------------------
-__device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch,
-                            const CUtensorMap& kt, const CUtensorMap& vt, int D) {
+struct PlanScratch {
+  int32_t *off, *cs, *order, *ubefore, *wcnt, *c2u, *perm;
+  __device__ PlanScratch(uint8_t* base, int n_user, int n_cand) {
+    off = reinterpret_cast<int32_t*>(base);   // n_user + 1
+    cs = off + (n_user + 1);                  // cand_start, n_user + 1
+    order = cs + (n_user + 1);                // n_user
+    ubefore = order + n_user;                 // n_user + 1
+    wcnt = ubefore + (n_user + 1);            // kSortWarps x n_user (unsorted only)
+    c2u = wcnt + kSortWarps * n_user;         // n_cand
+    perm = c2u + n_cand;                      // n_cand
+  }
+};
+
+__device__ __forceinline__ void plan_load(const AttnParams& p, uint8_t* scratch) {
+  const int n_cand = (int)p.n_cand, n_user = (int)p.n_user;
+  PlanScratch S(scratch, n_user, n_cand);
+  for (int u = threadIdx.x; u <= n_user; u += blockDim.x) S.off[u] = p.user_offsets[u];
+  for (int c = threadIdx.x; c < n_cand; c += blockDim.x) S.c2u[c] = p.cand_to_user[c];
+}
+
+__device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch, int D) {
   const int tid = threadIdx.x, nt = blockDim.x;
   const int grid = gridDim.x, b = blockIdx.x;
   const int n_cand = (int)p.n_cand, n_user = (int)p.n_user;
-  int32_t* off = reinterpret_cast<int32_t*>(scratch);   // n_user + 1
-  int32_t* cs = off + (n_user + 1);                     // cand_start, n_user + 1
-  int32_t* order = cs + (n_user + 1);                   // n_user
-  int32_t* ubefore = order + n_user;                    // n_user + 1
-  int32_t* wcnt = ubefore + (n_user + 1);               // 8 x n_user (unsorted only)
-  int32_t* c2u = wcnt + 8 * n_user;                     // n_cand
-  int32_t* perm = c2u + n_cand;                         // n_cand
+  PlanScratch S(scratch, n_user, n_cand);
+  int32_t* const off = S.off;
+  int32_t* const cs = S.cs;
+  int32_t* const order = S.order;
+  int32_t* const ubefore = S.ubefore;
+  int32_t* const c2u = S.c2u;
 
-  for (int u = tid; u <= n_user; u += nt) off[u] = p.user_offsets[u];
-  for (int c = tid; c < n_cand; c += nt) c2u[c] = p.cand_to_user[c];
-  __syncthreads();
-  // K/V tensor maps: row count T, into this CTA's global slots
-  if (tid == 0) {
-    const int T = off[n_user];
-    const int rows = T > 0 ? T : 1;
-#pragma unroll
-    for (int mi = 0; mi < 2; ++mi) {
-      CUtensorMap* dst = p.map_slots + 2 * b + mi;
-      const uint4* s4 = reinterpret_cast<const uint4*>(mi == 0 ? &kt : &vt);
-      uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-      for (int i = 0; i < (int)(sizeof(CUtensorMap) / 16); ++i) d4[i] = s4[i];
-      asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 1, %1;" ::"l"(dst),
-                   "r"(rows)
-                   : "memory");
-    }
-    asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
+  // One pass: validation, sortedness, empty sequences, and for sorted input
+  // the first candidate of every user (users prev+1 .. x start at c).
+  constexpr int kBadOff = 1, kBadIdx = 2, kUnsorted = 4, kEmpty = 8, kGap = 16;
+  int flags = 0;
+  if (tid == 0 && off[0] != 0) flags |= kBadOff;
+  for (int u = tid; u < n_user; u += nt) {
+    if (off[u + 1] < off[u]) flags |= kBadOff;
+    if (off[u + 1] == off[u]) flags |= kEmpty;
   }
-  // validation
-  int e_off = 0, e_idx = 0, unsorted = 0;
-  if (tid == 0 && off[0] != 0) e_off = 1;
-  for (int u = tid; u < n_user; u += nt)
-    if (off[u + 1] < off[u]) e_off = 1;
   for (int c = tid; c < n_cand; c += nt) {
     const int x = c2u[c];
-    if (x < 0 || x >= n_user) e_idx = 1;
-    if (c > 0 && c2u[c - 1] > x) unsorted = 1;
+    const int prev = c == 0 ? -1 : c2u[c - 1];
+    if (x < 0 || x >= n_user) flags |= kBadIdx;
+    if (prev > x) {
+      flags |= kUnsorted;
+    } else if (prev < x && x < n_user) {
+      if (x - prev <= kSmallGap) {
+        for (int uu = max(prev + 1, 0); uu <= x; ++uu) cs[uu] = c;
+      } else {
+        flags |= kGap;
+      }
+    }
+    if (c == n_cand - 1 && x >= 0 && x < n_user) {
+      if (n_user - x <= kSmallGap) {
+        for (int uu = x + 1; uu <= n_user; ++uu) cs[uu] = n_cand;
+      } else {
+        flags |= kGap;
+      }
+    }
   }
-  const int any_off = __syncthreads_or(e_off);
-  const int any_idx = __syncthreads_or(e_idx);
-  const int any_uns = __syncthreads_or(unsorted);
-  if (any_off || any_idx) {
+  if (flags) atomicOr(&ctl->flags, flags);
+  __syncthreads();
+  flags = ctl->flags;
+  trace_pro(p, 4);
+  if (flags & (kBadOff | kBadIdx)) {
     if (tid == 0) {
       ctl->mode = kModeSkip;
       ctl->n_my_items = 0;
       ctl->sorted = 1;
-      if (b == 0) atomicOr(p.err_word, (any_off ? kErrOffsets : 0) | (any_idx ? kErrIndex : 0));
+      if (b == 0)
+        atomicOr(p.err_word, ((flags & kBadOff) ? kErrOffsets : 0) | ((flags & kBadIdx) ? kErrIndex : 0));
     }
     __syncthreads();
     return;
   }
-  // group candidates by user
-  if (!any_uns) {
+  const bool unsorted = (flags & kUnsorted) != 0;
+  if (!unsorted && (flags & kGap)) {
+    // sorted, with wide gaps between consecutive users: fill those now
     for (int c = tid; c < n_cand; c += nt) {
       const int x = c2u[c];
       const int prev = c == 0 ? -1 : c2u[c - 1];
-      for (int uu = prev + 1; uu <= x; ++uu) cs[uu] = c;
+      if (x - prev > kSmallGap)
+        for (int uu = prev + 1; uu <= x; ++uu) cs[uu] = c;
+      if (c == n_cand - 1 && n_user - x > kSmallGap)
+        for (int uu = x + 1; uu <= n_user; ++uu) cs[uu] = n_cand;
     }
-    for (int uu = c2u[n_cand - 1] + 1 + tid; uu <= n_user; uu += nt) cs[uu] = n_cand;
     __syncthreads();
-  } else {
-    // stable counting sort: warp w owns a contiguous segment of candidates
-    const int warp = tid >> 5, lane = tid & 31, nw = nt >> 5;
+  }
+  if (unsorted) {
+    // stable counting sort: sort warp w < kSortWarps owns a contiguous segment
+    // of candidates; the other warps only take part in the barriers
+    int32_t* const wcnt = S.wcnt;
+    int32_t* const perm = S.perm;
+    const int warp = tid >> 5, lane = tid & 31, nw = kSortWarps;
+    const bool sorter = warp < nw;
     const int seg = (n_cand + nw - 1) / nw;
-    const int seg_end = min(n_cand, (warp + 1) * seg);
+    const int seg_end = sorter ? min(n_cand, (warp + 1) * seg) : 0;
     for (int i = tid; i < nw * n_user; i += nt) wcnt[i] = 0;
     __syncthreads();
-    for (int c = warp * seg + lane; c < seg_end; c += 32) atomicAdd(&wcnt[warp * n_user + c2u[c]], 1);
+    if (sorter)
+      for (int c = warp * seg + lane; c < seg_end; c += 32) atomicAdd(&wcnt[warp * n_user + c2u[c]], 1);
     __syncthreads();
     // per-user totals -> cand_start (exclusive scan over users)
     int carry = 0;
@@ -303,7 +361,7 @@ __device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch,
       if (u < n_user)
         for (int w = 0; w < nw; ++w) tot_u += wcnt[w * n_user + u];
       int tot;
-      const int ex = block_scan_excl(tot_u, ctl->red_i, &tot);
+      const int ex = block_scan_excl(tot_u, ctl->red, &tot);
       if (u < n_user) cs[u] = carry + ex;
       carry += tot;
     }
@@ -320,7 +378,7 @@ __device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch,
     }
     __syncthreads();
     const unsigned lt = (1u << lane) - 1u;
-    for (int base = warp * seg; base < seg_end; base += 32) {
+    for (int base = warp * seg; sorter && base < seg_end; base += 32) {
       const int c = base + lane;
       const bool valid = c < seg_end;
       const int x = valid ? c2u[c] : -1;
@@ -336,8 +394,9 @@ __device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch,
     // every CTA writes the same permutation; each reads back only its own writes
     for (int i = tid; i < n_cand; i += nt) p.perm_ws[i] = perm[i];
   }
+  trace_pro(p, 5);
   // rows of candidates whose user has an empty sequence are zero
-  {
+  if (flags & kEmpty) {
     const int64_t elems = (int64_t)p.H * p.Lq * D;
     for (int c = b * nt + tid; c < n_cand; c += grid * nt) {
       const int x = c2u[c];
@@ -347,9 +406,50 @@ __device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch,
       }
     }
   }
-  // users, longest first (index order beyond kLptMaxUsersFused users)
-  for (int u = tid; u < n_user; u += nt) {
-    if (n_user <= kLptMaxUsersFused) {
+  // Units (H x query tiles of users with candidates and keys), prefix-summed
+  // over the users in index order, or longest first (below).
+  const int cpt = p.cands_per_tile;
+  bool lpt = false;
+  auto user_at = [&](int rk) { return lpt ? order[rk] : rk; };
+  auto units_of = [&](int u) {
+    const int r = cs[u + 1] - cs[u], L = off[u + 1] - off[u];
+    return (r > 0 && L > 0) ? p.H * ceil_div(r, cpt) : 0;
+  };
+  auto prefix = [&]() {
+    if (n_user <= 32) {
+      if (tid < 32) {
+        const int nu = tid < n_user ? units_of(user_at(tid)) : 0;
+        int v = nu;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, v, o);
+          if (tid >= o) v += y;
+        }
+        if (tid < n_user) ubefore[tid] = v - nu;
+        if (tid == 31) ubefore[n_user] = v;
+      }
+    } else {
+      int carry = 0;
+      for (int base = 0; base < n_user; base += nt) {
+        const int rk = base + tid;
+        const int nu = rk < n_user ? units_of(user_at(rk)) : 0;
+        int tot;
+        const int ex = block_scan_excl(nu, ctl->red, &tot);
+        if (rk < n_user) ubefore[rk] = carry + ex;
+        carry += tot;
+      }
+      if (tid == 0) ubefore[n_user] = carry;
+    }
+    __syncthreads();
+  };
+  prefix();
+  const int N = ubefore[n_user];
+  // Pair mode when every unit gets a cluster of its own; otherwise units are
+  // dealt to independent CTAs, users longest first.
+  const bool pair = N > 0 && 2 * N <= grid;
+  if (!pair && n_user > 1 && n_user <= kLptMaxUsersFused) {
+    __syncthreads();   // everyone has read N before the prefix is rewritten
+    for (int u = tid; u < n_user; u += nt) {
       const int Lu = off[u + 1] - off[u];
       int rank = 0;
       for (int w = 0; w < n_user; ++w) {
@@ -357,33 +457,12 @@ __device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch,
         rank += (Lw > Lu) || (Lw == Lu && w < u);
       }
       order[rank] = u;
-    } else {
-      order[u] = u;
     }
-  }
-  __syncthreads();
-  // units per rank: H x query tiles of users with candidates and keys
-  const int cpt = p.cands_per_tile;
-  {
-    int carry = 0;
-    for (int base = 0; base < n_user; base += nt) {
-      const int rk = base + tid;
-      int nu = 0;
-      if (rk < n_user) {
-        const int u = order[rk];
-        const int r = cs[u + 1] - cs[u], L = off[u + 1] - off[u];
-        if (r > 0 && L > 0) nu = p.H * ceil_div(r, cpt);
-      }
-      int tot;
-      const int ex = block_scan_excl(nu, ctl->red_i, &tot);
-      if (rk < n_user) ubefore[rk] = carry + ex;
-      carry += tot;
-    }
-    if (tid == 0) ubefore[n_user] = carry;
+    lpt = true;
     __syncthreads();
+    prefix();
   }
-  const int N = ubefore[n_user];
-  const bool pair = N > 0 && 2 * N <= grid;
+  trace_pro(p, 6);
   // decode unit i into a work item
   auto decode = [&](int i, WorkItem& w) {
     int lo = 0, hi = n_user - 1;
@@ -391,7 +470,7 @@ __device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch,
       const int mid = (lo + hi + 1) >> 1;
       if (ubefore[mid] <= i) lo = mid; else hi = mid - 1;
     }
-    const int u = order[lo];
+    const int u = user_at(lo);
     const int r = cs[u + 1] - cs[u];
     const int nmt = ceil_div(r, cpt);
     const int local = i - ubefore[lo];
@@ -425,11 +504,9 @@ __device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch,
             w.kv_len -= first;
             w.unit = 1;
           }
-          mine[0] = w;
           ctl->items[0] = w;
           count = 1;
         } else if (rank == 0) {
-          mine[0] = w;
           ctl->items[0] = w;
           count = 1;
         }
@@ -445,14 +522,14 @@ __device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch,
       const int i = k * grid + ((k & 1) ? grid - 1 - b : b);
       WorkItem w;
       decode(i, w);
-      mine[k] = w;
-      if (k < kCtlItems) ctl->items[k] = w;
+      if (k < kCtlItems) ctl->items[k] = w; else mine[k] = w;
     }
     if (tid == 0) ctl->n_my_items = count;
   }
   if (tid == 0) {
     ctl->mode = pair ? kModePair : kModeIndep;
-    ctl->sorted = any_uns ? 0 : 1;
+    ctl->sorted = unsorted ? 0 : 1;
+    ctl->total_keys = off[n_user];
   }
   __syncthreads();
 }
@@ -465,76 +542,93 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
                     const __grid_constant__ CUtensorMap kmap_tmpl,
                     const __grid_constant__ CUtensorMap vmap_tmpl) {
   using C = TcConfig<D>;
-  extern __shared__ __align__(128) uint8_t smem_raw[];
-  TcCtrl* ctl = reinterpret_cast<TcCtrl*>(smem_raw);
-  uint8_t* data = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + kCtrlBytes + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* data = smem_raw;
+  TcCtrl* ctl = reinterpret_cast<TcCtrl*>(smem_raw + kDataBytes);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t cta_rank = ptx::cluster_ctarank();
+  // 128-byte swizzle atoms must start on 1 KB boundaries
+  const bool layout_ok = (ptx::smem_addr(smem_raw) & 1023u) == 0;
+  trace_pro(p, 0);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(ptx::smem_addr(&ctl->q_full[i]), 1);
       ptx::mbar_init(ptx::smem_addr(&ctl->q_empty[i]), 1);
       ptx::mbar_init(ptx::smem_addr(&ctl->s_full[i]), 1);
-      ptx::mbar_init(ptx::smem_addr(&ctl->p_full[i]), 4);
+      ptx::mbar_init(ptx::smem_addr(&ctl->p_full[i]), 8);
     }
     for (int i = 0; i < kMaxSlots; ++i) {
       ptx::mbar_init(ptx::smem_addr(&ctl->kv_full[i]), 1);
       ptx::mbar_init(ptx::smem_addr(&ctl->kv_empty[i]), 1);
     }
+    for (int i = 0; i < 4; ++i)
+      for (int j = 0; j < 2; ++j) ptx::mbar_init(ptx::smem_addr(&ctl->xbar[i][j]), 2);
     ptx::mbar_init(ptx::smem_addr(&ctl->pv_done), 1);
     ptx::mbar_init(ptx::smem_addr(&ctl->drain), 1);
     ptx::mbar_init(ptx::smem_addr(&ctl->pair_go), 1);
     ptx::mbar_init(ptx::smem_addr(&ctl->pair_recv), 1);
-    ptx::mbar_init(ptx::smem_addr(&ctl->stage_done), 4);
+    ptx::mbar_init(ptx::smem_addr(&ctl->stage_done), 8);
     ctl->go_sent = 0;
     ctl->abort_flag = 0;
-    ctl->wg_count = 0;
+    ctl->flags = 0;
     ptx::fence_mbar_init();
   }
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_addr(&ctl->tmem_base), C::kTmemCols);
     ptx::tmem_relinquish();
   }
+  if (warp == 2 && lane == 0) {
+    // the host-encoded descriptors into the TMA unit's cache ahead of use
+    ptx::prefetch_tensormap(&qmap);
+    ptx::prefetch_tensormap(&kmap_tmpl);
+    ptx::prefetch_tensormap(&vmap_tmpl);
+  }
   // A planning kernel may precede this one (programmatic dependent launch):
   // its work list is visible after this wait.  Without one it returns at once.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (p.fused) {
-    __syncthreads();
-    plan_in_cta(p, ctl, data, kmap_tmpl, vmap_tmpl, D);
+  if (p.fused && layout_ok) plan_load(p, data);
+  __syncthreads();
+  trace_pro(p, 1);
+  if (!layout_ok) {
+    if (threadIdx.x == 0) {
+      ctl->mode = kModeSkip;
+      ctl->n_my_items = 0;
+      ctl->sorted = 1;
+      atomicOr(p.err_word, kErrLayout);
+    }
+  } else if (p.fused) {
+    plan_in_cta(p, ctl, data, D);
+    trace_pro(p, 7);
     // the planning scratch is overwritten by TMA (async proxy) from here on
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    ptx::fence_proxy_async_smem();
   } else if (threadIdx.x == 0) {
     ctl->mode = kModeListed;
     ctl->sorted = p.header->sorted != 0;
+    ctl->total_keys = p.header->total_keys;
     const int n = p.header->n_items;
     ctl->n_my_items =
         n > (int)blockIdx.x ? (n - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
   }
-  if (threadIdx.x == 0) {
-    ctl->n_slots = C::kSlots;
-    trace(p, 0, kTrCtaStart);
-  }
+  if (threadIdx.x == 0) trace(p, 0, kTrCtaStart);
   ptx::tc_fence_before();
-  __syncthreads();
-  // the partner's barriers are initialised before any remote arrive
+  // every thread of both CTAs: the plan is visible in this CTA and the
+  // partner's barriers are initialised before any remote arrive
   ptx::cluster_sync();
   ptx::tc_fence_after();
+  trace_pro(p, 8);
 
   const uint32_t tmem = ctl->tmem_base;
   const int mode = ctl->mode;
   const int n_my = ctl->n_my_items;
   const bool sorted = ctl->sorted != 0;
-  const int NS = ctl->n_slots;
+  const int NS = C::kSlots;
   const int NQ = mode == kModePair ? 1 : 2;
   uint8_t* q_smem = data;
   uint8_t* kv_smem = data + 2 * C::kQBytes;
   const int32_t* perm = p.fused ? p.perm_ws : p.perm;
-  const void* kmap = p.fused ? (const void*)(p.map_slots + 2 * blockIdx.x) : p.kmap;
-  const void* vmap = p.fused ? (const void*)(p.map_slots + 2 * blockIdx.x + 1) : p.vmap;
   const Waiter W{&ctl->abort_flag, p.err_word, p.timeout_ns};
   const int Lq = p.Lq;
   auto item_at = [&](int k) -> WorkItem {
@@ -545,11 +639,43 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && mode != kModeSkip) {
-      ptx::tensormap_acquire(kmap);
-      ptx::tensormap_acquire(vmap);
+      const int T = ctl->total_keys;
+      // Fused mode loads through the host maps, whose row count is open; a
+      // tile that reaches past row T goes through a copy with the row count
+      // set to T (made on first need), so the TMA fills its missing rows with
+      // zeros instead of reading past the end of k / v.
+      const void* kmap = p.fused ? (const void*)&kmap_tmpl : p.kmap;
+      const void* vmap = p.fused ? (const void*)&vmap_tmpl : p.vmap;
+      CUtensorMap* tail_k = p.fused ? p.map_slots + 2 * blockIdx.x : nullptr;
+      CUtensorMap* tail_v = tail_k ? tail_k + 1 : nullptr;
+      bool tail_ready = false;
+      if (!p.fused) {
+        ptx::tensormap_acquire(kmap);
+        ptx::tensormap_acquire(vmap);
+      }
       uint32_t kv_it = 0, q_it = 0;
       bool ok = true;
-      auto load_tile = [&](const void* map, int head, int32_t row) -> bool {
+      auto load_tile = [&](bool is_v, int head, int32_t row) -> bool {
+        const void* map = is_v ? vmap : kmap;
+        if (p.fused && row + kBlockN > T) {
+          if (!tail_ready) {
+#pragma unroll
+            for (int mi = 0; mi < 2; ++mi) {
+              const uint4* s4 = reinterpret_cast<const uint4*>(mi == 0 ? &kmap_tmpl : &vmap_tmpl);
+              uint4* d4 = reinterpret_cast<uint4*>(mi == 0 ? tail_k : tail_v);
+#pragma unroll
+              for (int i = 0; i < (int)(sizeof(CUtensorMap) / 16); ++i) d4[i] = s4[i];
+              asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 1, %1;" ::"l"(d4),
+                           "r"(T)
+                           : "memory");
+            }
+            asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
+            ptx::tensormap_acquire(tail_k);
+            ptx::tensormap_acquire(tail_v);
+            tail_ready = true;
+          }
+          map = is_v ? (const void*)tail_v : (const void*)tail_k;
+        }
         const uint32_t slot = kv_it % NS;
         if (!W.wait(ptx::smem_addr(&ctl->kv_empty[slot]), ((kv_it / NS) & 1u) ^ 1u)) return false;
         const uint32_t bar = ptx::smem_addr(&ctl->kv_full[slot]);
@@ -592,16 +718,16 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
         ++q_it;
         // K/V tiles in the order the MMA warp consumes them: K0, K1, V0, K2, V1, ...
         for (int j = 0; j <= n && ok; ++j) {
-          if (j < n) ok = load_tile(kmap, w.head, w.kv_begin + j * kBlockN);
-          if (ok && j >= 1) ok = load_tile(vmap, w.head, w.kv_begin + (j - 1) * kBlockN);
+          if (j < n) ok = load_tile(false, w.head, w.kv_begin + j * kBlockN);
+          if (ok && j >= 1) ok = load_tile(true, w.head, w.kv_begin + (j - 1) * kBlockN);
         }
         trace(p, k, kTrProdIssued);
         if (ok && w.unit == 0 && w.unit_first) {
           // pair leader: once the last S has read Q, both Q buffers can receive
-          // the partner's O and (m, l); tell the partner so
+          // the partner's O and log-sum-exp; tell the partner so
           if (!W.wait(ptx::smem_addr(&ctl->q_empty[0]), 0)) break;
           const int rows = w.n_cand * Lq;
-          const uint32_t bytes = uint32_t(rows * D * 4 + ((rows + 1) & ~1) * 8);
+          const uint32_t bytes = uint32_t(rows * D * 4 + ((rows + 3) & ~3) * 4);
           ptx::mbar_arrive_expect_tx(ptx::smem_addr(&ctl->pair_recv), bytes);
           ctl->go_sent = 1;
           ptx::mbar_arrive_cluster(ptx::map_to_cta(ptx::smem_addr(&ctl->pair_go), cta_rank ^ 1u));
@@ -623,7 +749,7 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
     // -------------------------------------------------------------- MMA issuer
     if (lane == 0 && mode != kModeSkip) {
       constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(kTileM, kBlockN, 0);
-      constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(kTileM, 64, 1);
+      constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(kTileM, D, 1);
       uint32_t kv_it = 0, q_it = 0, g = 0;
       bool ok = true;
       for (int k = 0; k < n_my && ok; ++k) {
@@ -675,15 +801,14 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
             ptx::tc_fence_after();
             const uint32_t v_base = ptx::smem_addr(kv_smem + slot * C::kKVBytes);
             const uint32_t a_tmem = tmem + C::kSCol + pb * kBlockN;
+            // V is MN-major (d contiguous): 8-key groups 1 KB apart, the two
+            // 64-column blocks of a D = 128 tile kBlockN * 128 bytes apart
 #pragma unroll
             for (int kk = 0; kk < kBlockN / 16; ++kk) {
-#pragma unroll
-              for (int cb = 0; cb < C::kCB; ++cb) {
-                const uint64_t bdesc = ptx::smem_desc_sw128(
-                    v_base + cb * kBlockN * 128 + kk * 16 * 128, kBlockN * 128, 1024);
-                ptx::mma_ts(tmem + C::kOCol + cb * 64, a_tmem + kk * 8, bdesc, kIdescPV,
-                            (j > 1 || kk > 0) ? 1u : 0u);
-              }
+              const uint64_t bdesc =
+                  ptx::smem_desc_sw128(v_base + kk * 16 * 128, kBlockN * 128, 1024);
+              ptx::mma_ts(tmem + C::kOCol, a_tmem + kk * 8, bdesc, kIdescPV,
+                          (j > 1 || kk > 0) ? 1u : 0u);
             }
             ptx::mma_commit(ptx::smem_addr(&ctl->kv_empty[slot]));
             ptx::mma_commit(ptx::smem_addr(&ctl->pv_done));
@@ -699,12 +824,26 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
       W.drain(ptx::smem_addr(&ctl->drain), 0);
     }
     __syncwarp();
-  } else if (warp >= 4 && mode != kModeSkip) {
+  } else if (warp >= kSoftmaxWarp0 && mode != kModeSkip) {
     // ------------------------------------------- softmax / correction / epilogue
-    const int row = threadIdx.x - 128;                       // TMEM lane == tile row
-    const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
+    const int quarter = warp & 3;
+    const int half = (warp - kSoftmaxWarp0) >> 2;            // 0: columns 0-63, 1: 64-127
+    const int row = quarter * 32 + lane;                     // TMEM lane == tile row
+    const uint32_t lane_off = uint32_t(quarter * 32) << 16;
     const float sl2 = p.scale_log2;
-    uint32_t g = 0, pv_it = 0;
+    const float2 sl2x2 = make_float2(sl2, sl2);
+    uint32_t g = 0, pv_it = 0, xs = 0;
+    // Exchange one float per row with the other half (bounded, like every wait).
+    auto exchange = [&](float mine, float& theirs) -> bool {
+      const uint32_t par = xs & 1u;
+      ctl->xchg[par][half][row] = mine;
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&ctl->xbar[quarter][par]));
+      const bool ok = W.warp_wait(ptx::smem_addr(&ctl->xbar[quarter][par]), (xs >> 1) & 1u);
+      theirs = ctl->xchg[par][half ^ 1][row];
+      ++xs;
+      return ok;
+    };
     for (int k = 0; k < n_my; ++k) {
       const WorkItem w = item_at(k);
       const int n = ceil_div(w.kv_len, kBlockN);
@@ -719,59 +858,72 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
           break;
         }
         ptx::tc_fence_after();
-        if (j == 0 && row == 0) trace(p, k, kTrSmS0);
+        if (j == 0 && row == 0 && half == 0) trace(p, k, kTrSmS0);
         const uint32_t scol = tmem + lane_off + C::kSCol + sb * kBlockN;
-        uint32_t sr[4][32];
+        float t[64];
+        {
+          uint32_t r[2][32];
+          ptx::tmem_ld32(scol + half * 64, r[0]);
+          ptx::tmem_ld32(scol + half * 64 + 32, r[1]);
+          ptx::tmem_ld_wait();
+          // scaled scores t = s * scale * log2(e)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) ptx::tmem_ld32(scol + c * 32, sr[c]);
-        ptx::tmem_ld_wait();
-        const int valid = min(kBlockN, w.kv_len - j * kBlockN);
-        // row maximum of the scaled scores (of the raw minimum when scale < 0)
-        const float sgn = sl2 < 0.f ? -1.f : 1.f;
-        float mxv[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) mxv[e] = -INFINITY;
-        if (valid == kBlockN) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int e = 0; e < 32; ++e) mxv[e & 7] = fmaxf(mxv[e & 7], sgn * __uint_as_float(sr[c][e]));
-        } else {
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (c * 32 + e < valid) mxv[e & 7] = fmaxf(mxv[e & 7], sgn * __uint_as_float(sr[c][e]));
+          for (int e = 0; e < 64; e += 2) {
+            const float2 v = fmul2(make_float2(__uint_as_float(r[e >> 5][e & 31]),
+                                               __uint_as_float(r[e >> 5][(e & 31) + 1])),
+                                   sl2x2);
+            t[e] = v.x;
+            t[e + 1] = v.y;
+          }
         }
-        float mx = fmaxf(fmaxf(fmaxf(mxv[0], mxv[1]), fmaxf(mxv[2], mxv[3])),
-                         fmaxf(fmaxf(mxv[4], mxv[5]), fmaxf(mxv[6], mxv[7])));
-        mx *= sgn * sl2;
+        // keys of this half that exist (the tile's tail may be short)
+        const int valid = min(kBlockN, w.kv_len - j * kBlockN) - half * 64;
+        if (valid < 64) {
+#pragma unroll
+          for (int e = 0; e < 64; ++e)
+            if (e >= valid) t[e] = -INFINITY;
+        }
+        float mx;
+        {
+          float a = fmax3(t[0], t[1], t[2]), b2 = fmax3(t[3], t[4], t[5]);
+          float c2 = fmax3(t[6], t[7], t[8]), d2 = fmax3(t[9], t[10], t[11]);
+#pragma unroll
+          for (int e = 12; e < 60; e += 8) {
+            a = fmax3(a, t[e], t[e + 1]);
+            b2 = fmax3(b2, t[e + 2], t[e + 3]);
+            c2 = fmax3(c2, t[e + 4], t[e + 5]);
+            d2 = fmax3(d2, t[e + 6], t[e + 7]);
+          }
+          a = fmax3(a, t[60], t[61]);
+          b2 = fmax3(b2, t[62], t[63]);
+          mx = fmax3(a, b2, fmaxf(c2, d2));
+        }
+        // the other half of the row; its S reads are complete once it has arrived
+        ptx::tc_fence_before();
+        float mx_other;
+        if (!exchange(mx, mx_other)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        mx = fmaxf(mx, mx_other);
         const float m_new = (m == -INFINITY || mx > m + kLazyRescale) ? fmaxf(m, mx) : m;
         const float alpha = fast_exp2(m - m_new);   // 0 on the first tile, 1 when m stays
-        float sumv[8];
+        const float2 neg_m = make_float2(-m_new, -m_new);
+        float2 acc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+        uint32_t pk[32];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) sumv[e] = 0.f;
-        uint32_t pk[2][32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const int col = c * 32 + e;
-            float p0 = fast_exp2(fmaf(__uint_as_float(sr[c][e]), sl2, -m_new));
-            float p1 = fast_exp2(fmaf(__uint_as_float(sr[c][e + 1]), sl2, -m_new));
-            if (valid < kBlockN) {
-              p0 = col < valid ? p0 : 0.f;
-              p1 = col + 1 < valid ? p1 : 0.f;
-            }
-            sumv[(e >> 1) & 7] += p0 + p1;
-            pk[c >> 1][(c & 1) * 16 + (e >> 1)] = pack_bf16(p0, p1);
-          }
-        const float sum = ((sumv[0] + sumv[1]) + (sumv[2] + sumv[3])) +
-                          ((sumv[4] + sumv[5]) + (sumv[6] + sumv[7]));
+        for (int e = 0; e < 64; e += 2) {
+          const float2 x = fadd2(make_float2(t[e], t[e + 1]), neg_m);
+          const float2 pe = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+          acc[(e >> 1) & 3] = fadd2(acc[(e >> 1) & 3], pe);
+          pk[e >> 1] = pack_bf16(pe.x, pe.y);
+        }
+        const float sum = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y) +
+                          ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
         l = l * alpha + sum;
-        // P (bf16 pairs) overwrites the first half of this S buffer.
-        ptx::tmem_st32(scol, pk[0]);
-        ptx::tmem_st32(scol + 32, pk[1]);
+        // P (bf16 pairs) over the first half of this S buffer: keys 64h.. at column 32h
+        ptx::tmem_st32(scol + half * 32, pk);
         ptx::tmem_st_wait();
         if (j > 0) {
           // O holds P_0..P_{j-1} V: wait for PV_{j-1}, then rescale if m moved.
@@ -782,14 +934,20 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
           ++pv_it;
           ptx::tc_fence_after();
           if (__any_sync(0xffffffffu, m_new != m)) {
-            const uint32_t ocol = tmem + lane_off + C::kOCol;
+            const uint32_t ocol = tmem + lane_off + C::kOCol + half * C::kHalf;
+            const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < C::kChunks; ++c) {
               uint32_t o[32];
               ptx::tmem_ld32(ocol + c * 32, o);
               ptx::tmem_ld_wait();
 #pragma unroll
-              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+              for (int e = 0; e < 32; e += 2) {
+                const float2 v =
+                    fmul2(make_float2(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), a2);
+                o[e] = __float_as_uint(v.x);
+                o[e + 1] = __float_as_uint(v.y);
+              }
               ptx::tmem_st32(ocol + c * 32, o);
             }
             ptx::tmem_st_wait();
@@ -801,48 +959,56 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
         if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&ctl->p_full[sb]));
       }
       if (!ok) break;
-      if (row == 0) trace(p, k, kTrSmLastP);
+      if (row == 0 && half == 0) trace(p, k, kTrSmLastP);
       // ---- epilogue
       if (!W.warp_wait(ptx::smem_addr(&ctl->pv_done), pv_it & 1u)) break;
       ++pv_it;
       ptx::tc_fence_after();
-      if (row == 0) trace(p, k, kTrEpiO);
-      const uint32_t ocol = tmem + lane_off + C::kOCol;
+      if (row == 0 && half == 0) trace(p, k, kTrEpiO);
+      float l_other;
+      if (!exchange(l, l_other)) break;
+      const float lt = l + l_other;                // both halves share the running max m
+      const uint32_t ocol = tmem + lane_off + C::kOCol + half * C::kHalf;
       const bool live = row < rows;
       const int ci = live ? row / Lq : 0;
-      const int t = live ? row - ci * Lq : 0;
+      const int tq = live ? row - ci * Lq : 0;
+      const int vec0 = half * C::kHalf / 4;        // first 16-byte vector of this half row
       if (w.unit == 1) {
-        // pair sender: stage O (swizzled rows) and (m, l) in this CTA's ring,
-        // which no MMA reads any more, then one bulk copy into the leader
+        // pair sender: stage O / l (swizzled rows) and the log-sum-exp in this
+        // CTA's ring, which no MMA reads any more, then bulk copies into the leader
         uint8_t* stage = kv_smem;
-        float2* stage_ml = reinterpret_cast<float2*>(kv_smem + C::kRecvBytes);
+        float* stage_lse = reinterpret_cast<float*>(kv_smem + C::kRecvBytes);
+        const float inv = lt > 0.f ? 1.f / lt : 0.f;
+        const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
+        for (int cc = 0; cc < C::kChunks; ++cc) {
           uint32_t o[32];
           ptx::tmem_ld32(ocol + cc * 32, o);
           ptx::tmem_ld_wait();
           if (live) {
 #pragma unroll
             for (int q4 = 0; q4 < 8; ++q4) {
-              const int vec = cc * 8 + q4;                     // 16-byte vector of the row
-              *reinterpret_cast<uint4*>(stage + row * (D * 4) + ((vec ^ (row & 7)) * 16)) =
-                  make_uint4(o[q4 * 4 + 0], o[q4 * 4 + 1], o[q4 * 4 + 2], o[q4 * 4 + 3]);
+              const int vec = vec0 + cc * 8 + q4;
+              const float2 a = fmul2(make_float2(__uint_as_float(o[q4 * 4 + 0]), __uint_as_float(o[q4 * 4 + 1])), inv2);
+              const float2 b2 = fmul2(make_float2(__uint_as_float(o[q4 * 4 + 2]), __uint_as_float(o[q4 * 4 + 3])), inv2);
+              *reinterpret_cast<float4*>(stage + row * (D * 4) + ((vec ^ (row & 7)) * 16)) =
+                  make_float4(a.x, a.y, b2.x, b2.y);
             }
           }
         }
-        if (live) stage_ml[row] = make_float2(m, l);
+        if (live && half == 0) stage_lse[row] = lt > 0.f ? m + fast_log2(lt) : -INFINITY;
         ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&ctl->stage_done));
-        if (row == 0) {
+        if (row == 0 && half == 0) {
           if (W.wait(ptx::smem_addr(&ctl->stage_done), 0) &&
               W.wait(ptx::smem_addr(&ctl->pair_go), 0, true)) {
             const uint32_t peer = cta_rank ^ 1u;
             const uint32_t rbar = ptx::map_to_cta(ptx::smem_addr(&ctl->pair_recv), peer);
             ptx::bulk_copy_to_cta(ptx::map_to_cta(ptx::smem_addr(data), peer), ptx::smem_addr(stage),
                                   uint32_t(rows * D * 4), rbar);
-            ptx::bulk_copy_to_cta(ptx::map_to_cta(ptx::smem_addr(ctl->partner_ml), peer),
-                                  ptx::smem_addr(stage_ml), uint32_t(((rows + 1) & ~1) * 8), rbar);
+            ptx::bulk_copy_to_cta(ptx::map_to_cta(ptx::smem_addr(ctl->partner_lse), peer),
+                                  ptx::smem_addr(stage_lse), uint32_t(((rows + 3) & ~3) * 4), rbar);
             trace(p, k, kTrEpiStored);
           }
         }
@@ -850,58 +1016,54 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
       } else {
         const int32_t gpos = w.cand_begin + ci;
         const int64_t cidx = live ? (sorted ? gpos : perm[gpos]) : 0;
-        uint16_t* dst = p.out + (((cidx * p.H + w.head) * (int64_t)Lq + t) * D);
-        float mp = -INFINITY, lp = 0.f;
+        uint16_t* dst = p.out + (((cidx * p.H + w.head) * (int64_t)Lq + tq) * D) + half * C::kHalf;
+        float lse_p = -INFINITY;
         const bool merge = w.unit == 0 && w.unit_first != 0;
         if (merge) {
-          // pair leader: the partner's O and (m, l) arrive in the Q buffers
+          // pair leader: the partner's O / l and log-sum-exp arrive in the Q buffers
           if (!W.warp_wait(ptx::smem_addr(&ctl->pair_recv), 0, true)) break;
-          if (row == 0) trace(p, k, kTrArrived);
-          if (live) {
-            const float2 ml = ctl->partner_ml[row];
-            mp = ml.x;
-            lp = ml.y;
-          }
+          if (row == 0 && half == 0) trace(p, k, kTrArrived);
+          if (live) lse_p = ctl->partner_lse[row];
         }
-        const float M = fmaxf(m, mp);
-        const float a0 = fast_exp2(m - M), a1 = merge ? fast_exp2(mp - M) : 0.f;
-        const float L = a0 * l + a1 * lp;
+        // out = (2^(m-M) O + 2^(lse_p-M) O_p / l_p) / (2^(m-M) l + 2^(lse_p-M))
+        const float M = fmaxf(m, lse_p);
+        const float a0 = fast_exp2(m - M), a1 = merge ? fast_exp2(lse_p - M) : 0.f;
+        const float L = a0 * lt + a1;
         const float inv = L > 0.f ? 1.f / L : 0.f;
-        const float w0 = a0 * inv, w1 = a1 * inv;
+        const float2 w0 = make_float2(a0 * inv, a0 * inv), w1 = make_float2(a1 * inv, a1 * inv);
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
+        for (int cc = 0; cc < C::kChunks; ++cc) {
           uint32_t o[32];
           ptx::tmem_ld32(ocol + cc * 32, o);
           ptx::tmem_ld_wait();
           if (live) {
-            float x[32];
+            float2 x[16];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(o[e]) * w0;
+            for (int e = 0; e < 16; ++e)
+              x[e] = fmul2(make_float2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), w0);
             if (merge) {
 #pragma unroll
               for (int q4 = 0; q4 < 8; ++q4) {
-                const int vec = cc * 8 + q4;
+                const int vec = vec0 + cc * 8 + q4;
                 const float4 y = *reinterpret_cast<const float4*>(
                     data + row * (D * 4) + ((vec ^ (row & 7)) * 16));
-                x[q4 * 4 + 0] += y.x * w1;
-                x[q4 * 4 + 1] += y.y * w1;
-                x[q4 * 4 + 2] += y.z * w1;
-                x[q4 * 4 + 3] += y.w * w1;
+                x[2 * q4] = fadd2(x[2 * q4], fmul2(make_float2(y.x, y.y), w1));
+                x[2 * q4 + 1] = fadd2(x[2 * q4 + 1], fmul2(make_float2(y.z, y.w), w1));
               }
             }
             uint4* d4 = reinterpret_cast<uint4*>(dst + cc * 32);
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
               uint4 v;
-              v.x = pack_bf16(x[q4 * 8 + 0], x[q4 * 8 + 1]);
-              v.y = pack_bf16(x[q4 * 8 + 2], x[q4 * 8 + 3]);
-              v.z = pack_bf16(x[q4 * 8 + 4], x[q4 * 8 + 5]);
-              v.w = pack_bf16(x[q4 * 8 + 6], x[q4 * 8 + 7]);
+              v.x = pack_bf16(x[4 * q4].x, x[4 * q4].y);
+              v.y = pack_bf16(x[4 * q4 + 1].x, x[4 * q4 + 1].y);
+              v.z = pack_bf16(x[4 * q4 + 2].x, x[4 * q4 + 2].y);
+              v.w = pack_bf16(x[4 * q4 + 3].x, x[4 * q4 + 3].y);
               d4[q4] = v;
             }
           }
         }
-        if (row == 0) trace(p, k, merge ? kTrMerged : kTrEpiStored);
+        if (row == 0 && half == 0) trace(p, k, merge ? kTrMerged : kTrEpiStored);
       }
       g += n;
     }
@@ -909,6 +1071,7 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
 
   ptx::tc_fence_before();
   __syncthreads();
+  trace_pro(p, 9);
   // a leader that invited its partner's copy waits for it (bounded) before
   // its shared memory can go away, even if it gave up on the merge
   if (threadIdx.x == 0 && ctl->go_sent) W.drain(ptx::smem_addr(&ctl->pair_recv), 0);
@@ -920,6 +1083,7 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, C::kTmemCols);
   }
+  trace_pro(p, 10);
 }
 
 }  // namespace ikbo

@@ -154,6 +154,11 @@ int ikbo_get_timing(float* plan_ms, float* attn_ms);
  * arming the query-tile barrier, so the MMA and softmax warps wait until the
  * bound runs out: the kernel then records IKBO_ERR_TIMEOUT, skips all work
  * and exits normally (nothing traps, the context stays usable).
+ * flags = 4, with a trace buffer set (ikbo_set_trace), also stamps the
+ * prologue of every CTA into item slot 3: 0 entry, 1 barriers and tensor
+ * memory ready, 2 index tensors loaded, 3 tensor maps set, 4 validated,
+ * 5 grouped, 6 units counted, 7 planned, 8 cluster ready, 9 work done,
+ * 10 exit.  The bits combine.
  * timeout_ns bounds every in-kernel wait (0 = the default of 2 s).
  * flags = 0 restores normal operation.
  */
