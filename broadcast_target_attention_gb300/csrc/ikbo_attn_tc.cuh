@@ -36,11 +36,13 @@
 // zero-fills the missing rows.
 //
 // Pair mode.  When there are no more (user, head, query tile) units than
-// clusters, the two CTAs of a cluster split one unit's keys in half.  The
-// second CTA sends its un-normalised O and (m, l) through distributed shared
-// memory into the first, which merges them with the log-sum-exp rule of
-// "Chapter 4", §4.6.4 (Flash-Decoding): M = max(m0, m1),
-// out = (2^(m0-M) O0 + 2^(m1-M) O1) / (2^(m0-M) l0 + 2^(m1-M) l1).
+// clusters, the two CTAs of a cluster split one unit's keys in half.  Each
+// then finishes half of the query rows: it sends O / l and the log-sum-exp
+// m + log2(l) of the other half straight into its partner's shared memory
+// (asynchronous distributed-shared-memory stores, counted on an mbarrier
+// there) and merges what it receives with the log-sum-exp rule of
+// "Chapter 4", §4.6.4 (Flash-Decoding): with M = max(m0, lse1),
+// out = (2^(m0-M) O0 + 2^(lse1-M) O1/l1) / (2^(m0-M) l0 + 2^(lse1-M)).
 //
 // Warp roles (384 threads), after the Blackwell design of "Optimizing Jagged
 // Flash Attention with TLX", §2.1 (dedicated load, MMA and softmax warps;
@@ -116,7 +118,6 @@ struct TcConfig {
   static_assert(kOCol + D <= kTmemCols, "TMEM budget");
   static_assert(kSlots >= 3, "ring size");
   static_assert(kRecvBytes == 2 * kQBytes, "receive area = both Q buffers");
-  static_assert(kRecvBytes + 4 * kTileM <= kSlots * kKVBytes, "staging area");
 };
 
 static_assert(kTcSmemBytes <= 232448, "shared memory budget");
@@ -129,7 +130,7 @@ struct TcCtrl {
   uint64_t q_full[2], q_empty[2];
   uint64_t kv_full[kMaxSlots], kv_empty[kMaxSlots];
   uint64_t s_full[2], p_full[2];
-  uint64_t pv_done, drain, pair_go, pair_recv, stage_done;
+  uint64_t pv_done, drain, pair_go, pair_recv;
   uint64_t xbar[4][2];                  // row-maximum / row-sum exchange, [row quarter][parity]
   uint32_t tmem_base;
   int abort_flag;
@@ -243,6 +244,31 @@ __device__ __forceinline__ int block_scan_excl(int x, int* red, int* total) {
   return pre + v - x;
 }
 
+// Inputs (K, V and q together) up to this size are brought into L2 during
+// planning: each CTA prefetches its 1/grid share, so that DRAM latency
+// overlaps the prologue instead of following it.  Nothing is read twice from
+// DRAM for it: the tiles the TMA loads later hit in L2.
+constexpr int64_t kPrefetchMaxBytes = int64_t(48) << 20;
+
+__device__ void prefetch_inputs(const AttnParams& p, int T, int D) {
+  const int64_t kv = int64_t(T) * p.H * D * 2;
+  const int64_t qb = p.n_cand * p.H * p.Lq * D * 2;
+  if (2 * kv + qb > kPrefetchMaxBytes) return;
+  auto share = [&](const void* base, int64_t bytes) {
+    // byte counts are multiples of 128 (D is 64 or 128), so are the shares
+    const int64_t per = ((bytes + gridDim.x - 1) / gridDim.x + 15) & ~int64_t(15);
+    const int64_t lo = per * blockIdx.x;
+    const int64_t hi = lo + per < bytes ? lo + per : bytes;
+    for (int64_t a = lo; a < hi; a += 65536) {
+      const int64_t n = hi - a < 65536 ? hi - a : 65536;
+      ptx::prefetch_l2(static_cast<const char*>(base) + a, uint32_t(n));
+    }
+  };
+  share(p.k, kv);
+  share(p.v, kv);
+  share(p.q, qb);
+}
+
 // ---------------------------------------------------------------------------
 // In-kernel planning.  All threads of the CTA; `scratch` is the operand area,
 // already holding user_offsets and cand_to_user (plan_load).  Every CTA
@@ -326,6 +352,9 @@ __device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch, 
     __syncthreads();
     return;
   }
+  // the offsets are valid: one thread of an otherwise idle warp starts the
+  // DRAM reads of this CTA's share of the inputs
+  if (tid == 64) prefetch_inputs(p, off[n_user], D);
   const bool unsorted = (flags & kUnsorted) != 0;
   if (!unsorted && (flags & kGap)) {
     // sorted, with wide gaps between consecutive users: fill those now
@@ -570,7 +599,6 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
     ptx::mbar_init(ptx::smem_addr(&ctl->drain), 1);
     ptx::mbar_init(ptx::smem_addr(&ctl->pair_go), 1);
     ptx::mbar_init(ptx::smem_addr(&ctl->pair_recv), 1);
-    ptx::mbar_init(ptx::smem_addr(&ctl->stage_done), 8);
     ctl->go_sent = 0;
     ctl->abort_flag = 0;
     ctl->flags = 0;
@@ -615,7 +643,7 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
   if (threadIdx.x == 0) trace(p, 0, kTrCtaStart);
   ptx::tc_fence_before();
   // every thread of both CTAs: the plan is visible in this CTA and the
-  // partner's barriers are initialised before any remote arrive
+  // partner's barriers are initialised before any remote arrive or store
   ptx::cluster_sync();
   ptx::tc_fence_after();
   trace_pro(p, 8);
@@ -722,13 +750,14 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
           if (ok && j >= 1) ok = load_tile(true, w.head, w.kv_begin + (j - 1) * kBlockN);
         }
         trace(p, k, kTrProdIssued);
-        if (ok && w.unit == 0 && w.unit_first) {
-          // pair leader: once the last S has read Q, both Q buffers can receive
-          // the partner's O and log-sum-exp; tell the partner so
+        if (ok && w.unit >= 0) {
+          // pair item: once the last S has read Q, the Q buffers can receive
+          // the partner's O / l and log-sum-exp of the rows this CTA finishes
+          // (the first half for CTA 0, the second for CTA 1); tell the partner
           if (!W.wait(ptx::smem_addr(&ctl->q_empty[0]), 0)) break;
-          const int rows = w.n_cand * Lq;
-          const uint32_t bytes = uint32_t(rows * D * 4 + ((rows + 3) & ~3) * 4);
-          ptx::mbar_arrive_expect_tx(ptx::smem_addr(&ctl->pair_recv), bytes);
+          const int rows = w.n_cand * Lq, hrows = (rows + 1) >> 1;
+          const int recv = cta_rank == 0 ? hrows : rows - hrows;
+          ptx::mbar_arrive_expect_tx(ptx::smem_addr(&ctl->pair_recv), uint32_t(recv * (D * 4 + 4)));
           ctl->go_sent = 1;
           ptx::mbar_arrive_cluster(ptx::map_to_cta(ptx::smem_addr(&ctl->pair_go), cta_rank ^ 1u));
         }
@@ -970,14 +999,21 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
       const float lt = l + l_other;                // both halves share the running max m
       const uint32_t ocol = tmem + lane_off + C::kOCol + half * C::kHalf;
       const bool live = row < rows;
-      const int ci = live ? row / Lq : 0;
-      const int tq = live ? row - ci * Lq : 0;
+      // A split unit: each CTA of the pair finishes half of the rows (CTA 0
+      // the first, CTA 1 the second) and sends the other half to its partner.
+      const bool paired = w.unit >= 0;
+      const int hrows = (rows + 1) >> 1;
+      const bool mine = !paired || (cta_rank == 0 ? row < hrows : row >= hrows);
+      const bool keep = live && mine;
+      const bool send = live && !mine;
       const int vec0 = half * C::kHalf / 4;        // first 16-byte vector of this half row
-      if (w.unit == 1) {
-        // pair sender: stage O / l (swizzled rows) and the log-sum-exp in this
-        // CTA's ring, which no MMA reads any more, then bulk copies into the leader
-        uint8_t* stage = kv_smem;
-        float* stage_lse = reinterpret_cast<float*>(kv_smem + C::kRecvBytes);
+      if (__any_sync(0xffffffffu, send)) {
+        // O / l and the log-sum-exp m + log2(l), straight into the partner's
+        // Q buffers (rows of D fp32, 16-byte vectors swizzled by row)
+        if (!W.warp_wait(ptx::smem_addr(&ctl->pair_go), 0, true)) break;
+        const uint32_t peer = cta_rank ^ 1u;
+        const uint32_t rbar = ptx::map_to_cta(ptx::smem_addr(&ctl->pair_recv), peer);
+        const uint32_t rdst = ptx::map_to_cta(ptx::smem_addr(data), peer) + uint32_t(row * (D * 4));
         const float inv = lt > 0.f ? 1.f / lt : 0.f;
         const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
@@ -985,49 +1021,37 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
           uint32_t o[32];
           ptx::tmem_ld32(ocol + cc * 32, o);
           ptx::tmem_ld_wait();
-          if (live) {
+          if (send) {
 #pragma unroll
             for (int q4 = 0; q4 < 8; ++q4) {
               const int vec = vec0 + cc * 8 + q4;
               const float2 a = fmul2(make_float2(__uint_as_float(o[q4 * 4 + 0]), __uint_as_float(o[q4 * 4 + 1])), inv2);
               const float2 b2 = fmul2(make_float2(__uint_as_float(o[q4 * 4 + 2]), __uint_as_float(o[q4 * 4 + 3])), inv2);
-              *reinterpret_cast<float4*>(stage + row * (D * 4) + ((vec ^ (row & 7)) * 16)) =
-                  make_float4(a.x, a.y, b2.x, b2.y);
+              ptx::st_async_v4(rdst + uint32_t((vec ^ (row & 7)) * 16), a.x, a.y, b2.x, b2.y, rbar);
             }
           }
         }
-        if (live && half == 0) stage_lse[row] = lt > 0.f ? m + fast_log2(lt) : -INFINITY;
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&ctl->stage_done));
-        if (row == 0 && half == 0) {
-          if (W.wait(ptx::smem_addr(&ctl->stage_done), 0) &&
-              W.wait(ptx::smem_addr(&ctl->pair_go), 0, true)) {
-            const uint32_t peer = cta_rank ^ 1u;
-            const uint32_t rbar = ptx::map_to_cta(ptx::smem_addr(&ctl->pair_recv), peer);
-            ptx::bulk_copy_to_cta(ptx::map_to_cta(ptx::smem_addr(data), peer), ptx::smem_addr(stage),
-                                  uint32_t(rows * D * 4), rbar);
-            ptx::bulk_copy_to_cta(ptx::map_to_cta(ptx::smem_addr(ctl->partner_lse), peer),
-                                  ptx::smem_addr(stage_lse), uint32_t(((rows + 3) & ~3) * 4), rbar);
-            trace(p, k, kTrEpiStored);
-          }
-        }
-        __syncwarp();
-      } else {
+        if (send && half == 0)
+          ptx::st_async_f32(ptx::map_to_cta(ptx::smem_addr(&ctl->partner_lse[row]), peer),
+                            lt > 0.f ? m + fast_log2(lt) : -INFINITY, rbar);
+        if (row == 0 && half == 0) trace(p, k, kTrEpiStored);
+      }
+      if (__any_sync(0xffffffffu, keep)) {
+        const int ci = keep ? row / Lq : 0;
+        const int tq = keep ? row - ci * Lq : 0;
         const int32_t gpos = w.cand_begin + ci;
-        const int64_t cidx = live ? (sorted ? gpos : perm[gpos]) : 0;
+        const int64_t cidx = keep ? (sorted ? gpos : perm[gpos]) : 0;
         uint16_t* dst = p.out + (((cidx * p.H + w.head) * (int64_t)Lq + tq) * D) + half * C::kHalf;
         float lse_p = -INFINITY;
-        const bool merge = w.unit == 0 && w.unit_first != 0;
-        if (merge) {
-          // pair leader: the partner's O / l and log-sum-exp arrive in the Q buffers
+        if (paired) {
+          // the partner's O / l and log-sum-exp for these rows
           if (!W.warp_wait(ptx::smem_addr(&ctl->pair_recv), 0, true)) break;
           if (row == 0 && half == 0) trace(p, k, kTrArrived);
-          if (live) lse_p = ctl->partner_lse[row];
+          if (keep) lse_p = ctl->partner_lse[row];
         }
         // out = (2^(m-M) O + 2^(lse_p-M) O_p / l_p) / (2^(m-M) l + 2^(lse_p-M))
         const float M = fmaxf(m, lse_p);
-        const float a0 = fast_exp2(m - M), a1 = merge ? fast_exp2(lse_p - M) : 0.f;
+        const float a0 = fast_exp2(m - M), a1 = paired ? fast_exp2(lse_p - M) : 0.f;
         const float L = a0 * lt + a1;
         const float inv = L > 0.f ? 1.f / L : 0.f;
         const float2 w0 = make_float2(a0 * inv, a0 * inv), w1 = make_float2(a1 * inv, a1 * inv);
@@ -1036,12 +1060,12 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
           uint32_t o[32];
           ptx::tmem_ld32(ocol + cc * 32, o);
           ptx::tmem_ld_wait();
-          if (live) {
+          if (keep) {
             float2 x[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e)
               x[e] = fmul2(make_float2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), w0);
-            if (merge) {
+            if (paired) {
 #pragma unroll
               for (int q4 = 0; q4 < 8; ++q4) {
                 const int vec = vec0 + cc * 8 + q4;
@@ -1063,7 +1087,7 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
             }
           }
         }
-        if (row == 0 && half == 0) trace(p, k, merge ? kTrMerged : kTrEpiStored);
+        if (row == 0 && half == 0) trace(p, k, paired ? kTrMerged : kTrEpiStored);
       }
       g += n;
     }

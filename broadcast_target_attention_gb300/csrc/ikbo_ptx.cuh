@@ -74,6 +74,38 @@ __device__ __forceinline__ void cluster_sync() {
                    : "memory");
 }
 
+// Split cluster barrier, every thread of the cluster, warps converged: each
+// thread arrives once, then waits once, before it arrives again.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Asynchronous stores into the shared memory of another CTA of the cluster,
+// each completing its bytes on an mbarrier there (shared::cluster addresses).
+__device__ __forceinline__ void st_async_v4(uint32_t remote_addr, float a, float b, float c, float d,
+                                            uint32_t remote_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::
+          "r"(remote_addr),
+      "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar)
+      : "memory");
+}
+__device__ __forceinline__ void st_async_f32(uint32_t remote_addr, float a, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(
+                   remote_addr),
+               "f"(a), "r"(remote_bar)
+               : "memory");
+}
+
+// Hint: bring [addr, addr + bytes) of global memory into L2 (16-byte aligned,
+// bytes a multiple of 16).
+__device__ __forceinline__ void prefetch_l2(const void* addr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(addr), "r"(bytes) : "memory");
+}
+
 // Address of the same shared-memory location in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t map_to_cta(uint32_t addr, uint32_t rank) {
   uint32_t r;
