@@ -121,18 +121,12 @@ int check_args(const void* q, const void* k, const void* v, const int32_t* off, 
   return IKBO_OK;
 }
 
-// Candidates per query tile: floor(128 / Lq), rounded down to a whole number
-// of Q boxes (a box holds `qbox_cands(Lq)` candidates).
-int qbox_cands(int Lq) {
-  if (Lq >= 8) return 1;
-  int nb = 1;
-  while (nb * 2 * Lq <= 8) nb *= 2;
-  return nb;
-}
-int cands_per_tile(int Lq) {
-  const int nb = qbox_cands(Lq);
-  return (kTileM / Lq) / nb * nb;
-}
+// Candidates per query tile: floor(128 / Lq).  The sorted-order Q map's box
+// holds a whole tile, so one TMA copy per 64-column block loads a tile (rows
+// past the tile's own candidates belong to the next ones, or are zero-filled
+// past the end of q; they are never used or stored).
+int cands_per_tile(int Lq) { return kTileM / Lq; }
+int qbox_cands(int Lq) { return cands_per_tile(Lq); }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 

@@ -66,6 +66,8 @@
 
 #include <cuda_bf16.h>
 
+#include <cfloat>
+
 #include "ikbo_common.cuh"
 #include "ikbo_ptx.cuh"
 
@@ -97,6 +99,9 @@ constexpr int kSortWarps = 8;
 constexpr int kSmallGap = 64;
 
 enum TcMode { kModeSkip = -1, kModeListed = 0, kModeIndep = 1, kModePair = 2 };
+// S/P buffers in tensor memory: the MMA warp computes S two tiles ahead of
+// the softmax, so a tile's scores are ready when the softmax gets to it.
+constexpr int kSBufs = 3;
 constexpr int kCtlItems = 2;
 
 template <int D>
@@ -111,9 +116,9 @@ struct TcConfig {
   static constexpr int kRecvBytes = kTileM * D * 4;
   static constexpr int kHalf = D / 2;                   // output columns per softmax thread
   static constexpr int kChunks = kHalf / 32;            // 32-column TMEM loads per half row
-  // tensor-memory columns: two S/P buffers and the O accumulator
+  // tensor-memory columns: three S/P buffers and the O accumulator
   static constexpr int kSCol = 0;
-  static constexpr int kOCol = 2 * kBlockN;
+  static constexpr int kOCol = kSBufs * kBlockN;
   static constexpr int kTmemCols = 512;
   static_assert(kOCol + D <= kTmemCols, "TMEM budget");
   static_assert(kSlots >= 3, "ring size");
@@ -129,9 +134,9 @@ static_assert(4 * (4 * (kFusedMaxUser + 1) + kSortWarps * kFusedMaxUser + 2 * kF
 struct TcCtrl {
   uint64_t q_full[2], q_empty[2];
   uint64_t kv_full[kMaxSlots], kv_empty[kMaxSlots];
-  uint64_t s_full[2], p_full[2];
-  uint64_t pv_done, drain, pair_go, pair_recv;
-  uint64_t xbar[4][2];                  // row-maximum / row-sum exchange, [row quarter][parity]
+  uint64_t s_full[kSBufs], p_full[kSBufs];
+  uint64_t pv_done[kSBufs];             // PV of the tile in S buffer i complete
+  uint64_t drain, pair_go, pair_recv;
   uint32_t tmem_base;
   int abort_flag;
   int mode;
@@ -143,7 +148,10 @@ struct TcCtrl {
   int red[12];
   WorkItem items[kCtlItems];            // the first items of this CTA (the rest in global memory)
   alignas(16) float partner_lse[kTileM];
-  float xchg[2][2][kTileM];             // [parity][half][row]
+  // row maximum / row sum exchange between the two halves of a row:
+  // [parity][half][row], the value with the exchange's sequence number in
+  // its two low bits
+  uint32_t xtag[2][2][kTileM];
 };
 static_assert(sizeof(TcCtrl) <= kCtrlBytes, "control block");
 
@@ -157,6 +165,7 @@ struct Waiter {
     return cluster ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
   }
   __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, bool cluster = false) const {
+    if (!cluster && ptx::mbar_test_wait(bar, parity)) return true;
     if (poll(bar, parity, cluster)) return true;
     uint64_t t_end = 0;
     for (uint32_t spin = 1;; ++spin) {
@@ -191,8 +200,10 @@ struct Waiter {
       }
     }
   }
-  // One lane polls, the warp follows its verdict.
+  // Every lane tests a completed phase at once; otherwise one lane polls and
+  // the warp follows its verdict.
   __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, bool cluster = false) const {
+    if (!cluster && __all_sync(0xffffffffu, ptx::mbar_test_wait(bar, parity))) return true;
     int ok = 0;
     if ((threadIdx.x & 31) == 0) ok = wait(bar, parity, cluster) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -208,6 +219,13 @@ __device__ __forceinline__ void trace(const AttnParams& p, int ord, int point) {
 // Prologue timeline (debug_flags bit 4): item slot 3, points 0..10.
 __device__ __forceinline__ void trace_pro(const AttnParams& p, int point) {
   if ((p.debug_flags & 4) && threadIdx.x == 0) trace(p, 3, point);
+}
+
+// Per-tile timeline of a CTA's first item (debug_flags bit 2): softmax
+// tiles 0-3 in item slot 1 (4 points each), MMA tiles 0-7 in slot 2 (S and
+// PV issue).
+__device__ __forceinline__ void trace_tile(const AttnParams& p, int k, int slot, int point) {
+  if ((p.debug_flags & 2) && k == 0 && point < kTracePoints) trace(p, slot, point);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -250,23 +268,19 @@ __device__ __forceinline__ int block_scan_excl(int x, int* red, int* total) {
 // DRAM for it: the tiles the TMA loads later hit in L2.
 constexpr int64_t kPrefetchMaxBytes = int64_t(48) << 20;
 
-__device__ void prefetch_inputs(const AttnParams& p, int T, int D) {
+// Prefetch instructions are slow to issue, so three threads of different
+// warps issue one each: which = 0 for K, 1 for V, 2 for q.
+__device__ void prefetch_inputs(const AttnParams& p, int T, int D, int which) {
   const int64_t kv = int64_t(T) * p.H * D * 2;
   const int64_t qb = p.n_cand * p.H * p.Lq * D * 2;
   if (2 * kv + qb > kPrefetchMaxBytes) return;
-  auto share = [&](const void* base, int64_t bytes) {
-    // byte counts are multiples of 128 (D is 64 or 128), so are the shares
-    const int64_t per = ((bytes + gridDim.x - 1) / gridDim.x + 15) & ~int64_t(15);
-    const int64_t lo = per * blockIdx.x;
-    const int64_t hi = lo + per < bytes ? lo + per : bytes;
-    for (int64_t a = lo; a < hi; a += 65536) {
-      const int64_t n = hi - a < 65536 ? hi - a : 65536;
-      ptx::prefetch_l2(static_cast<const char*>(base) + a, uint32_t(n));
-    }
-  };
-  share(p.k, kv);
-  share(p.v, kv);
-  share(p.q, qb);
+  const void* base = which == 0 ? (const void*)p.k : which == 1 ? (const void*)p.v : (const void*)p.q;
+  const int64_t bytes = which == 2 ? qb : kv;
+  // byte counts are multiples of 128 (D is 64 or 128), so are the shares
+  const int64_t per = ((bytes + gridDim.x - 1) / gridDim.x + 15) & ~int64_t(15);
+  const int64_t lo = per * blockIdx.x;
+  const int64_t hi = lo + per < bytes ? lo + per : bytes;
+  if (hi > lo) ptx::prefetch_l2(static_cast<const char*>(base) + lo, uint32_t(hi - lo));
 }
 
 // ---------------------------------------------------------------------------
@@ -352,9 +366,9 @@ __device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch, 
     __syncthreads();
     return;
   }
-  // the offsets are valid: one thread of an otherwise idle warp starts the
-  // DRAM reads of this CTA's share of the inputs
-  if (tid == 64) prefetch_inputs(p, off[n_user], D);
+  // the offsets are valid: start the DRAM reads of this CTA's share of the
+  // inputs (lane 0 of warps 1-3)
+  if (tid == 32 || tid == 64 || tid == 96) prefetch_inputs(p, off[n_user], D, (tid >> 5) - 1);
   const bool unsorted = (flags & kUnsorted) != 0;
   if (!unsorted && (flags & kGap)) {
     // sorted, with wide gaps between consecutive users: fill those now
@@ -586,16 +600,16 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(ptx::smem_addr(&ctl->q_full[i]), 1);
       ptx::mbar_init(ptx::smem_addr(&ctl->q_empty[i]), 1);
+    }
+    for (int i = 0; i < kSBufs; ++i) {
       ptx::mbar_init(ptx::smem_addr(&ctl->s_full[i]), 1);
       ptx::mbar_init(ptx::smem_addr(&ctl->p_full[i]), 8);
+      ptx::mbar_init(ptx::smem_addr(&ctl->pv_done[i]), 1);
     }
     for (int i = 0; i < kMaxSlots; ++i) {
       ptx::mbar_init(ptx::smem_addr(&ctl->kv_full[i]), 1);
       ptx::mbar_init(ptx::smem_addr(&ctl->kv_empty[i]), 1);
     }
-    for (int i = 0; i < 4; ++i)
-      for (int j = 0; j < 2; ++j) ptx::mbar_init(ptx::smem_addr(&ctl->xbar[i][j]), 2);
-    ptx::mbar_init(ptx::smem_addr(&ctl->pv_done), 1);
     ptx::mbar_init(ptx::smem_addr(&ctl->drain), 1);
     ptx::mbar_init(ptx::smem_addr(&ctl->pair_go), 1);
     ptx::mbar_init(ptx::smem_addr(&ctl->pair_recv), 1);
@@ -608,6 +622,8 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
     ptx::tmem_alloc(ptx::smem_addr(&ctl->tmem_base), C::kTmemCols);
     ptx::tmem_relinquish();
   }
+  // exchange words start with sequence number 3, which no first use expects
+  for (int i = threadIdx.x; i < 2 * 2 * kTileM; i += blockDim.x) (&ctl->xtag[0][0][0])[i] = 3u;
   if (warp == 2 && lane == 0) {
     // the host-encoded descriptors into the TMA unit's cache ahead of use
     ptx::prefetch_tensormap(&qmap);
@@ -619,6 +635,11 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (p.fused && layout_ok) plan_load(p, data);
   __syncthreads();
+  // Split cluster barrier (every thread, warps converged): arrive now, this
+  // CTA's barriers being initialised; wait once planning is done, before any
+  // access to the partner's shared memory.  The partner has long arrived by
+  // then, so the wait costs nothing.
+  ptx::cluster_arrive();
   trace_pro(p, 1);
   if (!layout_ok) {
     if (threadIdx.x == 0) {
@@ -642,9 +663,8 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
   }
   if (threadIdx.x == 0) trace(p, 0, kTrCtaStart);
   ptx::tc_fence_before();
-  // every thread of both CTAs: the plan is visible in this CTA and the
-  // partner's barriers are initialised before any remote arrive or store
-  ptx::cluster_sync();
+  __syncthreads();
+  ptx::cluster_wait();
   ptx::tc_fence_after();
   trace_pro(p, 8);
 
@@ -744,10 +764,13 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
           }
         }
         ++q_it;
-        // K/V tiles in the order the MMA warp consumes them: K0, K1, V0, K2, V1, ...
-        for (int j = 0; j <= n && ok; ++j) {
-          if (j < n) ok = load_tile(false, w.head, w.kv_begin + j * kBlockN);
-          if (ok && j >= 1) ok = load_tile(true, w.head, w.kv_begin + (j - 1) * kBlockN);
+        // K/V tiles in the order the MMA warp consumes them:
+        // K0, K1, K2, V0, K3, V1, K4, V2, ...
+        for (int j = 0; j < n && j < kSBufs && ok; ++j)
+          ok = load_tile(false, w.head, w.kv_begin + j * kBlockN);
+        for (int j = 0; j < n && ok; ++j) {
+          ok = load_tile(true, w.head, w.kv_begin + j * kBlockN);
+          if (ok && j + kSBufs < n) ok = load_tile(false, w.head, w.kv_begin + (j + kSBufs) * kBlockN);
         }
         trace(p, k, kTrProdIssued);
         if (ok && w.unit >= 0) {
@@ -789,61 +812,62 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
         ptx::tc_fence_after();
         trace(p, k, kTrMmaQ);
         const uint32_t q_base = ptx::smem_addr(q_smem + qb * C::kQBytes);
-        for (int j = 0; j <= n; ++j) {
-          if (j < n) {
-            const uint32_t slot = kv_it % NS;
-            if (!W.wait(ptx::smem_addr(&ctl->kv_full[slot]), (kv_it / NS) & 1u)) {
-              ok = false;
-              break;
-            }
-            ptx::tc_fence_after();
-            const uint32_t k_base = ptx::smem_addr(kv_smem + slot * C::kKVBytes);
-            const uint32_t sb = (g + j) & 1u;
-            const uint32_t d_tmem = tmem + C::kSCol + sb * kBlockN;
+        // S_j = Q K_j^T into S buffer (g + j) % 3
+        auto issue_s = [&](int j) -> bool {
+          const uint32_t slot = kv_it % NS;
+          if (!W.wait(ptx::smem_addr(&ctl->kv_full[slot]), (kv_it / NS) & 1u)) return false;
+          ptx::tc_fence_after();
+          const uint32_t k_base = ptx::smem_addr(kv_smem + slot * C::kKVBytes);
+          const uint32_t sb = (g + j) % kSBufs;
+          const uint32_t d_tmem = tmem + C::kSCol + sb * kBlockN;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const int cb = kk >> 2;
-              const uint32_t koff = (kk & 3) * 32;
-              const uint64_t a = ptx::smem_desc_sw128(q_base + cb * kTileM * 128 + koff, 16, 1024);
-              const uint64_t bdesc = ptx::smem_desc_sw128(k_base + cb * kBlockN * 128 + koff, 16, 1024);
-              ptx::mma_ss(d_tmem, a, bdesc, kIdescQK, kk > 0 ? 1u : 0u);
-            }
-            if (j == 0) trace(p, k, kTrMmaFirstS);
-            ptx::mma_commit(ptx::smem_addr(&ctl->kv_empty[slot]));
-            ptx::mma_commit(ptx::smem_addr(&ctl->s_full[sb]));
-            if (j == n - 1) ptx::mma_commit(ptx::smem_addr(&ctl->q_empty[qb]));
-            ++kv_it;
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const int cb = kk >> 2;
+            const uint32_t koff = (kk & 3) * 32;
+            const uint64_t a = ptx::smem_desc_sw128(q_base + cb * kTileM * 128 + koff, 16, 1024);
+            const uint64_t bdesc = ptx::smem_desc_sw128(k_base + cb * kBlockN * 128 + koff, 16, 1024);
+            ptx::mma_ss(d_tmem, a, bdesc, kIdescQK, kk > 0 ? 1u : 0u);
           }
-          if (j >= 1) {
-            const uint32_t pj = g + j - 1;
-            const uint32_t pb = pj & 1u;
-            if (!W.wait(ptx::smem_addr(&ctl->p_full[pb]), (pj >> 1) & 1u)) {
-              ok = false;
-              break;
-            }
-            ptx::tc_fence_after();
-            const uint32_t slot = kv_it % NS;
-            if (!W.wait(ptx::smem_addr(&ctl->kv_full[slot]), (kv_it / NS) & 1u)) {
-              ok = false;
-              break;
-            }
-            ptx::tc_fence_after();
-            const uint32_t v_base = ptx::smem_addr(kv_smem + slot * C::kKVBytes);
-            const uint32_t a_tmem = tmem + C::kSCol + pb * kBlockN;
-            // V is MN-major (d contiguous): 8-key groups 1 KB apart, the two
-            // 64-column blocks of a D = 128 tile kBlockN * 128 bytes apart
+          if (j == 0) trace(p, k, kTrMmaFirstS);
+          if (j < 8) trace_tile(p, k, 2, 2 * j);
+          ptx::mma_commit(ptx::smem_addr(&ctl->kv_empty[slot]));
+          ptx::mma_commit(ptx::smem_addr(&ctl->s_full[sb]));
+          if (j == n - 1) ptx::mma_commit(ptx::smem_addr(&ctl->q_empty[qb]));
+          ++kv_it;
+          return true;
+        };
+        for (int j = 0; j < n && j < kSBufs && ok; ++j) ok = issue_s(j);
+        for (int j = 0; j < n && ok; ++j) {
+          // O += P_j V_j once the softmax has written P_j over S_j
+          const uint32_t gj = g + j;
+          const uint32_t pb = gj % kSBufs;
+          if (!W.wait(ptx::smem_addr(&ctl->p_full[pb]), (gj / kSBufs) & 1u)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t slot = kv_it % NS;
+          if (!W.wait(ptx::smem_addr(&ctl->kv_full[slot]), (kv_it / NS) & 1u)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t v_base = ptx::smem_addr(kv_smem + slot * C::kKVBytes);
+          const uint32_t a_tmem = tmem + C::kSCol + pb * kBlockN;
+          // V is MN-major (d contiguous): 8-key groups 1 KB apart, the two
+          // 64-column blocks of a D = 128 tile kBlockN * 128 bytes apart
 #pragma unroll
-            for (int kk = 0; kk < kBlockN / 16; ++kk) {
-              const uint64_t bdesc =
-                  ptx::smem_desc_sw128(v_base + kk * 16 * 128, kBlockN * 128, 1024);
-              ptx::mma_ts(tmem + C::kOCol, a_tmem + kk * 8, bdesc, kIdescPV,
-                          (j > 1 || kk > 0) ? 1u : 0u);
-            }
-            ptx::mma_commit(ptx::smem_addr(&ctl->kv_empty[slot]));
-            ptx::mma_commit(ptx::smem_addr(&ctl->pv_done));
-            if (j == n) trace(p, k, kTrMmaLastPV);
-            ++kv_it;
+          for (int kk = 0; kk < kBlockN / 16; ++kk) {
+            const uint64_t bdesc = ptx::smem_desc_sw128(v_base + kk * 16 * 128, kBlockN * 128, 1024);
+            ptx::mma_ts(tmem + C::kOCol, a_tmem + kk * 8, bdesc, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
           }
+          if (j < 8) trace_tile(p, k, 2, 2 * j + 1);
+          ptx::mma_commit(ptx::smem_addr(&ctl->kv_empty[slot]));
+          ptx::mma_commit(ptx::smem_addr(&ctl->pv_done[pb]));
+          if (j == n - 1) trace(p, k, kTrMmaLastPV);
+          ++kv_it;
+          // the S buffer of P_j is free once PV_j has read it (MMAs run in order)
+          if (j + kSBufs < n) ok = issue_s(j + kSBufs);
         }
         g += n;
         ++q_it;
@@ -861,144 +885,195 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
     const uint32_t lane_off = uint32_t(quarter * 32) << 16;
     const float sl2 = p.scale_log2;
     const float2 sl2x2 = make_float2(sl2, sl2);
-    uint32_t g = 0, pv_it = 0, xs = 0;
-    // Exchange one float per row with the other half (bounded, like every wait).
-    auto exchange = [&](float mine, float& theirs) -> bool {
-      const uint32_t par = xs & 1u;
-      ctl->xchg[par][half][row] = mine;
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&ctl->xbar[quarter][par]));
-      const bool ok = W.warp_wait(ptx::smem_addr(&ctl->xbar[quarter][par]), (xs >> 1) & 1u);
-      theirs = ctl->xchg[par][half ^ 1][row];
+    uint32_t g = 0, xs = 0;
+    // PV(x) commits to pv_done[x % 3], phase x / 3.  A wait for PV(x) is
+    // made only on tile x + 1 (to rescale O) or after the item's last tile
+    // x: by then S(x) is complete, so PV(x - 3), the barrier's previous
+    // phase, is complete (the MMA warp issues S(x) after it), and PV(x + 3),
+    // its next phase, needs this warp's p_full(x + 3).  The parity of the
+    // phase is therefore unambiguous without observing every phase.
+    // PV(x) complete implies every earlier PV complete (MMAs run in order).
+    auto pv_wait = [&](uint32_t x) -> bool {
+      if (!W.warp_wait(ptx::smem_addr(&ctl->pv_done[x % kSBufs]), (x / kSBufs) & 1u)) return false;
+      ptx::tc_fence_after();
+      return true;
+    };
+    // Row values shared with the other half of the row: a value goes out with
+    // the exchange's sequence number in its two low bits (it moves by at most
+    // 3 ulp; -inf and NaN go out as -FLT_MAX) and the partner's value is taken
+    // once its word carries the same number.  Both halves then use the same
+    // two words.  The wait is bounded like every wait.
+    auto publish = [&](float v) -> float {
+      const float vv = v > -FLT_MAX ? v : -FLT_MAX;
+      const uint32_t wv = (__float_as_uint(vv) & ~3u) | (xs & 3u);
+      asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(
+                       ptx::smem_addr(&ctl->xtag[xs & 1u][half][row])),
+                   "r"(wv)
+                   : "memory");
+      return __uint_as_float(wv & ~3u);
+    };
+    auto collect = [&](float& v) -> bool {
+      const uint32_t addr = ptx::smem_addr(&ctl->xtag[xs & 1u][half ^ 1][row]);
+      const uint32_t tag = xs & 3u;
       ++xs;
-      return ok;
+      uint32_t wv = 0;
+      bool ok = true;
+      uint64_t t_end = 0;
+      for (uint32_t spin = 0;; ++spin) {
+        asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(wv) : "r"(addr) : "memory");
+        if ((wv & 3u) == tag) break;
+        if ((spin & 127u) == 127u) {
+          if (*W.abort) {
+            ok = false;
+            break;
+          }
+          const uint64_t now = ptx::globaltimer();
+          if (t_end == 0) {
+            t_end = now + p.timeout_ns;
+          } else if (now > t_end) {
+            *W.abort = 1;
+            atomicOr(p.err_word, kErrTimeout);
+            ok = false;
+            break;
+          }
+        }
+      }
+      v = __uint_as_float(wv & ~3u);
+      return __all_sync(0xffffffffu, ok);
     };
     for (int k = 0; k < n_my; ++k) {
       const WorkItem w = item_at(k);
       const int n = ceil_div(w.kv_len, kBlockN);
       const int rows = w.n_cand * Lq;
+      // Rows past the item's queries hold stale shared memory; their results
+      // are never stored, and they are left out of every decision below.
+      const bool live = row < rows;
       float m = -INFINITY, l = 0.f;
       bool ok = true;
       for (int j = 0; j < n; ++j) {
         const uint32_t gj = g + j;
-        const uint32_t sb = gj & 1u;
-        if (!W.warp_wait(ptx::smem_addr(&ctl->s_full[sb]), (gj >> 1) & 1u)) {
+        const uint32_t sb = gj % kSBufs;
+        if (!W.warp_wait(ptx::smem_addr(&ctl->s_full[sb]), (gj / kSBufs) & 1u)) {
           ok = false;
           break;
         }
         ptx::tc_fence_after();
         if (j == 0 && row == 0 && half == 0) trace(p, k, kTrSmS0);
+        const bool tr_t = row == 0 && half == 0 && j < 4;
+        if (tr_t) trace_tile(p, k, 1, 4 * j);
         const uint32_t scol = tmem + lane_off + C::kSCol + sb * kBlockN;
-        float t[64];
-        {
-          uint32_t r[2][32];
-          ptx::tmem_ld32(scol + half * 64, r[0]);
-          ptx::tmem_ld32(scol + half * 64 + 32, r[1]);
-          ptx::tmem_ld_wait();
-          // scaled scores t = s * scale * log2(e)
-#pragma unroll
-          for (int e = 0; e < 64; e += 2) {
-            const float2 v = fmul2(make_float2(__uint_as_float(r[e >> 5][e & 31]),
-                                               __uint_as_float(r[e >> 5][(e & 31) + 1])),
-                                   sl2x2);
-            t[e] = v.x;
-            t[e + 1] = v.y;
-          }
-        }
-        // keys of this half that exist (the tile's tail may be short)
+        uint32_t r[2][32];
+        ptx::tmem_ld32(scol + half * 64, r[0]);
+        ptx::tmem_ld32(scol + half * 64 + 32, r[1]);
+        ptx::tmem_ld_wait();
+#define IKBO_S(e) __uint_as_float(r[(e) >> 5][(e) & 31])
+        // Scores enter the exponent as fma(s, sc, -ref).  On a tile whose
+        // tail is short, or for scale <= 0, they are scaled here first and
+        // the missing keys set to -inf (sc = 1); otherwise sc = scale and the
+        // order of the raw scores is that of the scaled ones.
         const int valid = min(kBlockN, w.kv_len - j * kBlockN) - half * 64;
-        if (valid < 64) {
+        float sc = sl2;
+        if (valid < 64 || !(sl2 > 0.f)) {
 #pragma unroll
-          for (int e = 0; e < 64; ++e)
-            if (e >= valid) t[e] = -INFINITY;
+          for (int e = 0; e < 64; ++e) {
+            const float tt = IKBO_S(e) * sl2;
+            r[e >> 5][e & 31] = __float_as_uint(e < valid ? tt : -INFINITY);
+          }
+          sc = 1.f;
         }
         float mx;
         {
-          float a = fmax3(t[0], t[1], t[2]), b2 = fmax3(t[3], t[4], t[5]);
-          float c2 = fmax3(t[6], t[7], t[8]), d2 = fmax3(t[9], t[10], t[11]);
+          // four independent chains
+          float a0 = fmaxf(IKBO_S(0), IKBO_S(1)), a1 = fmaxf(IKBO_S(2), IKBO_S(3));
+          float a2 = fmaxf(IKBO_S(4), IKBO_S(5)), a3 = fmaxf(IKBO_S(6), IKBO_S(7));
 #pragma unroll
-          for (int e = 12; e < 60; e += 8) {
-            a = fmax3(a, t[e], t[e + 1]);
-            b2 = fmax3(b2, t[e + 2], t[e + 3]);
-            c2 = fmax3(c2, t[e + 4], t[e + 5]);
-            d2 = fmax3(d2, t[e + 6], t[e + 7]);
+          for (int e = 8; e < 64; e += 8) {
+            a0 = fmax3(a0, IKBO_S(e), IKBO_S(e + 1));
+            a1 = fmax3(a1, IKBO_S(e + 2), IKBO_S(e + 3));
+            a2 = fmax3(a2, IKBO_S(e + 4), IKBO_S(e + 5));
+            a3 = fmax3(a3, IKBO_S(e + 6), IKBO_S(e + 7));
           }
-          a = fmax3(a, t[60], t[61]);
-          b2 = fmax3(b2, t[62], t[63]);
-          mx = fmax3(a, b2, fmaxf(c2, d2));
+          mx = fmax3(a0, a1, fmaxf(a2, a3)) * sc;
         }
-        // the other half of the row; its S reads are complete once it has arrived
+        // This half's S reads are complete: the other half may write P over
+        // them once it has seen this maximum.
         ptx::tc_fence_before();
+        if (tr_t) trace_tile(p, k, 1, 4 * j + 1);
+        const float mx_mine = publish(mx);
+        // P = 2^(t - ref) as bf16 pairs, and its row sum
+        uint32_t pk[32];
+        float sum = 0.f;
+        auto exps = [&](float ref) {
+          const float2 sc2 = make_float2(sc, sc), nr2 = make_float2(-ref, -ref);
+          float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int e = 0; e < 64; e += 2) {
+            const float2 x = ffma2(make_float2(IKBO_S(e), IKBO_S(e + 1)), sc2, nr2);
+            const float2 pe = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+            if ((e >> 1) & 1) a1 = fadd2(a1, pe); else a0 = fadd2(a0, pe);
+            pk[e >> 1] = pack_bf16(pe.x, pe.y);
+          }
+          const float2 u = fadd2(a0, a1);
+          sum = u.x + u.y;
+        };
+        // Against the running maximum while the partner's maximum is on its
+        // way (it stands unless the maximum moves); against the new maximum
+        // on the first tile and when it moves.
+        if (j > 0) exps(m);
         float mx_other;
-        if (!exchange(mx, mx_other)) {
+        if (!collect(mx_other)) {
           ok = false;
           break;
         }
+        const float mxa = fmaxf(mx_mine, mx_other);
+        const float m_new = (j == 0 || mxa > m + kLazyRescale) ? mxa : m;
+        if (j == 0 || __any_sync(0xffffffffu, live && m_new != m)) exps(m_new);
+#undef IKBO_S
+        if (!ok) break;
         ptx::tc_fence_after();
-        mx = fmaxf(mx, mx_other);
-        const float m_new = (m == -INFINITY || mx > m + kLazyRescale) ? fmaxf(m, mx) : m;
+        if (tr_t) trace_tile(p, k, 1, 4 * j + 2);
         const float alpha = fast_exp2(m - m_new);   // 0 on the first tile, 1 when m stays
-        const float2 neg_m = make_float2(-m_new, -m_new);
-        float2 acc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
-        uint32_t pk[32];
-#pragma unroll
-        for (int e = 0; e < 64; e += 2) {
-          const float2 x = fadd2(make_float2(t[e], t[e + 1]), neg_m);
-          const float2 pe = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-          acc[(e >> 1) & 3] = fadd2(acc[(e >> 1) & 3], pe);
-          pk[e >> 1] = pack_bf16(pe.x, pe.y);
-        }
-        const float sum = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y) +
-                          ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
         l = l * alpha + sum;
         // P (bf16 pairs) over the first half of this S buffer: keys 64h.. at column 32h
         ptx::tmem_st32(scol + half * 32, pk);
         ptx::tmem_st_wait();
-        if (j > 0) {
-          // O holds P_0..P_{j-1} V: wait for PV_{j-1}, then rescale if m moved.
-          if (!W.warp_wait(ptx::smem_addr(&ctl->pv_done), pv_it & 1u)) {
+        if (j > 0 && __any_sync(0xffffffffu, live && m_new != m)) {
+          // O must hold exactly P_0..P_{j-1} V when it is rescaled: PV_{j-1}
+          // complete (MMAs complete in order), PV_j not issued before p_full
+          if (!pv_wait(gj - 1)) {
             ok = false;
             break;
           }
-          ++pv_it;
-          ptx::tc_fence_after();
-          if (__any_sync(0xffffffffu, m_new != m)) {
-            const uint32_t ocol = tmem + lane_off + C::kOCol + half * C::kHalf;
-            const float2 a2 = make_float2(alpha, alpha);
+          const uint32_t ocol = tmem + lane_off + C::kOCol + half * C::kHalf;
 #pragma unroll
-            for (int c = 0; c < C::kChunks; ++c) {
-              uint32_t o[32];
-              ptx::tmem_ld32(ocol + c * 32, o);
-              ptx::tmem_ld_wait();
+          for (int c = 0; c < C::kChunks; ++c) {
+            uint32_t o[32];
+            ptx::tmem_ld32(ocol + c * 32, o);
+            ptx::tmem_ld_wait();
 #pragma unroll
-              for (int e = 0; e < 32; e += 2) {
-                const float2 v =
-                    fmul2(make_float2(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), a2);
-                o[e] = __float_as_uint(v.x);
-                o[e + 1] = __float_as_uint(v.y);
-              }
-              ptx::tmem_st32(ocol + c * 32, o);
-            }
-            ptx::tmem_st_wait();
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            ptx::tmem_st32(ocol + c * 32, o);
           }
+          ptx::tmem_st_wait();
         }
         m = m_new;
         ptx::tc_fence_before();
         __syncwarp();
+        if (tr_t) trace_tile(p, k, 1, 4 * j + 3);
         if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&ctl->p_full[sb]));
       }
       if (!ok) break;
       if (row == 0 && half == 0) trace(p, k, kTrSmLastP);
-      // ---- epilogue
-      if (!W.warp_wait(ptx::smem_addr(&ctl->pv_done), pv_it & 1u)) break;
-      ++pv_it;
-      ptx::tc_fence_after();
+      // ---- epilogue: the row sum goes out now, O is complete after the last PV
+      const float l_mine = publish(l);
+      if (!pv_wait(g + n - 1)) break;
       if (row == 0 && half == 0) trace(p, k, kTrEpiO);
       float l_other;
-      if (!exchange(l, l_other)) break;
-      const float lt = l + l_other;                // both halves share the running max m
+      if (!collect(l_other)) break;
+      const float lt = l_mine + l_other;           // both halves share the running max m
+      const bool tr_epi = row == 32 && half == 0;  // epilogue timeline: one thread
+      if (tr_epi) trace(p, k, kTrEpiSums);
       const uint32_t ocol = tmem + lane_off + C::kOCol + half * C::kHalf;
-      const bool live = row < rows;
       // A split unit: each CTA of the pair finishes half of the rows (CTA 0
       // the first, CTA 1 the second) and sends the other half to its partner.
       const bool paired = w.unit >= 0;
@@ -1035,6 +1110,7 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
           ptx::st_async_f32(ptx::map_to_cta(ptx::smem_addr(&ctl->partner_lse[row]), peer),
                             lt > 0.f ? m + fast_log2(lt) : -INFINITY, rbar);
         if (row == 0 && half == 0) trace(p, k, kTrEpiStored);
+        if (tr_epi) trace(p, k, kTrEpiSent);
       }
       if (__any_sync(0xffffffffu, keep)) {
         const int ci = keep ? row / Lq : 0;
@@ -1088,6 +1164,7 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
           }
         }
         if (row == 0 && half == 0) trace(p, k, paired ? kTrMerged : kTrEpiStored);
+        if (tr_epi) trace(p, k, kTrEpiKept);
       }
       g += n;
     }

@@ -57,7 +57,7 @@ struct PlanParams {
   int64_t n_cand;
   int64_t n_user;
   int32_t H;
-  int32_t cands_per_tile;   // floor(128 / Lq), rounded down to the Q-box granularity
+  int32_t cands_per_tile;   // floor(128 / Lq)
   int32_t block_n;          // keys per K/V tile
   int32_t num_sms;          // SMs of the device
   int32_t max_items;        // capacity of the work list
@@ -127,7 +127,10 @@ enum TracePoint {
   kTrEpiStored = 9,     // epilogue: output / partial stored
   kTrArrived = 10,      // split: arrival counted
   kTrMerged = 11,       // split: merge done (last arriver)
-  kTrCtaEnd = 12        // before teardown (item slot 0 only)
+  kTrCtaEnd = 12,       // before teardown (item slot 0 only)
+  kTrEpiSums = 13,      // epilogue, row 32: row sums of both halves combined
+  kTrEpiSent = 14,      // epilogue, row 32: its warp's rows for the partner sent
+  kTrEpiKept = 15       // epilogue, row 32: its warp's own rows stored
 };
 
 __device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
@@ -164,6 +167,17 @@ __device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
   asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
   asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(rd) : "l"(ra), "l"(rb));
+  float2 d;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
+  return d;
+}
+
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  uint64_t ra, rb, rc, rd;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(rc) : "f"(c.x), "f"(c.y));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
   float2 d;
   asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
   return d;

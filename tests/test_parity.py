@@ -109,6 +109,19 @@ def test_unsorted_mapping(gpu_lib, D, kernel):
     assert_close(out_f64(out), oracle.attention_wl(wl), f"unsorted D={D} kernel={kernel}")
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("scale", [0.0, -0.125, 1.0, 4.0])
+def test_scale_values(gpu_lib, scale, kernel):
+    """Any finite scale: 0 gives uniform weights, a negative one reverses the
+    order of the scores, large ones move the running maximum tile after tile
+    (the rescaling path)."""
+    base = W.custom(n_user=3, counts=[70, 5, 33], lens=[900, 129, 300], H=2, D=64, Lq=2, seed=21)
+    wl = W.Workload(cfg=base.cfg, q=base.q, k=base.k, v=base.v, user_offsets=base.user_offsets,
+                    cand_to_user=base.cand_to_user, scale=scale)
+    out = run(gpu_lib, wl, kernel)
+    assert_close(out_f64(out), oracle.attention_wl(wl), f"scale={scale} kernel={kernel}")
+
+
 def test_kernels_agree_at_full_size(gpu_lib):
     wl = workload("odd_groups_2048x16")
     a = run(gpu_lib, wl, 0).float()
