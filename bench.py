@@ -65,30 +65,87 @@ def config_block(wl, extra=None):
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle sampling while the GPU is busy."""
+    """SM clock and clock-event reasons while the GPU works, read (never set)
+    through NVML from a background thread every ~2 ms; nvidia-smi sampling
+    (every 100 ms) when NVML cannot be loaded.  mark_start()/mark_end()
+    bracket the timed region: the summary uses the samples inside it."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NVML_CLOCK_SM = 1
+    REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                   0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+    SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
+    def __init__(self, cuda_index: int):
+        self.cuda_index = cuda_index
+        self.samples = []            # (t, sm_mhz, max_mhz, reason bits)
+        self.window = [None, None]
+        self.thread = None
+        self.stop = False
         self.proc = None
         self.path = None
+        self.source = None
+
+    def _nvml_handle(self):
+        import ctypes
+        import torch
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        props = torch.cuda.get_device_properties(self.cuda_index)
+        bus = getattr(props, "pci_bus_id", None)
+        ok = False
+        if bus is not None:
+            pci = "%08X:%02X:%02X.0" % (getattr(props, "pci_domain_id", 0), bus, getattr(props, "pci_device_id", 0))
+            ok = lib.nvmlDeviceGetHandleByPciBusId_v2(pci.encode(), ctypes.byref(h)) == 0
+        if not ok and lib.nvmlDeviceGetHandleByIndex_v2(self.cuda_index, ctypes.byref(h)) != 0:
+            raise RuntimeError("no NVML handle")
+        reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        return lib, h, reasons
+
+    def _run(self, lib, h, reasons_fn):
+        import ctypes
+        clk, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self.stop:
+            if (lib.nvmlDeviceGetClockInfo(h, self.NVML_CLOCK_SM, ctypes.byref(clk)) == 0
+                    and lib.nvmlDeviceGetMaxClockInfo(h, self.NVML_CLOCK_SM, ctypes.byref(mx)) == 0):
+                r = rs.value if reasons_fn(h, ctypes.byref(rs)) == 0 else 0
+                self.samples.append((time.perf_counter(), float(clk.value), float(mx.value), int(r)))
+            time.sleep(0.002)
 
     def __enter__(self):
+        import threading
         try:
-            fd, self.path = tempfile.mkstemp(suffix=".csv")
-            os.close(fd)
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100", "-f", self.path],
-                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+            lib, h, reasons = self._nvml_handle()
+            self.thread = threading.Thread(target=self._run, args=(lib, h, reasons), daemon=True)
+            self.thread.start()
+            self.source = "nvml"
         except Exception:
-            self.proc = None
+            try:
+                fd, self.path = tempfile.mkstemp(suffix=".csv")
+                os.close(fd)
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", f"--id={self.cuda_index}", f"--query-gpu={self.SMI_FIELDS}",
+                     "--format=csv,noheader,nounits", "-lms", "100", "-f", self.path],
+                    stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+                self.source = "nvidia-smi"
+            except Exception:
+                self.proc = None
         return self
 
+    def mark_start(self):
+        self.window[0] = time.perf_counter()
+
+    def mark_end(self):
+        self.window[1] = time.perf_counter()
+
     def __exit__(self, *exc):
+        self.stop = True
+        if self.thread is not None:
+            self.thread.join(timeout=5)
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -97,6 +154,20 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
+        if self.source == "nvml":
+            t0, t1 = self.window
+            inside = [s for s in self.samples if t0 is not None and t1 is not None and t0 <= s[0] <= t1]
+            used = inside or self.samples
+            if not used:
+                return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "source": "nvml"}
+            reasons = set()
+            for s in used:
+                for bit, name in self.REASON_BITS.items():
+                    if s[3] & bit:
+                        reasons.add(name)
+            return {"sm_mhz": statistics.median(s[1] for s in used), "sm_max_mhz": max(s[2] for s in used),
+                    "samples": len(used), "in_timed_region": bool(inside), "reasons": sorted(reasons),
+                    "source": "nvml"}
         if not self.path or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
         sm, smax, reasons = [], [], set()
@@ -119,7 +190,7 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         busy = [x for x in sm if x > 0.5 * max(sm)] or sm
         return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(smax),
-                "samples": len(sm), "reasons": sorted(reasons)}
+                "samples": len(sm), "reasons": sorted(reasons), "source": "nvidia-smi"}
 
 
 # the files the tcgen05 attention kernel is compiled from
@@ -267,12 +338,14 @@ def run_ikbo(args):
         starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         barrier()
+        clk.mark_start()
         for i in range(args.steps):
             flush.fill_(i & 0xFF)
             starts[i].record()
             step()
             ends[i].record()
         barrier()
+        clk.mark_end()
         step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
         # 2. per-kernel durations (events recorded by the library around each kernel)
         ikbo.set_timing(True)
