@@ -66,64 +66,71 @@ def config_block(wl, extra=None):
 
 class ClockSampler:
     """SM clock and clock-event reasons while the GPU works, read (never set)
-    through NVML from a background thread every ~2 ms; nvidia-smi sampling
-    (every 100 ms) when NVML cannot be loaded.  mark_start()/mark_end()
-    bracket the timed region: the summary uses the samples inside it."""
+    through NVML by a poller process every ~1 ms; nvidia-smi sampling (every
+    100 ms) when NVML cannot be loaded.  mark_start()/mark_end() bracket the
+    timed region: the summary uses the samples inside it."""
 
-    NVML_CLOCK_SM = 1
     REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
                    0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
     SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                   "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                   "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # In a process of its own, so that it samples whatever the benchmark's
+    # Python thread is doing.  NVML clock type 1 is the SM clock.
+    POLLER = r"""
+import ctypes, sys, time
+lib = ctypes.CDLL("libnvidia-ml.so.1")
+assert lib.nvmlInit_v2() == 0
+h = ctypes.c_void_p()
+bus = sys.argv[1]
+if not (bus and lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) == 0):
+    assert lib.nvmlDeviceGetHandleByIndex_v2(int(sys.argv[2]), ctypes.byref(h)) == 0
+reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or lib.nvmlDeviceGetCurrentClocksThrottleReasons
+clk, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+print("ready", flush=True)
+while True:
+    if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+        r = rs.value if reasons(h, ctypes.byref(rs)) == 0 else 0
+        print(time.monotonic(), clk.value, mx.value, r, flush=True)
+    time.sleep(0.001)
+"""
 
     def __init__(self, cuda_index: int):
         self.cuda_index = cuda_index
         self.samples = []            # (t, sm_mhz, max_mhz, reason bits)
         self.window = [None, None]
-        self.thread = None
-        self.stop = False
+        self.out = None
         self.proc = None
         self.path = None
         self.source = None
 
-    def _nvml_handle(self):
-        import ctypes
+    def _start_nvml(self):
         import torch
-        lib = ctypes.CDLL("libnvidia-ml.so.1")
-        if lib.nvmlInit_v2() != 0:
-            raise RuntimeError("nvmlInit failed")
-        h = ctypes.c_void_p()
         props = torch.cuda.get_device_properties(self.cuda_index)
-        bus = getattr(props, "pci_bus_id", None)
-        ok = False
-        if bus is not None:
-            pci = "%08X:%02X:%02X.0" % (getattr(props, "pci_domain_id", 0), bus, getattr(props, "pci_device_id", 0))
-            ok = lib.nvmlDeviceGetHandleByPciBusId_v2(pci.encode(), ctypes.byref(h)) == 0
-        if not ok and lib.nvmlDeviceGetHandleByIndex_v2(self.cuda_index, ctypes.byref(h)) != 0:
-            raise RuntimeError("no NVML handle")
-        reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
-            lib.nvmlDeviceGetCurrentClocksThrottleReasons
-        return lib, h, reasons
-
-    def _run(self, lib, h, reasons_fn):
-        import ctypes
-        clk, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
-        while not self.stop:
-            if (lib.nvmlDeviceGetClockInfo(h, self.NVML_CLOCK_SM, ctypes.byref(clk)) == 0
-                    and lib.nvmlDeviceGetMaxClockInfo(h, self.NVML_CLOCK_SM, ctypes.byref(mx)) == 0):
-                r = rs.value if reasons_fn(h, ctypes.byref(rs)) == 0 else 0
-                self.samples.append((time.perf_counter(), float(clk.value), float(mx.value), int(r)))
-            time.sleep(0.002)
+        bus = ""
+        if getattr(props, "pci_bus_id", None) is not None:
+            bus = "%08X:%02X:%02X.0" % (getattr(props, "pci_domain_id", 0), props.pci_bus_id,
+                                        getattr(props, "pci_device_id", 0))
+        fd, self.path = tempfile.mkstemp(suffix=".txt")
+        self.out = os.fdopen(fd, "w")
+        self.proc = subprocess.Popen([sys.executable, "-c", self.POLLER, bus, str(self.cuda_index)],
+                                     stdout=self.out, stderr=subprocess.DEVNULL)
+        t_end = time.monotonic() + 10          # wait (bounded) until the poller runs
+        while time.monotonic() < t_end and self.proc.poll() is None:
+            with open(self.path) as f:
+                if f.readline().startswith("ready"):
+                    return
+            time.sleep(0.01)
+        raise RuntimeError("NVML poller did not start")
 
     def __enter__(self):
-        import threading
         try:
-            lib, h, reasons = self._nvml_handle()
-            self.thread = threading.Thread(target=self._run, args=(lib, h, reasons), daemon=True)
-            self.thread.start()
+            self._start_nvml()
             self.source = "nvml"
         except Exception:
+            if self.proc is not None:
+                self.proc.kill()
+                self.proc = None
             try:
                 fd, self.path = tempfile.mkstemp(suffix=".csv")
                 os.close(fd)
@@ -137,35 +144,40 @@ class ClockSampler:
         return self
 
     def mark_start(self):
-        self.window[0] = time.perf_counter()
+        self.window[0] = time.monotonic()
 
     def mark_end(self):
-        self.window[1] = time.perf_counter()
+        self.window[1] = time.monotonic()
 
     def __exit__(self, *exc):
-        self.stop = True
-        if self.thread is not None:
-            self.thread.join(timeout=5)
         if self.proc is not None:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
+        if self.out is not None:
+            self.out.close()
 
     def summary(self):
         if self.source == "nvml":
+            with open(self.path) as f:
+                for line in f:
+                    parts = line.split()
+                    if len(parts) == 4:
+                        self.samples.append((float(parts[0]), float(parts[1]), float(parts[2]), int(parts[3])))
+            os.unlink(self.path)
             t0, t1 = self.window
-            inside = [s for s in self.samples if t0 is not None and t1 is not None and t0 <= s[0] <= t1]
+            inside = [x for x in self.samples if t0 is not None and t1 is not None and t0 <= x[0] <= t1]
             used = inside or self.samples
             if not used:
                 return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "source": "nvml"}
             reasons = set()
-            for s in used:
+            for x in used:
                 for bit, name in self.REASON_BITS.items():
-                    if s[3] & bit:
+                    if x[3] & bit:
                         reasons.add(name)
-            return {"sm_mhz": statistics.median(s[1] for s in used), "sm_max_mhz": max(s[2] for s in used),
+            return {"sm_mhz": statistics.median(x[1] for x in used), "sm_max_mhz": max(x[2] for x in used),
                     "samples": len(used), "in_timed_region": bool(inside), "reasons": sorted(reasons),
                     "source": "nvml"}
         if not self.path or not os.path.exists(self.path):

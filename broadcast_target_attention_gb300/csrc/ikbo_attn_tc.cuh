@@ -77,6 +77,9 @@ namespace ikbo {
 constexpr int kBlockN = 128;      // keys per K/V tile
 constexpr int kTcThreads = 384;
 constexpr int kSoftmaxWarp0 = 4;  // warps 4..11 run the softmax
+// Hardware barrier 1: warp 0 releases the other warps when the plan is done
+// (barrier 0 is __syncthreads).
+constexpr int kBarPlanDone = 1;
 // The running maximum is moved only when a tile's maximum exceeds it by more
 // than this (base-2 units), so un-normalised weights stay <= 2^8 and the
 // O correction is skipped on most tiles; the final O / l is exact either way.
@@ -145,6 +148,8 @@ struct TcCtrl {
   int go_sent;
   int total_keys;
   int flags;
+  int n_units;                          // planning: units in all (read by every thread)
+  int early_loads;                      // ring loads of item 0 issued before the roles start
   int red[12];
   WorkItem items[kCtlItems];            // the first items of this CTA (the rest in global memory)
   alignas(16) float partner_lse[kTileM];
@@ -306,8 +311,33 @@ struct PlanScratch {
 __device__ __forceinline__ void plan_load(const AttnParams& p, uint8_t* scratch) {
   const int n_cand = (int)p.n_cand, n_user = (int)p.n_user;
   PlanScratch S(scratch, n_user, n_cand);
-  for (int u = threadIdx.x; u <= n_user; u += blockDim.x) S.off[u] = p.user_offsets[u];
-  for (int c = threadIdx.x; c < n_cand; c += blockDim.x) S.c2u[c] = p.cand_to_user[c];
+  // up to four loads of each thread in flight at once
+  for (int base = 0; base <= n_user; base += 4 * blockDim.x) {
+    int v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int u = base + i * blockDim.x + threadIdx.x;
+      v[i] = u <= n_user ? p.user_offsets[u] : 0;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int u = base + i * blockDim.x + threadIdx.x;
+      if (u <= n_user) S.off[u] = v[i];
+    }
+  }
+  for (int base = 0; base < n_cand; base += 4 * blockDim.x) {
+    int v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int c = base + i * blockDim.x + threadIdx.x;
+      v[i] = c < n_cand ? p.cand_to_user[c] : 0;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int c = base + i * blockDim.x + threadIdx.x;
+      if (c < n_cand) S.c2u[c] = v[i];
+    }
+  }
 }
 
 __device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch, int D) {
@@ -469,7 +499,10 @@ __device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch, 
           if (tid >= o) v += y;
         }
         if (tid < n_user) ubefore[tid] = v - nu;
-        if (tid == 31) ubefore[n_user] = v;
+        if (tid == 31) {
+          ubefore[n_user] = v;
+          ctl->n_units = v;
+        }
       }
     } else {
       int carry = 0;
@@ -481,12 +514,20 @@ __device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch, 
         if (rk < n_user) ubefore[rk] = carry + ex;
         carry += tot;
       }
-      if (tid == 0) ubefore[n_user] = carry;
+      if (tid == 0) {
+        ubefore[n_user] = carry;
+        ctl->n_units = carry;
+      }
     }
+    // the scratch may be overwritten by TMA (async proxy) once the decode
+    // that follows is done
+    ptx::fence_proxy_async_smem();
     __syncthreads();
   };
   prefix();
-  const int N = ubefore[n_user];
+  // from the control block: after this barrier only thread 0 reads the
+  // scratch (the pair-mode decode), so it may start the TMA into it
+  const int N = ctl->n_units;
   // Pair mode when every unit gets a cluster of its own; otherwise units are
   // dealt to independent CTAs, users longest first.
   const bool pair = N > 0 && 2 * N <= grid;
@@ -574,7 +615,8 @@ __device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch, 
     ctl->sorted = unsorted ? 0 : 1;
     ctl->total_keys = off[n_user];
   }
-  __syncthreads();
+  // no closing barrier: the kernel's follows (after thread 0 may have
+  // started the first TMA loads)
 }
 
 // ---------------------------------------------------------------------------
@@ -616,6 +658,7 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
     ctl->go_sent = 0;
     ctl->abort_flag = 0;
     ctl->flags = 0;
+    ctl->early_loads = -1;
     ptx::fence_mbar_init();
   }
   if (warp == 1) {
@@ -661,9 +704,118 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
     ctl->n_my_items =
         n > (int)blockIdx.x ? (n - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
   }
+
+  uint8_t* q_smem = data;
+  uint8_t* kv_smem = data + 2 * C::kQBytes;
+  const int32_t* perm = p.fused ? p.perm_ws : p.perm;
+  const int Lq = p.Lq;
+  // ---- TMA issue, used by the producer (and by thread 0, the producer's
+  // lane, to start a pair item's loads before the other roles start)
+  bool tail_ready = false;
+  // Fused mode loads through the host maps, whose row count is open; a tile
+  // that reaches past row T goes through a copy with the row count set to T
+  // (made on first need), so the TMA fills its missing rows with zeros
+  // instead of reading past the end of k / v.
+  auto kv_map = [&](bool is_v, int32_t row) -> const void* {
+    if (!p.fused) return is_v ? p.vmap : p.kmap;
+    const int T = ctl->total_keys;
+    if (row + kBlockN <= T) return is_v ? (const void*)&vmap_tmpl : (const void*)&kmap_tmpl;
+    CUtensorMap* tail_k = p.map_slots + 2 * blockIdx.x;
+    CUtensorMap* tail_v = tail_k + 1;
+    if (!tail_ready) {
+#pragma unroll
+      for (int mi = 0; mi < 2; ++mi) {
+        const uint4* s4 = reinterpret_cast<const uint4*>(mi == 0 ? &kmap_tmpl : &vmap_tmpl);
+        uint4* d4 = reinterpret_cast<uint4*>(mi == 0 ? tail_k : tail_v);
+#pragma unroll
+        for (int i = 0; i < (int)(sizeof(CUtensorMap) / 16); ++i) d4[i] = s4[i];
+        asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 1, %1;" ::"l"(d4), "r"(T)
+                     : "memory");
+      }
+      asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
+      ptx::tensormap_acquire(tail_k);
+      ptx::tensormap_acquire(tail_v);
+      tail_ready = true;
+    }
+    return is_v ? (const void*)tail_v : (const void*)tail_k;
+  };
+  // one K or V tile (128 keys x D of one head) into ring slot `slot`
+  auto issue_tile = [&](bool is_v, int head, int32_t row, uint32_t slot) {
+    const void* map = kv_map(is_v, row);
+    const uint32_t bar = ptx::smem_addr(&ctl->kv_full[slot]);
+    const uint32_t dst = ptx::smem_addr(kv_smem + slot * C::kKVBytes);
+    ptx::mbar_arrive_expect_tx(bar, C::kKVBytes);
+#pragma unroll
+    for (int cb = 0; cb < C::kCB; ++cb)
+      ptx::tma_load_2d(dst + cb * kBlockN * 128, map, bar, head * D + cb * 64, row);
+  };
+  // the Q tile of item w into Q buffer qb
+  auto issue_q = [&](const WorkItem& w, uint32_t qb) {
+    const uint32_t qbar = ptx::smem_addr(&ctl->q_full[qb]);
+    const uint32_t qdst = ptx::smem_addr(q_smem + qb * C::kQBytes);
+    if (ctl->sorted) {
+      const int nb = p.qbox;
+      const int nbox = ceil_div(w.n_cand, nb);
+      ptx::mbar_arrive_expect_tx(qbar, uint32_t(nbox * nb * Lq * 128 * C::kCB));
+      for (int cb = 0; cb < C::kCB; ++cb)
+        for (int bx = 0; bx < nbox; ++bx)
+          ptx::tma_load_4d(qdst + cb * kTileM * 128 + bx * nb * Lq * 128, &qmap, qbar, cb * 64, 0, w.head,
+                           w.cand_begin + bx * nb);
+    } else {
+      ptx::mbar_arrive_expect_tx(qbar, uint32_t(w.n_cand * Lq * 128 * C::kCB));
+      for (int i = 0; i < w.n_cand; ++i) {
+        const int32_t c = perm[w.cand_begin + i];
+        for (int cb = 0; cb < C::kCB; ++cb)
+          ptx::tma_load_4d(qdst + cb * kTileM * 128 + i * Lq * 128, &qmap1, qbar, cb * 64, 0, w.head, c);
+      }
+    }
+  };
+  // The i-th ring load of an item of n tiles, in the MMA warp's order
+  // K0, K1, K2, V0, K3, V1, K4, ..., V(n-1): is it V, and which tile.
+  auto load_at = [](int i, int n, bool& is_v, int& tile) {
+    const int k0 = n < kSBufs ? n : kSBufs;
+    const int a = n > kSBufs ? n - kSBufs : 0;   // tiles j followed by K(j+3)
+    if (i < k0) {
+      is_v = false;
+      tile = i;
+    } else if (i - k0 < 2 * a) {
+      const int t = i - k0;
+      is_v = (t & 1) == 0;
+      tile = is_v ? (t >> 1) : (t >> 1) + kSBufs;
+    } else {
+      is_v = true;
+      tile = a + (i - k0 - 2 * a);
+    }
+  };
   if (threadIdx.x == 0) trace(p, 0, kTrCtaStart);
   ptx::tc_fence_before();
-  __syncthreads();
+  if (warp == 0) {
+    // The plan is complete: warp 0 releases the other warps and only then
+    // starts a pair item's loads.  One warp arrives while the others wait,
+    // so this takes the non-aligned barrier forms on a barrier of its own
+    // (the aligned ones require every thread to run the same instruction).
+    asm volatile("barrier.arrive %0, %1;" ::"r"(kBarPlanDone), "r"(kTcThreads) : "memory");
+    if (lane == 0 && p.fused && ctl->mode == kModePair && ctl->n_my_items > 0 && !(p.debug_flags & 1)) {
+      // Pair item: start its Q and the first ring loads now, while the other
+      // warps set out.  Since the last planning barrier only this thread has
+      // read the scratch that the loads overwrite.
+      ptx::fence_proxy_async_smem();
+      const WorkItem w = ctl->items[0];
+      const int n = ceil_div(w.kv_len, kBlockN);
+      issue_q(w, 0);
+      int e = 0;
+      for (; e < 2 * n && e < C::kSlots; ++e) {
+        bool is_v;
+        int t;
+        load_at(e, n, is_v, t);
+        issue_tile(is_v, w.head, w.kv_begin + t * kBlockN, (uint32_t)e);
+      }
+      ctl->early_loads = e;
+    }
+    __syncwarp();
+  } else {
+    asm volatile("barrier.sync %0, %1;" ::"r"(kBarPlanDone), "r"(kTcThreads) : "memory");
+  }
   ptx::cluster_wait();
   ptx::tc_fence_after();
   trace_pro(p, 8);
@@ -674,11 +826,7 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
   const bool sorted = ctl->sorted != 0;
   const int NS = C::kSlots;
   const int NQ = mode == kModePair ? 1 : 2;
-  uint8_t* q_smem = data;
-  uint8_t* kv_smem = data + 2 * C::kQBytes;
-  const int32_t* perm = p.fused ? p.perm_ws : p.perm;
   const Waiter W{&ctl->abort_flag, p.err_word, p.timeout_ns};
-  const int Lq = p.Lq;
   auto item_at = [&](int k) -> WorkItem {
     if (p.fused) return k < kCtlItems ? ctl->items[k] : p.cta_items[(size_t)blockIdx.x * p.max_cta_items + k];
     return p.items[blockIdx.x + (size_t)k * gridDim.x];
@@ -687,90 +835,36 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0 && mode != kModeSkip) {
-      const int T = ctl->total_keys;
-      // Fused mode loads through the host maps, whose row count is open; a
-      // tile that reaches past row T goes through a copy with the row count
-      // set to T (made on first need), so the TMA fills its missing rows with
-      // zeros instead of reading past the end of k / v.
-      const void* kmap = p.fused ? (const void*)&kmap_tmpl : p.kmap;
-      const void* vmap = p.fused ? (const void*)&vmap_tmpl : p.vmap;
-      CUtensorMap* tail_k = p.fused ? p.map_slots + 2 * blockIdx.x : nullptr;
-      CUtensorMap* tail_v = tail_k ? tail_k + 1 : nullptr;
-      bool tail_ready = false;
       if (!p.fused) {
-        ptx::tensormap_acquire(kmap);
-        ptx::tensormap_acquire(vmap);
+        ptx::tensormap_acquire(p.kmap);
+        ptx::tensormap_acquire(p.vmap);
       }
       uint32_t kv_it = 0, q_it = 0;
       bool ok = true;
-      auto load_tile = [&](bool is_v, int head, int32_t row) -> bool {
-        const void* map = is_v ? vmap : kmap;
-        if (p.fused && row + kBlockN > T) {
-          if (!tail_ready) {
-#pragma unroll
-            for (int mi = 0; mi < 2; ++mi) {
-              const uint4* s4 = reinterpret_cast<const uint4*>(mi == 0 ? &kmap_tmpl : &vmap_tmpl);
-              uint4* d4 = reinterpret_cast<uint4*>(mi == 0 ? tail_k : tail_v);
-#pragma unroll
-              for (int i = 0; i < (int)(sizeof(CUtensorMap) / 16); ++i) d4[i] = s4[i];
-              asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 1, %1;" ::"l"(d4),
-                           "r"(T)
-                           : "memory");
-            }
-            asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
-            ptx::tensormap_acquire(tail_k);
-            ptx::tensormap_acquire(tail_v);
-            tail_ready = true;
-          }
-          map = is_v ? (const void*)tail_v : (const void*)tail_k;
-        }
-        const uint32_t slot = kv_it % NS;
-        if (!W.wait(ptx::smem_addr(&ctl->kv_empty[slot]), ((kv_it / NS) & 1u) ^ 1u)) return false;
-        const uint32_t bar = ptx::smem_addr(&ctl->kv_full[slot]);
-        const uint32_t dst = ptx::smem_addr(kv_smem + slot * C::kKVBytes);
-        ptx::mbar_arrive_expect_tx(bar, C::kKVBytes);
-#pragma unroll
-        for (int cb = 0; cb < C::kCB; ++cb)
-          ptx::tma_load_2d(dst + cb * kBlockN * 128, map, bar, head * D + cb * 64, row);
-        ++kv_it;
-        return true;
-      };
       for (int k = 0; k < n_my && ok; ++k) {
         const WorkItem w = item_at(k);
         const int n = ceil_div(w.kv_len, kBlockN);
+        // item 0 of a pair may have been started before the roles began
+        const int e0 = (k == 0 && ctl->early_loads >= 0) ? ctl->early_loads : 0;
         const uint32_t qb = q_it % NQ;
-        const uint32_t qpar = ((q_it / NQ) & 1u) ^ 1u;
         trace(p, k, kTrProdItem);
-        if (!W.wait(ptx::smem_addr(&ctl->q_empty[qb]), qpar)) break;
-        const uint32_t qbar = ptx::smem_addr(&ctl->q_full[qb]);
-        const uint32_t qdst = ptx::smem_addr(q_smem + qb * C::kQBytes);
-        if (!(p.debug_flags & 1)) {
-          if (sorted) {
-            const int nb = p.qbox;
-            const int nbox = ceil_div(w.n_cand, nb);
-            ptx::mbar_arrive_expect_tx(qbar, uint32_t(nbox * nb * Lq * 128 * C::kCB));
-            for (int cb = 0; cb < C::kCB; ++cb)
-              for (int bx = 0; bx < nbox; ++bx)
-                ptx::tma_load_4d(qdst + cb * kTileM * 128 + bx * nb * Lq * 128, &qmap, qbar,
-                                 cb * 64, 0, w.head, w.cand_begin + bx * nb);
-          } else {
-            ptx::mbar_arrive_expect_tx(qbar, uint32_t(w.n_cand * Lq * 128 * C::kCB));
-            for (int i = 0; i < w.n_cand; ++i) {
-              const int32_t c = perm[w.cand_begin + i];
-              for (int cb = 0; cb < C::kCB; ++cb)
-                ptx::tma_load_4d(qdst + cb * kTileM * 128 + i * Lq * 128, &qmap1, qbar, cb * 64, 0,
-                                 w.head, c);
-            }
-          }
+        if (!(k == 0 && ctl->early_loads >= 0)) {
+          if (!W.wait(ptx::smem_addr(&ctl->q_empty[qb]), ((q_it / NQ) & 1u) ^ 1u)) break;
+          if (!(p.debug_flags & 1)) issue_q(w, qb);
         }
         ++q_it;
-        // K/V tiles in the order the MMA warp consumes them:
-        // K0, K1, K2, V0, K3, V1, K4, V2, ...
-        for (int j = 0; j < n && j < kSBufs && ok; ++j)
-          ok = load_tile(false, w.head, w.kv_begin + j * kBlockN);
-        for (int j = 0; j < n && ok; ++j) {
-          ok = load_tile(true, w.head, w.kv_begin + j * kBlockN);
-          if (ok && j + kSBufs < n) ok = load_tile(false, w.head, w.kv_begin + (j + kSBufs) * kBlockN);
+        kv_it += (uint32_t)e0;
+        for (int i = e0; i < 2 * n; ++i) {
+          bool is_v;
+          int t;
+          load_at(i, n, is_v, t);
+          const uint32_t slot = kv_it % NS;
+          if (!W.wait(ptx::smem_addr(&ctl->kv_empty[slot]), ((kv_it / NS) & 1u) ^ 1u)) {
+            ok = false;
+            break;
+          }
+          issue_tile(is_v, w.head, w.kv_begin + t * kBlockN, slot);
+          ++kv_it;
         }
         trace(p, k, kTrProdIssued);
         if (ok && w.unit >= 0) {

@@ -77,6 +77,9 @@ EDGE = {
     "many_users": dict(n_user=300, counts=[1] * 300, lens=list(range(1, 301))),
     # more candidates than one query tile holds
     "multi_tile": dict(n_user=2, counts=[300, 7], lens=[200, 64]),
+    # a last user shorter than a key tile: the tiles of the users before it
+    # that reach past the end of k/v
+    "short_last": dict(n_user=4, counts=[4, 3, 2, 5], lens=[300, 170, 90, 20]),
 }
 
 
