@@ -75,8 +75,12 @@ namespace ikbo {
 
 
 constexpr int kBlockN = 128;      // keys per K/V tile
-constexpr int kTcThreads = 384;
-constexpr int kSoftmaxWarp0 = 4;  // warps 4..11 run the softmax
+// Each query row is worked on by kSplit threads (column groups of
+// kBlockN / kSplit keys), in kSplit x 4 softmax warps after the 4 others.
+constexpr int kSplit = 2;
+constexpr int kSoftmaxWarp0 = 4;
+constexpr int kSoftmaxWarps = 4 * kSplit;
+constexpr int kTcThreads = 32 * (kSoftmaxWarp0 + kSoftmaxWarps);
 // Hardware barrier 1: warp 0 releases the other warps when the plan is done
 // (barrier 0 is __syncthreads).
 constexpr int kBarPlanDone = 1;
@@ -86,8 +90,8 @@ constexpr int kBarPlanDone = 1;
 constexpr float kLazyRescale = 8.0f;
 // Dynamic shared memory: the operand area first (1 KB aligned: 128-byte
 // swizzle atoms), the control block after it; 227 KB, the per-CTA maximum.
-constexpr int kDataBytes = 229376;
-constexpr int kCtrlBytes = 3072;
+constexpr int kCtrlBytes = kSplit == 2 ? 3072 : 5120;
+constexpr int kDataBytes = 232448 - kCtrlBytes;
 constexpr int kTcSmemBytes = kDataBytes + kCtrlBytes;
 constexpr int kMaxSlots = 11;
 // In-kernel planning keeps off/cand_start/order/prefix (n_user), the per-warp
@@ -117,8 +121,9 @@ struct TcConfig {
   static constexpr int kFit = (kDataBytes - 2 * kQBytes) / kKVBytes;
   static constexpr int kSlots = kFit < kMaxSlots ? kFit : kMaxSlots;
   static constexpr int kRecvBytes = kTileM * D * 4;
-  static constexpr int kHalf = D / 2;                   // output columns per softmax thread
-  static constexpr int kChunks = kHalf / 32;            // 32-column TMEM loads per half row
+  static constexpr int kPart = D / kSplit;              // output columns per softmax thread
+  static constexpr int kOChunk = kPart < 32 ? kPart : 32;   // columns per TMEM load of O
+  static constexpr int kOChunks = kPart / kOChunk;
   // tensor-memory columns: three S/P buffers and the O accumulator
   static constexpr int kSCol = 0;
   static constexpr int kOCol = kSBufs * kBlockN;
@@ -150,13 +155,13 @@ struct TcCtrl {
   int flags;
   int n_units;                          // planning: units in all (read by every thread)
   int early_loads;                      // ring loads of item 0 issued before the roles start
-  int red[12];
+  int red[24];
   WorkItem items[kCtlItems];            // the first items of this CTA (the rest in global memory)
   alignas(16) float partner_lse[kTileM];
-  // row maximum / row sum exchange between the two halves of a row:
-  // [parity][half][row], the value with the exchange's sequence number in
-  // its two low bits
-  uint32_t xtag[2][2][kTileM];
+  // row maximum / row sum exchange among the kSplit threads of a row:
+  // [parity][column group][row], the value with the exchange's sequence
+  // number in its two low bits
+  uint32_t xtag[2][kSplit][kTileM];
 };
 static_assert(sizeof(TcCtrl) <= kCtrlBytes, "control block");
 
@@ -645,7 +650,7 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
     }
     for (int i = 0; i < kSBufs; ++i) {
       ptx::mbar_init(ptx::smem_addr(&ctl->s_full[i]), 1);
-      ptx::mbar_init(ptx::smem_addr(&ctl->p_full[i]), 8);
+      ptx::mbar_init(ptx::smem_addr(&ctl->p_full[i]), kSoftmaxWarps);
       ptx::mbar_init(ptx::smem_addr(&ctl->pv_done[i]), 1);
     }
     for (int i = 0; i < kMaxSlots; ++i) {
@@ -666,7 +671,7 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
     ptx::tmem_relinquish();
   }
   // exchange words start with sequence number 3, which no first use expects
-  for (int i = threadIdx.x; i < 2 * 2 * kTileM; i += blockDim.x) (&ctl->xtag[0][0][0])[i] = 3u;
+  for (int i = threadIdx.x; i < 2 * kSplit * kTileM; i += blockDim.x) (&ctl->xtag[0][0][0])[i] = 3u;
   if (warp == 2 && lane == 0) {
     // the host-encoded descriptors into the TMA unit's cache ahead of use
     ptx::prefetch_tensormap(&qmap);
@@ -973,12 +978,13 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
     __syncwarp();
   } else if (warp >= kSoftmaxWarp0 && mode != kModeSkip) {
     // ------------------------------------------- softmax / correction / epilogue
+    constexpr int kCols = kBlockN / kSplit;                  // key columns of a tile per thread
+    constexpr int kR = kCols / 32;                           // 32-column TMEM loads per tile
     const int quarter = warp & 3;
-    const int half = (warp - kSoftmaxWarp0) >> 2;            // 0: columns 0-63, 1: 64-127
+    const int cg = (warp - kSoftmaxWarp0) >> 2;              // column group of this thread
     const int row = quarter * 32 + lane;                     // TMEM lane == tile row
     const uint32_t lane_off = uint32_t(quarter * 32) << 16;
     const float sl2 = p.scale_log2;
-    const float2 sl2x2 = make_float2(sl2, sl2);
     uint32_t g = 0, xs = 0;
     // PV(x) commits to pv_done[x % 3], phase x / 3.  A wait for PV(x) is
     // made only on tile x + 1 (to rescale O) or after the item's last tile
@@ -992,49 +998,56 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
       ptx::tc_fence_after();
       return true;
     };
-    // Row values shared with the other half of the row: a value goes out with
-    // the exchange's sequence number in its two low bits (it moves by at most
-    // 3 ulp; -inf and NaN go out as -FLT_MAX) and the partner's value is taken
-    // once its word carries the same number.  Both halves then use the same
-    // two words.  The wait is bounded like every wait.
-    auto publish = [&](float v) -> float {
+    // Row values shared among the kSplit threads of a row: a value goes out
+    // with the exchange's sequence number in its two low bits (it moves by at
+    // most 3 ulp; -inf and NaN go out as -FLT_MAX), and a partner's word is
+    // taken once it carries the same number.  Every thread of the row then
+    // holds the same kSplit words.  The waits are bounded like every wait.
+    auto publish = [&](float v) -> uint32_t {
       const float vv = v > -FLT_MAX ? v : -FLT_MAX;
       const uint32_t wv = (__float_as_uint(vv) & ~3u) | (xs & 3u);
       asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(
-                       ptx::smem_addr(&ctl->xtag[xs & 1u][half][row])),
+                       ptx::smem_addr(&ctl->xtag[xs & 1u][cg][row])),
                    "r"(wv)
                    : "memory");
-      return __uint_as_float(wv & ~3u);
+      return wv;
     };
-    auto collect = [&](float& v) -> bool {
-      const uint32_t addr = ptx::smem_addr(&ctl->xtag[xs & 1u][half ^ 1][row]);
-      const uint32_t tag = xs & 3u;
+    auto collect = [&](uint32_t mine, uint32_t (&words)[kSplit]) -> bool {
+      const uint32_t tag = xs & 3u, par = xs & 1u;
       ++xs;
-      uint32_t wv = 0;
       bool ok = true;
       uint64_t t_end = 0;
-      for (uint32_t spin = 0;; ++spin) {
-        asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(wv) : "r"(addr) : "memory");
-        if ((wv & 3u) == tag) break;
-        if ((spin & 127u) == 127u) {
-          if (*W.abort) {
-            ok = false;
-            break;
-          }
-          const uint64_t now = ptx::globaltimer();
-          if (t_end == 0) {
-            t_end = now + p.timeout_ns;
-          } else if (now > t_end) {
-            *W.abort = 1;
-            atomicOr(p.err_word, kErrTimeout);
-            ok = false;
-            break;
+#pragma unroll
+      for (int o = 0; o < kSplit; ++o) {
+        if (o == cg) {
+          words[o] = mine;
+          continue;
+        }
+        const uint32_t addr = ptx::smem_addr(&ctl->xtag[par][o][row]);
+        uint32_t wv = 0;
+        for (uint32_t spin = 0; ok; ++spin) {
+          asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(wv) : "r"(addr) : "memory");
+          if ((wv & 3u) == tag) break;
+          if ((spin & 127u) == 127u) {
+            if (*W.abort) {
+              ok = false;
+              break;
+            }
+            const uint64_t now = ptx::globaltimer();
+            if (t_end == 0) {
+              t_end = now + p.timeout_ns;
+            } else if (now > t_end) {
+              *W.abort = 1;
+              atomicOr(p.err_word, kErrTimeout);
+              ok = false;
+            }
           }
         }
+        words[o] = wv;
       }
-      v = __uint_as_float(wv & ~3u);
       return __all_sync(0xffffffffu, ok);
     };
+    auto dec = [](uint32_t wv) { return __uint_as_float(wv & ~3u); };
     for (int k = 0; k < n_my; ++k) {
       const WorkItem w = item_at(k);
       const int n = ceil_div(w.kv_len, kBlockN);
@@ -1052,24 +1065,24 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
           break;
         }
         ptx::tc_fence_after();
-        if (j == 0 && row == 0 && half == 0) trace(p, k, kTrSmS0);
-        const bool tr_t = row == 0 && half == 0 && j < 4;
+        if (j == 0 && row == 0 && cg == 0) trace(p, k, kTrSmS0);
+        const bool tr_t = row == 0 && cg == 0 && j < 4;
         if (tr_t) trace_tile(p, k, 1, 4 * j);
         const uint32_t scol = tmem + lane_off + C::kSCol + sb * kBlockN;
-        uint32_t r[2][32];
-        ptx::tmem_ld32(scol + half * 64, r[0]);
-        ptx::tmem_ld32(scol + half * 64 + 32, r[1]);
+        uint32_t r[kR][32];
+#pragma unroll
+        for (int c = 0; c < kR; ++c) ptx::tmem_ld32(scol + cg * kCols + c * 32, r[c]);
         ptx::tmem_ld_wait();
 #define IKBO_S(e) __uint_as_float(r[(e) >> 5][(e) & 31])
         // Scores enter the exponent as fma(s, sc, -ref).  On a tile whose
         // tail is short, or for scale <= 0, they are scaled here first and
         // the missing keys set to -inf (sc = 1); otherwise sc = scale and the
         // order of the raw scores is that of the scaled ones.
-        const int valid = min(kBlockN, w.kv_len - j * kBlockN) - half * 64;
+        const int valid = min(kBlockN, w.kv_len - j * kBlockN) - cg * kCols;
         float sc = sl2;
-        if (valid < 64 || !(sl2 > 0.f)) {
+        if (valid < kCols || !(sl2 > 0.f)) {
 #pragma unroll
-          for (int e = 0; e < 64; ++e) {
+          for (int e = 0; e < kCols; ++e) {
             const float tt = IKBO_S(e) * sl2;
             r[e >> 5][e & 31] = __float_as_uint(e < valid ? tt : -INFINITY);
           }
@@ -1081,7 +1094,7 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
           float a0 = fmaxf(IKBO_S(0), IKBO_S(1)), a1 = fmaxf(IKBO_S(2), IKBO_S(3));
           float a2 = fmaxf(IKBO_S(4), IKBO_S(5)), a3 = fmaxf(IKBO_S(6), IKBO_S(7));
 #pragma unroll
-          for (int e = 8; e < 64; e += 8) {
+          for (int e = 8; e < kCols; e += 8) {
             a0 = fmax3(a0, IKBO_S(e), IKBO_S(e + 1));
             a1 = fmax3(a1, IKBO_S(e + 2), IKBO_S(e + 3));
             a2 = fmax3(a2, IKBO_S(e + 4), IKBO_S(e + 5));
@@ -1089,19 +1102,19 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
           }
           mx = fmax3(a0, a1, fmaxf(a2, a3)) * sc;
         }
-        // This half's S reads are complete: the other half may write P over
-        // them once it has seen this maximum.
+        // This thread's S reads are complete: the others of the row may write
+        // P over them once they have seen this maximum.
         ptx::tc_fence_before();
         if (tr_t) trace_tile(p, k, 1, 4 * j + 1);
-        const float mx_mine = publish(mx);
+        const uint32_t mx_w = publish(mx);
         // P = 2^(t - ref) as bf16 pairs, and its row sum
-        uint32_t pk[32];
+        uint32_t pk[kCols / 2];
         float sum = 0.f;
         auto exps = [&](float ref) {
           const float2 sc2 = make_float2(sc, sc), nr2 = make_float2(-ref, -ref);
           float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int e = 0; e < 64; e += 2) {
+          for (int e = 0; e < kCols; e += 2) {
             const float2 x = ffma2(make_float2(IKBO_S(e), IKBO_S(e + 1)), sc2, nr2);
             const float2 pe = make_float2(fast_exp2(x.x), fast_exp2(x.y));
             if ((e >> 1) & 1) a1 = fadd2(a1, pe); else a0 = fadd2(a0, pe);
@@ -1110,26 +1123,28 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
           const float2 u = fadd2(a0, a1);
           sum = u.x + u.y;
         };
-        // Against the running maximum while the partner's maximum is on its
+        // Against the running maximum while the others' maxima are on their
         // way (it stands unless the maximum moves); against the new maximum
         // on the first tile and when it moves.
         if (j > 0) exps(m);
-        float mx_other;
-        if (!collect(mx_other)) {
+        uint32_t mw[kSplit];
+        if (!collect(mx_w, mw)) {
           ok = false;
           break;
         }
-        const float mxa = fmaxf(mx_mine, mx_other);
+        float mxa = dec(mw[0]);
+#pragma unroll
+        for (int o = 1; o < kSplit; ++o) mxa = fmaxf(mxa, dec(mw[o]));
         const float m_new = (j == 0 || mxa > m + kLazyRescale) ? mxa : m;
         if (j == 0 || __any_sync(0xffffffffu, live && m_new != m)) exps(m_new);
 #undef IKBO_S
-        if (!ok) break;
         ptx::tc_fence_after();
         if (tr_t) trace_tile(p, k, 1, 4 * j + 2);
         const float alpha = fast_exp2(m - m_new);   // 0 on the first tile, 1 when m stays
         l = l * alpha + sum;
-        // P (bf16 pairs) over the first half of this S buffer: keys 64h.. at column 32h
-        ptx::tmem_st32(scol + half * 32, pk);
+        // P (bf16 pairs) over the first half of this S buffer: the keys of
+        // column group cg at columns cg * kCols / 2
+        ptx::tmem_st(scol + cg * (kCols / 2), pk);
         ptx::tmem_st_wait();
         if (j > 0 && __any_sync(0xffffffffu, live && m_new != m)) {
           // O must hold exactly P_0..P_{j-1} V when it is rescaled: PV_{j-1}
@@ -1138,15 +1153,15 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
             ok = false;
             break;
           }
-          const uint32_t ocol = tmem + lane_off + C::kOCol + half * C::kHalf;
+          const uint32_t ocol = tmem + lane_off + C::kOCol + cg * C::kPart;
 #pragma unroll
-          for (int c = 0; c < C::kChunks; ++c) {
-            uint32_t o[32];
-            ptx::tmem_ld32(ocol + c * 32, o);
+          for (int c = 0; c < C::kOChunks; ++c) {
+            uint32_t o[C::kOChunk];
+            ptx::tmem_ld(ocol + c * C::kOChunk, o);
             ptx::tmem_ld_wait();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            ptx::tmem_st32(ocol + c * 32, o);
+            for (int e = 0; e < C::kOChunk; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            ptx::tmem_st(ocol + c * C::kOChunk, o);
           }
           ptx::tmem_st_wait();
         }
@@ -1157,17 +1172,20 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
         if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(&ctl->p_full[sb]));
       }
       if (!ok) break;
-      if (row == 0 && half == 0) trace(p, k, kTrSmLastP);
+      if (row == 0 && cg == 0) trace(p, k, kTrSmLastP);
       // ---- epilogue: the row sum goes out now, O is complete after the last PV
-      const float l_mine = publish(l);
+      const uint32_t l_w = publish(l);
       if (!pv_wait(g + n - 1)) break;
-      if (row == 0 && half == 0) trace(p, k, kTrEpiO);
-      float l_other;
-      if (!collect(l_other)) break;
-      const float lt = l_mine + l_other;           // both halves share the running max m
-      const bool tr_epi = row == 32 && half == 0;  // epilogue timeline: one thread
+      if (row == 0 && cg == 0) trace(p, k, kTrEpiO);
+      uint32_t lw[kSplit];
+      if (!collect(l_w, lw)) break;
+      // the row sum, added in group order by every thread of the row alike
+      float lt = dec(lw[0]);
+#pragma unroll
+      for (int o = 1; o < kSplit; ++o) lt += dec(lw[o]);
+      const bool tr_epi = row == 32 && cg == 0;    // epilogue timeline: one thread
       if (tr_epi) trace(p, k, kTrEpiSums);
-      const uint32_t ocol = tmem + lane_off + C::kOCol + half * C::kHalf;
+      const uint32_t ocol = tmem + lane_off + C::kOCol + cg * C::kPart;
       // A split unit: each CTA of the pair finishes half of the rows (CTA 0
       // the first, CTA 1 the second) and sends the other half to its partner.
       const bool paired = w.unit >= 0;
@@ -1175,7 +1193,7 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
       const bool mine = !paired || (cta_rank == 0 ? row < hrows : row >= hrows);
       const bool keep = live && mine;
       const bool send = live && !mine;
-      const int vec0 = half * C::kHalf / 4;        // first 16-byte vector of this half row
+      const int vec0 = cg * C::kPart / 4;          // first 16-byte vector of this thread's columns
       if (__any_sync(0xffffffffu, send)) {
         // O / l and the log-sum-exp m + log2(l), straight into the partner's
         // Q buffers (rows of D fp32, 16-byte vectors swizzled by row)
@@ -1186,24 +1204,24 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
         const float inv = lt > 0.f ? 1.f / lt : 0.f;
         const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
-        for (int cc = 0; cc < C::kChunks; ++cc) {
-          uint32_t o[32];
-          ptx::tmem_ld32(ocol + cc * 32, o);
+        for (int cc = 0; cc < C::kOChunks; ++cc) {
+          uint32_t o[C::kOChunk];
+          ptx::tmem_ld(ocol + cc * C::kOChunk, o);
           ptx::tmem_ld_wait();
           if (send) {
 #pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4) {
-              const int vec = vec0 + cc * 8 + q4;
+            for (int q4 = 0; q4 < C::kOChunk / 4; ++q4) {
+              const int vec = vec0 + cc * (C::kOChunk / 4) + q4;
               const float2 a = fmul2(make_float2(__uint_as_float(o[q4 * 4 + 0]), __uint_as_float(o[q4 * 4 + 1])), inv2);
               const float2 b2 = fmul2(make_float2(__uint_as_float(o[q4 * 4 + 2]), __uint_as_float(o[q4 * 4 + 3])), inv2);
               ptx::st_async_v4(rdst + uint32_t((vec ^ (row & 7)) * 16), a.x, a.y, b2.x, b2.y, rbar);
             }
           }
         }
-        if (send && half == 0)
+        if (send && cg == 0)
           ptx::st_async_f32(ptx::map_to_cta(ptx::smem_addr(&ctl->partner_lse[row]), peer),
                             lt > 0.f ? m + fast_log2(lt) : -INFINITY, rbar);
-        if (row == 0 && half == 0) trace(p, k, kTrEpiStored);
+        if (row == 0 && cg == 0) trace(p, k, kTrEpiStored);
         if (tr_epi) trace(p, k, kTrEpiSent);
       }
       if (__any_sync(0xffffffffu, keep)) {
@@ -1211,12 +1229,12 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
         const int tq = keep ? row - ci * Lq : 0;
         const int32_t gpos = w.cand_begin + ci;
         const int64_t cidx = keep ? (sorted ? gpos : perm[gpos]) : 0;
-        uint16_t* dst = p.out + (((cidx * p.H + w.head) * (int64_t)Lq + tq) * D) + half * C::kHalf;
+        uint16_t* dst = p.out + (((cidx * p.H + w.head) * (int64_t)Lq + tq) * D) + cg * C::kPart;
         float lse_p = -INFINITY;
         if (paired) {
           // the partner's O / l and log-sum-exp for these rows
           if (!W.warp_wait(ptx::smem_addr(&ctl->pair_recv), 0, true)) break;
-          if (row == 0 && half == 0) trace(p, k, kTrArrived);
+          if (row == 0 && cg == 0) trace(p, k, kTrArrived);
           if (keep) lse_p = ctl->partner_lse[row];
         }
         // out = (2^(m-M) O + 2^(lse_p-M) O_p / l_p) / (2^(m-M) l + 2^(lse_p-M))
@@ -1226,28 +1244,28 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
         const float inv = L > 0.f ? 1.f / L : 0.f;
         const float2 w0 = make_float2(a0 * inv, a0 * inv), w1 = make_float2(a1 * inv, a1 * inv);
 #pragma unroll
-        for (int cc = 0; cc < C::kChunks; ++cc) {
-          uint32_t o[32];
-          ptx::tmem_ld32(ocol + cc * 32, o);
+        for (int cc = 0; cc < C::kOChunks; ++cc) {
+          uint32_t o[C::kOChunk];
+          ptx::tmem_ld(ocol + cc * C::kOChunk, o);
           ptx::tmem_ld_wait();
           if (keep) {
-            float2 x[16];
+            float2 x[C::kOChunk / 2];
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
+            for (int e = 0; e < C::kOChunk / 2; ++e)
               x[e] = fmul2(make_float2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), w0);
             if (paired) {
 #pragma unroll
-              for (int q4 = 0; q4 < 8; ++q4) {
-                const int vec = vec0 + cc * 8 + q4;
+              for (int q4 = 0; q4 < C::kOChunk / 4; ++q4) {
+                const int vec = vec0 + cc * (C::kOChunk / 4) + q4;
                 const float4 y = *reinterpret_cast<const float4*>(
                     data + row * (D * 4) + ((vec ^ (row & 7)) * 16));
                 x[2 * q4] = fadd2(x[2 * q4], fmul2(make_float2(y.x, y.y), w1));
                 x[2 * q4 + 1] = fadd2(x[2 * q4 + 1], fmul2(make_float2(y.z, y.w), w1));
               }
             }
-            uint4* d4 = reinterpret_cast<uint4*>(dst + cc * 32);
+            uint4* d4 = reinterpret_cast<uint4*>(dst + cc * C::kOChunk);
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
+            for (int q4 = 0; q4 < C::kOChunk / 8; ++q4) {
               uint4 v;
               v.x = pack_bf16(x[4 * q4].x, x[4 * q4].y);
               v.y = pack_bf16(x[4 * q4 + 1].x, x[4 * q4 + 1].y);
@@ -1257,7 +1275,7 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
             }
           }
         }
-        if (row == 0 && half == 0) trace(p, k, paired ? kTrMerged : kTrEpiStored);
+        if (row == 0 && cg == 0) trace(p, k, paired ? kTrMerged : kTrEpiStored);
         if (tr_epi) trace(p, k, kTrEpiKept);
       }
       g += n;
