@@ -205,14 +205,17 @@ while True:
                 "samples": len(sm), "reasons": sorted(reasons), "source": "nvidia-smi"}
 
 
-# the files the tcgen05 attention kernel is compiled from
-KERNEL_SOURCES = ("ikbo_attn_tc.cuh", "ikbo_common.cuh", "ikbo_ptx.cuh")
+# the files each tcgen05 attention kernel is compiled from
+KERNEL_SOURCES = {
+    "ikbo_attn_tc_kernel": ("ikbo_attn_tc.cuh", "ikbo_common.cuh", "ikbo_ptx.cuh"),
+    "ikbo_attn_pp_kernel": ("ikbo_attn_pp.cuh", "ikbo_attn_tc.cuh", "ikbo_common.cuh", "ikbo_ptx.cuh"),
+}
 
 
-def kernel_source_sha256() -> str:
+def kernel_source_sha256(kernel_name: str = "ikbo_attn_tc_kernel") -> str:
     src = os.path.join(ROOT, "broadcast_target_attention_gb300", "csrc")
     h = hashlib.sha256()
-    for fn in KERNEL_SOURCES:
+    for fn in KERNEL_SOURCES[kernel_name.split("<")[0]]:
         with open(os.path.join(src, fn), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
@@ -229,7 +232,7 @@ def kernel_traffic(kernel_name: str, workload: str):
     e = d.get(kernel_name, {}).get(workload)
     if not e:
         return None
-    if e.get("source_sha256") != kernel_source_sha256():
+    if e.get("source_sha256") != kernel_source_sha256(kernel_name):
         return None
     return float(e["dram_bytes_per_launch"])
 
@@ -400,19 +403,20 @@ def run_ikbo(args):
     pk = peaks()
     attn = statistics.mean(attn_ms)
     achieved_gbs = alg_bytes / (attn * 1e-3) / 1e9
-    traffic = kernel_traffic(f"ikbo_attn_tc_kernel<{c.D}>", c.name)
+    kname = f"{ikbo.KERNEL_NAMES[ikbo.selected_kernel(wl.n_cand, wl.n_user, c.Lq)]}<{c.D}>"
+    traffic = kernel_traffic(kname, c.name)
     ai = flops / alg_bytes
     ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
     if ai < ridge:
         roof = {"bound": "hbm", "achieved": achieved_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved_gbs / pk["hbm_gbs"], "traffic": traffic,
-                "kernel": f"ikbo_attn_tc_kernel<{c.D}>", "alg_bytes_per_launch": alg_bytes,
+                "kernel": kname, "alg_bytes_per_launch": alg_bytes,
                 "peak_source": pk["source"] + " (burst copy)"}
     else:
         tf = flops / (attn * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": tf, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
                 "frac": tf / pk["bf16_tflops"], "traffic": traffic,
-                "kernel": f"ikbo_attn_tc_kernel<{c.D}>", "flops_per_launch": flops,
+                "kernel": kname, "flops_per_launch": flops,
                 "peak_source": pk["source"] + " (burst cuBLAS bf16)"}
     qb = wl.q.nbytes
     h2d = qb + wl.k.nbytes + wl.v.nbytes + wl.user_offsets.nbytes + wl.cand_to_user.nbytes

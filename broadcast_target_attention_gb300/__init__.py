@@ -18,7 +18,7 @@ from . import _lib
 from ._lib import STATUS
 
 __all__ = ["attn_fwd", "broadcast_attn_fwd", "attn_fwd_host", "attn_fwd_noalloc", "get_device_error", "set_timing",
-           "get_timing", "set_kernel", "set_debug", "launches_per_call", "version", "load", "IkboError", "STATUS"]
+           "get_timing", "set_kernel", "selected_kernel", "set_debug", "launches_per_call", "version", "load", "IkboError", "STATUS"]
 
 
 class IkboError(RuntimeError):
@@ -174,9 +174,24 @@ def get_timing() -> Tuple[float, float]:
     return a.value, b.value
 
 
+# kernel choices of set_kernel / results of selected_kernel
+KERNEL_AUTO, KERNEL_SIMT, KERNEL_TC, KERNEL_TC2 = 0, 1, 2, 3
+KERNEL_NAMES = {KERNEL_SIMT: "ikbo_attn_simt_kernel", KERNEL_TC: "ikbo_attn_tc_kernel",
+                KERNEL_TC2: "ikbo_attn_pp_kernel"}
+
+
 def set_kernel(which: int) -> int:
-    """0 = tcgen05 kernel (default), 1 = SIMT cross-check kernel; returns the previous choice."""
+    """0 = automatic (default), 1 = SIMT cross-check kernel, 2 = tcgen05 kernel with one
+    query tile per work item, 3 = tcgen05 kernel with two query tiles of one user and head
+    per work item; returns the previous choice."""
     return int(_lib.lib().ikbo_set_kernel(int(which)))
+
+
+def selected_kernel(n_cand: int, n_user: int, Lq: int) -> int:
+    """The kernel (1, 2 or 3) a call of these sizes runs with this thread's choice."""
+    n = int(_lib.lib().ikbo_selected_kernel(int(n_cand), int(n_user), int(Lq)))
+    _check(min(n, 0), "selected_kernel")
+    return n
 
 
 def launches_per_call(n_cand: int, n_user: int) -> int:

@@ -11,6 +11,7 @@
 
 #include "../../include/ikbo.h"
 #include "ikbo_attn_simt.cuh"
+#include "ikbo_attn_pp.cuh"
 #include "ikbo_attn_tc.cuh"
 #include "ikbo_broadcast.cuh"
 #include "ikbo_common.cuh"
@@ -31,6 +32,7 @@ struct DeviceState {
   bool ready = false;
   int num_sms = 0;
   int tc_grid[2] = {0, 0};   // CTAs of the tcgen05 kernel (clusters of 2), D = 64 / 128
+  int pp_grid[2] = {0, 0};   // CTAs of the two-tile tcgen05 kernel, D = 64 / 128
   int* err_word = nullptr;
   cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
   bool ev_ready = false;
@@ -43,7 +45,10 @@ int g_timing_dev = -1;
 int g_debug_flags = 0;
 uint64_t* g_trace = nullptr;
 uint64_t g_timeout_ns = kDefaultTimeoutNs;
+// Kernel choice of this thread (ikbo_set_kernel): 0 = automatic, 1 = SIMT,
+// 2 = tcgen05 with one query tile per item, 3 = tcgen05 with two.
 thread_local int t_kernel = 0;
+enum { kKernAuto = 0, kKernSimt = 1, kKernTc = 2, kKernPp = 3 };
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -135,12 +140,33 @@ struct Workspace {
   size_t header, kmap, vmap, items, units, perm, cand_start, scratch, partial_o, partial_ml,
       cta_items, map_slots, total;
   int max_items, max_split_items, max_units, max_cta_items, grid;
+  int kernel;   // kKernSimt, kKernTc or kKernPp
   bool fused;
 };
 
-// kernel: 0 = tcgen05 (plans in-kernel when the inputs fit its shared memory,
+bool fits_in_kernel_planning(int64_t n_cand, int64_t n_user) {
+  return n_cand <= kFusedMaxCand && n_user <= kFusedMaxUser;
+}
+
+// Average query tiles per user from which the automatic choice takes the
+// two-tile kernel.  Measured on one GB300: it is 10-11 % faster with 8 to 64
+// tiles per user, and slower with 2 to 4 (many units there have a single
+// tile, which it runs with half the softmax warps of the one-tile kernel).
+constexpr int64_t kPpMinTilesPerUser = 8;
+
+// The kernel a call runs with the thread's choice.  The two-tile kernel plans
+// in-kernel only, so inputs beyond those limits take the one-tile kernel.
+int effective_kernel(int64_t n_cand, int64_t n_user, int Lq) {
+  if (t_kernel == kKernSimt) return kKernSimt;
+  if (t_kernel == kKernTc || !fits_in_kernel_planning(n_cand, n_user)) return kKernTc;
+  if (t_kernel == kKernPp) return kKernPp;
+  return n_cand >= kPpMinTilesPerUser * int64_t(cands_per_tile(Lq)) * n_user ? kKernPp : kKernTc;
+}
+
+// kernel: kKernTc (plans in-kernel when the inputs fit its shared memory,
 // otherwise reads the planning kernel's list; never splits a unit through
-// global memory), 1 = SIMT (planning kernel, may split).
+// global memory), kKernPp (always plans in-kernel), kKernSimt (planning
+// kernel, may split).
 Workspace plan_workspace(int64_t n_cand, int64_t n_user, int H, int Lq, int D, int num_sms,
                          int grid, int kernel) {
   Workspace w = {};
@@ -148,10 +174,11 @@ Workspace plan_workspace(int64_t n_cand, int64_t n_user, int H, int Lq, int D, i
   const int64_t units_bound =
       int64_t(H) * ((n_cand + cpt - 1) / cpt + (n_user < n_cand ? n_user : n_cand));
   w.grid = grid;
+  w.kernel = kernel;
   // keep in step with ikbo_launches_per_call
-  w.fused = kernel == 0 && n_cand <= kFusedMaxCand && n_user <= kFusedMaxUser;
+  w.fused = kernel != kKernSimt && fits_in_kernel_planning(n_cand, n_user);
   w.max_items = int(num_sms + units_bound);
-  w.max_split_items = kernel == 1 ? 3 * num_sms : 0;
+  w.max_split_items = kernel == kKernSimt ? 3 * num_sms : 0;
   w.max_units = w.max_split_items;
   w.max_cta_items = int((units_bound + grid - 1) / grid) + 1;
   size_t o = 0;
@@ -279,6 +306,25 @@ int tc_grid(DeviceState* ds) {
   return g;
 }
 
+// CTAs of the two-tile kernel: one per SM, no clusters.
+template <int D>
+int pp_grid(DeviceState* ds) {
+  int& g = ds->pp_grid[D == 128 ? 1 : 0];
+  if (g) return g;
+  if (cudaFuncSetAttribute(ikbo_attn_pp_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kTcSmemBytes) != cudaSuccess)
+    return 0;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ikbo_attn_pp_kernel<D>, kTcThreads,
+                                                    kTcSmemBytes) != cudaSuccess ||
+      per_sm <= 0) {
+    cudaGetLastError();
+    per_sm = 1;
+  }
+  g = ds->num_sms * per_sm;
+  return g;
+}
+
 template <int D>
 cudaError_t launch_attn_tc(const AttnParams& ap, const CUtensorMap& qmap, const CUtensorMap& qmap1,
                            const CUtensorMap& kt, const CUtensorMap& vt, int grid, bool pdl,
@@ -287,11 +333,18 @@ cudaError_t launch_attn_tc(const AttnParams& ap, const CUtensorMap& qmap, const 
                    ap, qmap, qmap1, kt, vt);
 }
 
+template <int D>
+cudaError_t launch_attn_pp(const AttnParams& ap, const CUtensorMap& qmap, const CUtensorMap& qmap1,
+                           const CUtensorMap& kt, const CUtensorMap& vt, int grid, cudaStream_t st) {
+  return launch_ex(ikbo_attn_pp_kernel<D>, dim3(grid), dim3(kTcThreads), kTcSmemBytes, st, false, 1,
+                   ap, qmap, qmap1, kt, vt);
+}
+
 // Plan + attention on device buffers, scratch from `ws` (>= plan_workspace().total).
 int run_ikbo(DeviceState* ds, const void* q, const void* k, const void* v, const int32_t* off,
              const int32_t* c2u, int64_t n_cand, int64_t n_user, int H, int Lq, int D, float scale,
              void* out, char* ws, const Workspace& L, cudaStream_t st) {
-  const int kernel = t_kernel;
+  const int kernel = L.kernel;
   PlanParams pp = {};
   pp.cand_to_user = c2u;
   pp.user_offsets = off;
@@ -304,7 +357,7 @@ int run_ikbo(DeviceState* ds, const void* q, const void* k, const void* v, const
   pp.max_items = L.max_items;
   pp.max_split_items = L.max_split_items;
   pp.max_units = L.max_units;
-  pp.allow_split = kernel == 1 ? 1 : 0;
+  pp.allow_split = kernel == kKernSimt ? 1 : 0;
   pp.header = reinterpret_cast<PlanHeader*>(ws + L.header);
   pp.items = reinterpret_cast<WorkItem*>(ws + L.items);
   pp.units = reinterpret_cast<UnitInfo*>(ws + L.units);
@@ -318,13 +371,13 @@ int run_ikbo(DeviceState* ds, const void* q, const void* k, const void* v, const
   px.out = out;
   px.Lq = Lq;
   px.D = D;
-  px.patch_maps = kernel == 0 ? 1 : 0;
+  px.patch_maps = kernel != kKernSimt ? 1 : 0;
   px.kmap_dst = reinterpret_cast<CUtensorMap*>(ws + L.kmap);
   px.vmap_dst = reinterpret_cast<CUtensorMap*>(ws + L.vmap);
   CUtensorMap qmap, qmap1;
   std::memset(&qmap, 0, sizeof qmap);
   std::memset(&qmap1, 0, sizeof qmap1);
-  if (kernel == 0) {
+  if (kernel != kKernSimt) {
     const cuuint64_t rows = L.fused ? kOpenRows : cuuint64_t(kBlockN);
     if (encode_kv_map(&px.kmap_tmpl, k, H, D, kBlockN, rows) != IKBO_OK ||
         encode_kv_map(&px.vmap_tmpl, v, H, D, kBlockN, rows) != IKBO_OK ||
@@ -374,12 +427,17 @@ int run_ikbo(DeviceState* ds, const void* q, const void* k, const void* v, const
   }
   if (timed) cudaEventRecord(ds->ev[1], st);
   cudaError_t e;
-  if (kernel == 1) {
+  if (kernel == kKernSimt) {
     const int grid = L.max_items < ds->num_sms * 8 ? L.max_items : ds->num_sms * 8;
     if (D == 64)
       e = launch_pdl(ikbo_attn_simt_kernel<64>, dim3(grid), dim3(kSimtThreads), 0, st, ap);
     else
       e = launch_pdl(ikbo_attn_simt_kernel<128>, dim3(grid), dim3(kSimtThreads), 0, st, ap);
+  } else if (kernel == kKernPp) {
+    if (D == 64)
+      e = launch_attn_pp<64>(ap, qmap, qmap1, px.kmap_tmpl, px.vmap_tmpl, L.grid, st);
+    else
+      e = launch_attn_pp<128>(ap, qmap, qmap1, px.kmap_tmpl, px.vmap_tmpl, L.grid, st);
   } else {
     // the planning kernel (listed mode) is followed with programmatic dependent launch
     if (D == 64)
@@ -401,12 +459,16 @@ int run_ikbo(DeviceState* ds, const void* q, const void* k, const void* v, const
 int call_workspace(DeviceState* ds, int64_t n_cand, int64_t n_user, int H, int Lq, int D,
                    Workspace* out) {
   int grid = 0;
-  if (t_kernel == 0) {
+  const int kernel = effective_kernel(n_cand, n_user, Lq);
+  if (kernel == kKernTc) {
     grid = D == 64 ? tc_grid<64>(ds) : tc_grid<128>(ds);
+    if (grid <= 0) return IKBO_ERR_CUDA;
+  } else if (kernel == kKernPp) {
+    grid = D == 64 ? pp_grid<64>(ds) : pp_grid<128>(ds);
     if (grid <= 0) return IKBO_ERR_CUDA;
   }
   *out = plan_workspace(n_cand, n_user, H, Lq, D, ds->num_sms, grid > 0 ? grid : ds->num_sms,
-                        t_kernel);
+                        kernel);
   return IKBO_OK;
 }
 
@@ -699,14 +761,19 @@ int ikbo_set_trace(uint64_t* device_buffer) {
 
 int ikbo_set_kernel(int which) {
   const int prev = t_kernel;
-  t_kernel = which == 1 ? 1 : 0;
+  t_kernel = (which >= kKernAuto && which <= kKernPp) ? which : kKernAuto;
   return prev;
+}
+
+int ikbo_selected_kernel(int64_t n_cand, int64_t n_user, int32_t Lq) {
+  if (n_cand < 0 || n_user < 0 || Lq < 1 || Lq > kTileM) return IKBO_ERR_SHAPE;
+  return effective_kernel(n_cand, n_user, Lq);
 }
 
 int ikbo_launches_per_call(int64_t n_cand, int64_t n_user) {
   if (n_cand < 0 || n_user < 0) return IKBO_ERR_SHAPE;
   if (n_cand == 0) return 0;
-  return (t_kernel == 0 && n_cand <= kFusedMaxCand && n_user <= kFusedMaxUser) ? 1 : 2;
+  return (t_kernel != kKernSimt && fits_in_kernel_planning(n_cand, n_user)) ? 1 : 2;
 }
 
 }  // extern "C"

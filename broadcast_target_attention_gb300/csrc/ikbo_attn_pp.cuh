@@ -1,0 +1,509 @@
+// IKBO target attention, tcgen05 kernel with two query tiles of one user and
+// head per work item, sharing one K/V stream.
+//
+// What it computes is what ikbo_attn_tc_kernel computes: the flash-attention
+// forward of "Chapter 4: High-performance Kernels", §4.6.1, over the query
+// tiles and user key ranges of "In-Kernel Broadcast Optimization", §3.1-§3.2.
+// It is meant for users with many candidates (two or more query tiles per
+// head), where the work is a dense contraction and the single-tile kernel
+// leaves the tensor cores idle while the softmax of a tile runs.  Here the
+// schedule is the ping-pong of "Optimizing Jagged Flash Attention with TLX",
+// §2.1: two query tiles A and B (consecutive candidates of the same user, the
+// same head) are in flight in one CTA, each with a softmax warpgroup of its
+// own, and while one warpgroup turns its scores into weights the tensor cores
+// work for the other.  Both tiles read the same K/V tile from shared memory,
+// so each K/V tile is loaded once for up to 256 query rows: the IKBO saving of
+// §3.1, twice over.
+//
+//   * tensor memory: S/P of A (128 columns), S/P of B, O of A and O of B
+//     (D columns each);
+//   * warp 0 (TMA producer): Q_A, K_0, Q_B, then V_0, K_1, V_1, K_2, ...;
+//   * warp 1 (MMA issuer): S_A(0), S_B(0), then for every key tile j:
+//     PV_A(j), S_A(j+1), PV_B(j), S_B(j+1).  S_A(j+1) overwrites the buffer
+//     that PV_A(j) reads P_A(j) from, which is safe as the MMAs of one thread
+//     run in order; and S_A(j+1) complete implies PV_A(j) complete, so the
+//     softmax may rescale O_A as soon as it sees S_A(j+1);
+//   * warps 4-7: softmax, correction and epilogue of tile A, warps 8-11 of
+//     tile B, one thread per query row (all 128 key columns of a tile).
+// An item whose user has an odd number of query tiles left has no tile B:
+// warps 8-11 skip it.  Every wait is bounded, as in the single-tile kernel.
+#pragma once
+
+#include "ikbo_attn_tc.cuh"
+
+namespace ikbo {
+
+constexpr int kPpGroups = 2;                 // query tiles per item
+constexpr int kPpSoftmaxWarps = 4;           // warps per tile: one thread per row
+
+template <int D>
+struct PpConfig {
+  static constexpr int kCB = D / 64;
+  static constexpr int kQBytes = kCB * kTileM * 128;
+  static constexpr int kKVBytes = kCB * kBlockN * 128;
+  static constexpr int kFit = (kDataBytes - kPpGroups * kQBytes) / kKVBytes;
+  static constexpr int kSlots = kFit < kMaxSlots ? kFit : kMaxSlots;
+  static constexpr int kTmemCols = 512;
+  __host__ __device__ static constexpr uint32_t kSCol(int g) { return uint32_t(g) * kBlockN; }
+  __host__ __device__ static constexpr uint32_t kOCol(int g) { return uint32_t(kPpGroups * kBlockN + g * D); }
+  static_assert(kPpGroups * (kBlockN + D) <= kTmemCols, "TMEM budget");
+  static_assert(kSlots >= 3, "ring size");
+};
+
+static_assert(kSoftmaxWarp0 + kPpGroups * kPpSoftmaxWarps == kTcThreads / 32, "warp roles");
+
+template <int D>
+__global__ void __launch_bounds__(kTcThreads, 1)
+ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap qmap,
+                    const __grid_constant__ CUtensorMap qmap1,
+                    const __grid_constant__ CUtensorMap kmap_tmpl,
+                    const __grid_constant__ CUtensorMap vmap_tmpl) {
+  using C = PpConfig<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* data = smem_raw;
+  TcCtrl* ctl = reinterpret_cast<TcCtrl*>(smem_raw + kDataBytes);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const bool layout_ok = (ptx::smem_addr(smem_raw) & 1023u) == 0;
+
+  if (threadIdx.x == 0) {
+    for (int g = 0; g < kPpGroups; ++g) {
+      ptx::mbar_init(ptx::smem_addr(&ctl->q_full[g]), 1);
+      ptx::mbar_init(ptx::smem_addr(&ctl->q_empty[g]), 1);
+      ptx::mbar_init(ptx::smem_addr(&ctl->s_full[g]), 1);
+      ptx::mbar_init(ptx::smem_addr(&ctl->p_full[g]), kPpSoftmaxWarps);
+      ptx::mbar_init(ptx::smem_addr(&ctl->p_half[g]), kPpSoftmaxWarps);
+      ptx::mbar_init(ptx::smem_addr(&ctl->pv_done[g]), 1);   // an item's last PV of tile g
+    }
+    for (int i = 0; i < kMaxSlots; ++i) {
+      ptx::mbar_init(ptx::smem_addr(&ctl->kv_full[i]), 1);
+      ptx::mbar_init(ptx::smem_addr(&ctl->kv_empty[i]), 1);
+    }
+    ptx::mbar_init(ptx::smem_addr(&ctl->drain), 1);
+    ctl->abort_flag = 0;
+    ctl->flags = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_addr(&ctl->tmem_base), C::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  if (warp == 2 && lane == 0) {
+    ptx::prefetch_tensormap(&qmap);
+    ptx::prefetch_tensormap(&kmap_tmpl);
+    ptx::prefetch_tensormap(&vmap_tmpl);
+  }
+  if (p.fused && layout_ok) plan_load(p, data);
+  __syncthreads();
+  if (!layout_ok || !p.fused) {
+    // this kernel plans in-kernel only; the host never launches it otherwise
+    if (threadIdx.x == 0) {
+      ctl->mode = kModeSkip;
+      ctl->n_my_items = 0;
+      ctl->sorted = 1;
+      atomicOr(p.err_word, kErrLayout);
+    }
+  } else {
+    plan_in_cta(p, ctl, data, D, kPpGroups);
+    ptx::fence_proxy_async_smem();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (threadIdx.x == 0) trace(p, 0, kTrCtaStart);
+
+  const uint32_t tmem = ctl->tmem_base;
+  const int mode = ctl->mode;
+  const int n_my = ctl->n_my_items;
+  const bool sorted = ctl->sorted != 0;
+  const int NS = C::kSlots;
+  const int Lq = p.Lq;
+  const int cpt = p.cands_per_tile;
+  uint8_t* q_smem = data;
+  uint8_t* kv_smem = data + kPpGroups * C::kQBytes;
+  const int32_t* perm = p.perm_ws;
+  const Waiter W{&ctl->abort_flag, p.err_word, p.timeout_ns};
+  auto item_at = [&](int k) -> WorkItem {
+    return k < kCtlItems ? ctl->items[k] : p.cta_items[(size_t)blockIdx.x * p.max_cta_items + k];
+  };
+  auto ntiles = [](const WorkItem& w) { return ceil_div(w.kv_len, kBlockN); };
+  // candidates of query tile g of an item (tile B holds those past the first cpt)
+  auto tile_cands = [&](const WorkItem& w, int g) {
+    return g == 0 ? min(w.n_cand, cpt) : max(w.n_cand - cpt, 0);
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0 && mode != kModeSkip) {
+      bool tail_ready = false;
+      // K/V maps with an open row count; a tile reaching past row T goes
+      // through a copy with the row count set to T (zero fill past the end)
+      auto kv_map = [&](bool is_v, int32_t row) -> const void* {
+        const int T = ctl->total_keys;
+        if (row + kBlockN <= T) return is_v ? (const void*)&vmap_tmpl : (const void*)&kmap_tmpl;
+        CUtensorMap* tail_k = p.map_slots + 2 * blockIdx.x;
+        CUtensorMap* tail_v = tail_k + 1;
+        if (!tail_ready) {
+#pragma unroll
+          for (int mi = 0; mi < 2; ++mi) {
+            const uint4* s4 = reinterpret_cast<const uint4*>(mi == 0 ? &kmap_tmpl : &vmap_tmpl);
+            uint4* d4 = reinterpret_cast<uint4*>(mi == 0 ? tail_k : tail_v);
+#pragma unroll
+            for (int i = 0; i < (int)(sizeof(CUtensorMap) / 16); ++i) d4[i] = s4[i];
+            asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 1, %1;" ::"l"(d4), "r"(T)
+                         : "memory");
+          }
+          asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
+          ptx::tensormap_acquire(tail_k);
+          ptx::tensormap_acquire(tail_v);
+          tail_ready = true;
+        }
+        return is_v ? (const void*)tail_v : (const void*)tail_k;
+      };
+      uint32_t kv_it = 0;
+      uint32_t qn[kPpGroups] = {0, 0};
+      // the next ring load: one K or V tile (128 keys x D of one head)
+      auto ring = [&](bool is_v, int head, int32_t row) -> bool {
+        const uint32_t slot = kv_it % NS;
+        if (!W.wait(ptx::smem_addr(&ctl->kv_empty[slot]), ((kv_it / NS) & 1u) ^ 1u)) return false;
+        const void* map = kv_map(is_v, row);
+        const uint32_t bar = ptx::smem_addr(&ctl->kv_full[slot]);
+        const uint32_t dst = ptx::smem_addr(kv_smem + slot * C::kKVBytes);
+        ptx::mbar_arrive_expect_tx(bar, C::kKVBytes);
+#pragma unroll
+        for (int cb = 0; cb < C::kCB; ++cb)
+          ptx::tma_load_2d(dst + cb * kBlockN * 128, map, bar, head * D + cb * 64, row);
+        ++kv_it;
+        return true;
+      };
+      // query tile g of item w into Q buffer g
+      auto load_q = [&](int g, const WorkItem& w) -> bool {
+        if (!W.wait(ptx::smem_addr(&ctl->q_empty[g]), (qn[g] & 1u) ^ 1u)) return false;
+        ++qn[g];
+        if (p.debug_flags & 1) return true;    // test hook: never arm the Q barrier
+        const int nc = tile_cands(w, g);
+        const int32_t c0 = w.cand_begin + g * cpt;
+        const uint32_t qbar = ptx::smem_addr(&ctl->q_full[g]);
+        const uint32_t qdst = ptx::smem_addr(q_smem + g * C::kQBytes);
+        if (sorted) {
+          const int nb = p.qbox;
+          const int nbox = ceil_div(nc, nb);
+          ptx::mbar_arrive_expect_tx(qbar, uint32_t(nbox * nb * Lq * 128 * C::kCB));
+          for (int cb = 0; cb < C::kCB; ++cb)
+            for (int bx = 0; bx < nbox; ++bx)
+              ptx::tma_load_4d(qdst + cb * kTileM * 128 + bx * nb * Lq * 128, &qmap, qbar, cb * 64, 0, w.head,
+                               c0 + bx * nb);
+        } else {
+          ptx::mbar_arrive_expect_tx(qbar, uint32_t(nc * Lq * 128 * C::kCB));
+          for (int i = 0; i < nc; ++i) {
+            const int32_t c = perm[c0 + i];
+            for (int cb = 0; cb < C::kCB; ++cb)
+              ptx::tma_load_4d(qdst + cb * kTileM * 128 + i * Lq * 128, &qmap1, qbar, cb * 64, 0, w.head, c);
+          }
+        }
+        return true;
+      };
+      bool ok = true;
+      for (int k = 0; k < n_my && ok; ++k) {
+        const WorkItem w = item_at(k);
+        const int n = ntiles(w);
+        const bool has_b = tile_cands(w, 1) > 0;
+        trace(p, k, kTrProdItem);
+        // Q_A and K_0 first: S_A(0) needs only these
+        ok = load_q(0, w) && ring(false, w.head, w.kv_begin) && (!has_b || load_q(1, w));
+        for (int j = 0; j < n && ok; ++j) {
+          ok = ring(true, w.head, w.kv_begin + j * kBlockN);
+          if (ok && j + 1 < n) ok = ring(false, w.head, w.kv_begin + (j + 1) * kBlockN);
+        }
+        trace(p, k, kTrProdIssued);
+      }
+      // Drain: every armed barrier phase must complete before the CTA exits.
+      for (uint32_t s = 0; s < (uint32_t)NS && s < kv_it; ++s) {
+        const uint32_t uses = (kv_it - s + NS - 1) / NS;
+        W.drain(ptx::smem_addr(&ctl->kv_full[s]), (uses - 1) & 1u);
+      }
+      if (!(p.debug_flags & 1))
+        for (int g = 0; g < kPpGroups; ++g)
+          if (qn[g]) W.drain(ptx::smem_addr(&ctl->q_full[g]), (qn[g] - 1) & 1u);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // -------------------------------------------------------------- MMA issuer
+    if (lane == 0 && mode != kModeSkip) {
+      constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(kTileM, kBlockN, 0);
+      constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(kTileM, D, 1);
+      uint32_t kv_base = 0;                       // ring index of the item's K_0
+      uint32_t qn[kPpGroups] = {0, 0}, pn[kPpGroups] = {0, 0};
+      auto kv_ready = [&](uint32_t idx) -> bool {
+        if (!W.wait(ptx::smem_addr(&ctl->kv_full[idx % NS]), (idx / NS) & 1u)) return false;
+        ptx::tc_fence_after();
+        return true;
+      };
+      // S_g = Q_g K^T, K in ring slot kslot, into S buffer g
+      auto issue_s = [&](int g, uint32_t kslot) {
+        const uint32_t q_base = ptx::smem_addr(q_smem + g * C::kQBytes);
+        const uint32_t k_base = ptx::smem_addr(kv_smem + kslot * C::kKVBytes);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const int cb = kk >> 2;
+          const uint32_t koff = (kk & 3) * 32;
+          const uint64_t a = ptx::smem_desc_sw128(q_base + cb * kTileM * 128 + koff, 16, 1024);
+          const uint64_t bdesc = ptx::smem_desc_sw128(k_base + cb * kBlockN * 128 + koff, 16, 1024);
+          ptx::mma_ss(tmem + C::kSCol(g), a, bdesc, kIdescQK, kk > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(ptx::smem_addr(&ctl->s_full[g]));
+      };
+      // O_g += P_g V over keys [64 h, 64 h + 64) of the tile, P from the
+      // first 64 columns of S buffer g, V (MN-major) in ring slot vslot
+      auto issue_pv_half = [&](int g, uint32_t vslot, int h, bool acc) {
+        const uint32_t v_base = ptx::smem_addr(kv_smem + vslot * C::kKVBytes);
+#pragma unroll
+        for (int q = 0; q < kBlockN / 32; ++q) {
+          const int kk = h * (kBlockN / 32) + q;
+          const uint64_t bdesc = ptx::smem_desc_sw128(v_base + kk * 16 * 128, kBlockN * 128, 1024);
+          ptx::mma_ts(tmem + C::kOCol(g), tmem + C::kSCol(g) + kk * 8, bdesc, kIdescPV,
+                      (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      // P_g of the current tile: first half (h = 0) or all of it (h = 1);
+      // one phase of each barrier per tile
+      auto p_ready = [&](int g, int h) -> bool {
+        if (!W.wait(ptx::smem_addr(h == 0 ? &ctl->p_half[g] : &ctl->p_full[g]), pn[g] & 1u)) return false;
+        if (h == 1) ++pn[g];
+        ptx::tc_fence_after();
+        return true;
+      };
+      // O_g += P_g V_j: each half once the softmax has written it
+      auto issue_pv = [&](int g, uint32_t vslot, bool acc) -> bool {
+        if (!p_ready(g, 0)) return false;
+        issue_pv_half(g, vslot, 0, acc);
+        if (!p_ready(g, 1)) return false;
+        issue_pv_half(g, vslot, 1, true);
+        return true;
+      };
+      bool ok = true;
+      for (int k = 0; k < n_my && ok; ++k) {
+        const WorkItem w = item_at(k);
+        const int n = ntiles(w);
+        const bool has_b = tile_cands(w, 1) > 0;
+        if (!W.wait(ptx::smem_addr(&ctl->q_full[0]), qn[0] & 1u)) break;
+        if (has_b && !W.wait(ptx::smem_addr(&ctl->q_full[1]), qn[1] & 1u)) break;
+        ptx::tc_fence_after();
+        trace(p, k, kTrMmaQ);
+        if (!kv_ready(kv_base)) break;
+        {
+          const uint32_t ks = kv_base % NS;
+          issue_s(0, ks);
+          if (n == 1) ptx::mma_commit(ptx::smem_addr(&ctl->q_empty[0]));
+          if (has_b) {
+            issue_s(1, ks);
+            if (n == 1) ptx::mma_commit(ptx::smem_addr(&ctl->q_empty[1]));
+          }
+          ptx::mma_commit(ptx::smem_addr(&ctl->kv_empty[ks]));
+        }
+        trace(p, k, kTrMmaFirstS);
+        for (int j = 0; j < n; ++j) {
+          const uint32_t vi = kv_base + 2 * j + 1, ki = vi + 1;
+          const bool more = j + 1 < n;
+          if (!kv_ready(vi) || !issue_pv(0, vi % NS, j > 0)) {
+            ok = false;
+            break;
+          }
+          if (!more) ptx::mma_commit(ptx::smem_addr(&ctl->pv_done[0]));
+          if (more) {
+            if (!kv_ready(ki)) {
+              ok = false;
+              break;
+            }
+            issue_s(0, ki % NS);
+            if (j + 2 == n) ptx::mma_commit(ptx::smem_addr(&ctl->q_empty[0]));
+          }
+          if (has_b) {
+            if (!issue_pv(1, vi % NS, j > 0)) {
+              ok = false;
+              break;
+            }
+            if (!more) ptx::mma_commit(ptx::smem_addr(&ctl->pv_done[1]));
+          }
+          ptx::mma_commit(ptx::smem_addr(&ctl->kv_empty[vi % NS]));
+          if (more) {
+            if (has_b) {
+              issue_s(1, ki % NS);
+              if (j + 2 == n) ptx::mma_commit(ptx::smem_addr(&ctl->q_empty[1]));
+            }
+            ptx::mma_commit(ptx::smem_addr(&ctl->kv_empty[ki % NS]));
+          }
+        }
+        trace(p, k, kTrMmaLastPV);
+        kv_base += 2 * n;
+        ++qn[0];
+        if (has_b) ++qn[1];
+      }
+      // All issued MMAs must finish before tensor memory is released.
+      ptx::mma_commit(ptx::smem_addr(&ctl->drain));
+      W.drain(ptx::smem_addr(&ctl->drain), 0);
+    }
+    __syncwarp();
+  } else if (warp >= kSoftmaxWarp0 && mode != kModeSkip) {
+    // ------------------------------------------- softmax / correction / epilogue
+    const int g = (warp - kSoftmaxWarp0) / kPpSoftmaxWarps;   // query tile of this warp
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;                      // TMEM lane == tile row
+    const uint32_t lane_off = uint32_t(quarter * 32) << 16;
+    const uint32_t scol = tmem + lane_off + C::kSCol(g);
+    const uint32_t ocol = tmem + lane_off + C::kOCol(g);
+    const float sl2 = p.scale_log2;
+    uint32_t tn = 0, dn = 0;                                  // S tiles and items of this tile so far
+    for (int k = 0; k < n_my; ++k) {
+      const WorkItem w = item_at(k);
+      const int nc = tile_cands(w, g);
+      if (nc == 0) continue;
+      const int n = ntiles(w);
+      // Rows past the tile's queries hold stale shared memory; their results
+      // are never stored, and they are left out of every decision below.
+      const bool live = row < nc * Lq;
+      float m = -INFINITY, l = 0.f;
+      bool ok = true;
+      for (int j = 0; j < n; ++j, ++tn) {
+        if (!W.warp_wait(ptx::smem_addr(&ctl->s_full[g]), tn & 1u)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        // All 128 scores of the row at once (one TMEM round trip); P is
+        // written over them in place, two keys per 32-bit word.
+        uint32_t r[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) ptx::tmem_ld32(scol + c * 32, r[c]);
+        ptx::tmem_ld_wait();
+#define IKBO_R(e) __uint_as_float(r[(e) >> 5][(e) & 31])
+        // Scores enter the exponent as fma(s, sc, -m): raw scores with
+        // sc = scale on full tiles for scale > 0 (their order is that of the
+        // scaled ones), else scaled here with the keys past the user's
+        // sequence at -inf (sc = 1).
+        const int valid = min(kBlockN, w.kv_len - j * kBlockN);
+        float sc = sl2;
+        if (valid < kBlockN || !(sl2 > 0.f)) {
+#pragma unroll
+          for (int e = 0; e < kBlockN; ++e) {
+            const float tt = IKBO_R(e) * sl2;
+            r[e >> 5][e & 31] = __float_as_uint(e < valid ? tt : -INFINITY);
+          }
+          sc = 1.f;
+        }
+        float mx;
+        {
+          // four independent chains
+          float a0 = fmaxf(IKBO_R(0), IKBO_R(1)), a1 = fmaxf(IKBO_R(2), IKBO_R(3));
+          float a2 = fmaxf(IKBO_R(4), IKBO_R(5)), a3 = fmaxf(IKBO_R(6), IKBO_R(7));
+#pragma unroll
+          for (int e = 8; e < kBlockN; e += 8) {
+            a0 = fmax3(a0, IKBO_R(e), IKBO_R(e + 1));
+            a1 = fmax3(a1, IKBO_R(e + 2), IKBO_R(e + 3));
+            a2 = fmax3(a2, IKBO_R(e + 4), IKBO_R(e + 5));
+            a3 = fmax3(a3, IKBO_R(e + 6), IKBO_R(e + 7));
+          }
+          mx = fmax3(a0, a1, fmaxf(a2, a3)) * sc;
+        }
+        // The running maximum moves only when the tile's exceeds it by more
+        // than kLazyRescale (weights stay <= 2^8), and always on an item's
+        // first tile.
+        const float m_new = (j == 0 || mx > m + kLazyRescale) ? mx : m;
+        const float alpha = fast_exp2(m - m_new);   // 0 on the first tile, 1 when m stays
+        if (j > 0 && __any_sync(0xffffffffu, live && m_new != m)) {
+          // O must hold exactly P_0..P_{j-1} V when it is rescaled: S_g(j)
+          // complete implies PV_g(j-1) complete (issued before it), and
+          // PV_g(j) waits for this tile's P
+          // (16 columns at a time: the scores are live in registers here)
+#pragma unroll 1
+          for (int c = 0; c < D / 16; ++c) {
+            uint32_t o[16];
+            ptx::tmem_ld16(ocol + c * 16, o);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            ptx::tmem_st16(ocol + c * 16, o);
+          }
+        }
+        // P = 2^(s sc - m_new) as bf16 pairs, key pair e / 2 into word e / 2
+        // (a word whose scores were read already), in two halves of 64 keys:
+        // the MMA warp starts O += P V on the first while the second is made.
+        float sum = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float2 sc2 = make_float2(sc, sc), nr2 = make_float2(-m_new, -m_new);
+          float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int e = 64 * h; e < 64 * h + 64; e += 2) {
+            const float2 x = ffma2(make_float2(IKBO_R(e), IKBO_R(e + 1)), sc2, nr2);
+            const float2 pe = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+            if ((e >> 1) & 1) a1 = fadd2(a1, pe); else a0 = fadd2(a0, pe);
+            r[e >> 6][(e >> 1) & 31] = pack_bf16(pe.x, pe.y);
+          }
+          const float2 u = fadd2(a0, a1);
+          sum += u.x + u.y;
+          ptx::tc_fence_before();
+          ptx::tmem_st32(scol + 32 * h, r[h]);
+          ptx::tmem_st_wait();
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(h == 0 ? &ctl->p_half[g] : &ctl->p_full[g]));
+        }
+#undef IKBO_R
+        l = l * alpha + sum;
+        m = m_new;
+      }
+      if (!ok) break;
+      // ---- epilogue: O after the item's last PV of this tile
+      if (!W.warp_wait(ptx::smem_addr(&ctl->pv_done[g]), dn & 1u)) break;
+      ++dn;
+      ptx::tc_fence_after();
+      if (row == 0 && g == 0) trace(p, k, kTrEpiO);
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float2 inv2 = make_float2(inv, inv);
+      const int ci = live ? row / Lq : 0;
+      const int tq = live ? row - ci * Lq : 0;
+      const int32_t gpos = w.cand_begin + g * cpt + ci;
+      const int64_t cidx = live ? (sorted ? gpos : perm[gpos]) : 0;
+      uint16_t* dst = p.out + (((cidx * p.H + w.head) * (int64_t)Lq + tq) * D);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        ptx::tmem_ld32(ocol + c * 32, o);
+        ptx::tmem_ld_wait();
+        if (live) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const float2 x0 = fmul2(make_float2(__uint_as_float(o[8 * q4 + 0]), __uint_as_float(o[8 * q4 + 1])), inv2);
+            const float2 x1 = fmul2(make_float2(__uint_as_float(o[8 * q4 + 2]), __uint_as_float(o[8 * q4 + 3])), inv2);
+            const float2 x2 = fmul2(make_float2(__uint_as_float(o[8 * q4 + 4]), __uint_as_float(o[8 * q4 + 5])), inv2);
+            const float2 x3 = fmul2(make_float2(__uint_as_float(o[8 * q4 + 6]), __uint_as_float(o[8 * q4 + 7])), inv2);
+            uint4 v;
+            v.x = pack_bf16(x0.x, x0.y);
+            v.y = pack_bf16(x1.x, x1.y);
+            v.z = pack_bf16(x2.x, x2.y);
+            v.w = pack_bf16(x3.x, x3.y);
+            d4[q4] = v;
+          }
+        }
+      }
+      if (row == 0 && g == 0) trace(p, k, kTrEpiStored);
+      // the next item's PV_g(0) overwrites O_g: it waits for that item's
+      // first P of this tile, which these warps hand over only after the
+      // reads above
+      ptx::tc_fence_before();
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0) trace(p, 0, kTrCtaEnd);
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+}  // namespace ikbo

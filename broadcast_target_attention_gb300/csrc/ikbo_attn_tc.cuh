@@ -145,6 +145,7 @@ struct TcCtrl {
   uint64_t s_full[kSBufs], p_full[kSBufs];
   uint64_t pv_done[kSBufs];             // PV of the tile in S buffer i complete
   uint64_t drain, pair_go, pair_recv;
+  uint64_t p_half[2];                   // two-tile kernel: first half of P written
   uint32_t tmem_base;
   int abort_flag;
   int mode;
@@ -155,7 +156,7 @@ struct TcCtrl {
   int flags;
   int n_units;                          // planning: units in all (read by every thread)
   int early_loads;                      // ring loads of item 0 issued before the roles start
-  int red[24];
+  int red[kTcThreads / 32];             // block scan: one word per warp
   WorkItem items[kCtlItems];            // the first items of this CTA (the rest in global memory)
   alignas(16) float partner_lse[kTileM];
   // row maximum / row sum exchange among the kSplit threads of a row:
@@ -345,7 +346,10 @@ __device__ __forceinline__ void plan_load(const AttnParams& p, uint8_t* scratch)
   }
 }
 
-__device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch, int D) {
+// A unit is (user, head, up to tiles_per_unit query tiles of the user's
+// candidates): 1 for this kernel, 2 for the two-tile kernel.
+__device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch, int D,
+                            int tiles_per_unit) {
   const int tid = threadIdx.x, nt = blockDim.x;
   const int grid = gridDim.x, b = blockIdx.x;
   const int n_cand = (int)p.n_cand, n_user = (int)p.n_user;
@@ -484,9 +488,9 @@ __device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch, 
       }
     }
   }
-  // Units (H x query tiles of users with candidates and keys), prefix-summed
-  // over the users in index order, or longest first (below).
-  const int cpt = p.cands_per_tile;
+  // Units (H x groups of query tiles of users with candidates and keys),
+  // prefix-summed over the users in index order, or longest first (below).
+  const int cpt = p.cands_per_tile * tiles_per_unit;   // candidates per unit
   bool lpt = false;
   auto user_at = [&](int rk) { return lpt ? order[rk] : rk; };
   auto units_of = [&](int u) {
@@ -535,7 +539,7 @@ __device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch, 
   const int N = ctl->n_units;
   // Pair mode when every unit gets a cluster of its own; otherwise units are
   // dealt to independent CTAs, users longest first.
-  const bool pair = N > 0 && 2 * N <= grid;
+  const bool pair = tiles_per_unit == 1 && N > 0 && 2 * N <= grid;
   if (!pair && n_user > 1 && n_user <= kLptMaxUsersFused) {
     __syncthreads();   // everyone has read N before the prefix is rewritten
     for (int u = tid; u < n_user; u += nt) {
@@ -697,7 +701,7 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
       atomicOr(p.err_word, kErrLayout);
     }
   } else if (p.fused) {
-    plan_in_cta(p, ctl, data, D);
+    plan_in_cta(p, ctl, data, D, 1);
     trace_pro(p, 7);
     // the planning scratch is overwritten by TMA (async proxy) from here on
     ptx::fence_proxy_async_smem();

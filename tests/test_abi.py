@@ -99,3 +99,29 @@ def test_python_binding_raises_on_bad_status(lib):
     with pytest.raises(ikbo.IkboError) as e:
         ikbo._check(_lib.IKBO_ERR_SHAPE, "x")
     assert "IKBO_ERR_SHAPE" in str(e.value)
+
+
+def test_selected_kernel(lib):
+    """Automatic choice: two query tiles per item when the users have on average at least
+    eight query tiles each and the inputs fit the in-kernel planning limits."""
+    sel = lib.ikbo_selected_kernel
+    assert sel(1024, 15, 1) == 2            # 1024 candidates / 15 users, Lq 1: < 1 tile per user
+    assert sel(8, 2, 1) == 2
+    assert sel(2048, 16, 4) == 2            # 32 candidates per tile: 4 tiles per user
+    assert sel(4096, 4, 8) == 3             # 16 candidates per tile: 64 tiles per user
+    assert sel(16384, 64, 1) == 2           # two tiles per user
+    assert sel(16384, 64, 4) == 3           # exactly eight tiles per user
+    assert sel(16383, 64, 4) == 2
+    assert sel(20481, 4, 8) == 2            # beyond the in-kernel planning limits
+    assert sel(4096, 1025, 1) == 2
+    assert sel(-1, 2, 1) == _lib.IKBO_ERR_SHAPE
+    assert sel(8, 2, 0) == _lib.IKBO_ERR_SHAPE
+    assert sel(8, 2, 129) == _lib.IKBO_ERR_SHAPE
+    for which, expect in ((1, 1), (2, 2), (3, 3), (7, 2)):
+        prev = lib.ikbo_set_kernel(which)
+        try:
+            assert sel(1024, 15, 1) == expect
+            assert sel(20481, 4, 8) == (1 if which == 1 else 2)   # two tiles: in-kernel planning only
+            assert lib.ikbo_launches_per_call(1024, 15) == (2 if which == 1 else 1)
+        finally:
+            lib.ikbo_set_kernel(prev)

@@ -4,8 +4,10 @@ Every configuration of the workload table, plus edge cases: ragged tails,
 odd and single-candidate groups, empty sequences, users without candidates,
 an unsorted candidate map, Lq from 1 to 128, D = 64 and 128, split-KV units.
 Tolerance: max-abs 2e-2 and mean-abs 2e-3 for bf16 inputs with fp32
-accumulation.  Both GPU kernels are checked: the tcgen05 kernel (0, the
-default) and the SIMT kernel (1).
+accumulation.  Every GPU kernel is checked: the SIMT kernel (1), the tcgen05
+kernel with one query tile per work item (2) and the one with two query tiles
+of one user and head per item (3); the full-size configurations also with the
+automatic choice (0).
 """
 import numpy as np
 import pytest
@@ -17,7 +19,8 @@ from _helpers import assert_close, out_f64, to_device
 
 pytestmark = pytest.mark.gpu
 
-KERNELS = [0, 1]
+KERNELS = [1, 2, 3]
+CONFIG_KERNELS = [0, 1, 2, 3]
 # (config, number of candidates checked against the oracle; None = all)
 CONFIG_SAMPLES = [
     ("tiny_8x2", None),
@@ -41,6 +44,20 @@ def workload(name):
     return _cache[name]
 
 
+_ref_cache = {}
+
+
+def config_reference(name, n_sample):
+    """(workload, sampled candidates, oracle rows) of a configuration, computed once."""
+    if name not in _ref_cache:
+        wl = workload(name)
+        cands = None if n_sample is None else W.sample_candidates(wl, n_sample)
+        _ref_cache.clear()
+        _ref_cache[name] = (cands, oracle.attention_wl(wl, cands))
+    cands, ref = _ref_cache[name]
+    return workload(name), cands, ref
+
+
 def run(ikbo, wl, kernel, **kw):
     prev = ikbo.set_kernel(kernel)
     try:
@@ -53,13 +70,11 @@ def run(ikbo, wl, kernel, **kw):
     return out
 
 
-@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("name,n_sample", CONFIG_SAMPLES)
+@pytest.mark.parametrize("kernel", CONFIG_KERNELS)
 def test_config_matches_oracle(gpu_lib, name, n_sample, kernel):
-    wl = workload(name)
-    cands = None if n_sample is None else W.sample_candidates(wl, n_sample)
+    wl, cands, ref = config_reference(name, n_sample)
     out = run(gpu_lib, wl, kernel)
-    ref = oracle.attention_wl(wl, cands)
     assert_close(out_f64(out, cands), ref, f"{name} kernel={kernel}")
     # properties that hold for every row, checked at full size
     assert torch.isfinite(out.float()).all()
@@ -80,6 +95,10 @@ EDGE = {
     # a last user shorter than a key tile: the tiles of the users before it
     # that reach past the end of k/v
     "short_last": dict(n_user=4, counts=[4, 3, 2, 5], lens=[300, 170, 90, 20]),
+    # groups around one and two query tiles (Lq = 1: 128 candidates a tile):
+    # full pairs, a pair whose second tile has one candidate, a lone tile,
+    # an odd number of tiles
+    "tile_pairs": dict(n_user=5, counts=[256, 129, 128, 1, 383], lens=[200, 64, 129, 40, 300]),
 }
 
 
@@ -127,16 +146,21 @@ def test_scale_values(gpu_lib, scale, kernel):
 
 def test_kernels_agree_at_full_size(gpu_lib):
     wl = workload("odd_groups_2048x16")
-    a = run(gpu_lib, wl, 0).float()
-    b = run(gpu_lib, wl, 1).float()
-    assert (a - b).abs().max().item() <= 2e-2
+    a = run(gpu_lib, wl, 1).float()
+    for kernel in (2, 3):
+        b = run(gpu_lib, wl, kernel).float()
+        assert (a - b).abs().max().item() <= 2e-2, kernel
 
 
-def test_identical_queries_give_identical_rows(gpu_lib):
-    """A property at any size: candidates of one user with the same queries get the same rows."""
-    wl = workload("ratio_1024x15")
+@pytest.mark.parametrize("name", ["ratio_1024x15", "extreme_4096x4"])
+def test_identical_queries_give_identical_rows(gpu_lib, name):
+    """A property at any size: candidates of one user with the same queries get the same
+    rows (for the second configuration across the 64 query tiles of its largest user, run
+    two tiles per work item)."""
+    wl = workload(name)
     q = wl.q.copy()
-    first = np.nonzero(wl.cand_to_user == 3)[0]
+    user = 3 if name == "ratio_1024x15" else int(np.bincount(wl.cand_to_user).argmax())
+    first = np.nonzero(wl.cand_to_user == user)[0]
     q[first[1:]] = q[first[0]]
     wl2 = W.Workload(cfg=wl.cfg, q=q, k=wl.k, v=wl.v, user_offsets=wl.user_offsets,
                      cand_to_user=wl.cand_to_user, scale=wl.scale)
@@ -153,8 +177,9 @@ def test_empty_batch_is_a_noop(gpu_lib):
     assert out.shape[0] == 0
 
 
-def test_repeated_calls_are_deterministic(gpu_lib):
-    wl = workload("ratio_1024x15")
+@pytest.mark.parametrize("name", ["ratio_1024x15", "extreme_4096x4"])
+def test_repeated_calls_are_deterministic(gpu_lib, name):
+    wl = workload(name)
     a = run(gpu_lib, wl, 0)
     b = run(gpu_lib, wl, 0)
     assert torch.equal(a, b)

@@ -54,7 +54,7 @@ def _sentinel_call(gpu_lib, wl, c2u=None, off=None):
     return gpu_lib.get_device_error(), out
 
 
-@pytest.mark.parametrize("kernel", [0, 1])
+@pytest.mark.parametrize("kernel", [1, 2, 3])
 def test_bad_candidate_index_is_reported_not_trapped(gpu_lib, kernel):
     wl = W.custom(n_user=2, counts=[2, 2], lens=[10, 20], H=2, D=64, Lq=1)
     prev = gpu_lib.set_kernel(kernel)
@@ -76,15 +76,18 @@ def test_bad_offsets_are_reported(gpu_lib):
     assert rc == _lib.IKBO_ERR_OFFSETS
 
 
-def test_bounded_wait_reports_timeout_and_context_survives(gpu_lib):
+@pytest.mark.parametrize("kernel", [2, 3])
+def test_bounded_wait_reports_timeout_and_context_survives(gpu_lib, kernel):
     """The producer is told never to arm the query barrier: every waiting warp
     gives up after 50 ms, the kernel exits normally and reports the timeout."""
     wl = W.custom(n_user=2, counts=[5, 3], lens=[300, 40], H=2, D=128, Lq=1, seed=5)
     gpu_lib.set_debug(1, 50_000_000)
+    prev = gpu_lib.set_kernel(kernel)
     try:
         rc, _ = _sentinel_call(gpu_lib, wl)
     finally:
         gpu_lib.set_debug(0, 0)
+        gpu_lib.set_kernel(prev)
     assert rc == _lib.IKBO_ERR_TIMEOUT
     rc, out = _sentinel_call(gpu_lib, wl)     # the context is still usable
     assert rc == 0
