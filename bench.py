@@ -403,7 +403,7 @@ def run_ikbo(args):
     pk = peaks()
     attn = statistics.mean(attn_ms)
     achieved_gbs = alg_bytes / (attn * 1e-3) / 1e9
-    kname = f"{ikbo.KERNEL_NAMES[ikbo.selected_kernel(wl.n_cand, wl.n_user, c.Lq)]}<{c.D}>"
+    kname = f"{ikbo.KERNEL_NAMES[ikbo.selected_kernel(wl.n_cand, wl.n_user, c.H, c.Lq)]}<{c.D}>"
     traffic = kernel_traffic(kname, c.name)
     ai = flops / alg_bytes
     ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)

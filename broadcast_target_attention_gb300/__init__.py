@@ -187,9 +187,9 @@ def set_kernel(which: int) -> int:
     return int(_lib.lib().ikbo_set_kernel(int(which)))
 
 
-def selected_kernel(n_cand: int, n_user: int, Lq: int) -> int:
+def selected_kernel(n_cand: int, n_user: int, H: int, Lq: int) -> int:
     """The kernel (1, 2 or 3) a call of these sizes runs with this thread's choice."""
-    n = int(_lib.lib().ikbo_selected_kernel(int(n_cand), int(n_user), int(Lq)))
+    n = int(_lib.lib().ikbo_selected_kernel(int(n_cand), int(n_user), int(H), int(Lq)))
     _check(min(n, 0), "selected_kernel")
     return n
 

@@ -148,19 +148,25 @@ bool fits_in_kernel_planning(int64_t n_cand, int64_t n_user) {
   return n_cand <= kFusedMaxCand && n_user <= kFusedMaxUser;
 }
 
-// Average query tiles per user from which the automatic choice takes the
-// two-tile kernel.  Measured on one GB300: it is 10-11 % faster with 8 to 64
-// tiles per user, and slower with 2 to 4 (many units there have a single
-// tile, which it runs with half the softmax warps of the one-tile kernel).
-constexpr int64_t kPpMinTilesPerUser = 8;
+// The automatic choice takes the two-tile kernel when the users have on
+// average at least two query tiles each and the batch makes at least this
+// many two-tile items (about four per SM of a GB300).  Measured on one GB300
+// it is 3-19 % faster than the one-tile kernel on such batches (2 to 64
+// tiles per user, 1024 to 4096 items), and 12 % slower on a batch of ~260
+// items of very unequal cost (Zipf-distributed candidates, 64 to 4096 keys),
+// which it cannot spread evenly over the SMs.
+constexpr int64_t kPpMinItems = 600;
 
 // The kernel a call runs with the thread's choice.  The two-tile kernel plans
 // in-kernel only, so inputs beyond those limits take the one-tile kernel.
-int effective_kernel(int64_t n_cand, int64_t n_user, int Lq) {
+int effective_kernel(int64_t n_cand, int64_t n_user, int H, int Lq) {
   if (t_kernel == kKernSimt) return kKernSimt;
   if (t_kernel == kKernTc || !fits_in_kernel_planning(n_cand, n_user)) return kKernTc;
   if (t_kernel == kKernPp) return kKernPp;
-  return n_cand >= kPpMinTilesPerUser * int64_t(cands_per_tile(Lq)) * n_user ? kKernPp : kKernTc;
+  const int64_t pair = 2 * int64_t(cands_per_tile(Lq));        // candidates of a two-tile item
+  const bool two_tiles = n_cand >= pair * n_user;
+  const int64_t items = int64_t(H) * ((n_cand + pair - 1) / pair);
+  return (two_tiles && items >= kPpMinItems) ? kKernPp : kKernTc;
 }
 
 // kernel: kKernTc (plans in-kernel when the inputs fit its shared memory,
@@ -459,7 +465,7 @@ int run_ikbo(DeviceState* ds, const void* q, const void* k, const void* v, const
 int call_workspace(DeviceState* ds, int64_t n_cand, int64_t n_user, int H, int Lq, int D,
                    Workspace* out) {
   int grid = 0;
-  const int kernel = effective_kernel(n_cand, n_user, Lq);
+  const int kernel = effective_kernel(n_cand, n_user, H, Lq);
   if (kernel == kKernTc) {
     grid = D == 64 ? tc_grid<64>(ds) : tc_grid<128>(ds);
     if (grid <= 0) return IKBO_ERR_CUDA;
@@ -765,9 +771,9 @@ int ikbo_set_kernel(int which) {
   return prev;
 }
 
-int ikbo_selected_kernel(int64_t n_cand, int64_t n_user, int32_t Lq) {
-  if (n_cand < 0 || n_user < 0 || Lq < 1 || Lq > kTileM) return IKBO_ERR_SHAPE;
-  return effective_kernel(n_cand, n_user, Lq);
+int ikbo_selected_kernel(int64_t n_cand, int64_t n_user, int32_t H, int32_t Lq) {
+  if (n_cand < 0 || n_user < 0 || H < 1 || Lq < 1 || Lq > kTileM) return IKBO_ERR_SHAPE;
+  return effective_kernel(n_cand, n_user, H, Lq);
 }
 
 int ikbo_launches_per_call(int64_t n_cand, int64_t n_user) {

@@ -18,11 +18,12 @@
 //   * tensor memory: S/P of A (128 columns), S/P of B, O of A and O of B
 //     (D columns each);
 //   * warp 0 (TMA producer): Q_A, K_0, Q_B, then V_0, K_1, V_1, K_2, ...;
-//   * warp 1 (MMA issuer): S_A(0), S_B(0), then for every key tile j:
-//     PV_A(j), S_A(j+1), PV_B(j), S_B(j+1).  S_A(j+1) overwrites the buffer
-//     that PV_A(j) reads P_A(j) from, which is safe as the MMAs of one thread
-//     run in order; and S_A(j+1) complete implies PV_A(j) complete, so the
-//     softmax may rescale O_A as soon as it sees S_A(j+1);
+//   * warp 1 (MMA issuer, converged, one elected lane issuing): S_A(0),
+//     S_B(0), then for every key tile j: PV_A(j), S_A(j+1), PV_B(j),
+//     S_B(j+1).  S_A(j+1) overwrites the buffer that PV_A(j) reads P_A(j)
+//     from, which is safe as the MMAs of one thread run in order; and
+//     S_A(j+1) complete implies PV_A(j) complete, so the softmax may rescale
+//     O_A as soon as it sees S_A(j+1);
 //   * warps 4-7: softmax, correction and epilogue of tile A, warps 8-11 of
 //     tile B, one thread per query row (all 128 key columns of a tile).
 // An item whose user has an odd number of query tiles left has no tile B:
@@ -230,13 +231,15 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
     __syncwarp();
   } else if (warp == 1) {
     // -------------------------------------------------------------- MMA issuer
-    if (lane == 0 && mode != kModeSkip) {
+    // The whole warp runs this loop, converged (waits included), and the
+    // elected lane issues every MMA and commit.
+    if (mode != kModeSkip) {
       constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(kTileM, kBlockN, 0);
       constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(kTileM, D, 1);
       uint32_t kv_base = 0;                       // ring index of the item's K_0
       uint32_t qn[kPpGroups] = {0, 0}, pn[kPpGroups] = {0, 0};
       auto kv_ready = [&](uint32_t idx) -> bool {
-        if (!W.wait(ptx::smem_addr(&ctl->kv_full[idx % NS]), (idx / NS) & 1u)) return false;
+        if (!W.conv_wait(ptx::smem_addr(&ctl->kv_full[idx % NS]), (idx / NS) & 1u)) return false;
         ptx::tc_fence_after();
         return true;
       };
@@ -250,9 +253,9 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
           const uint32_t koff = (kk & 3) * 32;
           const uint64_t a = ptx::smem_desc_sw128(q_base + cb * kTileM * 128 + koff, 16, 1024);
           const uint64_t bdesc = ptx::smem_desc_sw128(k_base + cb * kBlockN * 128 + koff, 16, 1024);
-          ptx::mma_ss(tmem + C::kSCol(g), a, bdesc, kIdescQK, kk > 0 ? 1u : 0u);
+          ptx::mma_ss_warp(tmem + C::kSCol(g), a, bdesc, kIdescQK, kk > 0 ? 1u : 0u);
         }
-        ptx::mma_commit(ptx::smem_addr(&ctl->s_full[g]));
+        ptx::mma_commit_warp(ptx::smem_addr(&ctl->s_full[g]));
       };
       // O_g += P_g V over keys [64 h, 64 h + 64) of the tile, P from the
       // first 64 columns of S buffer g, V (MN-major) in ring slot vslot
@@ -262,14 +265,14 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
         for (int q = 0; q < kBlockN / 32; ++q) {
           const int kk = h * (kBlockN / 32) + q;
           const uint64_t bdesc = ptx::smem_desc_sw128(v_base + kk * 16 * 128, kBlockN * 128, 1024);
-          ptx::mma_ts(tmem + C::kOCol(g), tmem + C::kSCol(g) + kk * 8, bdesc, kIdescPV,
+          ptx::mma_ts_warp(tmem + C::kOCol(g), tmem + C::kSCol(g) + kk * 8, bdesc, kIdescPV,
                       (acc || kk > 0) ? 1u : 0u);
         }
       };
       // P_g of the current tile: first half (h = 0) or all of it (h = 1);
       // one phase of each barrier per tile
       auto p_ready = [&](int g, int h) -> bool {
-        if (!W.wait(ptx::smem_addr(h == 0 ? &ctl->p_half[g] : &ctl->p_full[g]), pn[g] & 1u)) return false;
+        if (!W.conv_wait(ptx::smem_addr(h == 0 ? &ctl->p_half[g] : &ctl->p_full[g]), pn[g] & 1u)) return false;
         if (h == 1) ++pn[g];
         ptx::tc_fence_after();
         return true;
@@ -287,22 +290,22 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
         const WorkItem w = item_at(k);
         const int n = ntiles(w);
         const bool has_b = tile_cands(w, 1) > 0;
-        if (!W.wait(ptx::smem_addr(&ctl->q_full[0]), qn[0] & 1u)) break;
-        if (has_b && !W.wait(ptx::smem_addr(&ctl->q_full[1]), qn[1] & 1u)) break;
+        if (!W.conv_wait(ptx::smem_addr(&ctl->q_full[0]), qn[0] & 1u)) break;
+        if (has_b && !W.conv_wait(ptx::smem_addr(&ctl->q_full[1]), qn[1] & 1u)) break;
         ptx::tc_fence_after();
-        trace(p, k, kTrMmaQ);
+        if (lane == 0) trace(p, k, kTrMmaQ);
         if (!kv_ready(kv_base)) break;
         {
           const uint32_t ks = kv_base % NS;
           issue_s(0, ks);
-          if (n == 1) ptx::mma_commit(ptx::smem_addr(&ctl->q_empty[0]));
+          if (n == 1) ptx::mma_commit_warp(ptx::smem_addr(&ctl->q_empty[0]));
           if (has_b) {
             issue_s(1, ks);
-            if (n == 1) ptx::mma_commit(ptx::smem_addr(&ctl->q_empty[1]));
+            if (n == 1) ptx::mma_commit_warp(ptx::smem_addr(&ctl->q_empty[1]));
           }
-          ptx::mma_commit(ptx::smem_addr(&ctl->kv_empty[ks]));
+          ptx::mma_commit_warp(ptx::smem_addr(&ctl->kv_empty[ks]));
         }
-        trace(p, k, kTrMmaFirstS);
+        if (lane == 0) trace(p, k, kTrMmaFirstS);
         for (int j = 0; j < n; ++j) {
           const uint32_t vi = kv_base + 2 * j + 1, ki = vi + 1;
           const bool more = j + 1 < n;
@@ -310,39 +313,39 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
             ok = false;
             break;
           }
-          if (!more) ptx::mma_commit(ptx::smem_addr(&ctl->pv_done[0]));
+          if (!more) ptx::mma_commit_warp(ptx::smem_addr(&ctl->pv_done[0]));
           if (more) {
             if (!kv_ready(ki)) {
               ok = false;
               break;
             }
             issue_s(0, ki % NS);
-            if (j + 2 == n) ptx::mma_commit(ptx::smem_addr(&ctl->q_empty[0]));
+            if (j + 2 == n) ptx::mma_commit_warp(ptx::smem_addr(&ctl->q_empty[0]));
           }
           if (has_b) {
             if (!issue_pv(1, vi % NS, j > 0)) {
               ok = false;
               break;
             }
-            if (!more) ptx::mma_commit(ptx::smem_addr(&ctl->pv_done[1]));
+            if (!more) ptx::mma_commit_warp(ptx::smem_addr(&ctl->pv_done[1]));
           }
-          ptx::mma_commit(ptx::smem_addr(&ctl->kv_empty[vi % NS]));
+          ptx::mma_commit_warp(ptx::smem_addr(&ctl->kv_empty[vi % NS]));
           if (more) {
             if (has_b) {
               issue_s(1, ki % NS);
-              if (j + 2 == n) ptx::mma_commit(ptx::smem_addr(&ctl->q_empty[1]));
+              if (j + 2 == n) ptx::mma_commit_warp(ptx::smem_addr(&ctl->q_empty[1]));
             }
-            ptx::mma_commit(ptx::smem_addr(&ctl->kv_empty[ki % NS]));
+            ptx::mma_commit_warp(ptx::smem_addr(&ctl->kv_empty[ki % NS]));
           }
         }
-        trace(p, k, kTrMmaLastPV);
+        if (lane == 0) trace(p, k, kTrMmaLastPV);
         kv_base += 2 * n;
         ++qn[0];
         if (has_b) ++qn[1];
       }
       // All issued MMAs must finish before tensor memory is released.
-      ptx::mma_commit(ptx::smem_addr(&ctl->drain));
-      W.drain(ptx::smem_addr(&ctl->drain), 0);
+      ptx::mma_commit_warp(ptx::smem_addr(&ctl->drain));
+      if (lane == 0) W.drain(ptx::smem_addr(&ctl->drain), 0);
     }
     __syncwarp();
   } else if (warp >= kSoftmaxWarp0 && mode != kModeSkip) {
@@ -448,7 +451,7 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
           ptx::tmem_st_wait();
           ptx::tc_fence_before();
           __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(ptx::smem_addr(h == 0 ? &ctl->p_half[g] : &ctl->p_full[g]));
+          ptx::mbar_arrive_warp(ptx::smem_addr(h == 0 ? &ctl->p_half[g] : &ctl->p_full[g]));
         }
 #undef IKBO_R
         l = l * alpha + sum;

@@ -211,6 +211,29 @@ struct Waiter {
       }
     }
   }
+  // The whole warp waits converged: every lane polls and the warp leaves
+  // together, with no divergent branch.  Bounded like wait().
+  __device__ __forceinline__ bool conv_wait(uint32_t bar, uint32_t parity) const {
+    if (__all_sync(0xffffffffu, ptx::mbar_test_wait(bar, parity))) return true;
+    uint64_t t_end = 0;
+    for (uint32_t spin = 1;; ++spin) {
+      if (__all_sync(0xffffffffu, ptx::mbar_try_wait(bar, parity))) return true;
+      if (__any_sync(0xffffffffu, *abort != 0)) return false;
+      if ((spin & 63u) == 0) {
+        const uint64_t now = __shfl_sync(0xffffffffu, ptx::globaltimer(), 0);
+        if (t_end == 0) {
+          t_end = now + timeout_ns;
+        } else if (now > t_end) {
+          if ((threadIdx.x & 31) == 0) {
+            *abort = 1;
+            atomicOr(err_word, kErrTimeout);
+          }
+          __syncwarp();
+          return false;
+        }
+      }
+    }
+  }
   // Every lane tests a completed phase at once; otherwise one lane polls and
   // the warp follows its verdict.
   __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, bool cluster = false) const {

@@ -182,9 +182,10 @@ int ikbo_set_trace(uint64_t* device_buffer);
  * Selects the attention kernel for later calls on this thread.  Returns the
  * previous value.
  *   0  automatic (the default): 3 when the users have on average at least
- *      eight query tiles each (n_cand >= 8 * floor(128 / Lq) * n_user) and
- *      the inputs fit the in-kernel planning limits (n_cand <= 20480,
- *      n_user <= 1024), else 2;
+ *      two query tiles each (n_cand >= 2 * c * n_user, c = floor(128 / Lq)),
+ *      the batch makes at least 600 two-tile items
+ *      (H * ceil(n_cand / (2 * c)) >= 600) and the inputs fit the in-kernel
+ *      planning limits (n_cand <= 20480, n_user <= 1024); else 2;
  *   1  the SIMT kernel, kept as an independent GPU cross-check;
  *   2  the tcgen05/TMEM/TMA kernel with one query tile (up to 128 rows of one
  *      user's candidates) per work item, whose pair mode splits the keys of
@@ -200,9 +201,9 @@ int ikbo_set_kernel(int which);
 /*
  * The kernel (1, 2 or 3 as above) that a call with these sizes would run
  * with this thread's current choice.  Host arithmetic only: it touches no
- * GPU.  Negative sizes, or Lq outside [1, 128], return IKBO_ERR_SHAPE.
+ * GPU.  Negative sizes, H < 1, or Lq outside [1, 128] return IKBO_ERR_SHAPE.
  */
-int ikbo_selected_kernel(int64_t n_cand, int64_t n_user, int32_t Lq);
+int ikbo_selected_kernel(int64_t n_cand, int64_t n_user, int32_t H, int32_t Lq);
 
 /*
  * Number of kernel launches that ikbo_attn_fwd (and ikbo_attn_fwd_host,

@@ -103,25 +103,28 @@ def test_python_binding_raises_on_bad_status(lib):
 
 def test_selected_kernel(lib):
     """Automatic choice: two query tiles per item when the users have on average at least
-    eight query tiles each and the inputs fit the in-kernel planning limits."""
+    two query tiles each, the batch makes at least 600 two-tile items and the inputs fit the
+    in-kernel planning limits."""
     sel = lib.ikbo_selected_kernel
-    assert sel(1024, 15, 1) == 2            # 1024 candidates / 15 users, Lq 1: < 1 tile per user
-    assert sel(8, 2, 1) == 2
-    assert sel(2048, 16, 4) == 2            # 32 candidates per tile: 4 tiles per user
-    assert sel(4096, 4, 8) == 3             # 16 candidates per tile: 64 tiles per user
-    assert sel(16384, 64, 1) == 2           # two tiles per user
-    assert sel(16384, 64, 4) == 3           # exactly eight tiles per user
-    assert sel(16383, 64, 4) == 2
-    assert sel(20481, 4, 8) == 2            # beyond the in-kernel planning limits
-    assert sel(4096, 1025, 1) == 2
-    assert sel(-1, 2, 1) == _lib.IKBO_ERR_SHAPE
-    assert sel(8, 2, 0) == _lib.IKBO_ERR_SHAPE
-    assert sel(8, 2, 129) == _lib.IKBO_ERR_SHAPE
+    assert sel(1024, 15, 4, 1) == 2         # 1024 candidates / 15 users, Lq 1: < 1 tile per user
+    assert sel(8, 2, 2, 1) == 2
+    assert sel(2048, 16, 8, 4) == 2         # 4 tiles per user, but only 256 items
+    assert sel(4096, 4, 8, 8) == 3          # 64 tiles per user, 1024 items
+    assert sel(16384, 64, 16, 1) == 3       # exactly two tiles per user, 1024 items
+    assert sel(16383, 64, 16, 1) == 2
+    assert sel(16384, 64, 16, 4) == 3
+    assert sel(16384, 64, 2, 1) == 2        # 128 items
+    assert sel(20481, 4, 8, 8) == 2         # beyond the in-kernel planning limits
+    assert sel(4096, 1025, 8, 1) == 2
+    assert sel(-1, 2, 1, 1) == _lib.IKBO_ERR_SHAPE
+    assert sel(8, 2, 0, 1) == _lib.IKBO_ERR_SHAPE
+    assert sel(8, 2, 1, 0) == _lib.IKBO_ERR_SHAPE
+    assert sel(8, 2, 1, 129) == _lib.IKBO_ERR_SHAPE
     for which, expect in ((1, 1), (2, 2), (3, 3), (7, 2)):
         prev = lib.ikbo_set_kernel(which)
         try:
-            assert sel(1024, 15, 1) == expect
-            assert sel(20481, 4, 8) == (1 if which == 1 else 2)   # two tiles: in-kernel planning only
+            assert sel(1024, 15, 4, 1) == expect
+            assert sel(20481, 4, 8, 8) == (1 if which == 1 else 2)   # two tiles: in-kernel planning only
             assert lib.ikbo_launches_per_call(1024, 15) == (2 if which == 1 else 1)
         finally:
             lib.ikbo_set_kernel(prev)
