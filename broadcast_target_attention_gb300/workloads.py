@@ -210,6 +210,29 @@ def custom(n_user: int, counts: Sequence[int], lens: Sequence[int], H: int, D: i
     return generate(cfg)
 
 
+def user_queries(wl: Workload) -> np.ndarray:
+    """Queries of the user sequence for self-attention: bf16 bits ``uint16[T, H, D]``, drawn
+    like ``k`` and ``v`` (same seed, their own stream, the config's std)."""
+    cfg = wl.cfg
+    T = int(wl.user_offsets[-1])
+    return _normal_bf16(cfg.seed, 3, (T, cfg.H, cfg.D), cfg.std)
+
+
+def sample_rows(wl: Workload, max_count: int) -> np.ndarray:
+    """A deterministic subset of sequence rows for large workloads: every user's first and
+    last row, plus an even stride over all rows, capped near ``max_count``; sorted, unique."""
+    T = int(wl.user_offsets[-1])
+    if T <= max_count:
+        return np.arange(T, dtype=np.int64)
+    picks = set(np.linspace(0, T - 1, num=max_count, dtype=np.int64).tolist())
+    off = wl.user_offsets.astype(np.int64)
+    for u in range(off.shape[0] - 1):
+        if off[u + 1] > off[u]:
+            picks.add(int(off[u]))
+            picks.add(int(off[u + 1] - 1))
+    return np.asarray(sorted(picks), dtype=np.int64)
+
+
 def sample_candidates(wl: Workload, max_count: int) -> np.ndarray:
     """A deterministic subset of candidate indices for large workloads.
 

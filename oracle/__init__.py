@@ -54,6 +54,9 @@ def _load():
             lib.ikbo_oracle_weights.argtypes = [p, p, p, p, i64, i64, i32, i32, i32,
                                                 ctypes.c_double, i64, i32, i32, p]
             lib.ikbo_oracle_weights.restype = ctypes.c_int
+            lib.ikbo_oracle_self_fwd.argtypes = [p, p, p, p, i64, i32, i32, ctypes.c_double, p, i64,
+                                                 p]
+            lib.ikbo_oracle_self_fwd.restype = ctypes.c_int
             lib.ikbo_oracle_num_threads.argtypes = []
             lib.ikbo_oracle_num_threads.restype = ctypes.c_int
             _lib = lib
@@ -115,6 +118,35 @@ def weights(q, k, user_offsets, cand_to_user, scale: float, c: int, h: int, t: i
     if rc != 0:
         raise ValueError(f"oracle: {ERRORS.get(rc, rc)}")
     return probs[:L]
+
+
+def self_attention(q_user, k, v, user_offsets, scale: float, rows=None) -> np.ndarray:
+    """fp64 self-attention of the user sequence over itself (full, no causal mask), for the
+    selected sequence rows (all when ``rows`` is None).
+
+    q_user, k, v: uint16 bf16 bits [T, H, D]; returns float64 [n_sel, H, D].
+    """
+    qu = np.ascontiguousarray(q_user, dtype=np.uint16)
+    k = np.ascontiguousarray(k, dtype=np.uint16)
+    v = np.ascontiguousarray(v, dtype=np.uint16)
+    off = np.ascontiguousarray(user_offsets, dtype=np.int32)
+    T, H, D = qu.shape
+    if k.shape != qu.shape or v.shape != qu.shape:
+        raise ValueError("oracle: q_user, k and v must share [T, H, D]")
+    n_user = off.shape[0] - 1
+    if rows is None:
+        sel = None
+        n_sel = T
+    else:
+        sel = np.ascontiguousarray(rows, dtype=np.int64)
+        n_sel = sel.shape[0]
+    out = np.zeros((n_sel, H, D), dtype=np.float64)
+    rc = _load().ikbo_oracle_self_fwd(_ptr(qu), _ptr(k), _ptr(v), _ptr(off), n_user, H, D,
+                                      float(scale), _ptr(sel) if sel is not None else None, n_sel,
+                                      _ptr(out))
+    if rc != 0:
+        raise ValueError(f"oracle: {ERRORS.get(rc, rc)}")
+    return out
 
 
 def num_threads() -> int:

@@ -187,6 +187,77 @@ int ikbo_oracle_weights(const uint16_t* q, const uint16_t* k, const int32_t* use
   return ORACLE_OK;
 }
 
+/*
+ * Self-attention over the user sequence ("In-Kernel Broadcast Optimization",
+ * §3.3 and §1: the user's history attends to itself, with the same keys and
+ * values as the target attention and queries taken from the user side; full
+ * attention, no causal mask, as the model is encoder driven).  For every
+ * selected sequence row r of user u (off[u] <= r < off[u+1]) and head h:
+ *
+ *     out[r,h,:] = sum_j softmax_j(scale * q_user[r,h,:] . K[off[u]+j,h,:]) V[off[u]+j,h,:]
+ *
+ * over j = 0 .. L_u - 1.  Layouts: q_user, k, v [T, H, D] bf16 bits with
+ * T = user_offsets[n_user]; out [n_sel, H, D] fp64, row i for sequence row
+ * rows[i] (all rows when rows is NULL and n_sel == T).
+ */
+int ikbo_oracle_self_fwd(const uint16_t* q_user, const uint16_t* k, const uint16_t* v,
+                         const int32_t* user_offsets, int64_t n_user, int32_t H, int32_t D,
+                         double scale, const int64_t* rows, int64_t n_sel, double* out) {
+  if (!q_user || !k || !v || !user_offsets || !out) return ORACLE_ERR_ARG;
+  if (n_user < 0 || H < 1 || D < 1 || n_sel < 0) return ORACLE_ERR_ARG;
+  int rc = check_structure(user_offsets, NULL, 0, n_user);
+  if (rc) return rc;
+  const int64_t T = user_offsets[n_user];
+  if (!rows && n_sel != T) return ORACLE_ERR_ARG;
+  if (rows)
+    for (int64_t i = 0; i < n_sel; ++i)
+      if (rows[i] < 0 || rows[i] >= T) return ORACLE_ERR_ARG;
+  int64_t Lmax = 0;
+  for (int64_t u = 0; u < n_user; ++u) {
+    int64_t L = (int64_t)user_offsets[u + 1] - user_offsets[u];
+    if (L > Lmax) Lmax = L;
+  }
+  int failed = 0;
+  const int64_t n_pairs = n_sel * (int64_t)H;
+
+#pragma omp parallel
+  {
+    double* Ku = (double*)malloc(sizeof(double) * (size_t)(Lmax > 0 ? Lmax : 1) * D);
+    double* Vu = (double*)malloc(sizeof(double) * (size_t)(Lmax > 0 ? Lmax : 1) * D);
+    double* s = (double*)malloc(sizeof(double) * (size_t)(Lmax > 0 ? Lmax : 1));
+    double* qrow = (double*)malloc(sizeof(double) * (size_t)D);
+    if (!Ku || !Vu || !s || !qrow) {
+#pragma omp atomic write
+      failed = 1;
+    } else {
+#pragma omp for schedule(dynamic, 1)
+      for (int64_t pair = 0; pair < n_pairs; ++pair) {
+        int64_t i = pair / H;
+        int h = (int)(pair % H);
+        int64_t r = rows ? rows[i] : i;
+        /* the user whose sequence holds row r (the last u with off[u] <= r) */
+        int64_t u = 0;
+        while (u + 1 < n_user && user_offsets[u + 1] <= r) ++u;
+        int64_t base = user_offsets[u];
+        int64_t L = (int64_t)user_offsets[u + 1] - base;
+        for (int64_t j = 0; j < L; ++j)
+          for (int d = 0; d < D; ++d) {
+            int64_t src = ((base + j) * H + h) * (int64_t)D + d;
+            Ku[j * D + d] = bf16_to_double(k[src]);
+            Vu[j * D + d] = bf16_to_double(v[src]);
+          }
+        for (int d = 0; d < D; ++d) qrow[d] = bf16_to_double(q_user[(r * H + h) * (int64_t)D + d]);
+        attend_row(qrow, Ku, Vu, L, D, scale, s, out + (i * H + h) * (int64_t)D);
+      }
+    }
+    free(Ku);
+    free(Vu);
+    free(s);
+    free(qrow);
+  }
+  return failed ? ORACLE_ERR_NOMEM : ORACLE_OK;
+}
+
 int ikbo_oracle_num_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();
