@@ -17,7 +17,7 @@ from typing import Optional, Tuple
 from . import _lib
 from ._lib import STATUS
 
-__all__ = ["attn_fwd", "broadcast_attn_fwd", "attn_fwd_host", "attn_fwd_noalloc", "get_device_error", "set_timing",
+__all__ = ["attn_fwd", "fused_attn_fwd", "broadcast_attn_fwd", "attn_fwd_host", "attn_fwd_noalloc", "get_device_error", "set_timing",
            "get_timing", "set_kernel", "selected_kernel", "set_debug", "launches_per_call", "version", "load", "IkboError", "STATUS"]
 
 
@@ -94,6 +94,40 @@ def attn_fwd(q, k, v, user_offsets, cand_to_user, scale: Optional[float] = None,
                                   _stream_handle(stream))
     _check(rc, "ikbo_attn_fwd")
     return out
+
+
+def fused_attn_fwd(q, q_user, k, v, user_offsets, cand_to_user, scale: Optional[float] = None,
+                   out=None, out_user=None, stream=None):
+    """Target attention of the candidates and self-attention of the user sequence in one
+    launch (device tensors); returns ``(out, out_user)``.
+
+    ``q_user`` is bf16 ``[T, H, D]`` like ``k``; ``q`` may have zero candidates.  See
+    ``ikbo_fused_attn_fwd`` in include/ikbo.h.
+    """
+    import torch
+    _validate(q, k, v, user_offsets, cand_to_user, device=True)
+    if q_user.dtype != torch.bfloat16 or not q_user.is_contiguous() or not q_user.is_cuda:
+        raise ValueError("q_user must be a contiguous bf16 CUDA tensor")
+    if q_user.shape != k.shape:
+        raise ValueError("q_user must have the shape of k, [T, H, D]")
+    T, H, D = (int(x) for x in k.shape)
+    n_cand = int(q.shape[0])
+    Lq = int(q.shape[2]) if q.dim() == 4 else 1
+    if n_cand and (q.dim() != 4 or int(q.shape[1]) != H or int(q.shape[3]) != D):
+        raise ValueError("q must be [n_cand, H, Lq, D] with the H and D of k")
+    n_user = int(user_offsets.shape[0]) - 1
+    if scale is None:
+        scale = D ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if out_user is None:
+        out_user = torch.empty_like(q_user)
+    p = lambda t: _ptr(t) if t.numel() else None
+    rc = _lib.lib().ikbo_fused_attn_fwd(p(q), p(q_user), p(k), p(v), _ptr(user_offsets),
+                                        p(cand_to_user), n_cand, n_user, T, H, Lq, D, float(scale),
+                                        p(out), p(out_user), _stream_handle(stream))
+    _check(rc, "ikbo_fused_attn_fwd")
+    return out, out_user
 
 
 def broadcast_attn_fwd(q, k, v, user_offsets, cand_to_user, scale: Optional[float] = None,

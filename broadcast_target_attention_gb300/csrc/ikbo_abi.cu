@@ -173,12 +173,14 @@ int effective_kernel(int64_t n_cand, int64_t n_user, int H, int Lq) {
 // otherwise reads the planning kernel's list; never splits a unit through
 // global memory), kKernPp (always plans in-kernel), kKernSimt (planning
 // kernel, may split).
+// extra_units: further work items the in-kernel planning may make (the
+// self-attention tiles of a fused call).
 Workspace plan_workspace(int64_t n_cand, int64_t n_user, int H, int Lq, int D, int num_sms,
-                         int grid, int kernel) {
+                         int grid, int kernel, int64_t extra_units = 0) {
   Workspace w = {};
   const int cpt = cands_per_tile(Lq);
   const int64_t units_bound =
-      int64_t(H) * ((n_cand + cpt - 1) / cpt + (n_user < n_cand ? n_user : n_cand));
+      int64_t(H) * ((n_cand + cpt - 1) / cpt + (n_user < n_cand ? n_user : n_cand)) + extra_units;
   w.grid = grid;
   w.kernel = kernel;
   // keep in step with ikbo_launches_per_call
@@ -333,10 +335,10 @@ int pp_grid(DeviceState* ds) {
 
 template <int D>
 cudaError_t launch_attn_tc(const AttnParams& ap, const CUtensorMap& qmap, const CUtensorMap& qmap1,
-                           const CUtensorMap& kt, const CUtensorMap& vt, int grid, bool pdl,
-                           cudaStream_t st) {
+                           const CUtensorMap& kt, const CUtensorMap& vt, const CUtensorMap& qut,
+                           int grid, bool pdl, cudaStream_t st) {
   return launch_ex(ikbo_attn_tc_kernel<D>, dim3(grid), dim3(kTcThreads), kTcSmemBytes, st, pdl, 2,
-                   ap, qmap, qmap1, kt, vt);
+                   ap, qmap, qmap1, kt, vt, qut);
 }
 
 template <int D>
@@ -346,10 +348,19 @@ cudaError_t launch_attn_pp(const AttnParams& ap, const CUtensorMap& qmap, const 
                    ap, qmap, qmap1, kt, vt);
 }
 
+// The self-attention part of a fused call: the user sequence's queries and
+// output, [T, H, D] each.
+struct SelfPart {
+  const void* q_user;
+  void* out_user;
+  int64_t T;
+};
+
 // Plan + attention on device buffers, scratch from `ws` (>= plan_workspace().total).
 int run_ikbo(DeviceState* ds, const void* q, const void* k, const void* v, const int32_t* off,
              const int32_t* c2u, int64_t n_cand, int64_t n_user, int H, int Lq, int D, float scale,
-             void* out, char* ws, const Workspace& L, cudaStream_t st) {
+             void* out, char* ws, const Workspace& L, cudaStream_t st,
+             const SelfPart* self = nullptr) {
   const int kernel = L.kernel;
   PlanParams pp = {};
   pp.cand_to_user = c2u;
@@ -380,15 +391,23 @@ int run_ikbo(DeviceState* ds, const void* q, const void* k, const void* v, const
   px.patch_maps = kernel != kKernSimt ? 1 : 0;
   px.kmap_dst = reinterpret_cast<CUtensorMap*>(ws + L.kmap);
   px.vmap_dst = reinterpret_cast<CUtensorMap*>(ws + L.vmap);
-  CUtensorMap qmap, qmap1;
+  CUtensorMap qmap, qmap1, qumap;
   std::memset(&qmap, 0, sizeof qmap);
   std::memset(&qmap1, 0, sizeof qmap1);
+  std::memset(&qumap, 0, sizeof qumap);
   if (kernel != kKernSimt) {
-    const cuuint64_t rows = L.fused ? kOpenRows : cuuint64_t(kBlockN);
+    // A fused call states T: its maps carry the row count itself.  Otherwise
+    // in-kernel planning loads through open maps (T is only known on the
+    // device), and the planning kernel patches a placeholder.
+    const cuuint64_t rows = self ? cuuint64_t(self->T > 0 ? self->T : 1)
+                                 : (L.fused ? kOpenRows : cuuint64_t(kBlockN));
     if (encode_kv_map(&px.kmap_tmpl, k, H, D, kBlockN, rows) != IKBO_OK ||
-        encode_kv_map(&px.vmap_tmpl, v, H, D, kBlockN, rows) != IKBO_OK ||
-        encode_q_map(&qmap, q, n_cand, H, Lq, D, qbox_cands(Lq)) != IKBO_OK ||
-        encode_q_map(&qmap1, q, n_cand, H, Lq, D, 1) != IKBO_OK)
+        encode_kv_map(&px.vmap_tmpl, v, H, D, kBlockN, rows) != IKBO_OK)
+      return IKBO_ERR_CUDA;
+    if (n_cand > 0 && (encode_q_map(&qmap, q, n_cand, H, Lq, D, qbox_cands(Lq)) != IKBO_OK ||
+                       encode_q_map(&qmap1, q, n_cand, H, Lq, D, 1) != IKBO_OK))
+      return IKBO_ERR_CUDA;
+    if (self && self->T > 0 && encode_kv_map(&qumap, self->q_user, H, D, kBlockN, rows) != IKBO_OK)
       return IKBO_ERR_CUDA;
   }
 
@@ -424,6 +443,12 @@ int run_ikbo(DeviceState* ds, const void* q, const void* k, const void* v, const
   ap.max_cta_items = L.max_cta_items;
   ap.perm_ws = pp.perm;
   ap.map_slots = reinterpret_cast<CUtensorMap*>(ws + L.map_slots);
+  if (self) {
+    ap.q_user = static_cast<const uint16_t*>(self->q_user);
+    ap.out_user = static_cast<uint16_t*>(self->out_user);
+    ap.total_rows = self->T;
+    ap.exact_rows = 1;
+  }
 
   const bool timed = g_timing;
   if (timed) cudaEventRecord(ds->ev[0], st);
@@ -447,9 +472,9 @@ int run_ikbo(DeviceState* ds, const void* q, const void* k, const void* v, const
   } else {
     // the planning kernel (listed mode) is followed with programmatic dependent launch
     if (D == 64)
-      e = launch_attn_tc<64>(ap, qmap, qmap1, px.kmap_tmpl, px.vmap_tmpl, L.grid, !L.fused, st);
+      e = launch_attn_tc<64>(ap, qmap, qmap1, px.kmap_tmpl, px.vmap_tmpl, qumap, L.grid, !L.fused, st);
     else
-      e = launch_attn_tc<128>(ap, qmap, qmap1, px.kmap_tmpl, px.vmap_tmpl, L.grid, !L.fused, st);
+      e = launch_attn_tc<128>(ap, qmap, qmap1, px.kmap_tmpl, px.vmap_tmpl, qumap, L.grid, !L.fused, st);
   }
   if (e != cudaSuccess) return cuda_fail(e);
   if (timed) {
@@ -462,10 +487,12 @@ int run_ikbo(DeviceState* ds, const void* q, const void* k, const void* v, const
 }
 
 // Workspace for a call on this device with the current kernel choice.
+// self_T >= 0: a fused self + target call over T sequence rows, which the
+// one-tile tcgen05 kernel runs (planning in-kernel).
 int call_workspace(DeviceState* ds, int64_t n_cand, int64_t n_user, int H, int Lq, int D,
-                   Workspace* out) {
+                   Workspace* out, int64_t self_T = -1) {
   int grid = 0;
-  const int kernel = effective_kernel(n_cand, n_user, H, Lq);
+  const int kernel = self_T >= 0 ? kKernTc : effective_kernel(n_cand, n_user, H, Lq);
   if (kernel == kKernTc) {
     grid = D == 64 ? tc_grid<64>(ds) : tc_grid<128>(ds);
     if (grid <= 0) return IKBO_ERR_CUDA;
@@ -473,8 +500,10 @@ int call_workspace(DeviceState* ds, int64_t n_cand, int64_t n_user, int H, int L
     grid = D == 64 ? pp_grid<64>(ds) : pp_grid<128>(ds);
     if (grid <= 0) return IKBO_ERR_CUDA;
   }
+  // a self-attention tile per 128 rows of every user, at most T / 128 + n_user per head
+  const int64_t extra = self_T > 0 ? int64_t(H) * ((self_T + kTileM - 1) / kTileM + n_user) : 0;
   *out = plan_workspace(n_cand, n_user, H, Lq, D, ds->num_sms, grid > 0 ? grid : ds->num_sms,
-                        kernel);
+                        kernel, extra);
   return IKBO_OK;
 }
 
@@ -691,6 +720,48 @@ int ikbo_broadcast_attn_fwd(const void* q, const void* k_user, const void* v_use
     g_timing_dev = dev;
   }
   cudaFreeAsync(meta, st);
+  return rc;
+}
+
+int ikbo_fused_attn_fwd(const void* q, const void* q_user, const void* k_user, const void* v_user,
+                        const int32_t* user_offsets, const int32_t* cand_to_user, int64_t n_cand,
+                        int64_t n_user, int64_t T, int32_t H, int32_t Lq, int32_t D, float scale,
+                        void* out, void* out_user, ikbo_stream_t stream) {
+  if (T < 0 || T >= (int64_t(1) << 31)) return IKBO_ERR_SHAPE;
+  int rc = check_args(q, k_user, v_user, user_offsets, cand_to_user, n_cand, n_user, H, Lq, D,
+                      scale, out);
+  if (rc != IKBO_OK) return rc;
+  if (n_cand == 0 && T == 0) return IKBO_OK;
+  if (T > 0) {
+    if (!q_user || !out_user || !k_user || !v_user || !user_offsets) return IKBO_ERR_NULL;
+    if (!aligned16(q_user) || !aligned16(out_user) || !aligned16(k_user) || !aligned16(v_user) ||
+        (reinterpret_cast<uintptr_t>(user_offsets) & 3u))
+      return IKBO_ERR_ALIGN;
+    // out_user may share no byte with an input or with out
+    const uintptr_t ub = reinterpret_cast<uintptr_t>(out_user);
+    const uintptr_t ue = ub + uintptr_t(T) * H * D * 2;
+    auto overlaps = [&](const void* x, uintptr_t bytes) {
+      const uintptr_t xb = reinterpret_cast<uintptr_t>(x);
+      return x && xb < ue && ub < xb + bytes;
+    };
+    const uintptr_t seq = uintptr_t(T) * H * D * 2, cand = uintptr_t(n_cand) * H * Lq * D * 2;
+    if (overlaps(q_user, seq) || overlaps(k_user, seq) || overlaps(v_user, seq) ||
+        (n_cand > 0 && (overlaps(q, cand) || overlaps(out, cand))))
+      return IKBO_ERR_ALIAS;
+  }
+  if (!fits_in_kernel_planning(n_cand, n_user)) return IKBO_ERR_SHAPE;
+  DeviceState* ds = nullptr;
+  if ((rc = device_state(&ds)) != IKBO_OK) return rc;
+  if (g_timing && (rc = ensure_events(ds)) != IKBO_OK) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  Workspace L;
+  if ((rc = call_workspace(ds, n_cand, n_user, H, Lq, D, &L, T)) != IKBO_OK) return rc;
+  void* ws = nullptr;
+  if (cudaMallocAsync(&ws, L.total, st) != cudaSuccess) return IKBO_ERR_CUDA;
+  const SelfPart self{q_user, out_user, T};
+  rc = run_ikbo(ds, q, k_user, v_user, user_offsets, cand_to_user, n_cand, n_user, H, Lq, D, scale,
+                out, static_cast<char*>(ws), L, st, &self);
+  if (cudaFreeAsync(ws, st) != cudaSuccess && rc == IKBO_OK) rc = IKBO_ERR_CUDA;
   return rc;
 }
 

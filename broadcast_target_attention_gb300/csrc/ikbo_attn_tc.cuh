@@ -388,6 +388,8 @@ __device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch, 
   constexpr int kBadOff = 1, kBadIdx = 2, kUnsorted = 4, kEmpty = 8, kGap = 16;
   int flags = 0;
   if (tid == 0 && off[0] != 0) flags |= kBadOff;
+  // a fused self-attention call states T: the offsets must end there
+  if (tid == 0 && p.q_user && (int64_t)off[n_user] != p.total_rows) flags |= kBadOff;
   for (int u = tid; u < n_user; u += nt) {
     if (off[u + 1] < off[u]) flags |= kBadOff;
     if (off[u + 1] == off[u]) flags |= kEmpty;
@@ -413,6 +415,10 @@ __device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch, 
       }
     }
   }
+  // no candidates at all (a self-attention-only call): the pass above wrote
+  // no cand_start entry, and every user has zero candidates
+  if (n_cand == 0)
+    for (int u = tid; u <= n_user; u += nt) cs[u] = 0;
   if (flags) atomicOr(&ctl->flags, flags);
   __syncthreads();
   flags = ctl->flags;
@@ -518,7 +524,11 @@ __device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch, 
   auto user_at = [&](int rk) { return lpt ? order[rk] : rk; };
   auto units_of = [&](int u) {
     const int r = cs[u + 1] - cs[u], L = off[u + 1] - off[u];
-    return (r > 0 && L > 0) ? p.H * ceil_div(r, cpt) : 0;
+    if (L <= 0) return 0;
+    // candidate tiles, plus (fused self-attention) the user's own sequence
+    // in tiles of 128 rows
+    const int tiles = (r > 0 ? ceil_div(r, cpt) : 0) + (p.q_user ? ceil_div(L, kTileM) : 0);
+    return p.H * tiles;
   };
   auto prefix = [&]() {
     if (n_user <= 32) {
@@ -588,13 +598,24 @@ __device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch, 
     }
     const int u = user_at(lo);
     const int r = cs[u + 1] - cs[u];
-    const int nmt = ceil_div(r, cpt);
+    const int L = off[u + 1] - off[u];
+    const int nmt = r > 0 ? ceil_div(r, cpt) : 0;
+    const int per_head = nmt + (p.q_user ? ceil_div(L, kTileM) : 0);
     const int local = i - ubefore[lo];
-    const int h = local / nmt, mt = local - h * nmt;
+    const int h = local / per_head, mt = local - h * per_head;
     w.user = u;
     w.head = h;
-    w.cand_begin = cs[u] + mt * cpt;
-    w.n_cand = min(cpt, r - mt * cpt);
+    if (mt < nmt) {
+      w.cand_begin = cs[u] + mt * cpt;
+      w.n_cand = min(cpt, r - mt * cpt);
+      w.q_row = -1;
+    } else {
+      // a tile of the user's own sequence (self-attention)
+      const int t = mt - nmt;
+      w.cand_begin = 0;
+      w.n_cand = min(kTileM, L - t * kTileM);
+      w.q_row = off[u] + t * kTileM;
+    }
     w.kv_begin = off[u];
     w.kv_len = off[u + 1] - off[u];
     w.unit = -1;
@@ -657,7 +678,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap qmap,
                     const __grid_constant__ CUtensorMap qmap1,
                     const __grid_constant__ CUtensorMap kmap_tmpl,
-                    const __grid_constant__ CUtensorMap vmap_tmpl) {
+                    const __grid_constant__ CUtensorMap vmap_tmpl,
+                    const __grid_constant__ CUtensorMap qumap) {
   using C = TcConfig<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* data = smem_raw;
@@ -701,9 +723,10 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
   for (int i = threadIdx.x; i < 2 * kSplit * kTileM; i += blockDim.x) (&ctl->xtag[0][0][0])[i] = 3u;
   if (warp == 2 && lane == 0) {
     // the host-encoded descriptors into the TMA unit's cache ahead of use
-    ptx::prefetch_tensormap(&qmap);
+    if (p.n_cand > 0) ptx::prefetch_tensormap(&qmap);   // a self-only call encodes no Q map
     ptx::prefetch_tensormap(&kmap_tmpl);
     ptx::prefetch_tensormap(&vmap_tmpl);
+    if (p.q_user) ptx::prefetch_tensormap(&qumap);
   }
   // A planning kernel may precede this one (programmatic dependent launch):
   // its work list is visible after this wait.  Without one it returns at once.
@@ -750,6 +773,8 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
   // instead of reading past the end of k / v.
   auto kv_map = [&](bool is_v, int32_t row) -> const void* {
     if (!p.fused) return is_v ? p.vmap : p.kmap;
+    // maps encoded with the row count T itself (the caller stated T)
+    if (p.exact_rows) return is_v ? (const void*)&vmap_tmpl : (const void*)&kmap_tmpl;
     const int T = ctl->total_keys;
     if (row + kBlockN <= T) return is_v ? (const void*)&vmap_tmpl : (const void*)&kmap_tmpl;
     CUtensorMap* tail_k = p.map_slots + 2 * blockIdx.x;
@@ -785,7 +810,13 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
   auto issue_q = [&](const WorkItem& w, uint32_t qb) {
     const uint32_t qbar = ptx::smem_addr(&ctl->q_full[qb]);
     const uint32_t qdst = ptx::smem_addr(q_smem + qb * C::kQBytes);
-    if (ctl->sorted) {
+    if (w.q_row >= 0) {
+      // 128 rows of the user sequence's queries (rows past T read as zeros)
+      ptx::mbar_arrive_expect_tx(qbar, uint32_t(C::kCB * kTileM * 128));
+#pragma unroll
+      for (int cb = 0; cb < C::kCB; ++cb)
+        ptx::tma_load_2d(qdst + cb * kTileM * 128, &qumap, qbar, w.head * D + cb * 64, w.q_row);
+    } else if (ctl->sorted) {
       const int nb = p.qbox;
       const int nbox = ceil_div(w.n_cand, nb);
       ptx::mbar_arrive_expect_tx(qbar, uint32_t(nbox * nb * Lq * 128 * C::kCB));
@@ -904,7 +935,7 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
           // the partner's O / l and log-sum-exp of the rows this CTA finishes
           // (the first half for CTA 0, the second for CTA 1); tell the partner
           if (!W.wait(ptx::smem_addr(&ctl->q_empty[0]), 0)) break;
-          const int rows = w.n_cand * Lq, hrows = (rows + 1) >> 1;
+          const int rows = w.q_row >= 0 ? w.n_cand : w.n_cand * Lq, hrows = (rows + 1) >> 1;
           const int recv = cta_rank == 0 ? hrows : rows - hrows;
           ptx::mbar_arrive_expect_tx(ptx::smem_addr(&ctl->pair_recv), uint32_t(recv * (D * 4 + 4)));
           ctl->go_sent = 1;
@@ -1078,7 +1109,7 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
     for (int k = 0; k < n_my; ++k) {
       const WorkItem w = item_at(k);
       const int n = ceil_div(w.kv_len, kBlockN);
-      const int rows = w.n_cand * Lq;
+      const int rows = w.q_row >= 0 ? w.n_cand : w.n_cand * Lq;   // query rows of the tile
       // Rows past the item's queries hold stale shared memory; their results
       // are never stored, and they are left out of every decision below.
       const bool live = row < rows;
@@ -1252,11 +1283,18 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
         if (tr_epi) trace(p, k, kTrEpiSent);
       }
       if (__any_sync(0xffffffffu, keep)) {
-        const int ci = keep ? row / Lq : 0;
-        const int tq = keep ? row - ci * Lq : 0;
-        const int32_t gpos = w.cand_begin + ci;
-        const int64_t cidx = keep ? (sorted ? gpos : perm[gpos]) : 0;
-        uint16_t* dst = p.out + (((cidx * p.H + w.head) * (int64_t)Lq + tq) * D) + cg * C::kPart;
+        uint16_t* dst;
+        if (w.q_row >= 0) {
+          // a self-attention row: out_user[q_row + row, head, :]
+          const int64_t srow = keep ? (int64_t)w.q_row + row : 0;
+          dst = p.out_user + ((srow * p.H + w.head) * D) + cg * C::kPart;
+        } else {
+          const int ci = keep ? row / Lq : 0;
+          const int tq = keep ? row - ci * Lq : 0;
+          const int32_t gpos = w.cand_begin + ci;
+          const int64_t cidx = keep ? (sorted ? gpos : perm[gpos]) : 0;
+          dst = p.out + (((cidx * p.H + w.head) * (int64_t)Lq + tq) * D) + cg * C::kPart;
+        }
         float lse_p = -INFINITY;
         if (paired) {
           // the partner's O / l and log-sum-exp for these rows

@@ -19,18 +19,22 @@ constexpr int kErrTimeout = 4;  // a bounded wait ran out
 constexpr int kErrLayout = 8;   // the kernel found its launch unusable (shared-memory alignment)
 
 // One unit of work of the attention kernel: a query tile of one user and one
-// head, against one contiguous range of that user's keys.
+// head, against one contiguous range of that user's keys.  The tile holds
+// either candidates' queries (q_row = -1) or, in a fused self + target call,
+// up to 128 rows of the user's own sequence (q_user rows q_row ..
+// q_row + n_cand - 1).
 struct WorkItem {
   int32_t user;        // user index
   int32_t head;        // head index
   int32_t cand_begin;  // first position in the grouped candidate order
-  int32_t n_cand;      // candidates in this tile (<= cands per tile)
+  int32_t n_cand;      // candidates in this tile (<= cands per tile); sequence rows of a self tile
   int32_t kv_begin;    // first key row in k/v (absolute, = user_offsets[u] + split start)
   int32_t kv_len;      // keys in this item (> 0)
   int32_t unit;        // split-combine unit, or -1 when the item covers all keys
   int32_t unit_first;  // first item index of the unit (its n_split items are consecutive)
+  int32_t q_row;       // self-attention tile: its first row of q_user / out_user; else -1
 };
-static_assert(sizeof(WorkItem) == 32, "WorkItem layout");
+static_assert(sizeof(WorkItem) == 36, "WorkItem layout");
 
 struct PlanHeader {
   int32_t n_items;       // work items written
@@ -108,6 +112,11 @@ struct AttnParams {
   int32_t max_cta_items;
   int32_t* perm_ws;         // fused, unsorted input: grouped position -> candidate
   CUtensorMap* map_slots;   // fused: [grid][2] K/V tensor maps with the row count set on the device
+  // fused self + target attention (one-tile tcgen05 kernel, in-kernel planning)
+  const uint16_t* q_user;   // bf16 [T, H, D] queries of the user sequence, or null (target only)
+  uint16_t* out_user;       // bf16 [T, H, D]
+  int64_t total_rows;       // T as the caller gave it; user_offsets[n_user] must equal it
+  int32_t exact_rows;       // 1: the K/V maps were encoded with the row count T (no tail copy)
 };
 
 // In-kernel timeline tracing (ikbo_set_trace): the first kTraceItems items of

@@ -179,6 +179,36 @@ int ikbo_set_debug(int flags, uint64_t timeout_ns);
 int ikbo_set_trace(uint64_t* device_buffer);
 
 /*
+ * Fused self + target attention ("In-Kernel Broadcast Optimization", §3.3):
+ * in one launch, the target attention of ikbo_attn_fwd (q, out as there) and
+ * the self-attention of every user's sequence over itself, with the same
+ * keys and values and queries from the user side:
+ *
+ *   out_user[r, h, :] = sum_j softmax_j(scale * q_user[r, h, :] . k_user[o + j, h, :])
+ *                       * v_user[o + j, h, :],   j = 0 .. L_u - 1,
+ *
+ * for every sequence row r of user u (o = user_offsets[u] <= r < user_offsets[u + 1]);
+ * full attention, no causal mask.  Both kinds of query tile stream the same
+ * user's K/V tiles.
+ *
+ *   q_user, out_user   bf16 [T, H, D], device memory, 16-byte aligned; out_user
+ *                      shares no byte with any input or with out.
+ *   T                  the number of sequence rows; user_offsets[n_user] must
+ *                      equal it (checked on the device: IKBO_ERR_OFFSETS).
+ *   other arguments    as ikbo_attn_fwd; n_cand may be 0 (self-attention
+ *                      only; q, cand_to_user and out may then be NULL).
+ *
+ * Runs on the one-tile tcgen05 kernel (whatever ikbo_set_kernel chose), with
+ * its planning in-kernel: n_cand <= 20480 and n_user <= 1024, else
+ * IKBO_ERR_SHAPE.  T < 0 or T >= 2^31: IKBO_ERR_SHAPE.  n_cand == 0 and T == 0:
+ * no-op.  Errors and ownership otherwise as ikbo_attn_fwd.
+ */
+int ikbo_fused_attn_fwd(const void* q, const void* q_user, const void* k_user, const void* v_user,
+                        const int32_t* user_offsets, const int32_t* cand_to_user, int64_t n_cand,
+                        int64_t n_user, int64_t T, int32_t H, int32_t Lq, int32_t D, float scale,
+                        void* out, void* out_user, ikbo_stream_t stream);
+
+/*
  * Selects the attention kernel for later calls on this thread.  Returns the
  * previous value.
  *   0  automatic (the default): 3 when the users have on average at least
