@@ -448,6 +448,133 @@ def run_ikbo(args):
         dist.destroy_process_group()
 
 
+def run_fused(args):
+    """Fused self + target attention ("In-Kernel Broadcast Optimization", §3.3): the target
+    attention of the workload plus the self-attention of every user sequence over itself,
+    in one launch; timed beside the same work as two launches (target, then self only)."""
+    import torch
+
+    import broadcast_target_attention_gb300 as ikbo
+
+    ws, rank, local = R.dist_env()
+    if ws > 1:
+        raise SystemExit("--with-self measures one GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ikbo.load()
+    wl = workload_for_rank(args.config, rank)
+    c = wl.cfg
+    lens = np.diff(wl.user_offsets.astype(np.int64))
+    nums = A.workload_numbers(wl)
+    flops = nums["flops"] + A.self_flops(c.H, c.D, lens)
+    alg_bytes = nums["alg_bytes"] + A.self_extra_bytes(c.H, c.D, wl.T)
+    qu_bits = W.user_queries(wl)
+
+    def t(a, dt):
+        return torch.from_numpy(np.ascontiguousarray(a)).view(dt).to(dev)
+
+    q = t(wl.q.view(np.int16), torch.bfloat16)
+    qu = t(qu_bits.view(np.int16), torch.bfloat16)
+    k = t(wl.k.view(np.int16), torch.bfloat16)
+    v = t(wl.v.view(np.int16), torch.bfloat16)
+    off = t(wl.user_offsets, torch.int32)
+    c2u = t(wl.cand_to_user, torch.int32)
+    out, out_user = torch.empty_like(q), torch.empty_like(qu)
+    q0, c2u0, out0 = q[:0], c2u[:0], out[:0]
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.int32, device=dev)
+
+    def fused():
+        ikbo.fused_attn_fwd(q, qu, k, v, off, c2u, wl.scale, out=out, out_user=out_user)
+
+    def separate():
+        ikbo.attn_fwd(q, k, v, off, c2u, wl.scale, out=out)
+        ikbo.fused_attn_fwd(q0, qu, k, v, off, c2u0, wl.scale, out=out0, out_user=out_user)
+
+    def timed(fn, n):
+        evs = []
+        for i in range(n):
+            flush.fill_(i & 0xFF)
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            fn()
+            e.record()
+            evs.append((s, e))
+        torch.cuda.synchronize(dev)
+        return [s.elapsed_time(e) for s, e in evs]
+
+    with ClockSampler(local) as clk:
+        for _ in range(args.warmup):
+            flush.fill_(1)
+            fused()
+            separate()
+        assert ikbo.get_device_error() == 0
+        torch.cuda.synchronize(dev)
+        clk.mark_start()
+        fused_ms = timed(fused, args.steps)
+        clk.mark_end()
+        sep_ms = timed(separate, args.steps)
+        # end to end: host tensors copied in, the fused call, both outputs copied back
+        hq, hqu, hk, hv = (x.cpu().pin_memory() for x in (q, qu, k, v))
+        hoff, hc2u = off.cpu().pin_memory(), c2u.cpu().pin_memory()
+        ho, hou = torch.empty_like(hq).pin_memory(), torch.empty_like(hqu).pin_memory()
+
+        def e2e_step():
+            dq, dqu, dk, dv = (x.to(dev, non_blocking=True) for x in (hq, hqu, hk, hv))
+            doff, dc2u = hoff.to(dev, non_blocking=True), hc2u.to(dev, non_blocking=True)
+            o, ou = ikbo.fused_attn_fwd(dq, dqu, dk, dv, doff, dc2u, wl.scale)
+            ho.copy_(o, non_blocking=True)
+            hou.copy_(ou, non_blocking=True)
+            torch.cuda.synchronize(dev)
+
+        for _ in range(3):
+            e2e_step()
+        e2e_ms = []
+        for _ in range(min(args.steps, 50)):
+            t0 = time.perf_counter()
+            e2e_step()
+            e2e_ms.append((time.perf_counter() - t0) * 1e3)
+    assert ikbo.get_device_error() == 0
+    ms = statistics.mean(fused_ms)
+    sep = statistics.mean(sep_ms)
+    pk = peaks()
+    ai = flops / alg_bytes
+    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    kname = f"ikbo_attn_tc_kernel<{c.D}>"
+    if ai < ridge:
+        gbs = alg_bytes / (ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": gbs / pk["hbm_gbs"], "traffic": None, "kernel": kname,
+                "alg_bytes_per_launch": alg_bytes, "peak_source": pk["source"] + " (burst copy)"}
+    else:
+        tf = flops / (ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": tf, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": tf / pk["bf16_tflops"], "traffic": None, "kernel": kname,
+                "flops_per_launch": flops, "peak_source": pk["source"] + " (burst cuBLAS bf16)"}
+    h2d = sum(x.nbytes for x in (wl.q, qu_bits, wl.k, wl.v, wl.user_offsets, wl.cand_to_user))
+    d2h = wl.q.nbytes + qu_bits.nbytes
+    e2e = statistics.mean(e2e_ms)
+    line = {
+        "metric": METRIC + " -- fused self + target attention", "value": flops / (ms * 1e-3) / 1e12,
+        "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": config_block(wl, {"self_attention": "every user sequence over itself, full, "
+                                                      "queries drawn like k (seeded)",
+                                    "self_flops": A.self_flops(c.H, c.D, lens),
+                                    "target_flops": nums["flops"]}),
+        "roofline": roof,
+        "fusion": {"fused_ms": ms, "separate_ms": sep, "speedup": sep / ms,
+                   "separate": "target call, then a self-only call of the same kernel"},
+        "e2e": {"value": flops / (e2e * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+        "cpu_baseline": None,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -457,11 +584,15 @@ def main():
     ap.add_argument("--config", default=W.HEADLINE, choices=sorted(W.CONFIGS))
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--with-self", action="store_true",
+                    help="measure the fused self + target attention of the workload instead")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.with_self:
+        run_fused(args)
     else:
         run_ikbo(args)
 

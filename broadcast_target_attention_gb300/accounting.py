@@ -44,6 +44,17 @@ def ai_per_user_head(r: int, Lq: int, L: int) -> float:
     return r * Lq * L / (L + r * Lq)
 
 
+def self_flops(H: int, D: int, lens) -> int:
+    """Self-attention of every user sequence over itself: 4·H·D·Σ_u L_u²."""
+    return 4 * H * D * sum(int(L) * int(L) for L in lens)
+
+
+def self_extra_bytes(H: int, D: int, T: int) -> int:
+    """What fusing the self-attention adds to the algorithmic bytes: q_user read and
+    out_user written once (its K/V are the target attention's, read once for both)."""
+    return 2 * T * H * D * BF16
+
+
 def workload_numbers(wl) -> dict:
     """FLOPs, algorithmic bytes and the broadcast path's extra bytes of a workload."""
     c = wl.cfg
