@@ -254,6 +254,76 @@ def sample_candidates(wl: Workload, max_count: int) -> np.ndarray:
     return np.asarray(sorted(picks), dtype=np.int64)
 
 
+# ---------------------------------------------------------------------------
+# IKBO linear compression ("In-Kernel Broadcast Optimization", §2): each
+# candidate's K input embeddings (its user's K_user, then its own K_cand, each
+# of N values) are compressed to M by a learned W [M, K].  The library takes
+# the decomposed operands, each K block zero-padded to a multiple of 8 (§2.2:
+# padding is exact and keeps every row 16-byte aligned).
+
+def round_up8(x: int) -> int:
+    return (int(x) + 7) // 8 * 8
+
+
+@dataclass
+class LceConfig:
+    name: str
+    n_cand: int
+    n_user: int
+    M: int
+    K_user: int          # user embeddings (before padding)
+    K_cand: int          # candidate embeddings (before padding)
+    N: int
+    seed: int
+    description: str = ""
+
+
+@dataclass
+class LceWorkload:
+    cfg: LceConfig
+    W_user: np.ndarray       # bf16 bits [M, Ku8]   (Ku8 = K_user rounded up to 8; zero columns past K_user)
+    W_cand: np.ndarray       # bf16 bits [M, Kc8]
+    X_user: np.ndarray       # bf16 bits [n_user, Ku8, N]  (zero rows past K_user)
+    X_cand: np.ndarray       # bf16 bits [n_cand, Kc8, N]
+    cand_to_user: np.ndarray  # int32 [n_cand], sorted
+    counts: np.ndarray = field(repr=False, default=None)
+
+
+def lce_generate(cfg: LceConfig) -> LceWorkload:
+    """One seeded LCE workload: candidates per user 1 + Multinomial (uniform), sorted map;
+    X ~ N(0, 1), W ~ N(0, (0.5 / sqrt(K))^2) so that outputs are O(1)."""
+    rng = np.random.Generator(np.random.PCG64(cfg.seed))
+    counts = 1 + rng.multinomial(cfg.n_cand - cfg.n_user, np.full(cfg.n_user, 1.0 / cfg.n_user))
+    c2u = np.repeat(np.arange(cfg.n_user, dtype=np.int32), counts)
+    ku, kc = round_up8(cfg.K_user), round_up8(cfg.K_cand)
+    std_w = 0.5 / np.sqrt(cfg.K_user + cfg.K_cand)
+
+    def padded(tid, shape, pad_axis, valid, std):
+        x = _normal_bf16(cfg.seed, tid, shape, std).reshape(shape)
+        idx = [slice(None)] * len(shape)
+        idx[pad_axis] = slice(valid, None)
+        x[tuple(idx)] = 0
+        return x
+
+    W_user = padded(10, (cfg.M, ku), 1, cfg.K_user, std_w)
+    W_cand = padded(11, (cfg.M, kc), 1, cfg.K_cand, std_w)
+    X_user = padded(12, (cfg.n_user, ku, cfg.N), 1, cfg.K_user, 1.0)
+    X_cand = padded(13, (cfg.n_cand, kc, cfg.N), 1, cfg.K_cand, 1.0)
+    return LceWorkload(cfg=cfg, W_user=W_user, W_cand=W_cand, X_user=X_user, X_cand=X_cand,
+                       cand_to_user=c2u.astype(np.int32), counts=counts)
+
+
+LCE_CONFIGS = {
+    "lce_tiny_8x3": LceConfig(name="lce_tiny_8x3", n_cand=8, n_user=3, M=37, K_user=13, K_cand=21,
+                              N=64, seed=20,
+                              description="8 candidates over 3 users, M=37, K=13+21 (padded 16+24), N=64"),
+    "lce_1024x15": LceConfig(name="lce_1024x15", n_cand=1024, n_user=15, M=433, K_user=1022,
+                             K_cand=1022, N=256, seed=21,
+                             description="1024 candidates over 15 users (~70:1), M=433, "
+                                         "K=1022+1022 (padded 1024+1024), N=256"),
+}
+
+
 CONFIGS = {
     "tiny_8x2": Config(
         name="tiny_8x2", n_cand=8, n_user=2, H=2, D=64, Lq=1, seed=0,

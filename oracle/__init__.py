@@ -149,6 +149,12 @@ def self_attention(q_user, k, v, user_offsets, scale: float, rows=None) -> np.nd
     return out
 
 
+def lce(W_user, W_cand, X_user, X_cand, cand_to_user, cands=None) -> np.ndarray:
+    """fp64 IKBO linear compression (see ``oracle/linear_compression.py``)."""
+    from . import linear_compression
+    return linear_compression.lce(W_user, W_cand, X_user, X_cand, cand_to_user, cands)
+
+
 def num_threads() -> int:
     """OpenMP threads the oracle runs on (OMP_NUM_THREADS, else all cores)."""
     return int(_load().ikbo_oracle_num_threads())
