@@ -17,7 +17,7 @@ from typing import Optional, Tuple
 from . import _lib
 from ._lib import STATUS
 
-__all__ = ["attn_fwd", "fused_attn_fwd", "broadcast_attn_fwd", "attn_fwd_host", "attn_fwd_noalloc", "get_device_error", "set_timing",
+__all__ = ["attn_fwd", "fused_attn_fwd", "lce_fwd", "broadcast_attn_fwd", "attn_fwd_host", "attn_fwd_noalloc", "get_device_error", "set_timing",
            "get_timing", "set_kernel", "selected_kernel", "set_debug", "launches_per_call", "version", "load", "IkboError", "STATUS"]
 
 
@@ -128,6 +128,30 @@ def fused_attn_fwd(q, q_user, k, v, user_offsets, cand_to_user, scale: Optional[
                                         p(out), p(out_user), _stream_handle(stream))
     _check(rc, "ikbo_fused_attn_fwd")
     return out, out_user
+
+
+def lce_fwd(W_user, W_cand, X_user, X_cand, cand_to_user, out=None, stream=None):
+    """IKBO linear compression on device tensors (see ``ikbo_lce_fwd`` in include/ikbo.h):
+    ``out[b] = W_user @ X_user[cand_to_user[b]] + W_cand @ X_cand[b]``; returns ``out``."""
+    import torch
+    for name, t in (("W_cand", W_cand), ("X_cand", X_cand), ("W_user", W_user), ("X_user", X_user)):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
+    if cand_to_user.dtype != torch.int32 or not cand_to_user.is_contiguous() or not cand_to_user.is_cuda:
+        raise ValueError("cand_to_user must be a contiguous int32 CUDA tensor")
+    n_cand, K_cand, N = (int(x) for x in X_cand.shape)
+    n_user, K_user = int(X_user.shape[0]), int(X_user.shape[1])
+    M = int(W_cand.shape[0])
+    if W_cand.shape != (M, K_cand) or W_user.shape != (M, K_user) or X_user.shape[2] != N:
+        raise ValueError("shapes: W_user [M, K_user], W_cand [M, K_cand], X_user [n_user, K_user, N], "
+                         "X_cand [n_cand, K_cand, N]")
+    if out is None:
+        out = torch.empty((n_cand, M, N), dtype=torch.bfloat16, device=X_cand.device)
+    p = lambda t: _ptr(t) if t.numel() else None
+    rc = _lib.lib().ikbo_lce_fwd(p(W_user), p(W_cand), p(X_user), p(X_cand), p(cand_to_user), n_cand,
+                                 n_user, M, K_user, K_cand, N, p(out), _stream_handle(stream))
+    _check(rc, "ikbo_lce_fwd")
+    return out
 
 
 def broadcast_attn_fwd(q, k, v, user_offsets, cand_to_user, scale: Optional[float] = None,

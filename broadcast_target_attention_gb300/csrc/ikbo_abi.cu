@@ -14,6 +14,7 @@
 #include "ikbo_attn_pp.cuh"
 #include "ikbo_attn_tc.cuh"
 #include "ikbo_broadcast.cuh"
+#include "ikbo_lce.cuh"
 #include "ikbo_common.cuh"
 #include "ikbo_plan.cuh"
 
@@ -33,6 +34,7 @@ struct DeviceState {
   int num_sms = 0;
   int tc_grid[2] = {0, 0};   // CTAs of the tcgen05 kernel (clusters of 2), D = 64 / 128
   int pp_grid[2] = {0, 0};   // CTAs of the two-tile tcgen05 kernel, D = 64 / 128
+  bool lce_ready[4] = {false, false, false, false};   // shared-memory attribute set, N = 64 .. 256
   int* err_word = nullptr;
   cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
   bool ev_ready = false;
@@ -763,6 +765,162 @@ int ikbo_fused_attn_fwd(const void* q, const void* q_user, const void* k_user, c
                 out, static_cast<char*>(ws), L, st, &self);
   if (cudaFreeAsync(ws, st) != cudaSuccess && rc == IKBO_OK) rc = IKBO_ERR_CUDA;
   return rc;
+}
+
+}  // extern "C"
+
+namespace ikbo {
+namespace {
+
+// W [M, K] row-major as a 2-D map {K, M}: boxes of 64 K-columns x 128 rows.
+int encode_lce_w_map(CUtensorMap* m, const void* W, int M, int K) {
+  cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(M)};
+  cuuint64_t strides[1] = {cuuint64_t(K) * 2};
+  cuuint32_t box[2] = {cuuint32_t(kLceKStep), cuuint32_t(kTileM)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W), dims, strides,
+                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? IKBO_OK : IKBO_ERR_CUDA;
+}
+
+// X [B, K, N] as a 3-D map {N, K, B}: boxes of 64 columns x 64 K-rows of one batch entry.
+int encode_lce_x_map(CUtensorMap* m, const void* X, int64_t B, int K, int N) {
+  cuuint64_t dims[3] = {cuuint64_t(N), cuuint64_t(K), cuuint64_t(B)};
+  cuuint64_t strides[2] = {cuuint64_t(N) * 2, cuuint64_t(K) * N * 2};
+  cuuint32_t box[3] = {64, cuuint32_t(kLceKStep), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(X), dims, strides,
+                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? IKBO_OK : IKBO_ERR_CUDA;
+}
+
+template <int NB>
+cudaError_t launch_lce(DeviceState* ds, const LceParams& lp, const CUtensorMap& wm,
+                       const CUtensorMap& xm, int grid, bool pdl, cudaStream_t st) {
+  if (!ds->lce_ready[NB - 1]) {
+    cudaError_t e = cudaFuncSetAttribute(ikbo_lce_kernel<NB>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kLceSmemBytes);
+    if (e != cudaSuccess) return e;
+    ds->lce_ready[NB - 1] = true;
+  }
+  return launch_ex(ikbo_lce_kernel<NB>, dim3(grid), dim3(kLceThreads), kLceSmemBytes, st, pdl, 1, lp,
+                   wm, xm);
+}
+
+cudaError_t launch_lce_nb(DeviceState* ds, int NB, const LceParams& lp, const CUtensorMap& wm,
+                          const CUtensorMap& xm, int grid, bool pdl, cudaStream_t st) {
+  switch (NB) {
+    case 1: return launch_lce<1>(ds, lp, wm, xm, grid, pdl, st);
+    case 2: return launch_lce<2>(ds, lp, wm, xm, grid, pdl, st);
+    case 3: return launch_lce<3>(ds, lp, wm, xm, grid, pdl, st);
+    default: return launch_lce<4>(ds, lp, wm, xm, grid, pdl, st);
+  }
+}
+
+}  // namespace
+}  // namespace ikbo
+
+extern "C" {
+
+int ikbo_lce_fwd(const void* W_user, const void* W_cand, const void* X_user, const void* X_cand,
+                 const int32_t* cand_to_user, int64_t n_cand, int64_t n_user, int32_t M,
+                 int32_t K_user, int32_t K_cand, int32_t N, void* out, ikbo_stream_t stream) {
+  if (n_cand < 0 || n_user < 0 || M < 1 || K_user < 0 || K_cand < 8 || (K_user % 8) ||
+      (K_cand % 8) || N < 64 || N > 256 || (N % 64))
+    return IKBO_ERR_SHAPE;
+  if (n_cand >= (int64_t(1) << 31) || n_user >= (int64_t(1) << 31) || M >= (1 << 24) ||
+      K_user >= (1 << 24) || K_cand >= (1 << 24))
+    return IKBO_ERR_SHAPE;
+  if (n_cand == 0) return IKBO_OK;
+  const bool user_part = K_user > 0;
+  if (!W_cand || !X_cand || !out || (user_part && (!W_user || !X_user || !cand_to_user)))
+    return IKBO_ERR_NULL;
+  if (user_part && n_user == 0) return IKBO_ERR_INDEX;
+  if (!aligned16(W_cand) || !aligned16(X_cand) || !aligned16(out) ||
+      (user_part && (!aligned16(W_user) || !aligned16(X_user) ||
+                     (reinterpret_cast<uintptr_t>(cand_to_user) & 3u))))
+    return IKBO_ERR_ALIGN;
+  {
+    const uintptr_t ob = reinterpret_cast<uintptr_t>(out), oe = ob + uintptr_t(n_cand) * M * N * 2;
+    auto overlaps = [&](const void* x, uintptr_t bytes) {
+      const uintptr_t xb = reinterpret_cast<uintptr_t>(x);
+      return x && xb < oe && ob < xb + bytes;
+    };
+    if (overlaps(W_cand, uintptr_t(M) * K_cand * 2) || overlaps(X_cand, uintptr_t(n_cand) * K_cand * N * 2) ||
+        (user_part && (overlaps(W_user, uintptr_t(M) * K_user * 2) ||
+                       overlaps(X_user, uintptr_t(n_user) * K_user * N * 2))))
+      return IKBO_ERR_ALIAS;
+  }
+  DeviceState* ds = nullptr;
+  int rc = device_state(&ds);
+  if (rc != IKBO_OK) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int NB = N / 64;
+  const int mt = (M + kTileM - 1) / kTileM;
+  CUtensorMap wc_map, xc_map, wu_map, xu_map;
+  std::memset(&wu_map, 0, sizeof wu_map);
+  std::memset(&xu_map, 0, sizeof xu_map);
+  if (encode_lce_w_map(&wc_map, W_cand, M, K_cand) != IKBO_OK ||
+      encode_lce_x_map(&xc_map, X_cand, n_cand, K_cand, N) != IKBO_OK)
+    return IKBO_ERR_CUDA;
+  float* Y = nullptr;
+  if (user_part) {
+    if (encode_lce_w_map(&wu_map, W_user, M, K_user) != IKBO_OK ||
+        encode_lce_x_map(&xu_map, X_user, n_user, K_user, N) != IKBO_OK)
+      return IKBO_ERR_CUDA;
+    if (cudaMallocAsync(reinterpret_cast<void**>(&Y), size_t(n_user) * M * N * 4, st) != cudaSuccess)
+      return IKBO_ERR_CUDA;
+  }
+  LceParams lp = {};
+  lp.cand_to_user = cand_to_user;
+  lp.Y = Y;
+  lp.Y_out = Y;
+  lp.out = static_cast<uint16_t*>(out);
+  lp.n_user = n_user;
+  lp.M = M;
+  lp.N = N;
+  lp.add_user = user_part ? 1 : 0;
+  lp.err_word = ds->err_word;
+  lp.timeout_ns = g_timeout_ns;
+  cudaError_t e = cudaSuccess;
+  const bool timed = g_timing;
+  if (timed && (rc = ensure_events(ds)) != IKBO_OK) {
+    if (Y) cudaFreeAsync(Y, st);
+    return rc;
+  }
+  if (timed) cudaEventRecord(ds->ev[0], st);
+  if (user_part) {
+    LceParams l0 = lp;
+    l0.W = static_cast<const uint16_t*>(W_user);
+    l0.n_batch = n_user;
+    l0.K = K_user;
+    l0.stage = 0;
+    const int64_t units = n_user * mt;
+    e = launch_lce_nb(ds, NB, l0, wu_map, xu_map, int(units < ds->num_sms ? units : ds->num_sms), false,
+                      st);
+  }
+  if (timed) cudaEventRecord(ds->ev[1], st);
+  if (e == cudaSuccess) {
+    LceParams l1 = lp;
+    l1.W = static_cast<const uint16_t*>(W_cand);
+    l1.n_batch = n_cand;
+    l1.K = K_cand;
+    l1.stage = 1;
+    const int64_t units = n_cand * mt;
+    // a programmatic dependent of the user stage: its epilogue waits for Y
+    e = launch_lce_nb(ds, NB, l1, wc_map, xc_map, int(units < ds->num_sms ? units : ds->num_sms),
+                      user_part, st);
+  }
+  if (timed) {
+    cudaEventRecord(ds->ev[2], st);
+    int dev = 0;
+    cudaGetDevice(&dev);
+    g_timing_dev = dev;
+  }
+  if (Y) cudaFreeAsync(Y, st);
+  return e == cudaSuccess ? IKBO_OK : cuda_fail(e);
 }
 
 int ikbo_get_device_error(ikbo_stream_t stream) {

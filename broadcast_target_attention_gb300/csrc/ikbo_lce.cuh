@@ -1,0 +1,278 @@
+// IKBO linear compression on the 5th-generation tensor cores (sm_103a).
+//
+// What it computes ("In-Kernel Broadcast Optimization: Co-Designing Kernels
+// for RecSys Inference", §2): linear compression of embeddings projects each
+// candidate's K input embeddings X[b] (K x N) with a learned W (M x K),
+// out[b] = W @ X[b].  The K embeddings are the candidate's user's block
+// followed by its own, so with W = [W_user | W_cand]
+//
+//     out[b] = W_user @ X_user[u(b)] + W_cand @ X_cand[b],   u(b) = cand_to_user[b]
+//
+// (§2.1: the broadcast pushed past the matrix product; the user term is
+// computed once per user, at the user batch size).  Two stages, one kernel:
+//   stage 0  Y[u] = W_user @ X_user[u] for every user, kept in fp32;
+//   stage 1  out[b] = W_cand @ X_cand[b] + Y[u(b)]: the broadcast add is fused
+//            into the epilogue (§2.3), which finds Y through cand_to_user, so
+//            no broadcast tensor is ever written.
+// Each K block arrives zero-padded to a multiple of 8 (§2.2), so every row is
+// 16-byte aligned for the TMA.
+//
+// Work unit: (batch index, 128-row tile of M).  Persistent CTAs, warp roles
+// (256 threads):
+//   warp 0     TMA producer: per 64-wide step of K, the W tile (128 x 64,
+//              K-major) and the X tile (64 x N, N contiguous) into a ring;
+//   warp 1     MMA warp, converged, one elected lane issuing: D = W X in
+//              tensor memory (M = 128, N = the full width, K = 16 per MMA),
+//              two accumulators so that the epilogue of one unit overlaps the
+//              MMAs of the next;
+//   warps 4-7  epilogue: TMEM lane r = row r of the tile; 32 columns at a time,
+//              + Y (stage 1), to bf16 (stage 1) or fp32 (stage 0), stored.
+// Stage 1 is launched as a programmatic dependent of stage 0; only its
+// epilogue waits for stage 0's Y, so its loads and MMAs overlap stage 0.
+// Every wait is bounded, as in the attention kernels.
+#pragma once
+
+#include "ikbo_attn_tc.cuh"
+
+namespace ikbo {
+
+constexpr int kLceThreads = 256;
+constexpr int kLceEpiWarp0 = 4;
+constexpr int kLceKStep = 64;                  // K per ring stage (one 128-byte swizzle atom of bf16)
+constexpr int kLceSmemBytes = 232448;          // the per-CTA maximum
+constexpr int kLceCtrlBytes = 1024;
+constexpr int kLceMaxStages = 8;
+
+struct LceParams {
+  const uint16_t* W;          // bf16 [M, K] of this stage (W_user or W_cand)
+  const int32_t* cand_to_user;
+  const float* Y;             // stage 1: fp32 [n_user, M, N] user terms
+  float* Y_out;               // stage 0: fp32 [n_user, M, N]
+  uint16_t* out;              // stage 1: bf16 [n_cand, M, N]
+  int64_t n_batch;            // users (stage 0) or candidates (stage 1)
+  int64_t n_user;
+  int32_t M, K, N;
+  int32_t stage;              // 0: user GEMM, 1: candidate GEMM with the broadcast add
+  int32_t add_user;           // stage 1: add Y (0 when there is no user block)
+  int* err_word;
+  uint64_t timeout_ns;
+};
+
+template <int NB>
+struct LceConfig {
+  static constexpr int N = NB * 64;
+  static constexpr int kABytes = kTileM * 128;          // 128 rows x 64 bf16
+  static constexpr int kBBytes = NB * kLceKStep * 128;  // NB blocks of 64 rows x 64 bf16
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages0 = (kLceSmemBytes - kLceCtrlBytes) / kStageBytes;
+  static constexpr int kStages = kStages0 < kLceMaxStages ? kStages0 : kLceMaxStages;
+  static constexpr int kDataBytes = kStages * kStageBytes;
+  static_assert(kStages >= 2, "ring");
+  static_assert(kDataBytes + kLceCtrlBytes <= kLceSmemBytes, "shared memory");
+  static_assert(2 * N <= 512, "two accumulators in tensor memory");
+};
+
+struct LceCtrl {
+  uint64_t full[kLceMaxStages], empty[kLceMaxStages];
+  uint64_t acc_full[2], acc_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(LceCtrl) <= kLceCtrlBytes, "control block");
+
+template <int NB>
+__global__ void __launch_bounds__(kLceThreads, 1)
+ikbo_lce_kernel(const __grid_constant__ LceParams p, const __grid_constant__ CUtensorMap wmap,
+                const __grid_constant__ CUtensorMap xmap) {
+  using C = LceConfig<NB>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* data = smem_raw;
+  LceCtrl* ctl = reinterpret_cast<LceCtrl*>(smem_raw + C::kDataBytes);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  // the user stage lets the candidate stage start at once (it waits for Y
+  // only in its epilogue)
+  if (p.stage == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const bool layout_ok = (ptx::smem_addr(smem_raw) & 1023u) == 0;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kStages; ++i) {
+      ptx::mbar_init(ptx::smem_addr(&ctl->full[i]), 1);
+      ptx::mbar_init(ptx::smem_addr(&ctl->empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(ptx::smem_addr(&ctl->acc_full[i]), 1);
+      ptx::mbar_init(ptx::smem_addr(&ctl->acc_empty[i]), 4);   // the 4 epilogue warps
+    }
+    ptx::mbar_init(ptx::smem_addr(&ctl->drain), 1);
+    ctl->abort_flag = 0;
+    ptx::fence_mbar_init();
+    if (!layout_ok) atomicOr(p.err_word, kErrLayout);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_addr(&ctl->tmem_base), 512);
+    ptx::tmem_relinquish();
+  }
+  if (warp == 2 && lane == 0) {
+    ptx::prefetch_tensormap(&wmap);
+    ptx::prefetch_tensormap(&xmap);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  const Waiter W{&ctl->abort_flag, p.err_word, p.timeout_ns};
+  const int mt_count = (p.M + kTileM - 1) / kTileM;
+  const int64_t n_units = p.n_batch * mt_count;
+  const int ksteps = (p.K + kLceKStep - 1) / kLceKStep;
+
+  if (layout_ok && warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int64_t unit = blockIdx.x; unit < n_units && ok; unit += gridDim.x) {
+        const int b = int(unit / mt_count), mt = int(unit % mt_count);
+        for (int ks = 0; ks < ksteps; ++ks, ++it) {
+          const uint32_t slot = it % C::kStages;
+          if (!W.wait(ptx::smem_addr(&ctl->empty[slot]), ((it / C::kStages) & 1u) ^ 1u)) {
+            ok = false;
+            break;
+          }
+          const uint32_t bar = ptx::smem_addr(&ctl->full[slot]);
+          const uint32_t dst = ptx::smem_addr(data + slot * C::kStageBytes);
+          ptx::mbar_arrive_expect_tx(bar, C::kStageBytes);
+          // W[mt*128 .. +128, k .. k+64] (rows past M and columns past K read as zeros)
+          ptx::tma_load_2d(dst, &wmap, bar, ks * kLceKStep, mt * kTileM);
+          // X[b, k .. k+64, 64 c .. 64 c + 64] for each 64-column block c
+#pragma unroll
+          for (int c = 0; c < NB; ++c)
+            ptx::tma_load_3d(dst + C::kABytes + c * kLceKStep * 128, &xmap, bar, c * 64, ks * kLceKStep, b);
+        }
+      }
+      // every armed phase must complete before the CTA exits
+      for (uint32_t s = 0; s < (uint32_t)C::kStages && s < it; ++s) {
+        const uint32_t uses = (it - s + C::kStages - 1) / C::kStages;
+        W.drain(ptx::smem_addr(&ctl->full[s]), (uses - 1) & 1u);
+      }
+    }
+    __syncwarp();
+  } else if (layout_ok && warp == 1) {
+    // -------------------------------------------------------------- MMA warp
+    // converged; the elected lane issues every MMA and commit
+    constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kTileM, C::N, 1);
+    uint32_t it = 0, ui = 0;
+    bool ok = true;
+    for (int64_t unit = blockIdx.x; unit < n_units && ok; unit += gridDim.x, ++ui) {
+      const uint32_t buf = ui & 1u;
+      // the epilogue has read this accumulator's previous unit
+      if (!W.conv_wait(ptx::smem_addr(&ctl->acc_empty[buf]), ((ui >> 1) & 1u) ^ 1u)) break;
+      ptx::tc_fence_after();
+      const uint32_t d_tmem = tmem + buf * C::N;
+      for (int ks = 0; ks < ksteps; ++ks, ++it) {
+        const uint32_t slot = it % C::kStages;
+        if (!W.conv_wait(ptx::smem_addr(&ctl->full[slot]), (it / C::kStages) & 1u)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t a_base = ptx::smem_addr(data + slot * C::kStageBytes);
+        const uint32_t b_base = a_base + C::kABytes;
+#pragma unroll
+        for (int kk = 0; kk < kLceKStep / 16; ++kk) {
+          // A: K-major, 128-byte swizzle, 32 bytes per K = 16 step
+          const uint64_t adesc = ptx::smem_desc_sw128(a_base + kk * 32, 16, 1024);
+          // B: N contiguous (MN-major): 16 K-rows per step, 64-column blocks
+          // kLceKStep * 128 bytes apart, 8-row groups 1 KB apart
+          const uint64_t bdesc = ptx::smem_desc_sw128(b_base + kk * 16 * 128, kLceKStep * 128, 1024);
+          ptx::mma_ss_warp(d_tmem, adesc, bdesc, kIdesc, (ks > 0 || kk > 0) ? 1u : 0u);
+        }
+        ptx::mma_commit_warp(ptx::smem_addr(&ctl->empty[slot]));
+      }
+      if (!ok) break;
+      ptx::mma_commit_warp(ptx::smem_addr(&ctl->acc_full[buf]));
+    }
+    ptx::mma_commit_warp(ptx::smem_addr(&ctl->drain));
+    if (lane == 0) W.drain(ptx::smem_addr(&ctl->drain), 0);
+    __syncwarp();
+  } else if (layout_ok && warp >= kLceEpiWarp0) {
+    // ------------------------------------------------------------- epilogue
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;                      // TMEM lane == tile row
+    const uint32_t lane_off = uint32_t(quarter * 32) << 16;
+    bool y_ready = p.stage == 0 || !p.add_user;
+    uint32_t ui = 0;
+    for (int64_t unit = blockIdx.x; unit < n_units; unit += gridDim.x, ++ui) {
+      const uint32_t buf = ui & 1u;
+      const int b = int(unit / mt_count), mt = int(unit % mt_count);
+      if (!W.warp_wait(ptx::smem_addr(&ctl->acc_full[buf]), (ui >> 1) & 1u)) break;
+      ptx::tc_fence_after();
+      const int m = mt * kTileM + r;
+      const bool live = m < p.M;
+      int u = 0;
+      bool bad = false;
+      if (p.stage == 1 && p.add_user) {
+        if (!y_ready) {
+          // Y is stage 0's output: visible once that grid has completed
+          asm volatile("griddepcontrol.wait;" ::: "memory");
+          y_ready = true;
+        }
+        u = p.cand_to_user[b];
+        bad = u < 0 || int64_t(u) >= p.n_user;
+        if (bad && r == 0) atomicOr(p.err_word, kErrIndex);
+      }
+      const uint32_t acc = tmem + lane_off + buf * C::N;
+#pragma unroll 1
+      for (int c = 0; c < C::N / 32; ++c) {
+        uint32_t o[32];
+        ptx::tmem_ld32(acc + c * 32, o);
+        ptx::tmem_ld_wait();
+        if (live && !bad) {
+          if (p.stage == 0) {
+            float4* dst = reinterpret_cast<float4*>(p.Y_out + ((int64_t)b * p.M + m) * p.N + c * 32);
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4)
+              dst[q4] = make_float4(__uint_as_float(o[4 * q4]), __uint_as_float(o[4 * q4 + 1]),
+                                    __uint_as_float(o[4 * q4 + 2]), __uint_as_float(o[4 * q4 + 3]));
+          } else {
+            float x[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(o[e]);
+            if (p.add_user) {
+              const float4* y = reinterpret_cast<const float4*>(p.Y + ((int64_t)u * p.M + m) * p.N + c * 32);
+#pragma unroll
+              for (int q4 = 0; q4 < 8; ++q4) {
+                const float4 t = y[q4];
+                x[4 * q4] += t.x;
+                x[4 * q4 + 1] += t.y;
+                x[4 * q4 + 2] += t.z;
+                x[4 * q4 + 3] += t.w;
+              }
+            }
+            uint4* dst = reinterpret_cast<uint4*>(p.out + ((int64_t)b * p.M + m) * p.N + c * 32);
+#pragma unroll
+            for (int q8 = 0; q8 < 4; ++q8) {
+              uint4 v;
+              v.x = pack_bf16(x[8 * q8], x[8 * q8 + 1]);
+              v.y = pack_bf16(x[8 * q8 + 2], x[8 * q8 + 3]);
+              v.z = pack_bf16(x[8 * q8 + 4], x[8 * q8 + 5]);
+              v.w = pack_bf16(x[8 * q8 + 6], x[8 * q8 + 7]);
+              dst[q8] = v;
+            }
+          }
+        }
+      }
+      // this accumulator may take the next unit's MMAs
+      ptx::tc_fence_before();
+      ptx::mbar_arrive_warp(ptx::smem_addr(&ctl->acc_empty[buf]));
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace ikbo

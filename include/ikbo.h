@@ -209,6 +209,36 @@ int ikbo_fused_attn_fwd(const void* q, const void* q_user, const void* k_user, c
                         void* out, void* out_user, ikbo_stream_t stream);
 
 /*
+ * IKBO linear compression ("In-Kernel Broadcast Optimization", §2): for every
+ * candidate b of user u = cand_to_user[b], the compression of its K input
+ * embeddings (its user's K_user, then its own K_cand, each of N values) by
+ * W = [W_user | W_cand]:
+ *
+ *   out[b] = W_user @ X_user[u] + W_cand @ X_cand[b]         (M x N)
+ *
+ * The user term is computed once per user (fp32, kept in a library-owned
+ * buffer) and added in the epilogue of the candidate product, so the user
+ * block is never copied per candidate (§2.1-§2.3).  Two launches of one
+ * tcgen05 kernel, the second a programmatic dependent of the first.
+ *
+ *   W_user  bf16 [M, K_user]        W_cand  bf16 [M, K_cand]
+ *   X_user  bf16 [n_user, K_user, N]  X_cand  bf16 [n_cand, K_cand, N]
+ *   out     bf16 [n_cand, M, N]; shares no byte with an input
+ *   All device memory, 16-byte aligned (cand_to_user 4-byte aligned).
+ *   K_user, K_cand: multiples of 8 (blocks zero-padded by the caller, which
+ *   §2.2 shows to be exact); K_cand >= 8; K_user = 0 means no user block
+ *   (then W_user, X_user, cand_to_user may be NULL).  N in {64, 128, 192, 256}.
+ *   Accumulation in fp32; out rounded to bf16 (nearest even).
+ * Errors: bad sizes IKBO_ERR_SHAPE, NULL IKBO_ERR_NULL, misaligned
+ * IKBO_ERR_ALIGN, overlap IKBO_ERR_ALIAS; a cand_to_user value outside
+ * [0, n_user) sets IKBO_ERR_INDEX in the device error word and that
+ * candidate's rows are not written.  n_cand == 0: no-op.
+ */
+int ikbo_lce_fwd(const void* W_user, const void* W_cand, const void* X_user, const void* X_cand,
+                 const int32_t* cand_to_user, int64_t n_cand, int64_t n_user, int32_t M,
+                 int32_t K_user, int32_t K_cand, int32_t N, void* out, ikbo_stream_t stream);
+
+/*
  * Selects the attention kernel for later calls on this thread.  Returns the
  * previous value.
  *   0  automatic (the default): 3 when the users have on average at least
