@@ -575,6 +575,131 @@ def run_fused(args):
     print(json.dumps(line), flush=True)
 
 
+def run_lce(args):
+    """IKBO linear compression ("In-Kernel Broadcast Optimization", §2) on one GPU, timed
+    beside the broadcast form it replaces (the user block copied to every candidate, then one
+    batched product through torch / cuBLAS)."""
+    import torch
+
+    import broadcast_target_attention_gb300 as ikbo
+
+    ws, rank, local = R.dist_env()
+    if ws > 1:
+        raise SystemExit("--lce measures one GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ikbo.load()
+    wl = W.lce_generate(W.LCE_CONFIGS[args.lce])
+    c = wl.cfg
+    ku, kc = wl.X_user.shape[1], wl.X_cand.shape[1]
+    flops = 2 * c.M * c.N * (c.n_user * c.K_user + c.n_cand * c.K_cand)
+    alg_bytes = 2 * (c.M * (ku + kc) + c.n_user * ku * c.N + c.n_cand * kc * c.N + c.n_cand * c.M * c.N) \
+        + 2 * 4 * c.n_user * c.M * c.N + 4 * c.n_cand
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    Wu, Wc, Xu, Xc = bf(wl.W_user), bf(wl.W_cand), bf(wl.X_user), bf(wl.X_cand)
+    c2u = torch.from_numpy(wl.cand_to_user).to(dev)
+    out = torch.empty((c.n_cand, c.M, c.N), dtype=torch.bfloat16, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.int32, device=dev)
+    Wfull = torch.cat([Wu, Wc], dim=1)
+
+    def ikbo_step():
+        ikbo.lce_fwd(Wu, Wc, Xu, Xc, c2u, out=out)
+
+    def broadcast_step():
+        X = torch.cat([Xu[c2u.long()], Xc], dim=1)          # the materialised broadcast
+        return torch.matmul(Wfull, X)
+
+    def timed(fn, n):
+        evs = []
+        for i in range(n):
+            flush.fill_(i & 0xFF)
+            s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s_.record()
+            fn()
+            e_.record()
+            evs.append((s_, e_))
+        torch.cuda.synchronize(dev)
+        return [a.elapsed_time(b) for a, b in evs]
+
+    with ClockSampler(local) as clk:
+        for _ in range(args.warmup):
+            flush.fill_(1)
+            ikbo_step()
+            broadcast_step()
+        assert ikbo.get_device_error() == 0
+        torch.cuda.synchronize(dev)
+        clk.mark_start()
+        ms_list = timed(ikbo_step, args.steps)
+        clk.mark_end()
+        bc_list = timed(broadcast_step, min(args.steps, 20))
+        # per-kernel times: the user stage and the candidate stage (events around each launch)
+        ikbo.set_timing(True)
+        st0, st1 = [], []
+        for i in range(min(args.steps, 50)):
+            flush.fill_(i & 0xFF)
+            ikbo_step()
+            a_, b_ = ikbo.get_timing()
+            st0.append(a_)
+            st1.append(b_)
+        ikbo.set_timing(False)
+        # end to end: host tensors copied in, the call, the output copied back
+        hWu, hWc, hXu, hXc, hc2u = (x.cpu().pin_memory() for x in (Wu, Wc, Xu, Xc, c2u))
+        hout = torch.empty_like(out, device="cpu").pin_memory()
+
+        def e2e_step():
+            d = [x.to(dev, non_blocking=True) for x in (hWu, hWc, hXu, hXc, hc2u)]
+            o = ikbo.lce_fwd(*d)
+            hout.copy_(o, non_blocking=True)
+            torch.cuda.synchronize(dev)
+
+        for _ in range(3):
+            e2e_step()
+        e2e_ms = []
+        for _ in range(min(args.steps, 20)):
+            t0 = time.perf_counter()
+            e2e_step()
+            e2e_ms.append((time.perf_counter() - t0) * 1e3)
+    assert ikbo.get_device_error() == 0
+    ms = statistics.mean(ms_list)
+    bc = statistics.mean(bc_list)
+    pk = peaks()
+    tf = flops / (ms * 1e-3) / 1e12
+    ai = flops / alg_bytes
+    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    gbs = alg_bytes / (ms * 1e-3) / 1e9
+    if ai < ridge:
+        roof = {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": gbs / pk["hbm_gbs"], "traffic": None, "kernel": f"ikbo_lce_kernel<{c.N // 64}>",
+                "alg_bytes_per_launch": alg_bytes, "peak_source": pk["source"] + " (burst copy)"}
+    else:
+        roof = {"bound": "tensor", "achieved": tf, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": tf / pk["bf16_tflops"], "traffic": None, "kernel": f"ikbo_lce_kernel<{c.N // 64}>",
+                "flops_per_launch": flops, "peak_source": pk["source"] + " (burst cuBLAS bf16)"}
+    h2d = sum(x.nbytes for x in (wl.W_user, wl.W_cand, wl.X_user, wl.X_cand, wl.cand_to_user))
+    e2e = statistics.mean(e2e_ms)
+    line = {
+        "metric": "IKBO linear compression BF16 TFLOP/s (decomposed work)", "value": tf,
+        "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{c.name}: {c.description}", "n_cand": c.n_cand, "n_user": c.n_user,
+                   "M": c.M, "K_user": c.K_user, "K_cand": c.K_cand, "N": c.N,
+                   "l2": "flushed before every timed step (write of 2x L2 size)",
+                   "ai_flop_per_byte": ai},
+        "kernel_ms": {"user_stage": statistics.mean(st0), "candidate_stage": statistics.mean(st1)},
+        "roofline": roof,
+        "broadcast_path": {"ms_per_step": bc, "ikbo_speedup": bc / ms,
+                           "what": "torch: X = cat(X_user[cand_to_user], X_cand); matmul(W, X)"},
+        "e2e": {"value": flops / (e2e * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": int(out.numel() * 2), "ms_per_step": e2e},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk.summary(),
+        "cpu_baseline": None,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -584,6 +709,8 @@ def main():
     ap.add_argument("--config", default=W.HEADLINE, choices=sorted(W.CONFIGS))
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--lce", default=None, choices=sorted(W.LCE_CONFIGS),
+                    help="measure IKBO linear compression on this workload instead")
     ap.add_argument("--with-self", action="store_true",
                     help="measure the fused self + target attention of the workload instead")
     args = ap.parse_args()
@@ -591,6 +718,8 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.lce:
+        run_lce(args)
     elif args.with_self:
         run_fused(args)
     else:
