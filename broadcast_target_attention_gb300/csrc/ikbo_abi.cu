@@ -35,6 +35,7 @@ struct DeviceState {
   int tc_grid[2] = {0, 0};   // CTAs of the tcgen05 kernel (clusters of 2), D = 64 / 128
   int pp_grid[2] = {0, 0};   // CTAs of the two-tile tcgen05 kernel, D = 64 / 128
   bool lce_ready[4] = {false, false, false, false};   // shared-memory attribute set, N = 64 .. 256
+  int lce_clusters[4][9] = {};   // co-resident clusters of the LCE kernel, by N / 64 and cluster size
   int* err_word = nullptr;
   cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
   bool ev_ready = false;
@@ -796,26 +797,56 @@ int encode_lce_x_map(CUtensorMap* m, const void* X, int64_t B, int K, int N) {
   return r == CUDA_SUCCESS ? IKBO_OK : IKBO_ERR_CUDA;
 }
 
+// Units of the batch: one per batch entry and row tile, or, with clusters, one
+// per batch entry (a cluster of cluster_n CTAs takes its row tiles).  Grid:
+// as many CTAs as there are units, at most as many as fit at once.
 template <int NB>
 cudaError_t launch_lce(DeviceState* ds, const LceParams& lp, const CUtensorMap& wm,
-                       const CUtensorMap& xm, int grid, bool pdl, cudaStream_t st) {
+                       const CUtensorMap& xm, bool pdl, cudaStream_t st) {
   if (!ds->lce_ready[NB - 1]) {
     cudaError_t e = cudaFuncSetAttribute(ikbo_lce_kernel<NB>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kLceSmemBytes);
     if (e != cudaSuccess) return e;
     ds->lce_ready[NB - 1] = true;
   }
-  return launch_ex(ikbo_lce_kernel<NB>, dim3(grid), dim3(kLceThreads), kLceSmemBytes, st, pdl, 1, lp,
+  const int cn = lp.cluster_n;
+  int grid = 0;
+  if (cn > 1) {
+    int& fit = ds->lce_clusters[NB - 1][cn];
+    if (!fit) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((ds->num_sms / cn) * cn);
+      cfg.blockDim = dim3(kLceThreads);
+      cfg.dynamicSmemBytes = kLceSmemBytes;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = cn;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&fit, ikbo_lce_kernel<NB>, &cfg) != cudaSuccess || fit <= 0) {
+        cudaGetLastError();
+        fit = ds->num_sms / cn;
+      }
+    }
+    const int64_t clusters = lp.n_batch < fit ? lp.n_batch : fit;
+    grid = int(clusters) * cn;
+  } else {
+    const int64_t units = lp.n_batch * ((lp.M + kTileM - 1) / kTileM);
+    grid = int(units < ds->num_sms ? units : ds->num_sms);
+  }
+  return launch_ex(ikbo_lce_kernel<NB>, dim3(grid), dim3(kLceThreads), kLceSmemBytes, st, pdl, cn, lp,
                    wm, xm);
 }
 
 cudaError_t launch_lce_nb(DeviceState* ds, int NB, const LceParams& lp, const CUtensorMap& wm,
-                          const CUtensorMap& xm, int grid, bool pdl, cudaStream_t st) {
+                          const CUtensorMap& xm, bool pdl, cudaStream_t st) {
   switch (NB) {
-    case 1: return launch_lce<1>(ds, lp, wm, xm, grid, pdl, st);
-    case 2: return launch_lce<2>(ds, lp, wm, xm, grid, pdl, st);
-    case 3: return launch_lce<3>(ds, lp, wm, xm, grid, pdl, st);
-    default: return launch_lce<4>(ds, lp, wm, xm, grid, pdl, st);
+    case 1: return launch_lce<1>(ds, lp, wm, xm, pdl, st);
+    case 2: return launch_lce<2>(ds, lp, wm, xm, pdl, st);
+    case 3: return launch_lce<3>(ds, lp, wm, xm, pdl, st);
+    default: return launch_lce<4>(ds, lp, wm, xm, pdl, st);
   }
 }
 
@@ -884,6 +915,8 @@ int ikbo_lce_fwd(const void* W_user, const void* W_cand, const void* X_user, con
   lp.add_user = user_part ? 1 : 0;
   lp.err_word = ds->err_word;
   lp.timeout_ns = g_timeout_ns;
+  // the row tiles of one batch entry share its X tiles through a cluster
+  lp.cluster_n = (mt > 1 && mt <= 8) ? mt : 1;
   cudaError_t e = cudaSuccess;
   const bool timed = g_timing;
   if (timed && (rc = ensure_events(ds)) != IKBO_OK) {
@@ -897,9 +930,7 @@ int ikbo_lce_fwd(const void* W_user, const void* W_cand, const void* X_user, con
     l0.n_batch = n_user;
     l0.K = K_user;
     l0.stage = 0;
-    const int64_t units = n_user * mt;
-    e = launch_lce_nb(ds, NB, l0, wu_map, xu_map, int(units < ds->num_sms ? units : ds->num_sms), false,
-                      st);
+    e = launch_lce_nb(ds, NB, l0, wu_map, xu_map, false, st);
   }
   if (timed) cudaEventRecord(ds->ev[1], st);
   if (e == cudaSuccess) {
@@ -908,10 +939,8 @@ int ikbo_lce_fwd(const void* W_user, const void* W_cand, const void* X_user, con
     l1.n_batch = n_cand;
     l1.K = K_cand;
     l1.stage = 1;
-    const int64_t units = n_cand * mt;
     // a programmatic dependent of the user stage: its epilogue waits for Y
-    e = launch_lce_nb(ds, NB, l1, wc_map, xc_map, int(units < ds->num_sms ? units : ds->num_sms),
-                      user_part, st);
+    e = launch_lce_nb(ds, NB, l1, wc_map, xc_map, user_part, st);
   }
   if (timed) {
     cudaEventRecord(ds->ev[2], st);

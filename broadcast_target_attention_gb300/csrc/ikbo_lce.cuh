@@ -29,6 +29,21 @@
 //              + Y (stage 1), to bf16 (stage 1) or fp32 (stage 0), stored.
 // Stage 1 is launched as a programmatic dependent of stage 0; only its
 // epilogue waits for stage 0's Y, so its loads and MMAs overlap stage 0.
+//
+// Clusters (M of at most 8 row tiles): the CTAs of a cluster take the row
+// tiles of one batch entry at a time, CTA r tile r, so they share every X
+// tile.  Each CTA loads its own W tile and multicasts its share of the X
+// tile's 64-column blocks to the whole cluster (this GPU's own memory); a
+// ring slot is free once all the cluster's MMAs have read it, so every MMA
+// warp's commit arrives on that slot's barrier in all of the cluster's CTAs.
+// An X tile is thus read once from L2 for all the row tiles (a 128 x 256
+// tile alone needs 48 KB from L2 per 64-wide K step, more than L2 can feed
+// 152 SMs at the tensor pipe's rate), and a cluster sits on one die, so it
+// comes from DRAM once.
+// Teardown: every byte that reaches a CTA is counted on one of its own ring
+// barriers, which its producer drains, and no CTA leaves before the whole
+// cluster has; after an abort (a wait that ran out) a CTA also waits 1 ms,
+// bounded, so that a peer's copy already in flight lands first.
 // Every wait is bounded, as in the attention kernels.
 #pragma once
 
@@ -54,6 +69,7 @@ struct LceParams {
   int32_t M, K, N;
   int32_t stage;              // 0: user GEMM, 1: candidate GEMM with the broadcast add
   int32_t add_user;           // stage 1: add Y (0 when there is no user block)
+  int32_t cluster_n;          // CTAs per cluster: the row tiles of M (<= 8), or 1
   int* err_word;
   uint64_t timeout_ns;
 };
@@ -98,7 +114,7 @@ ikbo_lce_kernel(const __grid_constant__ LceParams p, const __grid_constant__ CUt
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kStages; ++i) {
       ptx::mbar_init(ptx::smem_addr(&ctl->full[i]), 1);
-      ptx::mbar_init(ptx::smem_addr(&ctl->empty[i]), 1);
+      ptx::mbar_init(ptx::smem_addr(&ctl->empty[i]), p.cluster_n);   // every MMA warp of the cluster
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(ptx::smem_addr(&ctl->acc_full[i]), 1);
@@ -123,16 +139,35 @@ ikbo_lce_kernel(const __grid_constant__ LceParams p, const __grid_constant__ CUt
   const uint32_t tmem = ctl->tmem_base;
   const Waiter W{&ctl->abort_flag, p.err_word, p.timeout_ns};
   const int mt_count = (p.M + kTileM - 1) / kTileM;
-  const int64_t n_units = p.n_batch * mt_count;
   const int ksteps = (p.K + kLceKStep - 1) / kLceKStep;
+  // units: with clusters, the batch entries, one per cluster at a time, row
+  // tile = rank; without, (batch entry, row tile) pairs
+  const int cn = p.cluster_n;
+  const int rank = cn > 1 ? int(ptx::cluster_ctarank()) : 0;
+  const uint16_t cmask = uint16_t((1u << cn) - 1u);
+  const int64_t first = cn > 1 ? blockIdx.x / cn : blockIdx.x;
+  const int64_t stride = cn > 1 ? gridDim.x / cn : gridDim.x;
+  const int64_t n_units = cn > 1 ? p.n_batch : p.n_batch * mt_count;
+  auto unit_bm = [&](int64_t unit, int& b, int& mt) {
+    if (cn > 1) {
+      b = int(unit);
+      mt = rank;
+    } else {
+      b = int(unit / mt_count);
+      mt = int(unit % mt_count);
+    }
+  };
+  // every CTA's barriers exist before a peer's multicast or commit reaches them
+  if (cn > 1) ptx::cluster_sync();
 
   if (layout_ok && warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (int64_t unit = blockIdx.x; unit < n_units && ok; unit += gridDim.x) {
-        const int b = int(unit / mt_count), mt = int(unit % mt_count);
+      for (int64_t unit = first; unit < n_units && ok; unit += stride) {
+        int b, mt;
+        unit_bm(unit, b, mt);
         for (int ks = 0; ks < ksteps; ++ks, ++it) {
           const uint32_t slot = it % C::kStages;
           if (!W.wait(ptx::smem_addr(&ctl->empty[slot]), ((it / C::kStages) & 1u) ^ 1u)) {
@@ -144,10 +179,16 @@ ikbo_lce_kernel(const __grid_constant__ LceParams p, const __grid_constant__ CUt
           ptx::mbar_arrive_expect_tx(bar, C::kStageBytes);
           // W[mt*128 .. +128, k .. k+64] (rows past M and columns past K read as zeros)
           ptx::tma_load_2d(dst, &wmap, bar, ks * kLceKStep, mt * kTileM);
-          // X[b, k .. k+64, 64 c .. 64 c + 64] for each 64-column block c
+          // X[b, k .. k+64, 64 c .. 64 c + 64] for each 64-column block c; in
+          // a cluster this CTA multicasts the blocks c = rank, rank + cn, ...
 #pragma unroll
-          for (int c = 0; c < NB; ++c)
-            ptx::tma_load_3d(dst + C::kABytes + c * kLceKStep * 128, &xmap, bar, c * 64, ks * kLceKStep, b);
+          for (int c = 0; c < NB; ++c) {
+            const uint32_t xdst = dst + C::kABytes + c * kLceKStep * 128;
+            if (cn == 1)
+              ptx::tma_load_3d(xdst, &xmap, bar, c * 64, ks * kLceKStep, b);
+            else if (c % cn == rank)
+              ptx::tma_load_3d_mc(xdst, &xmap, bar, c * 64, ks * kLceKStep, b, cmask);
+          }
         }
       }
       // every armed phase must complete before the CTA exits
@@ -163,7 +204,7 @@ ikbo_lce_kernel(const __grid_constant__ LceParams p, const __grid_constant__ CUt
     constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kTileM, C::N, 1);
     uint32_t it = 0, ui = 0;
     bool ok = true;
-    for (int64_t unit = blockIdx.x; unit < n_units && ok; unit += gridDim.x, ++ui) {
+    for (int64_t unit = first; unit < n_units && ok; unit += stride, ++ui) {
       const uint32_t buf = ui & 1u;
       // the epilogue has read this accumulator's previous unit
       if (!W.conv_wait(ptx::smem_addr(&ctl->acc_empty[buf]), ((ui >> 1) & 1u) ^ 1u)) break;
@@ -187,7 +228,11 @@ ikbo_lce_kernel(const __grid_constant__ LceParams p, const __grid_constant__ CUt
           const uint64_t bdesc = ptx::smem_desc_sw128(b_base + kk * 16 * 128, kLceKStep * 128, 1024);
           ptx::mma_ss_warp(d_tmem, adesc, bdesc, kIdesc, (ks > 0 || kk > 0) ? 1u : 0u);
         }
-        ptx::mma_commit_warp(ptx::smem_addr(&ctl->empty[slot]));
+        // the slot is free for the cluster once every CTA's MMAs have read it
+        if (cn == 1)
+          ptx::mma_commit_warp(ptx::smem_addr(&ctl->empty[slot]));
+        else
+          ptx::mma_commit_mc_warp(ptx::smem_addr(&ctl->empty[slot]), cmask);
       }
       if (!ok) break;
       ptx::mma_commit_warp(ptx::smem_addr(&ctl->acc_full[buf]));
@@ -202,9 +247,10 @@ ikbo_lce_kernel(const __grid_constant__ LceParams p, const __grid_constant__ CUt
     const uint32_t lane_off = uint32_t(quarter * 32) << 16;
     bool y_ready = p.stage == 0 || !p.add_user;
     uint32_t ui = 0;
-    for (int64_t unit = blockIdx.x; unit < n_units; unit += gridDim.x, ++ui) {
+    for (int64_t unit = first; unit < n_units; unit += stride, ++ui) {
       const uint32_t buf = ui & 1u;
-      const int b = int(unit / mt_count), mt = int(unit % mt_count);
+      int b, mt;
+      unit_bm(unit, b, mt);
       if (!W.warp_wait(ptx::smem_addr(&ctl->acc_full[buf]), (ui >> 1) & 1u)) break;
       ptx::tc_fence_after();
       const int m = mt * kTileM + r;
@@ -222,8 +268,25 @@ ikbo_lce_kernel(const __grid_constant__ LceParams p, const __grid_constant__ CUt
         if (bad && r == 0) atomicOr(p.err_word, kErrIndex);
       }
       const uint32_t acc = tmem + lane_off + buf * C::N;
+      // the user term of this row, one 32-column chunk ahead of its use
+      const bool add = p.stage == 1 && p.add_user && live && !bad;
+      const float4* yrow = add ? reinterpret_cast<const float4*>(p.Y + ((int64_t)u * p.M + m) * p.N) : nullptr;
+      float4 ynext[8];
+      if (add) {
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4) ynext[q4] = yrow[q4];
+      }
 #pragma unroll 1
       for (int c = 0; c < C::N / 32; ++c) {
+        float4 ycur[8];
+        if (add) {
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) ycur[q4] = ynext[q4];
+          if (c + 1 < C::N / 32) {
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) ynext[q4] = yrow[(c + 1) * 8 + q4];
+          }
+        }
         uint32_t o[32];
         ptx::tmem_ld32(acc + c * 32, o);
         ptx::tmem_ld_wait();
@@ -238,11 +301,10 @@ ikbo_lce_kernel(const __grid_constant__ LceParams p, const __grid_constant__ CUt
             float x[32];
 #pragma unroll
             for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(o[e]);
-            if (p.add_user) {
-              const float4* y = reinterpret_cast<const float4*>(p.Y + ((int64_t)u * p.M + m) * p.N + c * 32);
+            if (add) {
 #pragma unroll
               for (int q4 = 0; q4 < 8; ++q4) {
-                const float4 t = y[q4];
+                const float4 t = ycur[q4];
                 x[4 * q4] += t.x;
                 x[4 * q4 + 1] += t.y;
                 x[4 * q4 + 2] += t.z;
@@ -269,6 +331,16 @@ ikbo_lce_kernel(const __grid_constant__ LceParams p, const __grid_constant__ CUt
   }
   ptx::tc_fence_before();
   __syncthreads();
+  if (cn > 1) {
+    // no CTA leaves while a peer's multicast or commit may still reach it
+    ptx::cluster_sync();
+    if (threadIdx.x == 0 && ctl->abort_flag) {
+      const uint64_t t_end = ptx::globaltimer() + 1000000ull;   // 1 ms
+      while (ptx::globaltimer() < t_end) {
+      }
+    }
+    __syncthreads();
+  }
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, 512);
