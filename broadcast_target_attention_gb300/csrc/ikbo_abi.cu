@@ -36,6 +36,8 @@ struct DeviceState {
   int pp_grid[2] = {0, 0};   // CTAs of the two-tile tcgen05 kernel, D = 64 / 128
   bool lce_ready[4] = {false, false, false, false};   // shared-memory attribute set, N = 64 .. 256
   int lce_clusters[4][9] = {};   // co-resident clusters of the LCE kernel, by N / 64 and cluster size
+  int* err_host = nullptr;       // pinned copy of the error word for the host-buffer entry point
+  std::mutex* host_call = nullptr;   // serialises that entry point's use of err_host
   int* err_word = nullptr;
   cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
   bool ev_ready = false;
@@ -96,6 +98,10 @@ int device_state(DeviceState** out) {
         return IKBO_ERR_CUDA;
       g_encode = reinterpret_cast<EncodeTiledFn>(fn);
     }
+    void* h = nullptr;
+    if (cudaHostAlloc(&h, sizeof(int), cudaHostAllocDefault) != cudaSuccess) return IKBO_ERR_CUDA;
+    s.err_host = static_cast<int*>(h);
+    s.host_call = new std::mutex();   // lives as long as the process, like this state
     s.num_sms = sms;
     s.err_word = static_cast<int*>(p);
     s.ready = true;
@@ -546,6 +552,15 @@ int ikbo_attn_fwd(const void* q, const void* k_user, const void* v_user,
   return rc;
 }
 
+// Status of a device error word (0 = none).
+int status_of_error_word(int word) {
+  if (word & kErrIndex) return IKBO_ERR_INDEX;
+  if (word & kErrOffsets) return IKBO_ERR_OFFSETS;
+  if (word & kErrTimeout) return IKBO_ERR_TIMEOUT;
+  if (word & kErrLayout) return IKBO_ERR_CUDA;
+  return IKBO_OK;
+}
+
 int ikbo_attn_fwd_host(const void* q, const void* k_user, const void* v_user,
                        const int32_t* user_offsets, const int32_t* cand_to_user, int64_t n_cand,
                        int64_t n_user, int32_t H, int32_t Lq, int32_t D, float scale, void* out,
@@ -587,9 +602,21 @@ int ikbo_attn_fwd_host(const void* q, const void* k_user, const void* v_user,
     if (rc == IKBO_OK) e = cudaMemcpyAsync(out, buf + o_out, qbytes, cudaMemcpyDeviceToHost, st);
   }
   cudaFreeAsync(buf, st);
+  // the device error word comes back with the output, under the same
+  // synchronisation (a pinned word per device, one host call at a time)
+  std::lock_guard<std::mutex> lock(*ds->host_call);
+  if (e == cudaSuccess && rc == IKBO_OK)
+    e = cudaMemcpyAsync(ds->err_host, ds->err_word, sizeof(int), cudaMemcpyDeviceToHost, st);
   if (cudaStreamSynchronize(st) != cudaSuccess || e != cudaSuccess) return IKBO_ERR_CUDA;
   if (rc != IKBO_OK) return rc;
-  return ikbo_get_device_error(stream);
+  const int word = *ds->err_host;
+  if (word) {
+    // clear it, as ikbo_get_device_error does
+    if (cudaMemsetAsync(ds->err_word, 0, sizeof(int), st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+      return IKBO_ERR_CUDA;
+  }
+  return status_of_error_word(word);
 }
 
 int ikbo_broadcast_attn_fwd(const void* q, const void* k_user, const void* v_user,
@@ -964,11 +991,7 @@ int ikbo_get_device_error(ikbo_stream_t stream) {
   const int zero = 0;
   if (word && cudaMemcpyToSymbol(g_ikbo_error_word, &zero, sizeof zero) != cudaSuccess)
     return IKBO_ERR_CUDA;
-  if (word & kErrIndex) return IKBO_ERR_INDEX;
-  if (word & kErrOffsets) return IKBO_ERR_OFFSETS;
-  if (word & kErrTimeout) return IKBO_ERR_TIMEOUT;
-  if (word & kErrLayout) return IKBO_ERR_CUDA;
-  return IKBO_OK;
+  return status_of_error_word(word);
 }
 
 const char* ikbo_strerror(int status) {

@@ -86,6 +86,14 @@ def test_shapes(gpu_lib, M, K_user, K_cand, N):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("M", [700, 1100])
+def test_many_row_tiles(gpu_lib, M):
+    """Clusters of six CTAs (M = 700: six row tiles) and no cluster (M = 1100: nine)."""
+    cfg = W.LceConfig(name="mt", n_cand=5, n_user=2, M=M, K_user=16, K_cand=80, N=64, seed=M)
+    check(gpu_lib, W.lce_generate(cfg), f"M={M}")
+
+
+@pytest.mark.gpu
 def test_no_user_block(gpu_lib):
     cfg = W.LceConfig(name="nu", n_cand=6, n_user=2, M=50, K_user=0, K_cand=40, N=128, seed=4)
     wl = W.lce_generate(cfg)
