@@ -324,6 +324,168 @@ LCE_CONFIGS = {
 }
 
 
+# ---------------------------------------------------------------------------
+# Multi-level broadcast ("In-Kernel Broadcast Optimization", §5): a user sees
+# several ads vendors and every vendor offers several ads items, so two nested
+# broadcast relations with independent, uneven ratios.  The structure is drawn
+# top-down: vendors per user, then items per vendor, each 1 + a multinomial
+# with Dirichlet(1) weights (uneven, independent at the two levels).  The maps
+# the library takes are item_to_vendor and vendor_to_user; ``item_user`` is the
+# user of every item as drawn (the structure itself, not a composition of the
+# maps), which the oracle's own walk of the maps is checked against.
+
+def draw_hierarchy(n_item: int, n_vendor: int, n_user: int, seed: int, shuffle: bool = False):
+    """Returns (item_to_vendor, vendor_to_user, item_user, vendors_per_user, items_per_vendor).
+
+    Unshuffled, both maps are sorted (vendors grouped by user, items by vendor).
+    ``shuffle`` relabels the vendors and reorders the items with seeded permutations.
+    """
+    assert 1 <= n_user <= n_vendor <= n_item
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 0x4D4C])))
+    vpu = 1 + rng.multinomial(n_vendor - n_user, rng.dirichlet(np.ones(n_user)))
+    ipv = 1 + rng.multinomial(n_item - n_vendor, rng.dirichlet(np.ones(n_vendor)))
+    v2u = np.repeat(np.arange(n_user, dtype=np.int64), vpu)
+    i2v = np.repeat(np.arange(n_vendor, dtype=np.int64), ipv)
+    vstart = np.concatenate([[0], np.cumsum(vpu)])
+    items_of_user = np.array([ipv[vstart[u]:vstart[u + 1]].sum() for u in range(n_user)])
+    item_user = np.repeat(np.arange(n_user, dtype=np.int64), items_of_user)
+    if shuffle:
+        relabel = rng.permutation(n_vendor)          # vendor j becomes relabel[j]
+        v2u_new = np.empty_like(v2u)
+        v2u_new[relabel] = v2u
+        v2u, i2v = v2u_new, relabel[i2v]
+        order = rng.permutation(n_item)
+        i2v, item_user = i2v[order], item_user[order]
+    return (i2v.astype(np.int32), v2u.astype(np.int32), item_user.astype(np.int32),
+            vpu.astype(np.int64), ipv.astype(np.int64))
+
+
+@dataclass(frozen=True)
+class MlConfig:
+    """Target attention over a user -> vendor -> item hierarchy: every item is a candidate
+    with Lq query tokens; the keys and values are the user sequences (lengths uniform in
+    [len_lo, len_hi])."""
+    name: str
+    n_item: int
+    n_vendor: int
+    n_user: int
+    H: int
+    D: int
+    Lq: int
+    seed: int
+    len_lo: int
+    len_hi: int
+    std: float = 1.0
+    shuffle: bool = False
+    description: str = ""
+
+
+@dataclass
+class MlWorkload:
+    cfg: MlConfig
+    wl: Workload                 # items as candidates; wl.cand_to_user is ``item_user`` as drawn
+    item_to_vendor: np.ndarray   # int32 [n_item]
+    vendor_to_user: np.ndarray   # int32 [n_vendor]
+    vendors_per_user: np.ndarray = field(repr=False, default=None)
+    items_per_vendor: np.ndarray = field(repr=False, default=None)
+
+
+def ml_generate(cfg: MlConfig) -> MlWorkload:
+    """One seeded multi-level workload (q, k, v drawn as ``generate`` draws them)."""
+    i2v, v2u, item_user, vpu, ipv = draw_hierarchy(cfg.n_item, cfg.n_vendor, cfg.n_user, cfg.seed,
+                                                    cfg.shuffle)
+    counts = np.bincount(item_user, minlength=cfg.n_user)
+    base = Config(name=cfg.name, n_cand=cfg.n_item, n_user=cfg.n_user, H=cfg.H, D=cfg.D, Lq=cfg.Lq,
+                  seed=cfg.seed, std=cfg.std, counts=tuple(int(c) for c in counts), lens="uniform",
+                  len_lo=cfg.len_lo, len_hi=cfg.len_hi, description=cfg.description)
+    wl = generate(base)
+    wl.cand_to_user = item_user.copy()               # the drawn order (sorted unless shuffled)
+    return MlWorkload(cfg=cfg, wl=wl, item_to_vendor=i2v, vendor_to_user=v2u,
+                      vendors_per_user=vpu, items_per_vendor=ipv)
+
+
+@dataclass
+class LceMlConfig:
+    name: str
+    n_item: int
+    n_vendor: int
+    n_user: int
+    M: int
+    K_user: int
+    K_vendor: int
+    K_item: int
+    N: int
+    seed: int
+    shuffle: bool = False
+    description: str = ""
+
+
+@dataclass
+class LceMlWorkload:
+    cfg: LceMlConfig
+    W_user: np.ndarray        # bf16 bits [M, Ku8]
+    W_vendor: np.ndarray      # bf16 bits [M, Kv8]
+    W_item: np.ndarray        # bf16 bits [M, Ki8]
+    X_user: np.ndarray        # bf16 bits [n_user, Ku8, N]
+    X_vendor: np.ndarray      # bf16 bits [n_vendor, Kv8, N]
+    X_item: np.ndarray        # bf16 bits [n_item, Ki8, N]
+    item_to_vendor: np.ndarray
+    vendor_to_user: np.ndarray
+    item_user: np.ndarray = field(repr=False, default=None)
+
+
+def lce_ml_generate(cfg: LceMlConfig) -> LceMlWorkload:
+    """Linear compression over a user -> vendor -> item hierarchy: an item's K input
+    embeddings are its user's block, its vendor's block and its own, each zero-padded to a
+    multiple of 8; X ~ N(0, 1), W ~ N(0, (0.5 / sqrt(K))^2)."""
+    i2v, v2u, item_user, _, _ = draw_hierarchy(cfg.n_item, cfg.n_vendor, cfg.n_user, cfg.seed,
+                                               cfg.shuffle)
+    std_w = 0.5 / np.sqrt(max(cfg.K_user + cfg.K_vendor + cfg.K_item, 1))
+
+    def padded(tid, shape, pad_axis, valid, std):
+        x = _normal_bf16(cfg.seed, tid, shape, std).reshape(shape)
+        idx = [slice(None)] * len(shape)
+        idx[pad_axis] = slice(valid, None)
+        x[tuple(idx)] = 0
+        return x
+
+    ku, kv, ki = round_up8(cfg.K_user), round_up8(cfg.K_vendor), round_up8(cfg.K_item)
+    return LceMlWorkload(
+        cfg=cfg,
+        W_user=padded(30, (cfg.M, ku), 1, cfg.K_user, std_w),
+        W_vendor=padded(31, (cfg.M, kv), 1, cfg.K_vendor, std_w),
+        W_item=padded(32, (cfg.M, ki), 1, cfg.K_item, std_w),
+        X_user=padded(33, (cfg.n_user, ku, cfg.N), 1, cfg.K_user, 1.0),
+        X_vendor=padded(34, (cfg.n_vendor, kv, cfg.N), 1, cfg.K_vendor, 1.0),
+        X_item=padded(35, (cfg.n_item, ki, cfg.N), 1, cfg.K_item, 1.0),
+        item_to_vendor=i2v, vendor_to_user=v2u, item_user=item_user)
+
+
+ML_CONFIGS = {
+    "ml_tiny_12x5x2": MlConfig(name="ml_tiny_12x5x2", n_item=12, n_vendor=5, n_user=2, H=2, D=64,
+                               Lq=1, seed=50, len_lo=16, len_hi=40,
+                               description="12 items over 5 vendors over 2 users, L~U[16,40], "
+                                           "H=2 D=64 Lq=1"),
+    "ml_1024x60x15": MlConfig(name="ml_1024x60x15", n_item=1024, n_vendor=60, n_user=15, H=4,
+                              D=128, Lq=1, seed=51, len_lo=256, len_hi=1024,
+                              description="1024 items over 60 vendors over 15 users (uneven "
+                                          "ratios), L~U[256,1024], H=4 D=128 Lq=1"),
+}
+
+LCE_ML_CONFIGS = {
+    "lce_ml_tiny_12x5x2": LceMlConfig(name="lce_ml_tiny_12x5x2", n_item=12, n_vendor=5, n_user=2,
+                                      M=37, K_user=13, K_vendor=9, K_item=21, N=64, seed=52,
+                                      description="12 items over 5 vendors over 2 users, M=37, "
+                                                  "K=13+9+21 (padded 16+16+24), N=64"),
+    "lce_ml_1024x60x15": LceMlConfig(name="lce_ml_1024x60x15", n_item=1024, n_vendor=60,
+                                     n_user=15, M=433, K_user=1022, K_vendor=510, K_item=1022,
+                                     N=256, seed=53,
+                                     description="1024 items over 60 vendors over 15 users, "
+                                                 "M=433, K=1022+510+1022 (padded 1024+512+1024), "
+                                                 "N=256"),
+}
+
+
 CONFIGS = {
     "tiny_8x2": Config(
         name="tiny_8x2", n_cand=8, n_user=2, H=2, D=64, Lq=1, seed=0,

@@ -155,6 +155,23 @@ def lce(W_user, W_cand, X_user, X_cand, cand_to_user, cands=None) -> np.ndarray:
     return linear_compression.lce(W_user, W_cand, X_user, X_cand, cand_to_user, cands)
 
 
+def ml_attention(q, k, v, user_offsets, item_to_vendor, vendor_to_user, scale: float,
+                 items=None) -> np.ndarray:
+    """fp64 target attention over a user -> vendor -> item hierarchy (see
+    ``oracle/multi_level.py``)."""
+    from . import multi_level
+    return multi_level.attention(q, k, v, user_offsets, item_to_vendor, vendor_to_user, scale, items)
+
+
+def ml_lce(W_user, W_vendor, W_item, X_user, X_vendor, X_item, item_to_vendor, vendor_to_user,
+           items=None) -> np.ndarray:
+    """fp64 linear compression over a user -> vendor -> item hierarchy (see
+    ``oracle/multi_level.py``)."""
+    from . import multi_level
+    return multi_level.lce(W_user, W_vendor, W_item, X_user, X_vendor, X_item, item_to_vendor,
+                           vendor_to_user, items)
+
+
 def num_threads() -> int:
     """OpenMP threads the oracle runs on (OMP_NUM_THREADS, else all cores)."""
     return int(_load().ikbo_oracle_num_threads())

@@ -1,5 +1,6 @@
 """The seeded input generators: determinism, bf16 rounding and the configs' structure."""
 import numpy as np
+import pytest
 import torch
 
 from broadcast_target_attention_gb300 import workloads as W
@@ -56,3 +57,19 @@ def test_shuffled_mapping_is_a_permutation():
     wl = W.custom(n_user=3, counts=[4, 2, 5], lens=[3, 4, 5], H=1, D=8, Lq=1, shuffle=True, seed=3)
     assert sorted(wl.cand_to_user.tolist()) == [0] * 4 + [1] * 2 + [2] * 5
     assert np.any(np.diff(wl.cand_to_user) < 0)
+
+
+@pytest.mark.parametrize("shuffle", [False, True])
+def test_hierarchy_structure(shuffle):
+    """Every user has at least one vendor and every vendor at least one item; the maps are
+    in range, sorted unless shuffled, and the same seed gives the same draw."""
+    i2v, v2u, item_user, vpu, ipv = W.draw_hierarchy(1024, 60, 15, seed=51, shuffle=shuffle)
+    assert i2v.shape == (1024,) and v2u.shape == (60,) and item_user.shape == (1024,)
+    assert vpu.sum() == 60 and ipv.sum() == 1024 and vpu.min() >= 1 and ipv.min() >= 1
+    assert np.bincount(v2u, minlength=15).min() >= 1 and np.bincount(i2v, minlength=60).min() >= 1
+    assert 0 <= i2v.min() and i2v.max() < 60 and 0 <= v2u.min() and v2u.max() < 15
+    assert (np.all(np.diff(i2v) >= 0) and np.all(np.diff(v2u) >= 0)) != shuffle
+    again = W.draw_hierarchy(1024, 60, 15, seed=51, shuffle=shuffle)
+    assert all(np.array_equal(a, b) for a, b in zip((i2v, v2u, item_user, vpu, ipv), again))
+    # uneven at both levels
+    assert vpu.max() >= 2 * vpu.min() and ipv.max() >= 4 * ipv.min()
