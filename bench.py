@@ -700,6 +700,230 @@ def run_lce(args):
     print(json.dumps(line), flush=True)
 
 
+def _timed(fn, n, flush, dev):
+    """CUDA-event times (ms) of n calls of fn, L2 flushed before each."""
+    import torch
+    evs = []
+    for i in range(n):
+        flush.fill_(i & 0xFF)
+        s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s_.record()
+        fn()
+        e_.record()
+        evs.append((s_, e_))
+    torch.cuda.synchronize(dev)
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def _roofline(flops, alg_bytes, ms, kname, traffic=None):
+    pk = peaks()
+    ai = flops / alg_bytes
+    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    if ai < ridge:
+        gbs = alg_bytes / (ms * 1e-3) / 1e9
+        return {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": gbs / pk["hbm_gbs"], "traffic": traffic, "kernel": kname,
+                "alg_bytes_per_launch": alg_bytes, "peak_source": pk["source"] + " (burst copy)"}
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"bound": "tensor", "achieved": tf, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": tf / pk["bf16_tflops"], "traffic": traffic, "kernel": kname,
+            "flops_per_launch": flops, "peak_source": pk["source"] + " (burst cuBLAS bf16)"}
+
+
+def run_ml(args):
+    """Target attention over a user -> vendor -> item hierarchy ("In-Kernel Broadcast
+    Optimization", §5): the library walks item_to_vendor and vendor_to_user itself; timed
+    beside the two-level call given the per-item user map."""
+    import torch
+
+    import broadcast_target_attention_gb300 as ikbo
+
+    ws, rank, local = R.dist_env()
+    if ws > 1:
+        raise SystemExit("--ml measures one GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ikbo.load()
+    m = W.ml_generate(W.ML_CONFIGS[args.ml])
+    wl, c = m.wl, m.cfg
+    nums = A.workload_numbers(wl)
+    flops = nums["flops"]
+    alg_bytes = nums["alg_bytes"] + 4 * c.n_vendor     # the vendor map as well
+
+    def t(a, dt):
+        return torch.from_numpy(np.ascontiguousarray(a)).view(dt).to(dev)
+
+    q, k, v = (t(x.view(np.int16), torch.bfloat16) for x in (wl.q, wl.k, wl.v))
+    off = t(wl.user_offsets, torch.int32)
+    i2v, v2u = t(m.item_to_vendor, torch.int32), t(m.vendor_to_user, torch.int32)
+    item_user = t(wl.cand_to_user, torch.int32)
+    out = torch.empty_like(q)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.int32, device=dev)
+
+    def ml_step():
+        ikbo.ml_attn_fwd(q, k, v, off, i2v, v2u, wl.scale, out=out)
+
+    def two_level_step():
+        ikbo.attn_fwd(q, k, v, off, item_user, wl.scale, out=out)
+
+    with ClockSampler(local) as clk:
+        for _ in range(args.warmup):
+            flush.fill_(1)
+            ml_step()
+            two_level_step()
+        assert ikbo.get_device_error() == 0
+        torch.cuda.synchronize(dev)
+        clk.mark_start()
+        ms_list = _timed(ml_step, args.steps, flush, dev)
+        clk.mark_end()
+        two_ms = _timed(two_level_step, args.steps, flush, dev)
+        ikbo.set_timing(True)
+        kern = []
+        for i in range(min(args.steps, 50)):
+            flush.fill_(i & 0xFF)
+            ml_step()
+            kern.append(ikbo.get_timing()[1])
+        ikbo.set_timing(False)
+        hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
+        hoff, hi2v, hv2u = (x.cpu().pin_memory() for x in (off, i2v, v2u))
+        hout = torch.empty_like(hq).pin_memory()
+
+        def e2e_step():
+            d = [x.to(dev, non_blocking=True) for x in (hq, hk, hv, hoff, hi2v, hv2u)]
+            o = ikbo.ml_attn_fwd(*d, wl.scale)
+            hout.copy_(o, non_blocking=True)
+            torch.cuda.synchronize(dev)
+
+        for _ in range(3):
+            e2e_step()
+        e2e_ms = []
+        for _ in range(min(args.steps, 50)):
+            t0 = time.perf_counter()
+            e2e_step()
+            e2e_ms.append((time.perf_counter() - t0) * 1e3)
+    assert ikbo.get_device_error() == 0
+    ms = statistics.mean(ms_list)
+    kms = statistics.mean(kern)
+    kname = f"{ikbo.KERNEL_NAMES[ikbo.selected_kernel(wl.n_cand, wl.n_user, c.H, c.Lq)]}<{c.D}>"
+    h2d = sum(x.nbytes for x in (wl.q, wl.k, wl.v, wl.user_offsets, m.item_to_vendor, m.vendor_to_user))
+    e2e = statistics.mean(e2e_ms)
+    line = {
+        "metric": METRIC + " -- user -> vendor -> item hierarchy", "value": flops / (ms * 1e-3) / 1e12,
+        "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": config_block(wl, {"workload": f"{c.name}: {c.description}", "n_item": c.n_item,
+                                    "n_vendor": c.n_vendor}),
+        "kernel_ms": {"attn": kms},
+        "roofline": _roofline(flops, alg_bytes, kms, kname),
+        "two_level_call": {"ms_per_step": statistics.mean(two_ms),
+                           "what": "ikbo_attn_fwd given the per-item user map (walked by the caller)"},
+        "e2e": {"value": flops / (e2e * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": wl.q.nbytes, "ms_per_step": e2e},
+        "gpu_launches": ikbo.launches_per_call(wl.n_cand, wl.n_user) * args.steps,
+        "clocks": clk.summary(),
+        "cpu_baseline": None,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ml_lce(args):
+    """Linear compression over a user -> vendor -> item hierarchy: one launch per level, each
+    level's product once per entry of that level; timed beside the broadcast form (both
+    blocks copied to every item, then one batched product through torch / cuBLAS)."""
+    import torch
+
+    import broadcast_target_attention_gb300 as ikbo
+
+    ws, rank, local = R.dist_env()
+    if ws > 1:
+        raise SystemExit("--lce-ml measures one GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ikbo.load()
+    l = W.lce_ml_generate(W.LCE_ML_CONFIGS[args.lce_ml])
+    c = l.cfg
+    ku, kv, ki = l.X_user.shape[1], l.X_vendor.shape[1], l.X_item.shape[1]
+    flops = 2 * c.M * c.N * (c.n_user * c.K_user + c.n_vendor * c.K_vendor + c.n_item * c.K_item)
+    # reads of W and X once per level, the fp32 terms written once and read once per level,
+    # the bf16 output, the maps
+    alg_bytes = 2 * (c.M * (ku + kv + ki) + c.n_user * ku * c.N + c.n_vendor * kv * c.N
+                     + c.n_item * ki * c.N + c.n_item * c.M * c.N) \
+        + 2 * 4 * (c.n_user + c.n_vendor) * c.M * c.N + 4 * (c.n_item + c.n_vendor)
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    Wu, Wv, Wi, Xu, Xv, Xi = (bf(x) for x in (l.W_user, l.W_vendor, l.W_item, l.X_user, l.X_vendor,
+                                              l.X_item))
+    i2v, v2u = (torch.from_numpy(x).to(dev) for x in (l.item_to_vendor, l.vendor_to_user))
+    item_user = torch.from_numpy(l.item_user).to(dev).long()
+    out = torch.empty((c.n_item, c.M, c.N), dtype=torch.bfloat16, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.int32, device=dev)
+    Wfull = torch.cat([Wu, Wv, Wi], dim=1)
+
+    def ikbo_step():
+        ikbo.ml_lce_fwd(Wu, Wv, Wi, Xu, Xv, Xi, i2v, v2u, out=out)
+
+    def broadcast_step():
+        X = torch.cat([Xu[item_user], Xv[i2v.long()], Xi], dim=1)   # the materialised broadcast
+        return torch.matmul(Wfull, X)
+
+    with ClockSampler(local) as clk:
+        for _ in range(args.warmup):
+            flush.fill_(1)
+            ikbo_step()
+            broadcast_step()
+        assert ikbo.get_device_error() == 0
+        torch.cuda.synchronize(dev)
+        clk.mark_start()
+        ms_list = _timed(ikbo_step, args.steps, flush, dev)
+        clk.mark_end()
+        bc_list = _timed(broadcast_step, min(args.steps, 20), flush, dev)
+        host = [x.cpu().pin_memory() for x in (Wu, Wv, Wi, Xu, Xv, Xi, i2v, v2u)]
+        hout = torch.empty_like(out, device="cpu").pin_memory()
+
+        def e2e_step():
+            d = [x.to(dev, non_blocking=True) for x in host]
+            o = ikbo.ml_lce_fwd(*d)
+            hout.copy_(o, non_blocking=True)
+            torch.cuda.synchronize(dev)
+
+        for _ in range(3):
+            e2e_step()
+        e2e_ms = []
+        for _ in range(min(args.steps, 20)):
+            t0 = time.perf_counter()
+            e2e_step()
+            e2e_ms.append((time.perf_counter() - t0) * 1e3)
+    assert ikbo.get_device_error() == 0
+    ms = statistics.mean(ms_list)
+    bc = statistics.mean(bc_list)
+    tf = flops / (ms * 1e-3) / 1e12
+    h2d = sum(x.nbytes for x in (l.W_user, l.W_vendor, l.W_item, l.X_user, l.X_vendor, l.X_item,
+                                 l.item_to_vendor, l.vendor_to_user))
+    e2e = statistics.mean(e2e_ms)
+    line = {
+        "metric": "IKBO linear compression BF16 TFLOP/s (decomposed work) -- user -> vendor -> item",
+        "value": tf, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{c.name}: {c.description}", "n_item": c.n_item,
+                   "n_vendor": c.n_vendor, "n_user": c.n_user, "M": c.M, "K_user": c.K_user,
+                   "K_vendor": c.K_vendor, "K_item": c.K_item, "N": c.N,
+                   "l2": "flushed before every timed step (write of 2x L2 size)",
+                   "ai_flop_per_byte": flops / alg_bytes},
+        "roofline": _roofline(flops, alg_bytes, ms, f"ikbo_lce_kernel<{c.N // 64}>"),
+        "broadcast_path": {"ms_per_step": bc, "ikbo_speedup": bc / ms,
+                           "what": "torch: X = cat(X_user[u], X_vendor[v], X_item); matmul(W, X)"},
+        "e2e": {"value": flops / (e2e * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": int(out.numel() * 2), "ms_per_step": e2e},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk.summary(),
+        "cpu_baseline": None,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -713,6 +937,10 @@ def main():
                     help="measure IKBO linear compression on this workload instead")
     ap.add_argument("--with-self", action="store_true",
                     help="measure the fused self + target attention of the workload instead")
+    ap.add_argument("--ml", default=None, choices=sorted(W.ML_CONFIGS),
+                    help="measure target attention over a user -> vendor -> item hierarchy")
+    ap.add_argument("--lce-ml", default=None, choices=sorted(W.LCE_ML_CONFIGS),
+                    help="measure linear compression over a user -> vendor -> item hierarchy")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -722,6 +950,10 @@ def main():
         run_lce(args)
     elif args.with_self:
         run_fused(args)
+    elif args.ml:
+        run_ml(args)
+    elif args.lce_ml:
+        run_ml_lce(args)
     else:
         run_ikbo(args)
 

@@ -96,6 +96,31 @@ def attn_fwd(q, k, v, user_offsets, cand_to_user, scale: Optional[float] = None,
     return out
 
 
+def ml_attn_fwd(q, k, v, user_offsets, item_to_vendor, vendor_to_user,
+                scale: Optional[float] = None, out=None, stream=None):
+    """Target attention over a user -> vendor -> item hierarchy (device tensors): item i
+    attends to the sequence of user ``vendor_to_user[item_to_vendor[i]]``; returns ``out``.
+    See ``ikbo_ml_attn_fwd`` in include/ikbo.h."""
+    import torch
+    _validate(q, k, v, user_offsets, item_to_vendor, device=True)
+    if (vendor_to_user.dtype != torch.int32 or not vendor_to_user.is_contiguous()
+            or not vendor_to_user.is_cuda):
+        raise ValueError("vendor_to_user must be a contiguous int32 CUDA tensor")
+    n_item, H, Lq, D = _shape(q, k)
+    n_user = int(user_offsets.shape[0]) - 1
+    n_vendor = int(vendor_to_user.shape[0])
+    if scale is None:
+        scale = D ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    rc = _lib.lib().ikbo_ml_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(user_offsets),
+                                     _ptr(item_to_vendor), _ptr(vendor_to_user), n_item, n_vendor,
+                                     n_user, H, Lq, D, float(scale), _ptr(out),
+                                     _stream_handle(stream))
+    _check(rc, "ikbo_ml_attn_fwd")
+    return out
+
+
 def fused_attn_fwd(q, q_user, k, v, user_offsets, cand_to_user, scale: Optional[float] = None,
                    out=None, out_user=None, stream=None):
     """Target attention of the candidates and self-attention of the user sequence in one
@@ -151,6 +176,41 @@ def lce_fwd(W_user, W_cand, X_user, X_cand, cand_to_user, out=None, stream=None)
     rc = _lib.lib().ikbo_lce_fwd(p(W_user), p(W_cand), p(X_user), p(X_cand), p(cand_to_user), n_cand,
                                  n_user, M, K_user, K_cand, N, p(out), _stream_handle(stream))
     _check(rc, "ikbo_lce_fwd")
+    return out
+
+
+def ml_lce_fwd(W_user, W_vendor, W_item, X_user, X_vendor, X_item, item_to_vendor,
+               vendor_to_user, out=None, stream=None):
+    """Linear compression over a user -> vendor -> item hierarchy on device tensors (see
+    ``ikbo_ml_lce_fwd`` in include/ikbo.h): ``out[i] = W_user @ X_user[u] + W_vendor @
+    X_vendor[v] + W_item @ X_item[i]`` with ``v = item_to_vendor[i]``, ``u =
+    vendor_to_user[v]``; returns ``out``.  A block with K = 0 is left out."""
+    import torch
+    for name, t in (("W_user", W_user), ("W_vendor", W_vendor), ("W_item", W_item),
+                    ("X_user", X_user), ("X_vendor", X_vendor), ("X_item", X_item)):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
+    for name, t in (("item_to_vendor", item_to_vendor), ("vendor_to_user", vendor_to_user)):
+        if t.dtype != torch.int32 or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError(f"{name} must be a contiguous int32 CUDA tensor")
+    n_item, K_item, N = (int(x) for x in X_item.shape)
+    n_vendor, K_vendor = int(X_vendor.shape[0]), int(X_vendor.shape[1])
+    n_user, K_user = int(X_user.shape[0]), int(X_user.shape[1])
+    M = int(W_item.shape[0])
+    if (W_item.shape != (M, K_item) or W_vendor.shape != (M, K_vendor) or W_user.shape != (M, K_user)
+            or X_vendor.shape[2] != N or X_user.shape[2] != N
+            or tuple(item_to_vendor.shape) != (n_item,) or tuple(vendor_to_user.shape) != (n_vendor,)):
+        raise ValueError("shapes: W_* [M, K_*], X_user [n_user, K_user, N], X_vendor [n_vendor, "
+                         "K_vendor, N], X_item [n_item, K_item, N], item_to_vendor [n_item], "
+                         "vendor_to_user [n_vendor]")
+    if out is None:
+        out = torch.empty((n_item, M, N), dtype=torch.bfloat16, device=X_item.device)
+    p = lambda t: _ptr(t) if t.numel() else None
+    rc = _lib.lib().ikbo_ml_lce_fwd(p(W_user), p(W_vendor), p(W_item), p(X_user), p(X_vendor),
+                                    p(X_item), p(item_to_vendor), p(vendor_to_user), n_item,
+                                    n_vendor, n_user, M, K_user, K_vendor, K_item, N, p(out),
+                                    _stream_handle(stream))
+    _check(rc, "ikbo_ml_lce_fwd")
     return out
 
 

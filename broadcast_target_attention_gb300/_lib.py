@@ -40,6 +40,10 @@ SIGNATURES = {
     "ikbo_selected_kernel": (ctypes.c_int, [_I64, _I64, ctypes.c_int32, ctypes.c_int32]),
     "ikbo_fused_attn_fwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _I32,
                                             _I32, _F, _P, _P, _P]),
+    "ikbo_ml_attn_fwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _I32, _I32,
+                                         _F, _P, _P]),
+    "ikbo_ml_lce_fwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _I32,
+                                        _I32, _I32, _I32, _P, _P]),
     "ikbo_lce_fwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I32, _I32, _I32, _I32, _P, _P]),
     "ikbo_attn_fwd_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I32, _I32, _I32, _F,
                                               _P, _P]),

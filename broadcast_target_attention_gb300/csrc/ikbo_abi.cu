@@ -147,7 +147,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Layout of the per-call scratch space.
 struct Workspace {
   size_t header, kmap, vmap, items, units, perm, cand_start, scratch, partial_o, partial_ml,
-      cta_items, map_slots, total;
+      cta_items, map_slots, item_user, total;
   int max_items, max_split_items, max_units, max_cta_items, grid;
   int kernel;   // kKernSimt, kKernTc or kKernPp
   bool fused;
@@ -184,8 +184,10 @@ int effective_kernel(int64_t n_cand, int64_t n_user, int H, int Lq) {
 // kernel, may split).
 // extra_units: further work items the in-kernel planning may make (the
 // self-attention tiles of a fused call).
+// multi_level: a user -> vendor -> item call; when the planning kernel plans
+// it, it writes every item's user to item_user first.
 Workspace plan_workspace(int64_t n_cand, int64_t n_user, int H, int Lq, int D, int num_sms,
-                         int grid, int kernel, int64_t extra_units = 0) {
+                         int grid, int kernel, int64_t extra_units = 0, bool multi_level = false) {
   Workspace w = {};
   const int cpt = cands_per_tile(Lq);
   const int64_t units_bound =
@@ -216,6 +218,7 @@ Workspace plan_workspace(int64_t n_cand, int64_t n_user, int H, int Lq, int D, i
     w.units = take(sizeof(UnitInfo) * size_t(w.max_units > 0 ? w.max_units : 1));
     w.cand_start = take(sizeof(int32_t) * size_t(n_user + 1));
     w.scratch = take(sizeof(int32_t) * size_t(3 * n_user + 2));
+    if (multi_level) w.item_user = take(sizeof(int32_t) * size_t(n_cand));
     if (w.max_split_items) {
       w.partial_o = take(sizeof(float) * size_t(w.max_split_items) * kTileM * D);
       w.partial_ml = take(sizeof(float2) * size_t(w.max_split_items) * kTileM);
@@ -365,11 +368,17 @@ struct SelfPart {
   int64_t T;
 };
 
+// The vendor level of a multi-level call: c2u then holds item_to_vendor.
+struct VendorLevel {
+  const int32_t* vendor_to_user;
+  int64_t n_vendor;
+};
+
 // Plan + attention on device buffers, scratch from `ws` (>= plan_workspace().total).
 int run_ikbo(DeviceState* ds, const void* q, const void* k, const void* v, const int32_t* off,
              const int32_t* c2u, int64_t n_cand, int64_t n_user, int H, int Lq, int D, float scale,
              void* out, char* ws, const Workspace& L, cudaStream_t st,
-             const SelfPart* self = nullptr) {
+             const SelfPart* self = nullptr, const VendorLevel* vendor = nullptr) {
   const int kernel = L.kernel;
   PlanParams pp = {};
   pp.cand_to_user = c2u;
@@ -391,6 +400,11 @@ int run_ikbo(DeviceState* ds, const void* q, const void* k, const void* v, const
   pp.cand_start = reinterpret_cast<int32_t*>(ws + L.cand_start);
   pp.scratch = reinterpret_cast<int32_t*>(ws + L.scratch);
   pp.err_word = ds->err_word;
+  if (vendor) {
+    pp.vendor_to_user = vendor->vendor_to_user;
+    pp.n_vendor = vendor->n_vendor;
+    pp.item_user = reinterpret_cast<int32_t*>(ws + L.item_user);
+  }
 
   PlanExtra px;
   std::memset(&px, 0, sizeof px);
@@ -458,6 +472,10 @@ int run_ikbo(DeviceState* ds, const void* q, const void* k, const void* v, const
     ap.total_rows = self->T;
     ap.exact_rows = 1;
   }
+  if (vendor) {
+    ap.vendor_to_user = vendor->vendor_to_user;
+    ap.n_vendor = vendor->n_vendor;
+  }
 
   const bool timed = g_timing;
   if (timed) cudaEventRecord(ds->ev[0], st);
@@ -499,7 +517,7 @@ int run_ikbo(DeviceState* ds, const void* q, const void* k, const void* v, const
 // self_T >= 0: a fused self + target call over T sequence rows, which the
 // one-tile tcgen05 kernel runs (planning in-kernel).
 int call_workspace(DeviceState* ds, int64_t n_cand, int64_t n_user, int H, int Lq, int D,
-                   Workspace* out, int64_t self_T = -1) {
+                   Workspace* out, int64_t self_T = -1, bool multi_level = false) {
   int grid = 0;
   const int kernel = self_T >= 0 ? kKernTc : effective_kernel(n_cand, n_user, H, Lq);
   if (kernel == kKernTc) {
@@ -512,7 +530,7 @@ int call_workspace(DeviceState* ds, int64_t n_cand, int64_t n_user, int H, int L
   // a self-attention tile per 128 rows of every user, at most T / 128 + n_user per head
   const int64_t extra = self_T > 0 ? int64_t(H) * ((self_T + kTileM - 1) / kTileM + n_user) : 0;
   *out = plan_workspace(n_cand, n_user, H, Lq, D, ds->num_sms, grid > 0 ? grid : ds->num_sms,
-                        kernel, extra);
+                        kernel, extra, multi_level);
   return IKBO_OK;
 }
 
@@ -795,6 +813,33 @@ int ikbo_fused_attn_fwd(const void* q, const void* q_user, const void* k_user, c
   return rc;
 }
 
+int ikbo_ml_attn_fwd(const void* q, const void* k_user, const void* v_user,
+                     const int32_t* user_offsets, const int32_t* item_to_vendor,
+                     const int32_t* vendor_to_user, int64_t n_item, int64_t n_vendor,
+                     int64_t n_user, int32_t H, int32_t Lq, int32_t D, float scale, void* out,
+                     ikbo_stream_t stream) {
+  if (n_vendor < 0 || n_vendor >= (int64_t(1) << 31)) return IKBO_ERR_SHAPE;
+  int rc = check_args(q, k_user, v_user, user_offsets, item_to_vendor, n_item, n_user, H, Lq, D,
+                      scale, out);
+  if (rc != IKBO_OK || n_item == 0) return rc;
+  if (!vendor_to_user) return IKBO_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(vendor_to_user) & 3u) return IKBO_ERR_ALIGN;
+  if (n_vendor == 0) return IKBO_ERR_INDEX;   // every item would name a vendor outside [0, 0)
+  DeviceState* ds = nullptr;
+  if ((rc = device_state(&ds)) != IKBO_OK) return rc;
+  if (g_timing && (rc = ensure_events(ds)) != IKBO_OK) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  Workspace L;
+  if ((rc = call_workspace(ds, n_item, n_user, H, Lq, D, &L, -1, true)) != IKBO_OK) return rc;
+  void* ws = nullptr;
+  if (cudaMallocAsync(&ws, L.total, st) != cudaSuccess) return IKBO_ERR_CUDA;
+  const VendorLevel vendor{vendor_to_user, n_vendor};
+  rc = run_ikbo(ds, q, k_user, v_user, user_offsets, item_to_vendor, n_item, n_user, H, Lq, D,
+                scale, out, static_cast<char*>(ws), L, st, nullptr, &vendor);
+  if (cudaFreeAsync(ws, st) != cudaSuccess && rc == IKBO_OK) rc = IKBO_ERR_CUDA;
+  return rc;
+}
+
 }  // extern "C"
 
 namespace ikbo {
@@ -932,14 +977,8 @@ int ikbo_lce_fwd(const void* W_user, const void* W_cand, const void* X_user, con
       return IKBO_ERR_CUDA;
   }
   LceParams lp = {};
-  lp.cand_to_user = cand_to_user;
-  lp.Y = Y;
-  lp.Y_out = Y;
-  lp.out = static_cast<uint16_t*>(out);
-  lp.n_user = n_user;
   lp.M = M;
   lp.N = N;
-  lp.add_user = user_part ? 1 : 0;
   lp.err_word = ds->err_word;
   lp.timeout_ns = g_timeout_ns;
   // the row tiles of one batch entry share its X tiles through a cluster
@@ -956,7 +995,9 @@ int ikbo_lce_fwd(const void* W_user, const void* W_cand, const void* X_user, con
     l0.W = static_cast<const uint16_t*>(W_user);
     l0.n_batch = n_user;
     l0.K = K_user;
-    l0.stage = 0;
+    l0.out_f32 = 1;
+    l0.Y_out = Y;
+    l0.has_dependent = 1;
     e = launch_lce_nb(ds, NB, l0, wu_map, xu_map, false, st);
   }
   if (timed) cudaEventRecord(ds->ev[1], st);
@@ -965,7 +1006,11 @@ int ikbo_lce_fwd(const void* W_user, const void* W_cand, const void* X_user, con
     l1.W = static_cast<const uint16_t*>(W_cand);
     l1.n_batch = n_cand;
     l1.K = K_cand;
-    l1.stage = 1;
+    l1.out = static_cast<uint16_t*>(out);
+    l1.add = user_part ? 1 : 0;
+    l1.map = cand_to_user;
+    l1.n_map = n_user;
+    l1.Y = Y;
     // a programmatic dependent of the user stage: its epilogue waits for Y
     e = launch_lce_nb(ds, NB, l1, wc_map, xc_map, user_part, st);
   }
@@ -976,6 +1021,147 @@ int ikbo_lce_fwd(const void* W_user, const void* W_cand, const void* X_user, con
     g_timing_dev = dev;
   }
   if (Y) cudaFreeAsync(Y, st);
+  return e == cudaSuccess ? IKBO_OK : cuda_fail(e);
+}
+
+int ikbo_ml_lce_fwd(const void* W_user, const void* W_vendor, const void* W_item,
+                    const void* X_user, const void* X_vendor, const void* X_item,
+                    const int32_t* item_to_vendor, const int32_t* vendor_to_user, int64_t n_item,
+                    int64_t n_vendor, int64_t n_user, int32_t M, int32_t K_user, int32_t K_vendor,
+                    int32_t K_item, int32_t N, void* out, ikbo_stream_t stream) {
+  if (n_item < 0 || n_vendor < 0 || n_user < 0 || M < 1 || K_user < 0 || K_vendor < 0 ||
+      K_item < 8 || (K_user % 8) || (K_vendor % 8) || (K_item % 8) || N < 64 || N > 256 || (N % 64))
+    return IKBO_ERR_SHAPE;
+  if (n_item >= (int64_t(1) << 31) || n_vendor >= (int64_t(1) << 31) ||
+      n_user >= (int64_t(1) << 31) || M >= (1 << 24) || K_user >= (1 << 24) ||
+      K_vendor >= (1 << 24) || K_item >= (1 << 24))
+    return IKBO_ERR_SHAPE;
+  if (n_item == 0) return IKBO_OK;
+  const bool has_u = K_user > 0, has_v = K_vendor > 0;
+  if (!W_item || !X_item || !out || (has_u && (!W_user || !X_user || !vendor_to_user)) ||
+      (has_v && (!W_vendor || !X_vendor)) || ((has_u || has_v) && !item_to_vendor))
+    return IKBO_ERR_NULL;
+  if ((has_u || has_v) && n_vendor == 0) return IKBO_ERR_INDEX;
+  if (has_u && n_user == 0) return IKBO_ERR_INDEX;
+  auto a4 = [](const void* x) { return (reinterpret_cast<uintptr_t>(x) & 3u) == 0; };
+  if (!aligned16(W_item) || !aligned16(X_item) || !aligned16(out) ||
+      (has_u && (!aligned16(W_user) || !aligned16(X_user) || !a4(vendor_to_user))) ||
+      (has_v && (!aligned16(W_vendor) || !aligned16(X_vendor))) ||
+      ((has_u || has_v) && !a4(item_to_vendor)))
+    return IKBO_ERR_ALIGN;
+  {
+    const uintptr_t ob = reinterpret_cast<uintptr_t>(out), oe = ob + uintptr_t(n_item) * M * N * 2;
+    auto overlaps = [&](bool used, const void* x, uintptr_t bytes) {
+      const uintptr_t xb = reinterpret_cast<uintptr_t>(x);
+      return used && x && xb < oe && ob < xb + bytes;
+    };
+    if (overlaps(true, W_item, uintptr_t(M) * K_item * 2) ||
+        overlaps(true, X_item, uintptr_t(n_item) * K_item * N * 2) ||
+        overlaps(has_u, W_user, uintptr_t(M) * K_user * 2) ||
+        overlaps(has_u, X_user, uintptr_t(n_user) * K_user * N * 2) ||
+        overlaps(has_v, W_vendor, uintptr_t(M) * K_vendor * 2) ||
+        overlaps(has_v, X_vendor, uintptr_t(n_vendor) * K_vendor * N * 2) ||
+        overlaps(has_u || has_v, item_to_vendor, uintptr_t(n_item) * 4) ||
+        overlaps(has_u, vendor_to_user, uintptr_t(n_vendor) * 4))
+      return IKBO_ERR_ALIAS;
+  }
+  DeviceState* ds = nullptr;
+  int rc = device_state(&ds);
+  if (rc != IKBO_OK) return rc;
+  if (g_timing && (rc = ensure_events(ds)) != IKBO_OK) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int NB = N / 64;
+  const int mt = (M + kTileM - 1) / kTileM;
+  CUtensorMap wi_map, xi_map, wv_map, xv_map, wu_map, xu_map;
+  std::memset(&wv_map, 0, sizeof wv_map);
+  std::memset(&xv_map, 0, sizeof xv_map);
+  std::memset(&wu_map, 0, sizeof wu_map);
+  std::memset(&xu_map, 0, sizeof xu_map);
+  if (encode_lce_w_map(&wi_map, W_item, M, K_item) != IKBO_OK ||
+      encode_lce_x_map(&xi_map, X_item, n_item, K_item, N) != IKBO_OK ||
+      (has_v && (encode_lce_w_map(&wv_map, W_vendor, M, K_vendor) != IKBO_OK ||
+                 encode_lce_x_map(&xv_map, X_vendor, n_vendor, K_vendor, N) != IKBO_OK)) ||
+      (has_u && (encode_lce_w_map(&wu_map, W_user, M, K_user) != IKBO_OK ||
+                 encode_lce_x_map(&xu_map, X_user, n_user, K_user, N) != IKBO_OK)))
+    return IKBO_ERR_CUDA;
+  // fp32 terms of the user and vendor levels, library-owned, freed in stream order
+  float* Yu = nullptr;
+  float* Yv = nullptr;
+  if (has_u && cudaMallocAsync(reinterpret_cast<void**>(&Yu), size_t(n_user) * M * N * 4, st) !=
+                   cudaSuccess)
+    return IKBO_ERR_CUDA;
+  if (has_v && cudaMallocAsync(reinterpret_cast<void**>(&Yv), size_t(n_vendor) * M * N * 4, st) !=
+                   cudaSuccess) {
+    if (Yu) cudaFreeAsync(Yu, st);
+    return IKBO_ERR_CUDA;
+  }
+  LceParams lp = {};
+  lp.M = M;
+  lp.N = N;
+  lp.err_word = ds->err_word;
+  lp.timeout_ns = g_timeout_ns;
+  lp.cluster_n = (mt > 1 && mt <= 8) ? mt : 1;
+  cudaError_t e = cudaSuccess;
+  if (g_timing) cudaEventRecord(ds->ev[0], st);
+  if (has_u) {
+    // users: Y_user[u] = W_user @ X_user[u]
+    LceParams l = lp;
+    l.W = static_cast<const uint16_t*>(W_user);
+    l.n_batch = n_user;
+    l.K = K_user;
+    l.out_f32 = 1;
+    l.Y_out = Yu;
+    l.has_dependent = 1;
+    e = launch_lce_nb(ds, NB, l, wu_map, xu_map, false, st);
+  }
+  if (g_timing) cudaEventRecord(ds->ev[1], st);
+  if (e == cudaSuccess && has_v) {
+    // vendors: Y_vendor[v] = W_vendor @ X_vendor[v] + Y_user[vendor_to_user[v]]
+    LceParams l = lp;
+    l.W = static_cast<const uint16_t*>(W_vendor);
+    l.n_batch = n_vendor;
+    l.K = K_vendor;
+    l.out_f32 = 1;
+    l.Y_out = Yv;
+    l.has_dependent = 1;
+    if (has_u) {
+      l.add = 1;
+      l.map = vendor_to_user;
+      l.n_map = n_user;
+      l.Y = Yu;
+    }
+    e = launch_lce_nb(ds, NB, l, wv_map, xv_map, has_u, st);
+  }
+  if (e == cudaSuccess) {
+    // items: out[i] = W_item @ X_item[i] + the terms above, through item_to_vendor
+    LceParams l = lp;
+    l.W = static_cast<const uint16_t*>(W_item);
+    l.n_batch = n_item;
+    l.K = K_item;
+    l.out = static_cast<uint16_t*>(out);
+    if (has_u || has_v) {
+      l.add = 1;
+      l.map = item_to_vendor;
+      l.n_map = n_vendor;
+      l.Y = has_v ? Yv : Yu;
+      if (has_u) {
+        // with a vendor block, vendor_to_user is only checked here (the vendor
+        // level has added the user term); without one, it finds the user's row
+        l.map2 = vendor_to_user;
+        l.n_map2 = n_user;
+        l.y_via_map2 = has_v ? 0 : 1;
+      }
+    }
+    e = launch_lce_nb(ds, NB, l, wi_map, xi_map, has_u || has_v, st);
+  }
+  if (g_timing) {
+    cudaEventRecord(ds->ev[2], st);
+    int dev = 0;
+    cudaGetDevice(&dev);
+    g_timing_dev = dev;
+  }
+  if (Yv) cudaFreeAsync(Yv, st);
+  if (Yu) cudaFreeAsync(Yu, st);
   return e == cudaSuccess ? IKBO_OK : cuda_fail(e);
 }
 

@@ -361,6 +361,13 @@ __device__ __forceinline__ void plan_load(const AttnParams& p, uint8_t* scratch)
       const int c = base + i * blockDim.x + threadIdx.x;
       v[i] = c < n_cand ? p.cand_to_user[c] : 0;
     }
+    if (p.vendor_to_user) {
+      // a multi-level call: the loaded values are vendors; an out-of-range
+      // one becomes -1, which the validation reports as a bad index
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        v[i] = (v[i] >= 0 && int64_t(v[i]) < p.n_vendor) ? p.vendor_to_user[v[i]] : -1;
+    }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int c = base + i * blockDim.x + threadIdx.x;

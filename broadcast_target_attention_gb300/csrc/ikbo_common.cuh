@@ -76,6 +76,12 @@ struct PlanParams {
   int32_t* cand_start;      // [n_user + 1] first grouped position of each user
   int32_t* scratch;         // [3 * n_user + 2] per-user counters, order and prefixes
   int* err_word;            // per-device error word
+  // multi-level call: cand_to_user holds item_to_vendor; the planner first writes every
+  // item's user, vendor_to_user[item_to_vendor[i]] (or -1 when a value is out of range),
+  // to item_user [n_cand] and plans from that
+  const int32_t* vendor_to_user;
+  int64_t n_vendor;
+  int32_t* item_user;
 };
 
 // Parameters shared by the attention kernels (host -> device).
@@ -117,6 +123,10 @@ struct AttnParams {
   uint16_t* out_user;       // bf16 [T, H, D]
   int64_t total_rows;       // T as the caller gave it; user_offsets[n_user] must equal it
   int32_t exact_rows;       // 1: the K/V maps were encoded with the row count T (no tail copy)
+  // multi-level call (user -> vendor -> item): cand_to_user holds item_to_vendor and an
+  // item's user is vendor_to_user[item_to_vendor[i]], looked up while planning; null otherwise
+  const int32_t* vendor_to_user;
+  int64_t n_vendor;
 };
 
 // In-kernel timeline tracing (ikbo_set_trace): the first kTraceItems items of

@@ -14,6 +14,12 @@
 //   stage 1  out[b] = W_cand @ X_cand[b] + Y[u(b)]: the broadcast add is fused
 //            into the epilogue (§2.3), which finds Y through cand_to_user, so
 //            no broadcast tensor is ever written.
+// A user -> vendor -> item hierarchy (§5: two nested broadcasts) adds a level
+// in the middle: Y_vendor[v] = W_vendor @ X_vendor[v] + Y_user[vendor_to_user[v]]
+// in fp32, then out[i] = W_item @ X_item[i] + Y_vendor[item_to_vendor[i]].  A
+// launch is one level: its product, plus, in the epilogue, the fp32 term of
+// the level above found through one map (or, when the middle level has no
+// block, through both maps), stored in fp32 for the level below or in bf16.
 // Each K block arrives zero-padded to a multiple of 8 (§2.2), so every row is
 // 16-byte aligned for the TMA.
 //
@@ -26,9 +32,11 @@
 //              two accumulators so that the epilogue of one unit overlaps the
 //              MMAs of the next;
 //   warps 4-7  epilogue: TMEM lane r = row r of the tile; 32 columns at a time,
-//              + Y (stage 1), to bf16 (stage 1) or fp32 (stage 0), stored.
-// Stage 1 is launched as a programmatic dependent of stage 0; only its
-// epilogue waits for stage 0's Y, so its loads and MMAs overlap stage 0.
+//              + Y of the level above, to fp32 (a term for the level below) or
+//              bf16 (the output), stored.
+// Each level is launched as a programmatic dependent of the one above; only
+// its epilogue waits for the Y it adds, so its loads and MMAs overlap the
+// level above.
 //
 // Clusters (M of at most 8 row tiles): the CTAs of a cluster take the row
 // tiles of one batch entry at a time, CTA r tile r, so they share every X
@@ -59,16 +67,20 @@ constexpr int kLceCtrlBytes = 1024;
 constexpr int kLceMaxStages = 8;
 
 struct LceParams {
-  const uint16_t* W;          // bf16 [M, K] of this stage (W_user or W_cand)
-  const int32_t* cand_to_user;
-  const float* Y;             // stage 1: fp32 [n_user, M, N] user terms
-  float* Y_out;               // stage 0: fp32 [n_user, M, N]
-  uint16_t* out;              // stage 1: bf16 [n_cand, M, N]
-  int64_t n_batch;            // users (stage 0) or candidates (stage 1)
-  int64_t n_user;
+  const uint16_t* W;          // bf16 [M, K] of this level's block
+  const int32_t* map;         // add: batch entry -> entry of the level above
+  const int32_t* map2;        // add, or null: entry of the level above -> the one above that
+  const float* Y;             // add: fp32 [rows, M, N] terms of the level(s) above
+  float* Y_out;               // out_f32: fp32 [n_batch, M, N]
+  uint16_t* out;              // otherwise: bf16 [n_batch, M, N]
+  int64_t n_batch;            // entries of this level (users, vendors, candidates or items)
+  int64_t n_map;              // map values must lie in [0, n_map)
+  int64_t n_map2;             // map2 values must lie in [0, n_map2)
   int32_t M, K, N;
-  int32_t stage;              // 0: user GEMM, 1: candidate GEMM with the broadcast add
-  int32_t add_user;           // stage 1: add Y (0 when there is no user block)
+  int32_t out_f32;            // 1: store fp32 to Y_out (a term of the level below); 0: bf16 to out
+  int32_t add;                // 1: add a row of Y (after the grid above has completed)
+  int32_t y_via_map2;         // add with map2: 1 = Y row map2[map[b]]; 0 = Y row map[b], map2 only checked
+  int32_t has_dependent;      // 1: the level below is this grid's programmatic dependent
   int32_t cluster_n;          // CTAs per cluster: the row tiles of M (<= 8), or 1
   int* err_word;
   uint64_t timeout_ns;
@@ -107,9 +119,9 @@ ikbo_lce_kernel(const __grid_constant__ LceParams p, const __grid_constant__ CUt
   LceCtrl* ctl = reinterpret_cast<LceCtrl*>(smem_raw + C::kDataBytes);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // the user stage lets the candidate stage start at once (it waits for Y
-  // only in its epilogue)
-  if (p.stage == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // the level below may start at once (it waits for this level's Y only in
+  // its epilogue)
+  if (p.has_dependent) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const bool layout_ok = (ptx::smem_addr(smem_raw) & 1023u) == 0;
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kStages; ++i) {
@@ -245,7 +257,7 @@ ikbo_lce_kernel(const __grid_constant__ LceParams p, const __grid_constant__ CUt
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;                      // TMEM lane == tile row
     const uint32_t lane_off = uint32_t(quarter * 32) << 16;
-    bool y_ready = p.stage == 0 || !p.add_user;
+    bool y_ready = !p.add;
     uint32_t ui = 0;
     for (int64_t unit = first; unit < n_units; unit += stride, ++ui) {
       const uint32_t buf = ui & 1u;
@@ -255,22 +267,27 @@ ikbo_lce_kernel(const __grid_constant__ LceParams p, const __grid_constant__ CUt
       ptx::tc_fence_after();
       const int m = mt * kTileM + r;
       const bool live = m < p.M;
-      int u = 0;
+      int64_t u = 0;
       bool bad = false;
-      if (p.stage == 1 && p.add_user) {
+      if (p.add) {
         if (!y_ready) {
-          // Y is stage 0's output: visible once that grid has completed
+          // Y is the level above's output: visible once that grid has completed
           asm volatile("griddepcontrol.wait;" ::: "memory");
           y_ready = true;
         }
-        u = p.cand_to_user[b];
-        bad = u < 0 || int64_t(u) >= p.n_user;
+        u = p.map[b];
+        bad = u < 0 || u >= p.n_map;
+        if (!bad && p.map2) {
+          const int64_t top = p.map2[u];
+          bad = top < 0 || top >= p.n_map2;
+          if (p.y_via_map2) u = top;
+        }
         if (bad && r == 0) atomicOr(p.err_word, kErrIndex);
       }
       const uint32_t acc = tmem + lane_off + buf * C::N;
-      // the user term of this row, one 32-column chunk ahead of its use
-      const bool add = p.stage == 1 && p.add_user && live && !bad;
-      const float4* yrow = add ? reinterpret_cast<const float4*>(p.Y + ((int64_t)u * p.M + m) * p.N) : nullptr;
+      // the term of the level above for this row, one 32-column chunk ahead of its use
+      const bool add = p.add && live && !bad;
+      const float4* yrow = add ? reinterpret_cast<const float4*>(p.Y + (u * p.M + m) * p.N) : nullptr;
       float4 ynext[8];
       if (add) {
 #pragma unroll
@@ -291,26 +308,25 @@ ikbo_lce_kernel(const __grid_constant__ LceParams p, const __grid_constant__ CUt
         ptx::tmem_ld32(acc + c * 32, o);
         ptx::tmem_ld_wait();
         if (live && !bad) {
-          if (p.stage == 0) {
+          float x[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(o[e]);
+          if (add) {
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {
+              const float4 t = ycur[q4];
+              x[4 * q4] += t.x;
+              x[4 * q4 + 1] += t.y;
+              x[4 * q4 + 2] += t.z;
+              x[4 * q4 + 3] += t.w;
+            }
+          }
+          if (p.out_f32) {
             float4* dst = reinterpret_cast<float4*>(p.Y_out + ((int64_t)b * p.M + m) * p.N + c * 32);
 #pragma unroll
             for (int q4 = 0; q4 < 8; ++q4)
-              dst[q4] = make_float4(__uint_as_float(o[4 * q4]), __uint_as_float(o[4 * q4 + 1]),
-                                    __uint_as_float(o[4 * q4 + 2]), __uint_as_float(o[4 * q4 + 3]));
+              dst[q4] = make_float4(x[4 * q4], x[4 * q4 + 1], x[4 * q4 + 2], x[4 * q4 + 3]);
           } else {
-            float x[32];
-#pragma unroll
-            for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(o[e]);
-            if (add) {
-#pragma unroll
-              for (int q4 = 0; q4 < 8; ++q4) {
-                const float4 t = ycur[q4];
-                x[4 * q4] += t.x;
-                x[4 * q4 + 1] += t.y;
-                x[4 * q4 + 2] += t.z;
-                x[4 * q4 + 3] += t.w;
-              }
-            }
             uint4* dst = reinterpret_cast<uint4*>(p.out + ((int64_t)b * p.M + m) * p.N + c * 32);
 #pragma unroll
             for (int q8 = 0; q8 < 4; ++q8) {

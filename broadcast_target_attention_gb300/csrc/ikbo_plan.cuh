@@ -90,12 +90,23 @@ ikbo_plan_kernel(const __grid_constant__ PlanParams p, const __grid_constant__ P
   const int nt = blockDim.x;
   const int64_t n_cand = p.n_cand;
   const int64_t n_user = p.n_user;
-  const int32_t* __restrict__ c2u = p.cand_to_user;
+  // not __restrict__: in a multi-level call it points at item_user, which
+  // this kernel writes first (plain loads, no read-only path)
+  const int32_t* c2u = p.cand_to_user;
   const int32_t* __restrict__ off = p.user_offsets;
 
   if (tid == 0) {
     s_err = 0;
     s_unsorted = 0;
+  }
+  if (p.vendor_to_user) {
+    // 0. multi-level call: every item's user through its vendor; an
+    // out-of-range vendor becomes -1, which step 1 reports as a bad index
+    for (int64_t c = tid; c < n_cand; c += nt) {
+      const int32_t vd = p.cand_to_user[c];
+      p.item_user[c] = (vd >= 0 && (int64_t)vd < p.n_vendor) ? p.vendor_to_user[vd] : -1;
+    }
+    c2u = p.item_user;
   }
   __syncthreads();
 

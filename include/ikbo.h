@@ -239,6 +239,70 @@ int ikbo_lce_fwd(const void* W_user, const void* W_cand, const void* X_user, con
                  int32_t K_user, int32_t K_cand, int32_t N, void* out, ikbo_stream_t stream);
 
 /*
+ * Linear compression over a user -> ads vendor -> ads item hierarchy ("In-Kernel
+ * Broadcast Optimization", §5 with §2): an item's K input embeddings are its
+ * user's block, its vendor's block and its own, so with v = item_to_vendor[i]
+ * and u = vendor_to_user[v]
+ *
+ *   out[i] = W_user @ X_user[u] + W_vendor @ X_vendor[v] + W_item @ X_item[i]
+ *
+ * Each level's product is computed once per entry of that level: up to three
+ * launches of the linear-compression kernel, each a programmatic dependent
+ * of the one before, users (fp32 terms), then vendors (their product plus
+ * their user's term, fp32), then items (their product plus their vendor's
+ * term, to bf16).  No block is ever copied per vendor or per item.
+ *
+ *   W_user [M, K_user], W_vendor [M, K_vendor], W_item [M, K_item]    bf16
+ *   X_user [n_user, K_user, N], X_vendor [n_vendor, K_vendor, N],
+ *   X_item [n_item, K_item, N]                                         bf16
+ *   item_to_vendor int32 [n_item], vendor_to_user int32 [n_vendor]; any order
+ *   out bf16 [n_item, M, N]; shares no byte with an input
+ *   All device memory, 16-byte aligned (the maps 4-byte aligned).
+ *   K_user, K_vendor: multiples of 8, 0 = no such block (its W and X may then
+ *   be NULL; with neither, the maps are not read and may be NULL; without a
+ *   user block vendor_to_user is not read).  K_item: a multiple of 8, >= 8.
+ *   N in {64, 128, 192, 256}.  Accumulation in fp32; out rounded to bf16.
+ * Errors as ikbo_lce_fwd.  On the device: an item_to_vendor value outside
+ * [0, n_vendor), or a vendor_to_user value outside [0, n_user) that an item
+ * reaches, sets IKBO_ERR_INDEX and that item's rows are not written.
+ * ikbo_get_timing, when enabled, reports the user level as its first value
+ * and the vendor and item levels together as its second.  n_item == 0: no-op.
+ */
+int ikbo_ml_lce_fwd(const void* W_user, const void* W_vendor, const void* W_item,
+                    const void* X_user, const void* X_vendor, const void* X_item,
+                    const int32_t* item_to_vendor, const int32_t* vendor_to_user, int64_t n_item,
+                    int64_t n_vendor, int64_t n_user, int32_t M, int32_t K_user, int32_t K_vendor,
+                    int32_t K_item, int32_t N, void* out, ikbo_stream_t stream);
+
+/*
+ * Target attention over a user -> ads vendor -> ads item hierarchy ("In-Kernel
+ * Broadcast Optimization", §5: a user sees several vendors, each vendor offers
+ * several items; two nested broadcasts with independent, uneven ratios).  Every
+ * item is a candidate: its Lq query tokens attend to the sequence of the user
+ * its vendor belongs to,
+ *
+ *   u(i) = vendor_to_user[item_to_vendor[i]],
+ *
+ * and out is that of ikbo_attn_fwd with cand_to_user[i] = u(i).  The kernels
+ * look the two maps up while they plan (in-kernel, or in the planning kernel
+ * beyond the in-kernel limits); no per-item user map is passed in.
+ *
+ *   item_to_vendor  int32 [n_item], values in [0, n_vendor), any order
+ *   vendor_to_user  int32 [n_vendor], values in [0, n_user), any order
+ *   other arguments as ikbo_attn_fwd, with n_item in place of n_cand.
+ * A value of either map out of range (only vendors that some item names are
+ * read) sets IKBO_ERR_INDEX in the device error word and nothing is written.
+ * n_item == 0: no-op.  n_vendor < 0 or >= 2^31: IKBO_ERR_SHAPE; n_vendor == 0
+ * with items: IKBO_ERR_INDEX; vendor_to_user NULL: IKBO_ERR_NULL, not 4-byte
+ * aligned: IKBO_ERR_ALIGN.  Kernel choice and other errors as ikbo_attn_fwd.
+ */
+int ikbo_ml_attn_fwd(const void* q, const void* k_user, const void* v_user,
+                     const int32_t* user_offsets, const int32_t* item_to_vendor,
+                     const int32_t* vendor_to_user, int64_t n_item, int64_t n_vendor,
+                     int64_t n_user, int32_t H, int32_t Lq, int32_t D, float scale, void* out,
+                     ikbo_stream_t stream);
+
+/*
  * Selects the attention kernel for later calls on this thread.  Returns the
  * previous value.
  *   0  automatic (the default): 3 when the users have on average at least
