@@ -744,7 +744,7 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
   // CTA's barriers being initialised; wait once planning is done, before any
   // access to the partner's shared memory.  The partner has long arrived by
   // then, so the wait costs nothing.
-  ptx::cluster_arrive();
+  ptx::cluster_arrive_relaxed();
   trace_pro(p, 1);
   if (!layout_ok) {
     if (threadIdx.x == 0) {
@@ -1362,8 +1362,15 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
   if (threadIdx.x == 0 && ctl->go_sent) W.drain(ptx::smem_addr(&ctl->pair_recv), 0);
   if (threadIdx.x == 0) trace(p, 0, kTrCtaEnd);
   __syncwarp();
-  // neither CTA of a pair may exit while the other can still touch its memory
-  ptx::cluster_sync();
+  // Neither CTA of a pair may exit while the other can still touch its
+  // memory.  The partner's copies complete on pair_recv, drained above; the
+  // one other remote access, the producer's arrival on the partner's pair_go,
+  // is ordered before this thread's barrier arrival by a fence (it may be
+  // unconsumed if the partner gave up).  No other thread's memory operations
+  // need ordering here, so the barrier itself is relaxed: it does not wait
+  // for the epilogue's global stores.
+  if (threadIdx.x == 0) ptx::fence_acq_rel_cluster();
+  ptx::cluster_sync_relaxed();
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, C::kTmemCols);

@@ -88,10 +88,23 @@ __device__ __forceinline__ void cluster_sync() {
                    : "memory");
 }
 
+// The same whose arrival orders no memory operation: for teardown, when
+// every access to another CTA's shared memory has completed on an mbarrier
+// or been fenced by the thread that made it.
+__device__ __forceinline__ void cluster_sync_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_acq_rel_cluster() {
+  asm volatile("fence.acq_rel.cluster;" ::: "memory");
+}
+
 // Split cluster barrier, every thread of the cluster, warps converged: each
-// thread arrives once, then waits once, before it arrives again.
-__device__ __forceinline__ void cluster_arrive() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+// thread arrives once, then waits once, before it arrives again.  The
+// arrival orders nothing: enough after fence_mbar_init when the peers touch
+// nothing of this CTA but its mbarriers before a later handshake.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
