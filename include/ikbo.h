@@ -34,6 +34,13 @@
  * partials, tensor maps) and takes it from the device's stream-ordered
  * memory pool on `stream`, releasing it on the same stream.
  *
+ * CUDA graphs: the device-pointer entry points (ikbo_attn_fwd and its
+ * no-alloc, fused, multi-level and linear-compression variants) can be
+ * captured on `stream`; their scratch allocations become graph memory
+ * nodes and a programmatic dependent launch becomes a programmatic edge.
+ * Make one call of each kind with the same device current before the
+ * capture: the first call sets the kernels' attributes up.
+ *
  * Errors: a negative status is returned at once, with nothing enqueued, for
  * anything the host can see (IKBO_ERR_NULL, _SHAPE, _ALIGN, _SCALE, _ALIAS,
  * _DEVICE).  Bad contents of the index tensors (a candidate mapped outside
