@@ -33,7 +33,7 @@ import os
 from concurrent.futures import ThreadPoolExecutor
 
 from dataclasses import dataclass, field
-from typing import Optional, Sequence
+from typing import Sequence
 
 import numpy as np
 

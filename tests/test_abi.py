@@ -1,6 +1,5 @@
 """The C ABI without a GPU: the library loads, exports what include/ikbo.h
 declares, and rejects bad host-visible arguments before touching CUDA."""
-import ctypes
 import os
 import re
 

@@ -1,6 +1,5 @@
 """The other entry points on the GPU: the explicit-broadcast comparison path,
 the host-buffer path, device-side error reporting, bounded waits, timing."""
-import numpy as np
 import pytest
 import torch
 

@@ -8,7 +8,6 @@ same array.  This file is collected last on purpose.
 """
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
