@@ -263,8 +263,6 @@ ikbo_lce_kernel(const __grid_constant__ LceParams p, const __grid_constant__ CUt
       const uint32_t buf = ui & 1u;
       int b, mt;
       unit_bm(unit, b, mt);
-      if (!W.warp_wait(ptx::smem_addr(&ctl->acc_full[buf]), (ui >> 1) & 1u)) break;
-      ptx::tc_fence_after();
       const int m = mt * kTileM + r;
       const bool live = m < p.M;
       int64_t u = 0;
@@ -284,25 +282,30 @@ ikbo_lce_kernel(const __grid_constant__ LceParams p, const __grid_constant__ CUt
         }
         if (bad && r == 0) atomicOr(p.err_word, kErrIndex);
       }
-      const uint32_t acc = tmem + lane_off + buf * C::N;
-      // the term of the level above for this row, one 32-column chunk ahead of its use
+      // The term of the level above for this row, in 32-column chunks: the
+      // first kYAhead are requested before the accumulator is waited for (they
+      // arrive while the unit's MMAs run), then each kYAhead chunks ahead of
+      // its use.
+      constexpr int kChunks = C::N / 32;
+      constexpr int kYAhead = 2;
       const bool add = p.add && live && !bad;
       const float4* yrow = add ? reinterpret_cast<const float4*>(p.Y + (u * p.M + m) * p.N) : nullptr;
-      float4 ynext[8];
+      float4 yb[kYAhead + 1][8];
       if (add) {
 #pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4) ynext[q4] = yrow[q4];
+        for (int c = 0; c < kYAhead && c < kChunks; ++c) {
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) yb[c][q4] = yrow[c * 8 + q4];
+        }
       }
-#pragma unroll 1
-      for (int c = 0; c < C::N / 32; ++c) {
-        float4 ycur[8];
-        if (add) {
+      if (!W.warp_wait(ptx::smem_addr(&ctl->acc_full[buf]), (ui >> 1) & 1u)) break;
+      ptx::tc_fence_after();
+      const uint32_t acc = tmem + lane_off + buf * C::N;
 #pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4) ycur[q4] = ynext[q4];
-          if (c + 1 < C::N / 32) {
+      for (int c = 0; c < kChunks; ++c) {
+        if (add && c + kYAhead < kChunks) {
 #pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4) ynext[q4] = yrow[(c + 1) * 8 + q4];
-          }
+          for (int q4 = 0; q4 < 8; ++q4) yb[(c + kYAhead) % (kYAhead + 1)][q4] = yrow[(c + kYAhead) * 8 + q4];
         }
         uint32_t o[32];
         ptx::tmem_ld32(acc + c * 32, o);
@@ -314,7 +317,7 @@ ikbo_lce_kernel(const __grid_constant__ LceParams p, const __grid_constant__ CUt
           if (add) {
 #pragma unroll
             for (int q4 = 0; q4 < 8; ++q4) {
-              const float4 t = ycur[q4];
+              const float4 t = yb[c % (kYAhead + 1)][q4];
               x[4 * q4] += t.x;
               x[4 * q4 + 1] += t.y;
               x[4 * q4 + 2] += t.z;
