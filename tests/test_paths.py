@@ -1,5 +1,6 @@
 """The other entry points on the GPU: the explicit-broadcast comparison path,
 the host-buffer path, device-side error reporting, bounded waits, timing."""
+import numpy as np
 import pytest
 import torch
 
@@ -31,15 +32,39 @@ def test_broadcast_path_rejects_a_budget_below_one_copy(gpu_lib):
     assert e.value.status == _lib.IKBO_ERR_BUDGET
 
 
-def test_host_path_equals_device_path(gpu_lib):
-    wl = W.generate(W.CONFIGS["ratio_1024x15"])
+def _host_call(gpu_lib, wl):
     d = to_device(wl)
-    dev_out = gpu_lib.attn_fwd(d["q"], d["k"], d["v"], d["user_offsets"], d["cand_to_user"], wl.scale)
     h = {k_: v_.cpu().pin_memory() for k_, v_ in d.items()}
-    host_out = torch.empty_like(h["q"]).pin_memory()
+    host_out = torch.full_like(h["q"], 7.0).pin_memory()
     gpu_lib.attn_fwd_host(h["q"], h["k"], h["v"], h["user_offsets"], h["cand_to_user"], wl.scale,
                           out=host_out)
+    return d, host_out
+
+
+def test_host_path_equals_device_path(gpu_lib):
+    """The host path copies in, runs the device path's kernels and copies out: bit-equal."""
+    wl = W.generate(W.CONFIGS["ratio_1024x15"])
+    d, host_out = _host_call(gpu_lib, wl)
+    dev_out = gpu_lib.attn_fwd(d["q"], d["k"], d["v"], d["user_offsets"], d["cand_to_user"], wl.scale)
     assert torch.equal(host_out, dev_out.cpu())
+
+
+HOST_CASES = {
+    # an empty sequence and users without candidates
+    "gaps": dict(n_user=5, counts=[30, 9, 0, 0, 41], lens=[2500, 0, 2600, 100, 2400]),
+    # one user with most of the keys
+    "first_heavy": dict(n_user=4, counts=[7, 100, 3, 1], lens=[9000, 300, 129, 1]),
+}
+
+
+@pytest.mark.parametrize("case", sorted(HOST_CASES))
+@pytest.mark.parametrize("shuffle", [False, True])
+def test_host_path_matches_oracle(gpu_lib, case, shuffle):
+    wl = W.custom(H=4, D=128, Lq=1, seed=len(case), shuffle=shuffle, **HOST_CASES[case])
+    _, host_out = _host_call(gpu_lib, wl)
+    cands = W.sample_candidates(wl, 200)
+    assert_close(host_out.float().numpy().astype(np.float64)[cands], oracle.attention_wl(wl, cands),
+                 f"host path {case} shuffle={shuffle}")
 
 
 def _sentinel_call(gpu_lib, wl, c2u=None, off=None):
