@@ -357,6 +357,8 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
       if (lane == 0) W.drain(ptx::smem_addr(&ctl->drain), 0);
     }
     __syncwarp();
+  } else if ((warp == 2 || warp == 3) && mode != kModeSkip) {
+    prefetch_v_late(p, ctl->total_keys, D);
   } else if (warp >= kSoftmaxWarp0 && mode != kModeSkip) {
     // ------------------------------------------- softmax / correction / epilogue
     const int g = (warp - kSoftmaxWarp0) / kPpSoftmaxWarps;   // query tile of this warp

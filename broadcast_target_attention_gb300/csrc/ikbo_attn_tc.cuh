@@ -302,19 +302,37 @@ __device__ __forceinline__ int block_scan_excl(int x, int* red, int* total) {
 // DRAM for it: the tiles the TMA loads later hit in L2.
 constexpr int64_t kPrefetchMaxBytes = int64_t(48) << 20;
 
-// Prefetch instructions are slow to issue, so three threads of different
-// warps issue one each: which = 0 for K, 1 for V, 2 for q.
+// Bulk prefetch instructions are slow to issue, so two threads of different
+// warps issue one each, once the offsets are validated: which = 0 for K,
+// 2 for q.  Those are what the first MMAs need.
 __device__ void prefetch_inputs(const AttnParams& p, int T, int D, int which) {
   const int64_t kv = int64_t(T) * p.H * D * 2;
   const int64_t qb = p.n_cand * p.H * p.Lq * D * 2;
   if (2 * kv + qb > kPrefetchMaxBytes) return;
-  const void* base = which == 0 ? (const void*)p.k : which == 1 ? (const void*)p.v : (const void*)p.q;
+  const void* base = which == 0 ? (const void*)p.k : (const void*)p.q;
   const int64_t bytes = which == 2 ? qb : kv;
   // byte counts are multiples of 128 (D is 64 or 128), so are the shares
   const int64_t per = ((bytes + gridDim.x - 1) / gridDim.x + 15) & ~int64_t(15);
   const int64_t lo = per * blockIdx.x;
   const int64_t hi = lo + per < bytes ? lo + per : bytes;
   if (hi > lo) ptx::prefetch_l2(static_cast<const char*>(base) + lo, uint32_t(hi - lo));
+}
+
+// V's share comes after planning, from the two warps (64 threads) that have
+// no role once the roles start, one 128-byte line per instruction through
+// the load/store path: the DRAM reads of q and K go first, and the TMA unit
+// stays free for the first tile loads.  (V prefetched with q and K, or K
+// also this way, measured slower: the first tiles' loads waited behind it.)
+__device__ __forceinline__ void prefetch_v_late(const AttnParams& p, int T, int D) {
+  const int64_t kv = int64_t(T) * p.H * D * 2;
+  const int64_t qb = p.n_cand * p.H * p.Lq * D * 2;
+  if (2 * kv + qb > kPrefetchMaxBytes) return;
+  const int64_t lines = (kv + 127) >> 7;
+  const int64_t per = (lines + gridDim.x - 1) / gridDim.x;
+  const int64_t lo = per * blockIdx.x;
+  const int64_t hi = lo + per < lines ? lo + per : lines;
+  for (int64_t l = lo + (threadIdx.x & 63); l < hi; l += 64)
+    ptx::prefetch_line_l2(reinterpret_cast<const char*>(p.v) + (l << 7));
 }
 
 // ---------------------------------------------------------------------------
@@ -443,7 +461,7 @@ __device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch, 
   }
   // the offsets are valid: start the DRAM reads of this CTA's share of the
   // inputs (lane 0 of warps 1-3)
-  if (tid == 32 || tid == 64 || tid == 96) prefetch_inputs(p, off[n_user], D, (tid >> 5) - 1);
+  if (tid == 32 || tid == 96) prefetch_inputs(p, off[n_user], D, (tid >> 5) - 1);
   const bool unsorted = (flags & kUnsorted) != 0;
   if (!unsorted && (flags & kGap)) {
     // sorted, with wide gaps between consecutive users: fill those now
@@ -1041,6 +1059,8 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
       W.drain(ptx::smem_addr(&ctl->drain), 0);
     }
     __syncwarp();
+  } else if ((warp == 2 || warp == 3) && p.fused && mode != kModeSkip) {
+    prefetch_v_late(p, ctl->total_keys, D);
   } else if (warp >= kSoftmaxWarp0 && mode != kModeSkip) {
     // ------------------------------------------- softmax / correction / epilogue
     constexpr int kCols = kBlockN / kSplit;                  // key columns of a tile per thread

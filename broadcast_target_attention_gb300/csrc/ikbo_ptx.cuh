@@ -129,6 +129,11 @@ __device__ __forceinline__ void st_async_f32(uint32_t remote_addr, float a, uint
 
 // Hint: bring [addr, addr + bytes) of global memory into L2 (16-byte aligned,
 // bytes a multiple of 16).
+// One 128-byte line into L2 (load/store path, not the TMA unit).
+__device__ __forceinline__ void prefetch_line_l2(const void* addr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(addr) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_l2(const void* addr, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(addr), "r"(bytes) : "memory");
 }
