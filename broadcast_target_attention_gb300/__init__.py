@@ -332,3 +332,9 @@ def set_trace(buffer) -> None:
 
 def version() -> int:
     return int(_lib.lib().ikbo_version())
+
+
+def shutdown() -> None:
+    """Release the library's per-device resources and trim the memory pools it used (see
+    ``ikbo_shutdown`` in include/ikbo.h); the next call sets a device up again."""
+    _check(_lib.lib().ikbo_shutdown(), "ikbo_shutdown")

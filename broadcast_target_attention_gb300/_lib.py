@@ -31,6 +31,7 @@ SIGNATURES = {
     "ikbo_get_device_error": (ctypes.c_int, [_P]),
     "ikbo_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "ikbo_version": (ctypes.c_int, []),
+    "ikbo_shutdown": (ctypes.c_int, []),
     "ikbo_set_timing": (ctypes.c_int, [ctypes.c_int]),
     "ikbo_get_timing": (ctypes.c_int, [ctypes.POINTER(_F), ctypes.POINTER(_F)]),
     "ikbo_set_debug": (ctypes.c_int, [ctypes.c_int, ctypes.c_uint64]),

@@ -1180,6 +1180,32 @@ int ikbo_get_device_error(ikbo_stream_t stream) {
   return status_of_error_word(word);
 }
 
+int ikbo_shutdown(void) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  bool any = false;
+  for (const DeviceState& s : g_dev) any = any || s.ready;
+  if (!any) return IKBO_OK;   // nothing set up: no CUDA call at all
+  int prev = 0;
+  if (cudaGetDevice(&prev) != cudaSuccess) return IKBO_ERR_CUDA;
+  int rc = IKBO_OK;
+  for (int d = 0; d < kMaxDevices; ++d) {
+    DeviceState& s = g_dev[d];
+    if (!s.ready) continue;
+    if (cudaSetDevice(d) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) rc = IKBO_ERR_CUDA;
+    for (auto& e : s.ev)
+      if (e) cudaEventDestroy(e);
+    if (s.err_host) cudaFreeHost(s.err_host);
+    delete s.host_call;
+    cudaMemPool_t pool;
+    if (cudaDeviceGetDefaultMemPool(&pool, d) != cudaSuccess || cudaMemPoolTrimTo(pool, 0) != cudaSuccess)
+      rc = IKBO_ERR_CUDA;
+    s = DeviceState{};
+  }
+  g_timing_dev = -1;
+  if (cudaSetDevice(prev) != cudaSuccess) rc = IKBO_ERR_CUDA;
+  return rc;
+}
+
 const char* ikbo_strerror(int status) {
   switch (status) {
     case IKBO_OK: return "ok";

@@ -146,6 +146,21 @@ const char* ikbo_strerror(int status);
 int ikbo_version(void);
 
 /*
+ * Releases what the library holds on every device it has used.
+ *   - Its events and second stream.
+ *   - The pinned error-word copy.
+ *   - The scratch that its calls returned to each device's stream-ordered
+ *     memory pool. That pool keeps freed memory between calls; it is
+ *     trimmed here.
+ * It first waits for each such device's work to finish.  No other library
+ * call may run meanwhile.  A later call sets the device up again.  The
+ * no-alloc entry point's fixed array is part of the library image and is
+ * not released.  Returns IKBO_OK, or IKBO_ERR_CUDA when a device call fails
+ * (the release goes on for the other devices).
+ */
+int ikbo_shutdown(void);
+
+/*
  * Kernel timing, for measurement.  When enabled, every ikbo_attn_fwd call
  * records CUDA events on its stream around its planning kernel and its
  * attention kernel; ikbo_get_timing() synchronises on the last call's events

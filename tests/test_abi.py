@@ -127,3 +127,9 @@ def test_selected_kernel(lib):
             assert lib.ikbo_launches_per_call(1024, 15) == (2 if which == 1 else 1)
         finally:
             lib.ikbo_set_kernel(prev)
+
+
+def test_shutdown_without_any_device_set_up(lib):
+    """Nothing set up in this process: no CUDA call, and OK (twice)."""
+    assert lib.ikbo_shutdown() == 0
+    assert lib.ikbo_shutdown() == 0

@@ -128,3 +128,25 @@ def test_timing_hooks(gpu_lib):
     finally:
         gpu_lib.set_timing(False)
     assert plan_ms > 0 and attn_ms > 0
+
+
+def test_shutdown_then_calls_again(gpu_lib):
+    """ikbo_shutdown releases the per-device state and trims the pool; the next calls set the
+    device up again and give the same results."""
+    wl = W.custom(n_user=3, counts=[40, 3, 70], lens=[300, 129, 500], H=2, D=128, Lq=1, seed=12)
+    d = to_device(wl)
+    first = gpu_lib.attn_fwd(d["q"], d["k"], d["v"], d["user_offsets"], d["cand_to_user"], wl.scale)
+    gpu_lib.set_timing(True)
+    gpu_lib.attn_fwd(d["q"], d["k"], d["v"], d["user_offsets"], d["cand_to_user"], wl.scale)
+    gpu_lib.set_timing(False)
+    assert gpu_lib.get_device_error() == 0
+    gpu_lib.shutdown()
+    gpu_lib.shutdown()                                   # again: nothing left to release
+    again = gpu_lib.attn_fwd(d["q"], d["k"], d["v"], d["user_offsets"], d["cand_to_user"], wl.scale)
+    assert gpu_lib.get_device_error() == 0
+    assert torch.equal(first, again)
+    h = {k_: v_.cpu().pin_memory() for k_, v_ in d.items()}
+    host_out = torch.empty_like(h["q"]).pin_memory()
+    gpu_lib.attn_fwd_host(h["q"], h["k"], h["v"], h["user_offsets"], h["cand_to_user"], wl.scale,
+                          out=host_out)
+    assert torch.equal(host_out, first.cpu())
