@@ -362,6 +362,13 @@ def run_ikbo(args):
         barrier()
         clk.mark_end()
         step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        # 1b. the same steps with no flush between them (inputs L2-resident), for reference
+        for i in range(min(args.steps, 200)):
+            starts[i].record()
+            step()
+            ends[i].record()
+        torch.cuda.synchronize(dev)
+        hot = [starts[i].elapsed_time(ends[i]) for i in range(min(args.steps, 200))]
         # 2. per-kernel durations (events recorded by the library around each kernel)
         ikbo.set_timing(True)
         plan_ms, attn_ms = [], []
@@ -435,6 +442,9 @@ def run_ikbo(args):
         "roofline": roof,
         "e2e": {"value": total_flops / (e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": qb, "ms_per_step": e2e},
+        "l2_hot": {"ms_per_step": statistics.mean(hot),
+                   "value": flops / (statistics.mean(hot) * 1e-3) / 1e12, "unit": "TFLOP/s",
+                   "what": "the same step with no L2 flush between steps (not the headline)"},
         "broadcast_path": {"ms_per_step": bc, "value": flops / (bc * 1e-3) / 1e12, "unit": "TFLOP/s",
                            "ikbo_speedup": bc / ms,
                            "extra_bytes": nums["broadcast_extra_bytes"]},
