@@ -934,6 +934,62 @@ def run_ml_lce(args):
     print(json.dumps(line), flush=True)
 
 
+# Candidate-to-user ratios of the sweep ("In-Kernel Broadcast Optimization", §4: IKBO was
+# validated from about 10,000:1 down to 10:1; the benefit grows with the ratio).
+RATIO_SWEEP = ((4096, 4096), (4096, 410), (4096, 41), (4096, 4), (10000, 1))
+
+
+def run_ratio_sweep(args):
+    """IKBO against the explicit-broadcast path over candidate-to-user ratios at one shape
+    (H=4, D=128, Lq=1, L ~ U[256, 1024]): one JSON line per ratio, each step timed between
+    events with the L2 flushed before it."""
+    import torch
+
+    import broadcast_target_attention_gb300 as ikbo
+
+    ws, rank, local = R.dist_env()
+    if ws > 1:
+        raise SystemExit("--ratio-sweep measures one GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ikbo.load()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.int32, device=dev)
+    for n_cand, n_user in RATIO_SWEEP:
+        cfg = W.Config(name=f"ratio_{n_cand}x{n_user}", n_cand=n_cand, n_user=n_user, H=4, D=128,
+                       Lq=1, seed=7, counts="multinomial", lens="uniform", len_lo=256, len_hi=1024,
+                       description=f"{n_cand} candidates over {n_user} users, L~U[256,1024], "
+                                   "H=4 D=128 Lq=1")
+        wl = W.generate(cfg)
+        nums = A.workload_numbers(wl)
+        t = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).view(dt).to(dev)
+        q, k, v = (t(x.view(np.int16), torch.bfloat16) for x in (wl.q, wl.k, wl.v))
+        off, c2u = t(wl.user_offsets, torch.int32), t(wl.cand_to_user, torch.int32)
+        out = torch.empty_like(q)
+        ikbo_step = lambda: ikbo.attn_fwd(q, k, v, off, c2u, wl.scale, out=out)
+        bc_step = lambda: ikbo.broadcast_attn_fwd(q, k, v, off, c2u, wl.scale, out=out)
+        for _ in range(args.warmup):
+            flush.fill_(1)
+            ikbo_step()
+            bc_step()
+        assert ikbo.get_device_error() == 0
+        ms = statistics.mean(_timed(ikbo_step, args.steps, flush, dev))
+        bc = statistics.mean(_timed(bc_step, min(args.steps, 10), flush, dev))
+        kname = f"{ikbo.KERNEL_NAMES[ikbo.selected_kernel(n_cand, n_user, 4, 1)]}<128>"
+        line = {
+            "metric": METRIC + " -- candidate-to-user ratio sweep",
+            "value": nums["flops"] / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": config_block(wl, {"ratio": n_cand / n_user}),
+            "roofline": _roofline(nums["flops"], nums["alg_bytes"], ms, kname),
+            "broadcast_path": {"ms_per_step": bc, "ikbo_speedup": bc / ms,
+                               "extra_bytes": nums["broadcast_extra_bytes"]},
+            "gpu_launches": ikbo.launches_per_call(n_cand, n_user) * args.steps,
+        }
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -951,6 +1007,8 @@ def main():
                     help="measure target attention over a user -> vendor -> item hierarchy")
     ap.add_argument("--lce-ml", default=None, choices=sorted(W.LCE_ML_CONFIGS),
                     help="measure linear compression over a user -> vendor -> item hierarchy")
+    ap.add_argument("--ratio-sweep", action="store_true",
+                    help="IKBO against the broadcast path over candidate-to-user ratios")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -964,6 +1022,8 @@ def main():
         run_ml(args)
     elif args.lce_ml:
         run_ml_lce(args)
+    elif args.ratio_sweep:
+        run_ratio_sweep(args)
     else:
         run_ikbo(args)
 
