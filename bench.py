@@ -2,8 +2,8 @@
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ikbo|reference]
 
-A step is one pass of the whole hot path (planning kernel + tcgen05 attention
-kernel) over one batch of the headline workload: 1024 candidates over 15
+A step is one pass of the whole hot path (the tcgen05 attention kernel, which
+plans in-kernel for this batch) over one batch of the headline workload: 1024 candidates over 15
 users (~70:1), user sequences of 256-1024 keys, H=4, D=128, Lq=1, bf16,
 seeded synthetic inputs already resident in HBM.  L2 is flushed (a write
 larger than L2) before every timed step.  `value` is whole-job TFLOP/s
@@ -13,7 +13,12 @@ region.  Under torchrun every rank runs its own replica (users shard with no
 exchange); the time is the max over ranks.
 
 --impl reference times the CPU fp64 oracle on the host cores on the same
-workload (bounded samples), the in-run baseline of this build.
+workload (bounded samples), as the in-run baseline.
+
+Other modes (one GPU each): --with-self (fused self + target attention),
+--lce / --lce-ml (linear compression, two or three levels), --ml (attention
+over a user -> vendor -> item hierarchy), --ratio-sweep (IKBO against the
+explicit-broadcast path over candidate-to-user ratios).
 """
 from __future__ import annotations
 
