@@ -183,3 +183,23 @@ def test_repeated_calls_are_deterministic(gpu_lib, name):
     a = run(gpu_lib, wl, 0)
     b = run(gpu_lib, wl, 0)
     assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("sharp", [1.0, 4.0])
+def test_very_long_sequence(gpu_lib, kernel, sharp):
+    """One user with 65,000 keys (508 key tiles, split over a cluster pair or planned apart):
+    the running maximum and the lazy rescale over hundreds of tiles.  A scale 4x the usual
+    one makes the weights peakier and the maximum move more often (inputs and outputs stay
+    of unit scale, the regime of the tolerance)."""
+    wl = W.custom(n_user=2, counts=[5, 2], lens=[65000, 300], H=2, D=128, Lq=3, seed=77)
+    scale = wl.scale * sharp
+    prev = gpu_lib.set_kernel(kernel)
+    try:
+        d = to_device(wl)
+        out = gpu_lib.attn_fwd(d["q"], d["k"], d["v"], d["user_offsets"], d["cand_to_user"], scale)
+        assert gpu_lib.get_device_error() == 0
+    finally:
+        gpu_lib.set_kernel(prev)
+    ref = oracle.attention(wl.q, wl.k, wl.v, wl.user_offsets, wl.cand_to_user, scale)
+    assert_close(out_f64(out), ref, f"65k keys kernel={kernel} scale x{sharp}")
