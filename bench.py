@@ -555,7 +555,9 @@ def run_fused(args):
     pk = peaks()
     ai = flops / alg_bytes
     ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
-    kname = f"ikbo_attn_tc_kernel<{c.D}>"
+    # the SIMT choice runs fused calls on the one-tile kernel
+    choice = ikbo.selected_kernel(wl.n_cand, wl.n_user, c.H, c.Lq)
+    kname = f"{ikbo.KERNEL_NAMES[ikbo.KERNEL_TC if choice == ikbo.KERNEL_SIMT else choice]}<{c.D}>"
     if ai < ridge:
         gbs = alg_bytes / (ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",

@@ -355,9 +355,10 @@ cudaError_t launch_attn_tc(const AttnParams& ap, const CUtensorMap& qmap, const 
 
 template <int D>
 cudaError_t launch_attn_pp(const AttnParams& ap, const CUtensorMap& qmap, const CUtensorMap& qmap1,
-                           const CUtensorMap& kt, const CUtensorMap& vt, int grid, cudaStream_t st) {
+                           const CUtensorMap& kt, const CUtensorMap& vt, const CUtensorMap& qut,
+                           int grid, cudaStream_t st) {
   return launch_ex(ikbo_attn_pp_kernel<D>, dim3(grid), dim3(kTcThreads), kTcSmemBytes, st, false, 1,
-                   ap, qmap, qmap1, kt, vt);
+                   ap, qmap, qmap1, kt, vt, qut);
 }
 
 // The self-attention part of a fused call: the user sequence's queries and
@@ -493,9 +494,9 @@ int run_ikbo(DeviceState* ds, const void* q, const void* k, const void* v, const
       e = launch_pdl(ikbo_attn_simt_kernel<128>, dim3(grid), dim3(kSimtThreads), 0, st, ap);
   } else if (kernel == kKernPp) {
     if (D == 64)
-      e = launch_attn_pp<64>(ap, qmap, qmap1, px.kmap_tmpl, px.vmap_tmpl, L.grid, st);
+      e = launch_attn_pp<64>(ap, qmap, qmap1, px.kmap_tmpl, px.vmap_tmpl, qumap, L.grid, st);
     else
-      e = launch_attn_pp<128>(ap, qmap, qmap1, px.kmap_tmpl, px.vmap_tmpl, L.grid, st);
+      e = launch_attn_pp<128>(ap, qmap, qmap1, px.kmap_tmpl, px.vmap_tmpl, qumap, L.grid, st);
   } else {
     // the planning kernel (listed mode) is followed with programmatic dependent launch
     if (D == 64)
@@ -514,12 +515,14 @@ int run_ikbo(DeviceState* ds, const void* q, const void* k, const void* v, const
 }
 
 // Workspace for a call on this device with the current kernel choice.
-// self_T >= 0: a fused self + target call over T sequence rows, which the
-// one-tile tcgen05 kernel runs (planning in-kernel).
+// self_T >= 0: a fused self + target call over T sequence rows, which a
+// tcgen05 kernel runs with its planning in-kernel (the one-tile kernel when
+// the choice is the SIMT kernel).
 int call_workspace(DeviceState* ds, int64_t n_cand, int64_t n_user, int H, int Lq, int D,
                    Workspace* out, int64_t self_T = -1, bool multi_level = false) {
   int grid = 0;
-  const int kernel = self_T >= 0 ? kKernTc : effective_kernel(n_cand, n_user, H, Lq);
+  int kernel = effective_kernel(n_cand, n_user, H, Lq);
+  if (self_T >= 0 && kernel == kKernSimt) kernel = kKernTc;
   if (kernel == kKernTc) {
     grid = D == 64 ? tc_grid<64>(ds) : tc_grid<128>(ds);
     if (grid <= 0) return IKBO_ERR_CUDA;

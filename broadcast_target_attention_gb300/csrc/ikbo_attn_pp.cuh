@@ -28,7 +28,8 @@
 //   * warps 4-7: softmax, correction and epilogue of tile A, warps 8-11 of
 //     tile B, one thread per query row (all 128 key columns of a tile).
 // An item whose user has an odd number of query tiles left has no tile B:
-// warps 8-11 skip it.  Every wait is bounded, as in the single-tile kernel.
+// warps 8-11 skip it.  In a fused self + target call an item may also be two
+// blocks of 128 rows of the user's own sequence (tile B the second block).  Every wait is bounded, as in the single-tile kernel.
 #pragma once
 
 #include "ikbo_attn_tc.cuh"
@@ -59,7 +60,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap qmap,
                     const __grid_constant__ CUtensorMap qmap1,
                     const __grid_constant__ CUtensorMap kmap_tmpl,
-                    const __grid_constant__ CUtensorMap vmap_tmpl) {
+                    const __grid_constant__ CUtensorMap vmap_tmpl,
+                    const __grid_constant__ CUtensorMap qumap) {
   using C = PpConfig<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* data = smem_raw;
@@ -92,9 +94,10 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
     ptx::tmem_relinquish();
   }
   if (warp == 2 && lane == 0) {
-    ptx::prefetch_tensormap(&qmap);
+    if (p.n_cand > 0) ptx::prefetch_tensormap(&qmap);   // a self-only call encodes no Q map
     ptx::prefetch_tensormap(&kmap_tmpl);
     ptx::prefetch_tensormap(&vmap_tmpl);
+    if (p.q_user) ptx::prefetch_tensormap(&qumap);
   }
   if (p.fused && layout_ok) plan_load(p, data);
   __syncthreads();
@@ -130,9 +133,16 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
     return k < kCtlItems ? ctl->items[k] : p.cta_items[(size_t)blockIdx.x * p.max_cta_items + k];
   };
   auto ntiles = [](const WorkItem& w) { return ceil_div(w.kv_len, kBlockN); };
-  // candidates of query tile g of an item (tile B holds those past the first cpt)
+  // candidates of query tile g of an item (tile B holds those past the
+  // first cpt); for a self-attention item (fused call), sequence rows (tile
+  // B holds those past the first 128)
   auto tile_cands = [&](const WorkItem& w, int g) {
-    return g == 0 ? min(w.n_cand, cpt) : max(w.n_cand - cpt, 0);
+    const int per = w.q_row >= 0 ? kTileM : cpt;
+    return g == 0 ? min(w.n_cand, per) : max(w.n_cand - per, 0);
+  };
+  // query rows of tile g
+  auto tile_rows = [&](const WorkItem& w, int g) {
+    return w.q_row >= 0 ? tile_cands(w, g) : tile_cands(w, g) * Lq;
   };
 
   if (warp == 0) {
@@ -145,7 +155,9 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
       // through a copy with the row count set to T (zero fill past the end)
       auto kv_map = [&](bool is_v, int32_t row) -> const void* {
         const int T = ctl->total_keys;
-        if (row + kBlockN <= T) return is_v ? (const void*)&vmap_tmpl : (const void*)&kmap_tmpl;
+        // maps encoded with the row count T itself (a fused call states T)
+        if (p.exact_rows || row + kBlockN <= T)
+          return is_v ? (const void*)&vmap_tmpl : (const void*)&kmap_tmpl;
         CUtensorMap* tail_k = p.map_slots + 2 * blockIdx.x;
         CUtensorMap* tail_v = tail_k + 1;
         if (!tail_ready) {
@@ -195,7 +207,13 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
         const int32_t c0 = w.cand_begin + g * cpt;
         const uint32_t qbar = ptx::smem_addr(&ctl->q_full[g]);
         const uint32_t qdst = ptx::smem_addr(q_smem + g * C::kQBytes);
-        if (sorted) {
+        if (w.q_row >= 0) {
+          // 128 rows of the user sequence's queries (rows past T read as zeros)
+          ptx::mbar_arrive_expect_tx_warp(qbar, uint32_t(C::kCB * kTileM * 128));
+          for (int cb = 0; cb < C::kCB; ++cb)
+            ptx::tma_load_2d_warp(qdst + cb * kTileM * 128, &qumap, qbar, w.head * D + cb * 64,
+                                  w.q_row + g * kTileM);
+        } else if (sorted) {
           const int nb = p.qbox;
           const int nbox = ceil_div(nc, nb);
           ptx::mbar_arrive_expect_tx_warp(qbar, uint32_t(nbox * nb * Lq * 128 * C::kCB));
@@ -376,7 +394,7 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
       const int n = ntiles(w);
       // Rows past the tile's queries hold stale shared memory; their results
       // are never stored, and they are left out of every decision below.
-      const bool live = row < nc * Lq;
+      const bool live = row < tile_rows(w, g);
       float m = -INFINITY, l = 0.f;
       bool ok = true;
       for (int j = 0; j < n; ++j, ++tn) {
@@ -476,11 +494,18 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
       if (row == 0 && g == 0) trace(p, k, kTrEpiO);
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const float2 inv2 = make_float2(inv, inv);
-      const int ci = live ? row / Lq : 0;
-      const int tq = live ? row - ci * Lq : 0;
-      const int32_t gpos = w.cand_begin + g * cpt + ci;
-      const int64_t cidx = live ? (sorted ? gpos : perm[gpos]) : 0;
-      uint16_t* dst = p.out + (((cidx * p.H + w.head) * (int64_t)Lq + tq) * D);
+      uint16_t* dst;
+      if (w.q_row >= 0) {
+        // a self-attention row: out_user[q_row + 128 g + row, head, :]
+        const int64_t srow = live ? (int64_t)w.q_row + g * kTileM + row : 0;
+        dst = p.out_user + ((srow * p.H + w.head) * D);
+      } else {
+        const int ci = live ? row / Lq : 0;
+        const int tq = live ? row - ci * Lq : 0;
+        const int32_t gpos = w.cand_begin + g * cpt + ci;
+        const int64_t cidx = live ? (sorted ? gpos : perm[gpos]) : 0;
+        dst = p.out + (((cidx * p.H + w.head) * (int64_t)Lq + tq) * D);
+      }
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];

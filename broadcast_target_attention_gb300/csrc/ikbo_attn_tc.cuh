@@ -545,14 +545,15 @@ __device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch, 
   // Units (H x groups of query tiles of users with candidates and keys),
   // prefix-summed over the users in index order, or longest first (below).
   const int cpt = p.cands_per_tile * tiles_per_unit;   // candidates per unit
+  const int srows = kTileM * tiles_per_unit;           // sequence rows per self-attention unit
   bool lpt = false;
   auto user_at = [&](int rk) { return lpt ? order[rk] : rk; };
   auto units_of = [&](int u) {
     const int r = cs[u + 1] - cs[u], L = off[u + 1] - off[u];
     if (L <= 0) return 0;
     // candidate tiles, plus (fused self-attention) the user's own sequence
-    // in tiles of 128 rows
-    const int tiles = (r > 0 ? ceil_div(r, cpt) : 0) + (p.q_user ? ceil_div(L, kTileM) : 0);
+    // in units of tiles_per_unit tiles of 128 rows
+    const int tiles = (r > 0 ? ceil_div(r, cpt) : 0) + (p.q_user ? ceil_div(L, srows) : 0);
     return p.H * tiles;
   };
   auto prefix = [&]() {
@@ -625,7 +626,7 @@ __device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch, 
     const int r = cs[u + 1] - cs[u];
     const int L = off[u + 1] - off[u];
     const int nmt = r > 0 ? ceil_div(r, cpt) : 0;
-    const int per_head = nmt + (p.q_user ? ceil_div(L, kTileM) : 0);
+    const int per_head = nmt + (p.q_user ? ceil_div(L, srows) : 0);
     const int local = i - ubefore[lo];
     const int h = local / per_head, mt = local - h * per_head;
     w.user = u;
@@ -635,11 +636,11 @@ __device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch, 
       w.n_cand = min(cpt, r - mt * cpt);
       w.q_row = -1;
     } else {
-      // a tile of the user's own sequence (self-attention)
+      // tiles of the user's own sequence (self-attention): up to srows rows
       const int t = mt - nmt;
       w.cand_begin = 0;
-      w.n_cand = min(kTileM, L - t * kTileM);
-      w.q_row = off[u] + t * kTileM;
+      w.n_cand = min(srows, L - t * srows);
+      w.q_row = off[u] + t * srows;
     }
     w.kv_begin = off[u];
     w.kv_len = off[u + 1] - off[u];

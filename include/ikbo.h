@@ -220,9 +220,11 @@ int ikbo_set_trace(uint64_t* device_buffer);
  *   other arguments    as ikbo_attn_fwd; n_cand may be 0 (self-attention
  *                      only; q, cand_to_user and out may then be NULL).
  *
- * Runs on the one-tile tcgen05 kernel (whatever ikbo_set_kernel chose), with
- * its planning in-kernel: n_cand <= 20480 and n_user <= 1024, else
- * IKBO_ERR_SHAPE.  T < 0 or T >= 2^31: IKBO_ERR_SHAPE.  n_cand == 0 and T == 0:
+ * Runs on the tcgen05 kernel that the automatic choice or ikbo_set_kernel
+ * picks for the candidates (the one-tile kernel when the choice is the SIMT
+ * kernel); on the two-tile kernel a self-attention item is two blocks of 128
+ * sequence rows sharing the user's key tiles.  Planning is in-kernel:
+ * n_cand <= 20480 and n_user <= 1024, else IKBO_ERR_SHAPE.  T < 0 or T >= 2^31: IKBO_ERR_SHAPE.  n_cand == 0 and T == 0:
  * no-op.  Errors and ownership otherwise as ikbo_attn_fwd.
  */
 int ikbo_fused_attn_fwd(const void* q, const void* q_user, const void* k_user, const void* v_user,

@@ -59,37 +59,47 @@ EDGE = {
 }
 
 
+@pytest.mark.parametrize("kernel", [2, 3])
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("Lq", [1, 3, 8])
 @pytest.mark.parametrize("case", sorted(EDGE))
-def test_edge_cases(gpu_lib, case, Lq, D):
+def test_edge_cases(gpu_lib, case, Lq, D, kernel):
+    """On the one-tile kernel (self tiles of 128 rows) and on the two-tile kernel (self items
+    of two 128-row blocks, the second partial or absent)."""
     wl = W.custom(H=2, D=D, Lq=Lq, seed=40 + Lq, **EDGE[case])
-    check(gpu_lib, wl, f"{case} Lq={Lq} D={D}")
+    check(gpu_lib, wl, f"{case} Lq={Lq} D={D} kernel={kernel}", kernel=kernel)
 
 
-def test_unsorted_mapping(gpu_lib):
+@pytest.mark.parametrize("kernel", [2, 3])
+def test_unsorted_mapping(gpu_lib, kernel):
     wl = W.custom(n_user=5, counts=[40, 3, 1, 90, 17], lens=[333, 20, 1, 700, 129], H=4, D=128,
                   Lq=2, seed=9, shuffle=True)
     assert np.any(np.diff(wl.cand_to_user) < 0)
-    check(gpu_lib, wl, "unsorted")
+    check(gpu_lib, wl, f"unsorted kernel={kernel}", kernel=kernel)
 
 
-@pytest.mark.parametrize("kernel", [0, 1, 3])
-def test_runs_on_the_one_tile_kernel_whatever_the_choice(gpu_lib, kernel):
+@pytest.mark.parametrize("kernel", [0, 1, 2, 3])
+def test_every_kernel_choice(gpu_lib, kernel):
+    """The SIMT choice runs on the one-tile kernel; the others as chosen."""
     wl = W.custom(n_user=3, counts=[300, 2, 40], lens=[200, 500, 64], H=2, D=64, Lq=1, seed=12)
     check(gpu_lib, wl, f"kernel choice {kernel}", kernel=kernel)
 
 
+@pytest.mark.parametrize("kernel", [2, 3])
 @pytest.mark.parametrize("D", [64, 128])
-def test_self_attention_only(gpu_lib, D):
+def test_self_attention_only(gpu_lib, D, kernel):
     """No candidates: the call computes the user sequence's self-attention alone."""
     base = W.custom(n_user=3, counts=[1, 1, 1], lens=[260, 5, 130], H=2, D=D, Lq=1, seed=6)
     qu = W.user_queries(base)
     d = to_device(base)
     dqu = torch.from_numpy(np.ascontiguousarray(qu).view(np.int16)).view(torch.bfloat16).cuda()
     q0 = d["q"][:0]
-    out, out_user = gpu_lib.fused_attn_fwd(q0, dqu, d["k"], d["v"], d["user_offsets"],
-                                           d["cand_to_user"][:0], base.scale)
+    prev = gpu_lib.set_kernel(kernel)
+    try:
+        out, out_user = gpu_lib.fused_attn_fwd(q0, dqu, d["k"], d["v"], d["user_offsets"],
+                                               d["cand_to_user"][:0], base.scale)
+    finally:
+        gpu_lib.set_kernel(prev)
     assert gpu_lib.get_device_error() == 0
     assert out.shape[0] == 0
     ref = oracle.self_attention(qu, base.k, base.v, base.user_offsets, base.scale)
