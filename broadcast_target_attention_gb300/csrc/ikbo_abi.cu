@@ -331,11 +331,13 @@ template <int D>
 int pp_grid(DeviceState* ds) {
   int& g = ds->pp_grid[D == 128 ? 1 : 0];
   if (g) return g;
-  if (cudaFuncSetAttribute(ikbo_attn_pp_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(ikbo_attn_pp_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kTcSmemBytes) != cudaSuccess ||
+      cudaFuncSetAttribute(ikbo_attn_pp_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kTcSmemBytes) != cudaSuccess)
     return 0;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ikbo_attn_pp_kernel<D>, kTcThreads,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ikbo_attn_pp_kernel<D, false>, kTcThreads,
                                                     kTcSmemBytes) != cudaSuccess ||
       per_sm <= 0) {
     cudaGetLastError();
@@ -357,7 +359,11 @@ template <int D>
 cudaError_t launch_attn_pp(const AttnParams& ap, const CUtensorMap& qmap, const CUtensorMap& qmap1,
                            const CUtensorMap& kt, const CUtensorMap& vt, const CUtensorMap& qut,
                            int grid, cudaStream_t st) {
-  return launch_ex(ikbo_attn_pp_kernel<D>, dim3(grid), dim3(kTcThreads), kTcSmemBytes, st, false, 1,
+  // the fused self + target form only for fused calls
+  if (ap.q_user)
+    return launch_ex(ikbo_attn_pp_kernel<D, true>, dim3(grid), dim3(kTcThreads), kTcSmemBytes, st, false,
+                     1, ap, qmap, qmap1, kt, vt, qut);
+  return launch_ex(ikbo_attn_pp_kernel<D, false>, dim3(grid), dim3(kTcThreads), kTcSmemBytes, st, false, 1,
                    ap, qmap, qmap1, kt, vt, qut);
 }
 

@@ -55,7 +55,9 @@ struct PpConfig {
 
 static_assert(kSoftmaxWarp0 + kPpGroups * kPpSoftmaxWarps == kTcThreads / 32, "warp roles");
 
-template <int D>
+// kSelf: a fused self + target call (items may be blocks of the user's own
+// sequence); the target-only kernel carries none of that code.
+template <int D, bool kSelf>
 __global__ void __launch_bounds__(kTcThreads, 1)
 ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant__ CUtensorMap qmap,
                     const __grid_constant__ CUtensorMap qmap1,
@@ -97,7 +99,7 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
     if (p.n_cand > 0) ptx::prefetch_tensormap(&qmap);   // a self-only call encodes no Q map
     ptx::prefetch_tensormap(&kmap_tmpl);
     ptx::prefetch_tensormap(&vmap_tmpl);
-    if (p.q_user) ptx::prefetch_tensormap(&qumap);
+    if (kSelf && p.q_user) ptx::prefetch_tensormap(&qumap);
   }
   if (p.fused && layout_ok) plan_load(p, data);
   __syncthreads();
@@ -137,12 +139,12 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
   // first cpt); for a self-attention item (fused call), sequence rows (tile
   // B holds those past the first 128)
   auto tile_cands = [&](const WorkItem& w, int g) {
-    const int per = w.q_row >= 0 ? kTileM : cpt;
+    const int per = (kSelf && w.q_row >= 0) ? kTileM : cpt;
     return g == 0 ? min(w.n_cand, per) : max(w.n_cand - per, 0);
   };
   // query rows of tile g
   auto tile_rows = [&](const WorkItem& w, int g) {
-    return w.q_row >= 0 ? tile_cands(w, g) : tile_cands(w, g) * Lq;
+    return (kSelf && w.q_row >= 0) ? tile_cands(w, g) : tile_cands(w, g) * Lq;
   };
 
   if (warp == 0) {
@@ -156,7 +158,7 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
       auto kv_map = [&](bool is_v, int32_t row) -> const void* {
         const int T = ctl->total_keys;
         // maps encoded with the row count T itself (a fused call states T)
-        if (p.exact_rows || row + kBlockN <= T)
+        if ((kSelf && p.exact_rows) || row + kBlockN <= T)
           return is_v ? (const void*)&vmap_tmpl : (const void*)&kmap_tmpl;
         CUtensorMap* tail_k = p.map_slots + 2 * blockIdx.x;
         CUtensorMap* tail_v = tail_k + 1;
@@ -207,7 +209,7 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
         const int32_t c0 = w.cand_begin + g * cpt;
         const uint32_t qbar = ptx::smem_addr(&ctl->q_full[g]);
         const uint32_t qdst = ptx::smem_addr(q_smem + g * C::kQBytes);
-        if (w.q_row >= 0) {
+        if (kSelf && w.q_row >= 0) {
           // 128 rows of the user sequence's queries (rows past T read as zeros)
           ptx::mbar_arrive_expect_tx_warp(qbar, uint32_t(C::kCB * kTileM * 128));
           for (int cb = 0; cb < C::kCB; ++cb)
@@ -495,7 +497,7 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const float2 inv2 = make_float2(inv, inv);
       uint16_t* dst;
-      if (w.q_row >= 0) {
+      if (kSelf && w.q_row >= 0) {
         // a self-attention row: out_user[q_row + 128 g + row, head, :]
         const int64_t srow = live ? (int64_t)w.q_row + g * kTileM + row : 0;
         dst = p.out_user + ((srow * p.H + w.head) * D);
