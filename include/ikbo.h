@@ -86,12 +86,15 @@ enum ikbo_status {
  * Inference", §3.1 (Fig. 10, right): candidates index their user's K/V at
  * run time instead of receiving a broadcast copy.
  *
- * Enqueues on `stream`: (1) a planning kernel that validates the index
- * tensors, groups candidates by user and writes the work list; (2) the
- * persistent tcgen05 attention kernel, which packs a user's candidates into
- * 128-row query tiles, streams that user's K/V tiles through shared memory
- * once per tile and, where a user-head is split across CTAs, merges the
- * partial results in the CTA that finishes last.
+ * Enqueues on `stream` one persistent tcgen05 attention kernel, which
+ * validates the index tensors, groups candidates by user and plans its
+ * work in its prologue (up to 20480 candidates and 1024 users; beyond, a
+ * planning kernel runs first and the attention kernel reads its work list),
+ * packs a user's candidates into 128-row query tiles, and streams that
+ * user's K/V tiles through shared memory once per tile (once per two tiles
+ * on the two-tile kernel, see ikbo_set_kernel).  When the (user, head)
+ * units are few, the two CTAs of a cluster split a unit's keys and merge
+ * their partial results through distributed shared memory.
  * All pointers are device pointers; q, k_user, v_user and out must be 16-byte
  * aligned; out must not overlap q, k_user or v_user.  n_cand == 0 is a no-op.
  */
