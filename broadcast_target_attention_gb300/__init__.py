@@ -7,7 +7,10 @@ library is missing the call raises.
 
 Layouts (see include/ikbo.h): q/out bf16 [n_cand, H, Lq, D]; k/v bf16
 [T, H, D] packed by user; user_offsets int32 [n_user+1]; cand_to_user int32
-[n_cand].
+[n_cand].  Besides the target attention: the fused self + target call, the
+user -> vendor -> item hierarchy (attention and linear compression), IKBO
+linear compression, the explicit-broadcast comparison path, the host-buffer
+and allocation-free entry points.
 """
 from __future__ import annotations
 
@@ -17,8 +20,10 @@ from typing import Optional, Tuple
 from . import _lib
 from ._lib import STATUS
 
-__all__ = ["attn_fwd", "fused_attn_fwd", "lce_fwd", "broadcast_attn_fwd", "attn_fwd_host", "attn_fwd_noalloc", "get_device_error", "set_timing",
-           "get_timing", "set_kernel", "selected_kernel", "set_debug", "launches_per_call", "version", "load", "IkboError", "STATUS"]
+__all__ = ["attn_fwd", "fused_attn_fwd", "ml_attn_fwd", "lce_fwd", "ml_lce_fwd", "broadcast_attn_fwd",
+           "attn_fwd_host", "attn_fwd_noalloc", "get_device_error", "set_timing", "get_timing",
+           "set_kernel", "selected_kernel", "set_debug", "set_trace", "launches_per_call", "version",
+           "shutdown", "load", "IkboError", "STATUS"]
 
 
 class IkboError(RuntimeError):
