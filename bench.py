@@ -214,6 +214,7 @@ while True:
 KERNEL_SOURCES = {
     "ikbo_attn_tc_kernel": ("ikbo_attn_tc.cuh", "ikbo_common.cuh", "ikbo_ptx.cuh"),
     "ikbo_attn_pp_kernel": ("ikbo_attn_pp.cuh", "ikbo_attn_tc.cuh", "ikbo_common.cuh", "ikbo_ptx.cuh"),
+    "ikbo_lce_kernel": ("ikbo_lce.cuh", "ikbo_attn_tc.cuh", "ikbo_common.cuh", "ikbo_ptx.cuh"),
 }
 
 
@@ -611,7 +612,7 @@ def run_lce(args):
     ku, kc = wl.X_user.shape[1], wl.X_cand.shape[1]
     flops = 2 * c.M * c.N * (c.n_user * c.K_user + c.n_cand * c.K_cand)
     alg_bytes = 2 * (c.M * (ku + kc) + c.n_user * ku * c.N + c.n_cand * kc * c.N + c.n_cand * c.M * c.N) \
-        + 2 * 4 * c.n_user * c.M * c.N + 4 * c.n_cand
+        + 2 * 2 * c.n_user * c.M * c.N + 4 * c.n_cand
     bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
     Wu, Wc, Xu, Xc = bf(wl.W_user), bf(wl.W_cand), bf(wl.X_user), bf(wl.X_cand)
     c2u = torch.from_numpy(wl.cand_to_user).to(dev)
@@ -685,13 +686,16 @@ def run_lce(args):
     ai = flops / alg_bytes
     ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
     gbs = alg_bytes / (ms * 1e-3) / 1e9
+    kname = f"ikbo_lce_kernel<{c.N // 64}>"
+    # DRAM bytes of the candidate stage (the launch that moves all but ~2 % of the bytes)
+    traffic = kernel_traffic(kname, c.name)
     if ai < ridge:
         roof = {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": gbs / pk["hbm_gbs"], "traffic": None, "kernel": f"ikbo_lce_kernel<{c.N // 64}>",
+                "frac": gbs / pk["hbm_gbs"], "traffic": traffic, "kernel": kname,
                 "alg_bytes_per_launch": alg_bytes, "peak_source": pk["source"] + " (burst copy)"}
     else:
         roof = {"bound": "tensor", "achieved": tf, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": tf / pk["bf16_tflops"], "traffic": None, "kernel": f"ikbo_lce_kernel<{c.N // 64}>",
+                "frac": tf / pk["bf16_tflops"], "traffic": traffic, "kernel": kname,
                 "flops_per_launch": flops, "peak_source": pk["source"] + " (burst cuBLAS bf16)"}
     h2d = sum(x.nbytes for x in (wl.W_user, wl.W_cand, wl.X_user, wl.X_cand, wl.cand_to_user))
     e2e = statistics.mean(e2e_ms)
@@ -863,11 +867,11 @@ def run_ml_lce(args):
     c = l.cfg
     ku, kv, ki = l.X_user.shape[1], l.X_vendor.shape[1], l.X_item.shape[1]
     flops = 2 * c.M * c.N * (c.n_user * c.K_user + c.n_vendor * c.K_vendor + c.n_item * c.K_item)
-    # reads of W and X once per level, the fp32 terms written once and read once per level,
+    # reads of W and X once per level, the bf16 terms written once and read once per level,
     # the bf16 output, the maps
     alg_bytes = 2 * (c.M * (ku + kv + ki) + c.n_user * ku * c.N + c.n_vendor * kv * c.N
                      + c.n_item * ki * c.N + c.n_item * c.M * c.N) \
-        + 2 * 4 * (c.n_user + c.n_vendor) * c.M * c.N + 4 * (c.n_item + c.n_vendor)
+        + 2 * 2 * (c.n_user + c.n_vendor) * c.M * c.N + 4 * (c.n_item + c.n_vendor)
     bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
     Wu, Wv, Wi, Xu, Xv, Xi = (bf(x) for x in (l.W_user, l.W_vendor, l.W_item, l.X_user, l.X_vendor,
                                               l.X_item))

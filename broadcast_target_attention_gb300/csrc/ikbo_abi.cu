@@ -977,12 +977,12 @@ int ikbo_lce_fwd(const void* W_user, const void* W_cand, const void* X_user, con
   if (encode_lce_w_map(&wc_map, W_cand, M, K_cand) != IKBO_OK ||
       encode_lce_x_map(&xc_map, X_cand, n_cand, K_cand, N) != IKBO_OK)
     return IKBO_ERR_CUDA;
-  float* Y = nullptr;
+  uint16_t* Y = nullptr;
   if (user_part) {
     if (encode_lce_w_map(&wu_map, W_user, M, K_user) != IKBO_OK ||
         encode_lce_x_map(&xu_map, X_user, n_user, K_user, N) != IKBO_OK)
       return IKBO_ERR_CUDA;
-    if (cudaMallocAsync(reinterpret_cast<void**>(&Y), size_t(n_user) * M * N * 4, st) != cudaSuccess)
+    if (cudaMallocAsync(reinterpret_cast<void**>(&Y), size_t(n_user) * M * N * 2, st) != cudaSuccess)
       return IKBO_ERR_CUDA;
   }
   LceParams lp = {};
@@ -1004,8 +1004,7 @@ int ikbo_lce_fwd(const void* W_user, const void* W_cand, const void* X_user, con
     l0.W = static_cast<const uint16_t*>(W_user);
     l0.n_batch = n_user;
     l0.K = K_user;
-    l0.out_f32 = 1;
-    l0.Y_out = Y;
+    l0.out = Y;
     l0.has_dependent = 1;
     e = launch_lce_nb(ds, NB, l0, wu_map, xu_map, false, st);
   }
@@ -1093,13 +1092,13 @@ int ikbo_ml_lce_fwd(const void* W_user, const void* W_vendor, const void* W_item
       (has_u && (encode_lce_w_map(&wu_map, W_user, M, K_user) != IKBO_OK ||
                  encode_lce_x_map(&xu_map, X_user, n_user, K_user, N) != IKBO_OK)))
     return IKBO_ERR_CUDA;
-  // fp32 terms of the user and vendor levels, library-owned, freed in stream order
-  float* Yu = nullptr;
-  float* Yv = nullptr;
-  if (has_u && cudaMallocAsync(reinterpret_cast<void**>(&Yu), size_t(n_user) * M * N * 4, st) !=
+  // bf16 terms of the user and vendor levels, library-owned, freed in stream order
+  uint16_t* Yu = nullptr;
+  uint16_t* Yv = nullptr;
+  if (has_u && cudaMallocAsync(reinterpret_cast<void**>(&Yu), size_t(n_user) * M * N * 2, st) !=
                    cudaSuccess)
     return IKBO_ERR_CUDA;
-  if (has_v && cudaMallocAsync(reinterpret_cast<void**>(&Yv), size_t(n_vendor) * M * N * 4, st) !=
+  if (has_v && cudaMallocAsync(reinterpret_cast<void**>(&Yv), size_t(n_vendor) * M * N * 2, st) !=
                    cudaSuccess) {
     if (Yu) cudaFreeAsync(Yu, st);
     return IKBO_ERR_CUDA;
@@ -1118,8 +1117,7 @@ int ikbo_ml_lce_fwd(const void* W_user, const void* W_vendor, const void* W_item
     l.W = static_cast<const uint16_t*>(W_user);
     l.n_batch = n_user;
     l.K = K_user;
-    l.out_f32 = 1;
-    l.Y_out = Yu;
+    l.out = Yu;
     l.has_dependent = 1;
     e = launch_lce_nb(ds, NB, l, wu_map, xu_map, false, st);
   }
@@ -1130,8 +1128,7 @@ int ikbo_ml_lce_fwd(const void* W_user, const void* W_vendor, const void* W_item
     l.W = static_cast<const uint16_t*>(W_vendor);
     l.n_batch = n_vendor;
     l.K = K_vendor;
-    l.out_f32 = 1;
-    l.Y_out = Yv;
+    l.out = Yv;
     l.has_dependent = 1;
     if (has_u) {
       l.add = 1;

@@ -10,16 +10,19 @@
 //
 // (§2.1: the broadcast pushed past the matrix product; the user term is
 // computed once per user, at the user batch size).  Two stages, one kernel:
-//   stage 0  Y[u] = W_user @ X_user[u] for every user, kept in fp32;
+//   stage 0  Y[u] = W_user @ X_user[u] for every user, accumulated in fp32
+//            and kept in bf16 (the term is read once per candidate row tile:
+//            in fp32 its reads cost as much L2 traffic as X itself);
 //   stage 1  out[b] = W_cand @ X_cand[b] + Y[u(b)]: the broadcast add is fused
 //            into the epilogue (§2.3), which finds Y through cand_to_user, so
 //            no broadcast tensor is ever written.
 // A user -> vendor -> item hierarchy (§5: two nested broadcasts) adds a level
 // in the middle: Y_vendor[v] = W_vendor @ X_vendor[v] + Y_user[vendor_to_user[v]]
-// in fp32, then out[i] = W_item @ X_item[i] + Y_vendor[item_to_vendor[i]].  A
-// launch is one level: its product, plus, in the epilogue, the fp32 term of
+// (in bf16), then out[i] = W_item @ X_item[i] + Y_vendor[item_to_vendor[i]].
+// A launch is one level: its product, plus, in the epilogue, the bf16 term of
 // the level above found through one map (or, when the middle level has no
-// block, through both maps), stored in fp32 for the level below or in bf16.
+// block, through both maps), summed in fp32 and stored in bf16 (the output,
+// or the term of the level below).
 // Each K block arrives zero-padded to a multiple of 8 (§2.2), so every row is
 // 16-byte aligned for the TMA.
 //
@@ -32,8 +35,7 @@
 //              two accumulators so that the epilogue of one unit overlaps the
 //              MMAs of the next;
 //   warps 4-7  epilogue: TMEM lane r = row r of the tile; 32 columns at a time,
-//              + Y of the level above, to fp32 (a term for the level below) or
-//              bf16 (the output), stored.
+//              + Y of the level above, rounded to bf16 and stored.
 // Each level is launched as a programmatic dependent of the one above; only
 // its epilogue waits for the Y it adds, so its loads and MMAs overlap the
 // level above.
@@ -70,14 +72,12 @@ struct LceParams {
   const uint16_t* W;          // bf16 [M, K] of this level's block
   const int32_t* map;         // add: batch entry -> entry of the level above
   const int32_t* map2;        // add, or null: entry of the level above -> the one above that
-  const float* Y;             // add: fp32 [rows, M, N] terms of the level(s) above
-  float* Y_out;               // out_f32: fp32 [n_batch, M, N]
-  uint16_t* out;              // otherwise: bf16 [n_batch, M, N]
+  const uint16_t* Y;          // add: bf16 [rows, M, N] terms of the level(s) above
+  uint16_t* out;              // bf16 [n_batch, M, N]: the output, or the term of the level below
   int64_t n_batch;            // entries of this level (users, vendors, candidates or items)
   int64_t n_map;              // map values must lie in [0, n_map)
   int64_t n_map2;             // map2 values must lie in [0, n_map2)
   int32_t M, K, N;
-  int32_t out_f32;            // 1: store fp32 to Y_out (a term of the level below); 0: bf16 to out
   int32_t add;                // 1: add a row of Y (after the grid above has completed)
   int32_t y_via_map2;         // add with map2: 1 = Y row map2[map[b]]; 0 = Y row map[b], map2 only checked
   int32_t has_dependent;      // 1: the level below is this grid's programmatic dependent
@@ -289,13 +289,13 @@ ikbo_lce_kernel(const __grid_constant__ LceParams p, const __grid_constant__ CUt
       constexpr int kChunks = C::N / 32;
       constexpr int kYAhead = 2;
       const bool add = p.add && live && !bad;
-      const float4* yrow = add ? reinterpret_cast<const float4*>(p.Y + (u * p.M + m) * p.N) : nullptr;
-      float4 yb[kYAhead + 1][8];
+      const uint4* yrow = add ? reinterpret_cast<const uint4*>(p.Y + (u * p.M + m) * p.N) : nullptr;
+      uint4 yb[kYAhead + 1][4];
       if (add) {
 #pragma unroll
         for (int c = 0; c < kYAhead && c < kChunks; ++c) {
 #pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4) yb[c][q4] = yrow[c * 8 + q4];
+          for (int q8 = 0; q8 < 4; ++q8) yb[c][q8] = yrow[c * 4 + q8];
         }
       }
       if (!W.warp_wait(ptx::smem_addr(&ctl->acc_full[buf]), (ui >> 1) & 1u)) break;
@@ -305,7 +305,7 @@ ikbo_lce_kernel(const __grid_constant__ LceParams p, const __grid_constant__ CUt
       for (int c = 0; c < kChunks; ++c) {
         if (add && c + kYAhead < kChunks) {
 #pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4) yb[(c + kYAhead) % (kYAhead + 1)][q4] = yrow[(c + kYAhead) * 8 + q4];
+          for (int q8 = 0; q8 < 4; ++q8) yb[(c + kYAhead) % (kYAhead + 1)][q8] = yrow[(c + kYAhead) * 4 + q8];
         }
         uint32_t o[32];
         ptx::tmem_ld32(acc + c * 32, o);
@@ -316,30 +316,25 @@ ikbo_lce_kernel(const __grid_constant__ LceParams p, const __grid_constant__ CUt
           for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(o[e]);
           if (add) {
 #pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4) {
-              const float4 t = yb[c % (kYAhead + 1)][q4];
-              x[4 * q4] += t.x;
-              x[4 * q4 + 1] += t.y;
-              x[4 * q4 + 2] += t.z;
-              x[4 * q4 + 3] += t.w;
+            for (int q8 = 0; q8 < 4; ++q8) {
+              const uint4 t = yb[c % (kYAhead + 1)][q8];
+              const uint32_t wv[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                x[8 * q8 + 2 * i] += __uint_as_float(wv[i] << 16);
+                x[8 * q8 + 2 * i + 1] += __uint_as_float(wv[i] & 0xffff0000u);
+              }
             }
           }
-          if (p.out_f32) {
-            float4* dst = reinterpret_cast<float4*>(p.Y_out + ((int64_t)b * p.M + m) * p.N + c * 32);
+          uint4* dst = reinterpret_cast<uint4*>(p.out + ((int64_t)b * p.M + m) * p.N + c * 32);
 #pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4)
-              dst[q4] = make_float4(x[4 * q4], x[4 * q4 + 1], x[4 * q4 + 2], x[4 * q4 + 3]);
-          } else {
-            uint4* dst = reinterpret_cast<uint4*>(p.out + ((int64_t)b * p.M + m) * p.N + c * 32);
-#pragma unroll
-            for (int q8 = 0; q8 < 4; ++q8) {
-              uint4 v;
-              v.x = pack_bf16(x[8 * q8], x[8 * q8 + 1]);
-              v.y = pack_bf16(x[8 * q8 + 2], x[8 * q8 + 3]);
-              v.z = pack_bf16(x[8 * q8 + 4], x[8 * q8 + 5]);
-              v.w = pack_bf16(x[8 * q8 + 6], x[8 * q8 + 7]);
-              dst[q8] = v;
-            }
+          for (int q8 = 0; q8 < 4; ++q8) {
+            uint4 v;
+            v.x = pack_bf16(x[8 * q8], x[8 * q8 + 1]);
+            v.y = pack_bf16(x[8 * q8 + 2], x[8 * q8 + 3]);
+            v.z = pack_bf16(x[8 * q8 + 4], x[8 * q8 + 5]);
+            v.w = pack_bf16(x[8 * q8 + 6], x[8 * q8 + 7]);
+            dst[q8] = v;
           }
         }
       }

@@ -243,7 +243,7 @@ int ikbo_fused_attn_fwd(const void* q, const void* q_user, const void* k_user, c
  *
  *   out[b] = W_user @ X_user[u] + W_cand @ X_cand[b]         (M x N)
  *
- * The user term is computed once per user (fp32, kept in a library-owned
+ * The user term is computed once per user (accumulated in fp32, kept in bf16 in a library-owned
  * buffer) and added in the epilogue of the candidate product, so the user
  * block is never copied per candidate (§2.1-§2.3).  Two launches of one
  * tcgen05 kernel, the second a programmatic dependent of the first.
@@ -275,8 +275,8 @@ int ikbo_lce_fwd(const void* W_user, const void* W_cand, const void* X_user, con
  *
  * Each level's product is computed once per entry of that level: up to three
  * launches of the linear-compression kernel, each a programmatic dependent
- * of the one before, users (fp32 terms), then vendors (their product plus
- * their user's term, fp32), then items (their product plus their vendor's
+ * of the one before, users (bf16 terms), then vendors (their product plus
+ * their user's term, bf16), then items (their product plus their vendor's
  * term, to bf16).  No block is ever copied per vendor or per item.
  *
  *   W_user [M, K_user], W_vendor [M, K_vendor], W_item [M, K_item]    bf16
