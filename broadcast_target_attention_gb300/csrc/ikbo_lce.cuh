@@ -11,8 +11,8 @@
 // (§2.1: the broadcast pushed past the matrix product; the user term is
 // computed once per user, at the user batch size).  Two stages, one kernel:
 //   stage 0  Y[u] = W_user @ X_user[u] for every user, accumulated in fp32
-//            and kept in bf16 (the term is read once per candidate row tile:
-//            in fp32 its reads cost as much L2 traffic as X itself);
+//            and kept in bf16 (the term is read once per candidate and row
+//            tile, 128 x N values each time: bf16 halves those reads);
 //   stage 1  out[b] = W_cand @ X_cand[b] + Y[u(b)]: the broadcast add is fused
 //            into the epilogue (§2.3), which finds Y through cand_to_user, so
 //            no broadcast tensor is ever written.
