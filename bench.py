@@ -559,15 +559,18 @@ def run_fused(args):
     # the SIMT choice runs fused calls on the one-tile kernel
     choice = ikbo.selected_kernel(wl.n_cand, wl.n_user, c.H, c.Lq)
     kname = f"{ikbo.KERNEL_NAMES[ikbo.KERNEL_TC if choice == ikbo.KERNEL_SIMT else choice]}<{c.D}>"
+    if choice == ikbo.KERNEL_TC2:
+        kname = kname[:-1] + ", true>"          # the fused instantiation of the two-tile kernel
+    traffic = kernel_traffic(kname, c.name)
     if ai < ridge:
         gbs = alg_bytes / (ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": gbs / pk["hbm_gbs"], "traffic": None, "kernel": kname,
+                "frac": gbs / pk["hbm_gbs"], "traffic": traffic, "kernel": kname,
                 "alg_bytes_per_launch": alg_bytes, "peak_source": pk["source"] + " (burst copy)"}
     else:
         tf = flops / (ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": tf, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": tf / pk["bf16_tflops"], "traffic": None, "kernel": kname,
+                "frac": tf / pk["bf16_tflops"], "traffic": traffic, "kernel": kname,
                 "flops_per_launch": flops, "peak_source": pk["source"] + " (burst cuBLAS bf16)"}
     h2d = sum(x.nbytes for x in (wl.q, qu_bits, wl.k, wl.v, wl.user_offsets, wl.cand_to_user))
     d2h = wl.q.nbytes + qu_bits.nbytes
