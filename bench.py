@@ -613,9 +613,8 @@ def run_lce(args):
     wl = W.lce_generate(W.LCE_CONFIGS[args.lce])
     c = wl.cfg
     ku, kc = wl.X_user.shape[1], wl.X_cand.shape[1]
-    flops = 2 * c.M * c.N * (c.n_user * c.K_user + c.n_cand * c.K_cand)
-    alg_bytes = 2 * (c.M * (ku + kc) + c.n_user * ku * c.N + c.n_cand * kc * c.N + c.n_cand * c.M * c.N) \
-        + 2 * 2 * c.n_user * c.M * c.N + 4 * c.n_cand
+    flops = A.lce_flops(c.M, c.N, c.n_user, c.K_user, c.n_cand, c.K_cand)
+    alg_bytes = A.lce_alg_bytes(c.M, c.N, c.n_user, ku, c.n_cand, kc)
     bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
     Wu, Wc, Xu, Xc = bf(wl.W_user), bf(wl.W_cand), bf(wl.X_user), bf(wl.X_cand)
     c2u = torch.from_numpy(wl.cand_to_user).to(dev)
@@ -869,12 +868,8 @@ def run_ml_lce(args):
     l = W.lce_ml_generate(W.LCE_ML_CONFIGS[args.lce_ml])
     c = l.cfg
     ku, kv, ki = l.X_user.shape[1], l.X_vendor.shape[1], l.X_item.shape[1]
-    flops = 2 * c.M * c.N * (c.n_user * c.K_user + c.n_vendor * c.K_vendor + c.n_item * c.K_item)
-    # reads of W and X once per level, the bf16 terms written once and read once per level,
-    # the bf16 output, the maps
-    alg_bytes = 2 * (c.M * (ku + kv + ki) + c.n_user * ku * c.N + c.n_vendor * kv * c.N
-                     + c.n_item * ki * c.N + c.n_item * c.M * c.N) \
-        + 2 * 2 * (c.n_user + c.n_vendor) * c.M * c.N + 4 * (c.n_item + c.n_vendor)
+    flops = A.ml_lce_flops(c.M, c.N, c.n_user, c.K_user, c.n_vendor, c.K_vendor, c.n_item, c.K_item)
+    alg_bytes = A.ml_lce_alg_bytes(c.M, c.N, c.n_user, ku, c.n_vendor, kv, c.n_item, ki)
     bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
     Wu, Wv, Wi, Xu, Xv, Xi = (bf(x) for x in (l.W_user, l.W_vendor, l.W_item, l.X_user, l.X_vendor,
                                               l.X_item))
