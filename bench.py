@@ -6,7 +6,10 @@ A step is one pass of the whole hot path (the tcgen05 attention kernel, which
 plans in-kernel for this batch) over one batch of the headline workload: 1024 candidates over 15
 users (~70:1), user sequences of 256-1024 keys, H=4, D=128, Lq=1, bf16,
 seeded synthetic inputs already resident in HBM.  L2 is flushed (a write
-larger than L2) before every timed step.  `value` is whole-job TFLOP/s
+larger than L2) before every timed step.  The block of --steps timed steps is
+repeated (`repeats` in the line) until it lasts --min-timed-s, so that the
+clock samples come from inside the timed region; ms_per_step is the mean over
+every timed step.  `value` is whole-job TFLOP/s
 (4*H*D*Lq*S FLOPs, S = keys visited over all candidates); `e2e` is the same
 metric through the host-buffer entry point with the copies inside the timed
 region.  Under torchrun every rank runs its own replica (users shard with no
@@ -214,6 +217,7 @@ while True:
 KERNEL_SOURCES = {
     "ikbo_attn_tc_kernel": ("ikbo_attn_tc.cuh", "ikbo_common.cuh", "ikbo_ptx.cuh"),
     "ikbo_attn_pp_kernel": ("ikbo_attn_pp.cuh", "ikbo_attn_tc.cuh", "ikbo_common.cuh", "ikbo_ptx.cuh"),
+    "ikbo_attn_ab_kernel": ("ikbo_attn_ab.cuh", "ikbo_attn_tc.cuh", "ikbo_common.cuh", "ikbo_ptx.cuh"),
     "ikbo_lce_kernel": ("ikbo_lce.cuh", "ikbo_attn_tc.cuh", "ikbo_common.cuh", "ikbo_ptx.cuh"),
 }
 
@@ -325,6 +329,7 @@ def run_ikbo(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     ikbo.load()
+    ikbo.set_kernel(args.kernel)
     wl = workload_for_rank(args.config, rank)
     c = wl.cfg
     nums = A.workload_numbers(wl)
@@ -355,12 +360,24 @@ def run_ikbo(args):
             flush.fill_(1)
             step()
         assert ikbo.get_device_error() == 0
-        # 1. timed steps: flush, then the hot path between two events, back to back
-        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        # 1. timed steps: flush, then the hot path between two events, back to back.
+        # The block of K steps is repeated R times, enqueued without a pause, so that the
+        # timed region lasts long enough for the clock samples to fall inside it; R comes
+        # from one untimed block and is the largest over the ranks.
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            step()
+        barrier()
+        block_s = max(time.perf_counter() - t0, 1e-6)
+        repeats = R.max_over_ranks(float(max(1, int(np.ceil(args.min_timed_s / block_s)))), dev)
+        repeats = int(min(repeats, max(1, 20000 // max(args.steps, 1))))
+        n_timed = repeats * args.steps
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(n_timed)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(n_timed)]
         barrier()
         clk.mark_start()
-        for i in range(args.steps):
+        for i in range(n_timed):
             flush.fill_(i & 0xFF)
             starts[i].record()
             step()
@@ -437,6 +454,7 @@ def run_ikbo(args):
     bc = statistics.mean(bc_ms)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "repeats": repeats, "timed_steps": n_timed,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": config_block(wl, {"parallelism": f"{ws} independent replica(s), users sharded, no exchange"}),
@@ -478,6 +496,7 @@ def run_fused(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     ikbo.load()
+    ikbo.set_kernel(args.kernel)
     wl = workload_for_rank(args.config, rank)
     c = wl.cfg
     lens = np.diff(wl.user_offsets.astype(np.int64))
@@ -1007,6 +1026,10 @@ def main():
     ap.add_argument("--impl", default="ikbo", choices=["ikbo", "reference"])
     ap.add_argument("--config", default=W.HEADLINE, choices=sorted(W.CONFIGS))
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--kernel", type=int, default=0, choices=[0, 1, 2, 3, 4],
+                    help="attention kernel (ikbo_set_kernel): 0 = the automatic choice")
+    ap.add_argument("--min-timed-s", type=float, default=0.25,
+                    help="repeat the block of --steps timed steps until it lasts this long")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--lce", default=None, choices=sorted(W.LCE_CONFIGS),
                     help="measure IKBO linear compression on this workload instead")

@@ -23,7 +23,7 @@ from ._lib import STATUS
 __all__ = ["attn_fwd", "fused_attn_fwd", "ml_attn_fwd", "lce_fwd", "ml_lce_fwd", "broadcast_attn_fwd",
            "attn_fwd_host", "attn_fwd_noalloc", "get_device_error", "set_timing", "get_timing",
            "set_kernel", "selected_kernel", "set_debug", "set_trace", "launches_per_call", "version",
-           "shutdown", "load", "IkboError", "STATUS"]
+           "shutdown", "pool_usage", "load", "IkboError", "STATUS"]
 
 
 class IkboError(RuntimeError):
@@ -280,6 +280,17 @@ def attn_fwd_noalloc(q, k, v, user_offsets, cand_to_user, scale: Optional[float]
     return out
 
 
+def pool_usage(reset: bool = False) -> Tuple[int, int]:
+    """(bytes held now, most bytes held at once since the last reset) of the library's own
+    stream-ordered pool on the current device; ``reset`` restarts the high-water mark
+    (test hook, see ikbo_pool_usage in include/ikbo.h)."""
+    now = ctypes.c_uint64()
+    high = ctypes.c_uint64()
+    _check(_lib.lib().ikbo_pool_usage(1 if reset else 0, ctypes.byref(now), ctypes.byref(high)),
+           "ikbo_pool_usage")
+    return now.value, high.value
+
+
 def get_device_error(stream=None) -> int:
     """Synchronise the stream; return and clear the device error word (0 = none)."""
     return int(_lib.lib().ikbo_get_device_error(_stream_handle(stream)))
@@ -298,20 +309,21 @@ def get_timing() -> Tuple[float, float]:
 
 
 # kernel choices of set_kernel / results of selected_kernel
-KERNEL_AUTO, KERNEL_SIMT, KERNEL_TC, KERNEL_TC2 = 0, 1, 2, 3
+KERNEL_AUTO, KERNEL_SIMT, KERNEL_TC, KERNEL_TC2, KERNEL_AB = 0, 1, 2, 3, 4
 KERNEL_NAMES = {KERNEL_SIMT: "ikbo_attn_simt_kernel", KERNEL_TC: "ikbo_attn_tc_kernel",
-                KERNEL_TC2: "ikbo_attn_pp_kernel"}
+                KERNEL_TC2: "ikbo_attn_pp_kernel", KERNEL_AB: "ikbo_attn_ab_kernel"}
 
 
 def set_kernel(which: int) -> int:
     """0 = automatic (default), 1 = SIMT cross-check kernel, 2 = tcgen05 kernel with one
     query tile per work item, 3 = tcgen05 kernel with two query tiles of one user and head
-    per work item; returns the previous choice."""
+    per work item, 4 = tcgen05 kernel with the key tiles of one query tile over two softmax
+    warpgroups; returns the previous choice."""
     return int(_lib.lib().ikbo_set_kernel(int(which)))
 
 
 def selected_kernel(n_cand: int, n_user: int, H: int, Lq: int) -> int:
-    """The kernel (1, 2 or 3) a call of these sizes runs with this thread's choice."""
+    """The kernel (1 to 4) a call of these sizes runs with this thread's choice."""
     n = int(_lib.lib().ikbo_selected_kernel(int(n_cand), int(n_user), int(H), int(Lq)))
     _check(min(n, 0), "selected_kernel")
     return n

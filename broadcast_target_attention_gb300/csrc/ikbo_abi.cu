@@ -6,11 +6,13 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <vector>
 
 #include "../../include/ikbo.h"
 #include "ikbo_attn_simt.cuh"
+#include "ikbo_attn_ab.cuh"
 #include "ikbo_attn_pp.cuh"
 #include "ikbo_attn_tc.cuh"
 #include "ikbo_broadcast.cuh"
@@ -34,10 +36,16 @@ struct DeviceState {
   int num_sms = 0;
   int tc_grid[2] = {0, 0};   // CTAs of the tcgen05 kernel (clusters of 2), D = 64 / 128
   int pp_grid[2] = {0, 0};   // CTAs of the two-tile tcgen05 kernel, D = 64 / 128
+  int ab_grid[2] = {0, 0};   // CTAs of the key-interleaved tcgen05 kernel, D = 64 / 128
+  std::atomic<uint64_t>* calls = nullptr;   // calls so far: the key-interleaved kernel's marker
   bool lce_ready[4] = {false, false, false, false};   // shared-memory attribute set, N = 64 .. 256
   int lce_clusters[4][9] = {};   // co-resident clusters of the LCE kernel, by N / 64 and cluster size
-  int* err_host = nullptr;       // pinned copy of the error word for the host-buffer entry point
+  int* err_host = nullptr;       // pinned copy of the error word, made by the host-buffer entry point
   std::mutex* host_call = nullptr;   // serialises that entry point's use of err_host
+  // The library's own stream-ordered pool on this device, made by the first
+  // call that allocates: it keeps freed scratch between calls (the device's
+  // default pool, which other code may use, is left as it is).
+  cudaMemPool_t pool = nullptr;
   int* err_word = nullptr;
   cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
   bool ev_ready = false;
@@ -51,9 +59,10 @@ int g_debug_flags = 0;
 uint64_t* g_trace = nullptr;
 uint64_t g_timeout_ns = kDefaultTimeoutNs;
 // Kernel choice of this thread (ikbo_set_kernel): 0 = automatic, 1 = SIMT,
-// 2 = tcgen05 with one query tile per item, 3 = tcgen05 with two.
+// 2 = tcgen05 with one query tile per item, 3 = tcgen05 with two, 4 =
+// tcgen05 with the key tiles of one query tile over two warpgroups.
 thread_local int t_kernel = 0;
-enum { kKernAuto = 0, kKernSimt = 1, kKernTc = 2, kKernPp = 3 };
+enum { kKernAuto = 0, kKernSimt = 1, kKernTc = 2, kKernPp = 3, kKernAb = 4 };
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                    const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -82,13 +91,6 @@ int device_state(DeviceState** out) {
     if (major != 10 || minor != 3) return IKBO_ERR_DEVICE;
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_ikbo_error_word) != cudaSuccess) return IKBO_ERR_CUDA;
-    // Keep freed scratch in the stream-ordered pool instead of returning it
-    // to the driver after every call.
-    cudaMemPool_t pool;
-    if (cudaDeviceGetDefaultMemPool(&pool, dev) == cudaSuccess) {
-      uint64_t thr = UINT64_MAX;
-      cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &thr);
-    }
     if (!g_encode) {
       cudaDriverEntryPointQueryResult q;
       void* fn = nullptr;
@@ -98,16 +100,49 @@ int device_state(DeviceState** out) {
         return IKBO_ERR_CUDA;
       g_encode = reinterpret_cast<EncodeTiledFn>(fn);
     }
-    void* h = nullptr;
-    if (cudaHostAlloc(&h, sizeof(int), cudaHostAllocDefault) != cudaSuccess) return IKBO_ERR_CUDA;
-    s.err_host = static_cast<int*>(h);
     s.host_call = new std::mutex();   // lives as long as the process, like this state
+    s.calls = new std::atomic<uint64_t>(0);
     s.num_sms = sms;
     s.err_word = static_cast<int*>(p);
     s.ready = true;
   }
   *out = &s;
   return IKBO_OK;
+}
+
+// `bytes` of scratch from the library's pool on the current device, in
+// stream order on `st` (made on first use; freed memory stays in the pool).
+// Under stream capture the allocation becomes a graph memory node.
+cudaError_t pool_alloc(DeviceState* ds, void** ptr, size_t bytes, cudaStream_t st) {
+  cudaMemPool_t pool = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!ds->pool) {
+      int dev = 0;
+      cudaError_t e = cudaGetDevice(&dev);
+      if (e != cudaSuccess) return e;
+      cudaMemPoolProps props = {};
+      props.allocType = cudaMemAllocationTypePinned;
+      props.handleTypes = cudaMemHandleTypeNone;
+      props.location.type = cudaMemLocationTypeDevice;
+      props.location.id = dev;
+      cudaMemPool_t made = nullptr;
+      if ((e = cudaMemPoolCreate(&made, &props)) != cudaSuccess) return e;
+      uint64_t keep = UINT64_MAX;
+      if ((e = cudaMemPoolSetAttribute(made, cudaMemPoolAttrReleaseThreshold, &keep)) != cudaSuccess) {
+        cudaMemPoolDestroy(made);
+        return e;
+      }
+      ds->pool = made;
+    }
+    pool = ds->pool;
+  }
+  return cudaMallocFromPoolAsync(ptr, bytes, pool, st);
+}
+
+template <typename T>
+cudaError_t pool_alloc(DeviceState* ds, T** ptr, size_t bytes, cudaStream_t st) {
+  return pool_alloc(ds, reinterpret_cast<void**>(ptr), bytes, st);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -147,8 +182,8 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Layout of the per-call scratch space.
 struct Workspace {
   size_t header, kmap, vmap, items, units, perm, cand_start, scratch, partial_o, partial_ml,
-      cta_items, map_slots, item_user, total;
-  int max_items, max_split_items, max_units, max_cta_items, grid;
+      cta_items, map_slots, item_user, ab_o, ab_lse, ab_flags, total;
+  int max_items, max_split_items, max_units, max_cta_items, grid, map_stride;
   int kernel;   // kKernSimt, kKernTc or kKernPp
   bool fused;
 };
@@ -166,13 +201,19 @@ bool fits_in_kernel_planning(int64_t n_cand, int64_t n_user) {
 // which it cannot spread evenly over the SMs.
 constexpr int64_t kPpMinItems = 600;
 
-// The kernel a call runs with the thread's choice.  The two-tile kernel plans
-// in-kernel only, so inputs beyond those limits take the one-tile kernel.
+// The kernel a call runs with the thread's choice.  The two-tile and the
+// key-interleaved kernels plan in-kernel only, so inputs beyond those limits
+// take the one-tile kernel.
 int effective_kernel(int64_t n_cand, int64_t n_user, int H, int Lq) {
   if (t_kernel == kKernSimt) return kKernSimt;
   if (t_kernel == kKernTc || !fits_in_kernel_planning(n_cand, n_user)) return kKernTc;
   if (t_kernel == kKernPp) return kKernPp;
-  const int64_t pair = 2 * int64_t(cands_per_tile(Lq));        // candidates of a two-tile item
+  // the key-interleaved kernel only when chosen: it is faster when a few
+  // units are very long, which the host cannot see (the sequence lengths are
+  // on the device), and slower on short ones
+  if (t_kernel == kKernAb) return kKernAb;
+  const int64_t cpt = cands_per_tile(Lq);
+  const int64_t pair = 2 * cpt;        // candidates of a two-tile item
   const bool two_tiles = n_cand >= pair * n_user;
   const int64_t items = int64_t(H) * ((n_cand + pair - 1) / pair);
   return (two_tiles && items >= kPpMinItems) ? kKernPp : kKernTc;
@@ -208,9 +249,18 @@ Workspace plan_workspace(int64_t n_cand, int64_t n_user, int H, int Lq, int D, i
   };
   w.header = take(sizeof(PlanHeader));
   w.perm = take(sizeof(int32_t) * size_t(n_cand));
+  // per CTA: the K and V maps with the row count T, then one bounded V map per work item
+  const int64_t listed_per_cta = (int64_t(w.max_items) + grid - 1) / grid;
+  w.map_stride = 2 + int(listed_per_cta > w.max_cta_items ? listed_per_cta : w.max_cta_items);
+  w.map_slots = take(sizeof(CUtensorMap) * size_t(grid) * size_t(w.map_stride));
   if (w.fused) {
     w.cta_items = take(sizeof(WorkItem) * size_t(grid) * size_t(w.max_cta_items));
-    w.map_slots = take(sizeof(CUtensorMap) * size_t(grid) * 2);
+    if (kernel == kKernAb) {
+      // partial results of units cut into key-range chunks: one chunk per CTA
+      w.ab_o = take(sizeof(float) * size_t(grid) * kTileM * D);
+      w.ab_lse = take(sizeof(float) * size_t(grid) * kTileM);
+      w.ab_flags = take(sizeof(unsigned long long) * size_t(grid));
+    }
   } else {
     w.kmap = take(sizeof(CUtensorMap));
     w.vmap = take(sizeof(CUtensorMap));
@@ -326,6 +376,26 @@ int tc_grid(DeviceState* ds) {
   return g;
 }
 
+// CTAs of the key-interleaved kernel: one per SM, no clusters, all resident
+// at once (a unit cut into chunks is merged by a CTA that waits for the others).
+template <int D>
+int ab_grid(DeviceState* ds) {
+  int& g = ds->ab_grid[D == 128 ? 1 : 0];
+  if (g) return g;
+  if (cudaFuncSetAttribute(ikbo_attn_ab_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kTcSmemBytes) != cudaSuccess)
+    return 0;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ikbo_attn_ab_kernel<D>, kTcThreads,
+                                                    kTcSmemBytes) != cudaSuccess ||
+      per_sm <= 0) {
+    cudaGetLastError();
+    return 0;
+  }
+  g = ds->num_sms * per_sm;
+  return g;
+}
+
 // CTAs of the two-tile kernel: one per SM, no clusters.
 template <int D>
 int pp_grid(DeviceState* ds) {
@@ -353,6 +423,13 @@ cudaError_t launch_attn_tc(const AttnParams& ap, const CUtensorMap& qmap, const 
                            int grid, bool pdl, cudaStream_t st) {
   return launch_ex(ikbo_attn_tc_kernel<D>, dim3(grid), dim3(kTcThreads), kTcSmemBytes, st, pdl, 2,
                    ap, qmap, qmap1, kt, vt, qut);
+}
+
+template <int D>
+cudaError_t launch_attn_ab(const AttnParams& ap, const CUtensorMap& qmap, const CUtensorMap& qmap1,
+                           const CUtensorMap& kt, const CUtensorMap& vt, int grid, cudaStream_t st) {
+  return launch_ex(ikbo_attn_ab_kernel<D>, dim3(grid), dim3(kTcThreads), kTcSmemBytes, st, false, 1, ap,
+                   qmap, qmap1, kt, vt);
 }
 
 template <int D>
@@ -473,6 +550,13 @@ int run_ikbo(DeviceState* ds, const void* q, const void* k, const void* v, const
   ap.max_cta_items = L.max_cta_items;
   ap.perm_ws = pp.perm;
   ap.map_slots = reinterpret_cast<CUtensorMap*>(ws + L.map_slots);
+  ap.map_stride = L.map_stride;
+  if (kernel == kKernAb) {
+    ap.ab_partial_o = reinterpret_cast<float4*>(ws + L.ab_o);
+    ap.ab_partial_lse = reinterpret_cast<float*>(ws + L.ab_lse);
+    ap.ab_flags = reinterpret_cast<unsigned long long*>(ws + L.ab_flags);
+    ap.ab_marker = ((ds->calls->fetch_add(1) + 1) << 1) | 1ull;
+  }
   if (self) {
     ap.q_user = static_cast<const uint16_t*>(self->q_user);
     ap.out_user = static_cast<uint16_t*>(self->out_user);
@@ -498,6 +582,11 @@ int run_ikbo(DeviceState* ds, const void* q, const void* k, const void* v, const
       e = launch_pdl(ikbo_attn_simt_kernel<64>, dim3(grid), dim3(kSimtThreads), 0, st, ap);
     else
       e = launch_pdl(ikbo_attn_simt_kernel<128>, dim3(grid), dim3(kSimtThreads), 0, st, ap);
+  } else if (kernel == kKernAb) {
+    if (D == 64)
+      e = launch_attn_ab<64>(ap, qmap, qmap1, px.kmap_tmpl, px.vmap_tmpl, L.grid, st);
+    else
+      e = launch_attn_ab<128>(ap, qmap, qmap1, px.kmap_tmpl, px.vmap_tmpl, L.grid, st);
   } else if (kernel == kKernPp) {
     if (D == 64)
       e = launch_attn_pp<64>(ap, qmap, qmap1, px.kmap_tmpl, px.vmap_tmpl, qumap, L.grid, st);
@@ -528,8 +617,12 @@ int call_workspace(DeviceState* ds, int64_t n_cand, int64_t n_user, int H, int L
                    Workspace* out, int64_t self_T = -1, bool multi_level = false) {
   int grid = 0;
   int kernel = effective_kernel(n_cand, n_user, H, Lq);
-  if (self_T >= 0 && kernel == kKernSimt) kernel = kKernTc;
-  if (kernel == kKernTc) {
+  // fused self + target calls run on the one- or two-tile kernel
+  if (self_T >= 0 && (kernel == kKernSimt || kernel == kKernAb)) kernel = kKernTc;
+  if (kernel == kKernAb) {
+    grid = D == 64 ? ab_grid<64>(ds) : ab_grid<128>(ds);
+    if (grid <= 0) return IKBO_ERR_CUDA;
+  } else if (kernel == kKernTc) {
     grid = D == 64 ? tc_grid<64>(ds) : tc_grid<128>(ds);
     if (grid <= 0) return IKBO_ERR_CUDA;
   } else if (kernel == kKernPp) {
@@ -572,7 +665,7 @@ int ikbo_attn_fwd(const void* q, const void* k_user, const void* v_user,
   Workspace L;
   if ((rc = call_workspace(ds, n_cand, n_user, H, Lq, D, &L)) != IKBO_OK) return rc;
   void* ws = nullptr;
-  if (cudaMallocAsync(&ws, L.total, st) != cudaSuccess) return IKBO_ERR_CUDA;
+  if (pool_alloc(ds, &ws, L.total, st) != cudaSuccess) return IKBO_ERR_CUDA;
   rc = run_ikbo(ds, q, k_user, v_user, user_offsets, cand_to_user, n_cand, n_user, H, Lq, D, scale,
                 out, static_cast<char*>(ws), L, st);
   if (cudaFreeAsync(ws, st) != cudaSuccess && rc == IKBO_OK) rc = IKBO_ERR_CUDA;
@@ -612,7 +705,7 @@ int ikbo_attn_fwd_host(const void* q, const void* k_user, const void* v_user,
   const size_t o_out = align_up(o_c2u + size_t(n_cand) * 4, 256);
   const size_t o_ws = align_up(o_out + qbytes, 256);
   char* buf = nullptr;
-  if (cudaMallocAsync(reinterpret_cast<void**>(&buf), o_ws + L.total, st) != cudaSuccess)
+  if (pool_alloc(ds, &buf, o_ws + L.total, st) != cudaSuccess)
     return IKBO_ERR_CUDA;
   cudaError_t e = cudaSuccess;
   if (e == cudaSuccess) e = cudaMemcpyAsync(buf + o_q, q, qbytes, cudaMemcpyHostToDevice, st);
@@ -630,8 +723,17 @@ int ikbo_attn_fwd_host(const void* q, const void* k_user, const void* v_user,
   }
   cudaFreeAsync(buf, st);
   // the device error word comes back with the output, under the same
-  // synchronisation (a pinned word per device, one host call at a time)
+  // synchronisation (a pinned word per device, made on the first such call;
+  // one host call at a time)
   std::lock_guard<std::mutex> lock(*ds->host_call);
+  if (!ds->err_host) {
+    void* h = nullptr;
+    if (cudaHostAlloc(&h, sizeof(int), cudaHostAllocDefault) != cudaSuccess) {
+      cudaStreamSynchronize(st);
+      return IKBO_ERR_CUDA;
+    }
+    ds->err_host = static_cast<int*>(h);
+  }
   if (e == cudaSuccess && rc == IKBO_OK)
     e = cudaMemcpyAsync(ds->err_host, ds->err_word, sizeof(int), cudaMemcpyDeviceToHost, st);
   if (cudaStreamSynchronize(st) != cudaSuccess || e != cudaSuccess) return IKBO_ERR_CUDA;
@@ -721,7 +823,7 @@ int ikbo_broadcast_attn_fwd(const void* q, const void* k_user, const void* v_use
   const size_t m_id = align_up(m_offb + offb.size() * 4, 256);
   const size_t m_total = align_up(m_id + id.size() * 4, 256);
   char* meta = nullptr;
-  if (cudaMallocAsync(reinterpret_cast<void**>(&meta), m_total, st) != cudaSuccess)
+  if (pool_alloc(ds, &meta, m_total, st) != cudaSuccess)
     return IKBO_ERR_CUDA;
   cudaError_t e = cudaMemcpyAsync(meta + m_src, src.data(), src.size() * 4, cudaMemcpyHostToDevice, st);
   if (e == cudaSuccess) e = cudaMemcpyAsync(meta + m_dst, dst.data(), dst.size() * 8, cudaMemcpyHostToDevice, st);
@@ -750,7 +852,7 @@ int ikbo_broadcast_attn_fwd(const void* q, const void* k_user, const void* v_use
     const size_t o_kb = 0, o_vb = align_up(size_t(rows) * row_bytes, 256);
     const size_t o_ws = align_up(o_vb + size_t(rows) * row_bytes, 256);
     char* buf = nullptr;
-    if (cudaMallocAsync(reinterpret_cast<void**>(&buf), o_ws + L.total, st) != cudaSuccess) {
+    if (pool_alloc(ds, &buf, o_ws + L.total, st) != cudaSuccess) {
       rc = IKBO_ERR_CUDA;
       break;
     }
@@ -814,7 +916,7 @@ int ikbo_fused_attn_fwd(const void* q, const void* q_user, const void* k_user, c
   Workspace L;
   if ((rc = call_workspace(ds, n_cand, n_user, H, Lq, D, &L, T)) != IKBO_OK) return rc;
   void* ws = nullptr;
-  if (cudaMallocAsync(&ws, L.total, st) != cudaSuccess) return IKBO_ERR_CUDA;
+  if (pool_alloc(ds, &ws, L.total, st) != cudaSuccess) return IKBO_ERR_CUDA;
   const SelfPart self{q_user, out_user, T};
   rc = run_ikbo(ds, q, k_user, v_user, user_offsets, cand_to_user, n_cand, n_user, H, Lq, D, scale,
                 out, static_cast<char*>(ws), L, st, &self);
@@ -841,7 +943,7 @@ int ikbo_ml_attn_fwd(const void* q, const void* k_user, const void* v_user,
   Workspace L;
   if ((rc = call_workspace(ds, n_item, n_user, H, Lq, D, &L, -1, true)) != IKBO_OK) return rc;
   void* ws = nullptr;
-  if (cudaMallocAsync(&ws, L.total, st) != cudaSuccess) return IKBO_ERR_CUDA;
+  if (pool_alloc(ds, &ws, L.total, st) != cudaSuccess) return IKBO_ERR_CUDA;
   const VendorLevel vendor{vendor_to_user, n_vendor};
   rc = run_ikbo(ds, q, k_user, v_user, user_offsets, item_to_vendor, n_item, n_user, H, Lq, D,
                 scale, out, static_cast<char*>(ws), L, st, nullptr, &vendor);
@@ -982,7 +1084,7 @@ int ikbo_lce_fwd(const void* W_user, const void* W_cand, const void* X_user, con
     if (encode_lce_w_map(&wu_map, W_user, M, K_user) != IKBO_OK ||
         encode_lce_x_map(&xu_map, X_user, n_user, K_user, N) != IKBO_OK)
       return IKBO_ERR_CUDA;
-    if (cudaMallocAsync(reinterpret_cast<void**>(&Y), size_t(n_user) * M * N * 2, st) != cudaSuccess)
+    if (pool_alloc(ds, &Y, size_t(n_user) * M * N * 2, st) != cudaSuccess)
       return IKBO_ERR_CUDA;
   }
   LceParams lp = {};
@@ -1095,10 +1197,10 @@ int ikbo_ml_lce_fwd(const void* W_user, const void* W_vendor, const void* W_item
   // bf16 terms of the user and vendor levels, library-owned, freed in stream order
   uint16_t* Yu = nullptr;
   uint16_t* Yv = nullptr;
-  if (has_u && cudaMallocAsync(reinterpret_cast<void**>(&Yu), size_t(n_user) * M * N * 2, st) !=
+  if (has_u && pool_alloc(ds, &Yu, size_t(n_user) * M * N * 2, st) !=
                    cudaSuccess)
     return IKBO_ERR_CUDA;
-  if (has_v && cudaMallocAsync(reinterpret_cast<void**>(&Yv), size_t(n_vendor) * M * N * 2, st) !=
+  if (has_v && pool_alloc(ds, &Yv, size_t(n_vendor) * M * N * 2, st) !=
                    cudaSuccess) {
     if (Yu) cudaFreeAsync(Yu, st);
     return IKBO_ERR_CUDA;
@@ -1202,8 +1304,8 @@ int ikbo_shutdown(void) {
       if (e) cudaEventDestroy(e);
     if (s.err_host) cudaFreeHost(s.err_host);
     delete s.host_call;
-    cudaMemPool_t pool;
-    if (cudaDeviceGetDefaultMemPool(&pool, d) != cudaSuccess || cudaMemPoolTrimTo(pool, 0) != cudaSuccess)
+    delete s.calls;
+    if (s.pool && (cudaMemPoolTrimTo(s.pool, 0) != cudaSuccess || cudaMemPoolDestroy(s.pool) != cudaSuccess))
       rc = IKBO_ERR_CUDA;
     s = DeviceState{};
   }
@@ -1259,6 +1361,32 @@ int ikbo_set_debug(int flags, uint64_t timeout_ns) {
   return IKBO_OK;
 }
 
+int ikbo_pool_usage(int reset, uint64_t* used_now, uint64_t* used_high) {
+  if (used_now) *used_now = 0;
+  if (used_high) *used_high = 0;
+  DeviceState* ds = nullptr;
+  const int rc = device_state(&ds);
+  if (rc != IKBO_OK) return rc;
+  cudaMemPool_t pool = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    pool = ds->pool;
+  }
+  if (!pool) return IKBO_OK;
+  uint64_t now = 0, high = 0;
+  if (cudaMemPoolGetAttribute(pool, cudaMemPoolAttrUsedMemCurrent, &now) != cudaSuccess ||
+      cudaMemPoolGetAttribute(pool, cudaMemPoolAttrUsedMemHigh, &high) != cudaSuccess)
+    return IKBO_ERR_CUDA;
+  if (used_now) *used_now = now;
+  if (used_high) *used_high = high;
+  if (reset) {
+    uint64_t zero = 0;
+    if (cudaMemPoolSetAttribute(pool, cudaMemPoolAttrUsedMemHigh, &zero) != cudaSuccess)
+      return IKBO_ERR_CUDA;
+  }
+  return IKBO_OK;
+}
+
 int ikbo_set_trace(uint64_t* device_buffer) {
   g_trace = device_buffer;
   return IKBO_OK;
@@ -1266,7 +1394,7 @@ int ikbo_set_trace(uint64_t* device_buffer) {
 
 int ikbo_set_kernel(int which) {
   const int prev = t_kernel;
-  t_kernel = (which >= kKernAuto && which <= kKernPp) ? which : kKernAuto;
+  t_kernel = (which >= kKernAuto && which <= kKernAb) ? which : kKernAuto;
   return prev;
 }
 

@@ -115,6 +115,7 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
     plan_in_cta(p, ctl, data, D, kPpGroups);
     ptx::fence_proxy_async_smem();
   }
+  if (threadIdx.x == 0) ctl->bmaps_ready = 0;   // the planning's scan words are free now
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
@@ -160,7 +161,7 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
         // maps encoded with the row count T itself (a fused call states T)
         if ((kSelf && p.exact_rows) || row + kBlockN <= T)
           return is_v ? (const void*)&vmap_tmpl : (const void*)&kmap_tmpl;
-        CUtensorMap* tail_k = p.map_slots + 2 * blockIdx.x;
+        CUtensorMap* tail_k = p.map_slots + (size_t)p.map_stride * blockIdx.x;
         CUtensorMap* tail_v = tail_k + 1;
         if (!tail_ready) {
           if (lane == 0) {   // one lane writes the copies
@@ -186,11 +187,30 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
       };
       uint32_t kv_it = 0;
       uint32_t qn[kPpGroups] = {0, 0};
-      // the next ring load: one K or V tile (128 keys x D of one head)
-      auto ring = [&](bool is_v, int head, int32_t row) -> bool {
+      // A user's partial last V tile goes through the item's copy of the V
+      // map bounded at the user's end row (the TMA fills the other users'
+      // rows with zeros), written by warp 2 after planning.
+      bool bm_ready = false;
+      int cur_item = 0;
+      auto v_map_for = [&](int32_t row, int32_t end) -> const void* {
+        if (row + kBlockN <= end) return kv_map(true, row);
+        if (!bm_ready) {
+          bool got = true;
+          if (lane == 0) got = wait_bounded_maps(p, ctl);
+          if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) return nullptr;
+          bm_ready = true;
+        }
+        CUtensorMap* m = p.map_slots + (size_t)p.map_stride * blockIdx.x + 2 + cur_item;
+        ptx::tensormap_acquire(m);
+        return m;
+      };
+      // the next ring load: one K or V tile (128 keys x D of one head); the
+      // item's keys end at row `end`
+      auto ring = [&](bool is_v, int head, int32_t row, int32_t end) -> bool {
         const uint32_t slot = kv_it % NS;
         if (!W.conv_wait(ptx::smem_addr(&ctl->kv_empty[slot]), ((kv_it / NS) & 1u) ^ 1u)) return false;
-        const void* map = kv_map(is_v, row);
+        const void* map = is_v ? v_map_for(row, end) : kv_map(false, row);
+        if (!map) return false;
         const uint32_t bar = ptx::smem_addr(&ctl->kv_full[slot]);
         const uint32_t dst = ptx::smem_addr(kv_smem + slot * C::kKVBytes);
         ptx::mbar_arrive_expect_tx_warp(bar, C::kKVBytes);
@@ -240,10 +260,12 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
         const bool has_b = tile_cands(w, 1) > 0;
         if (lane == 0) trace(p, k, kTrProdItem);
         // Q_A and K_0 first: S_A(0) needs only these
-        ok = load_q(0, w) && ring(false, w.head, w.kv_begin) && (!has_b || load_q(1, w));
+        const int32_t end = w.kv_begin + w.kv_len;
+        cur_item = k;
+        ok = load_q(0, w) && ring(false, w.head, w.kv_begin, end) && (!has_b || load_q(1, w));
         for (int j = 0; j < n && ok; ++j) {
-          ok = ring(true, w.head, w.kv_begin + j * kBlockN);
-          if (ok && j + 1 < n) ok = ring(false, w.head, w.kv_begin + (j + 1) * kBlockN);
+          ok = ring(true, w.head, w.kv_begin + j * kBlockN, end);
+          if (ok && j + 1 < n) ok = ring(false, w.head, w.kv_begin + (j + 1) * kBlockN, end);
         }
         if (lane == 0) trace(p, k, kTrProdIssued);
       }
@@ -379,6 +401,7 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
     __syncwarp();
   } else if ((warp == 2 || warp == 3) && mode != kModeSkip) {
     prefetch_v_late(p, ctl->total_keys, D);
+    if (warp == 2) write_bounded_maps(p, ctl, &vmap_tmpl, n_my, item_at);
   } else if (warp >= kSoftmaxWarp0 && mode != kModeSkip) {
     // ------------------------------------------- softmax / correction / epilogue
     const int g = (warp - kSoftmaxWarp0) / kPpSoftmaxWarps;   // query tile of this warp

@@ -156,13 +156,25 @@ struct TcCtrl {
   int flags;
   int n_units;                          // planning: units in all (read by every thread)
   int early_loads;                      // ring loads of item 0 issued before the roles start
-  int red[kTcThreads / 32];             // block scan: one word per warp
+  union {
+    int red[kTcThreads / 32];           // planning: block scan, one word per warp
+    int bmaps_ready;                    // after planning: 1 once the bounded V maps are written
+  };
   WorkItem items[kCtlItems];            // the first items of this CTA (the rest in global memory)
-  alignas(16) float partner_lse[kTileM];
-  // row maximum / row sum exchange among the kSplit threads of a row:
-  // [parity][column group][row], the value with the exchange's sequence
-  // number in its two low bits
-  uint32_t xtag[2][kSplit][kTileM];
+  union {
+    alignas(16) float partner_lse[kTileM];   // one-tile kernel, pair mode
+    uint64_t s_free[2];                      // key-interleaved kernel: S buffer read by the softmax
+  };
+  int ab_chunk_tiles;                   // key-interleaved kernel: chunk size of split units (0 = none)
+  int ab_units;                         // key-interleaved kernel: units (or chunks) in all
+  union {
+    // row maximum / row sum exchange among the kSplit threads of a row:
+    // [parity][column group][row], the value with the exchange's sequence
+    // number in its two low bits
+    uint32_t xtag[2][kSplit][kTileM];
+    // key-interleaved kernel: (running maximum, row sum) of every row, per warpgroup
+    float2 ab_ml[2][kTileM];
+  };
 };
 static_assert(sizeof(TcCtrl) <= kCtrlBytes, "control block");
 
@@ -268,6 +280,71 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// A user's last key tile may reach into the rows of the users after it.
+// Their keys are masked, so their weights in P are exactly 0, but 0 x inf or
+// a NaN in their V rows would spoil P.V ("In-Kernel Broadcast Optimization",
+// §3.1: a candidate attends to its own user's sequence only).  So a user's
+// last V tile, when it is partial, is loaded through a copy of the V tensor
+// map whose row count ends at the user's last row: the TMA fills the rows
+// past it with zeros.  The copies live in global memory, one per work item of
+// the CTA (slot 2 + k of the CTA's map slots; slots 0 and 1 are the K and V
+// maps with the row count T).  One warp without another role writes them all
+// right after planning, releases them to the tensor-map proxy with a single
+// fence and raises ctl->bmaps_ready; the producer acquires a copy before its
+// first load through it.
+
+// Copy `tmpl` into `m` with row count `rows` (one thread; a release fence
+// must follow before the TMA may read `m`).
+__device__ __forceinline__ void write_bounded_map(CUtensorMap* m, const CUtensorMap* tmpl, int32_t rows) {
+  const uint4* s4 = reinterpret_cast<const uint4*>(tmpl);
+  uint4* d4 = reinterpret_cast<uint4*>(m);
+#pragma unroll
+  for (int i = 0; i < (int)(sizeof(CUtensorMap) / 16); ++i) d4[i] = s4[i];
+  asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 1, %1;" ::"l"(d4), "r"(rows) : "memory");
+}
+
+// Does item w need a bounded V map (its last tile is partial)?
+__device__ __forceinline__ bool needs_bounded_map(const WorkItem& w) { return (w.kv_len % 128) != 0; }
+
+// All threads of one warp: write the bounded V maps of the CTA's n items
+// (item_at(k)), release them, set ctl->bmaps_ready.
+template <typename ItemAt>
+__device__ __forceinline__ void write_bounded_maps(const AttnParams& p, TcCtrl* ctl, const CUtensorMap* vtmpl,
+                                                   int n, ItemAt item_at) {
+  CUtensorMap* base = p.map_slots + (size_t)p.map_stride * blockIdx.x + 2;
+  for (int k = threadIdx.x & 31; k < n; k += 32) {
+    const WorkItem w = item_at(k);
+    if (needs_bounded_map(w)) write_bounded_map(base + k, vtmpl, w.kv_begin + w.kv_len);
+  }
+  asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0)
+    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(ptx::smem_addr(&ctl->bmaps_ready)), "r"(1)
+                 : "memory");
+}
+
+// The producer's wait for ctl->bmaps_ready (bounded, like every wait).
+__device__ __forceinline__ bool wait_bounded_maps(const AttnParams& p, TcCtrl* ctl) {
+  uint64_t t_end = 0;
+  for (uint32_t spin = 0;; ++spin) {
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(ptx::smem_addr(&ctl->bmaps_ready))
+                 : "memory");
+    if (v == 1) return true;
+    if ((spin & 63u) == 63u) {
+      if (*(volatile int*)&ctl->abort_flag) return false;
+      const uint64_t now = ptx::globaltimer();
+      if (t_end == 0) {
+        t_end = now + p.timeout_ns;
+      } else if (now > t_end) {
+        ctl->abort_flag = 1;
+        atomicOr(p.err_word, kErrTimeout);
+        return false;
+      }
+    }
+  }
+}
 
 // Block-wide exclusive scan of one int per thread (all threads call it).
 __device__ __forceinline__ int block_scan_excl(int x, int* red, int* total) {
@@ -394,23 +471,29 @@ __device__ __forceinline__ void plan_load(const AttnParams& p, uint8_t* scratch)
   }
 }
 
-// A unit is (user, head, up to tiles_per_unit query tiles of the user's
-// candidates): 1 for this kernel, 2 for the two-tile kernel.
-__device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch, int D,
-                            int tiles_per_unit) {
+// Flags found while validating and grouping.
+constexpr int kPlanBadOff = 1, kPlanBadIdx = 2, kPlanUnsorted = 4, kPlanEmpty = 8, kPlanGap = 16;
+
+// Validation and grouping, all threads of the CTA (the first part of every
+// in-kernel plan).  On return cand_start (the scratch's `cs`) holds the first
+// grouped position of every user, `perm_ws` the grouped order when the map
+// is unsorted, and the rows of candidates whose user has an empty sequence
+// are zero.  Returns the flags, or -1 when the index tensors are invalid:
+// then the CTA has no work (mode kModeSkip) and CTA 0 has set the error word.
+__device__ int plan_group(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch, int D,
+                          bool prefetch = true) {
   const int tid = threadIdx.x, nt = blockDim.x;
   const int grid = gridDim.x, b = blockIdx.x;
   const int n_cand = (int)p.n_cand, n_user = (int)p.n_user;
   PlanScratch S(scratch, n_user, n_cand);
   int32_t* const off = S.off;
   int32_t* const cs = S.cs;
-  int32_t* const order = S.order;
-  int32_t* const ubefore = S.ubefore;
   int32_t* const c2u = S.c2u;
+  constexpr int kBadOff = kPlanBadOff, kBadIdx = kPlanBadIdx, kUnsorted = kPlanUnsorted,
+                kEmpty = kPlanEmpty, kGap = kPlanGap;
 
   // One pass: validation, sortedness, empty sequences, and for sorted input
   // the first candidate of every user (users prev+1 .. x start at c).
-  constexpr int kBadOff = 1, kBadIdx = 2, kUnsorted = 4, kEmpty = 8, kGap = 16;
   int flags = 0;
   if (tid == 0 && off[0] != 0) flags |= kBadOff;
   // a fused self-attention call states T: the offsets must end there
@@ -457,11 +540,11 @@ __device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch, 
         atomicOr(p.err_word, ((flags & kBadOff) ? kErrOffsets : 0) | ((flags & kBadIdx) ? kErrIndex : 0));
     }
     __syncthreads();
-    return;
+    return -1;
   }
   // the offsets are valid: start the DRAM reads of this CTA's share of the
   // inputs (lane 0 of warps 1-3)
-  if (tid == 32 || tid == 96) prefetch_inputs(p, off[n_user], D, (tid >> 5) - 1);
+  if (prefetch && (tid == 32 || tid == 96)) prefetch_inputs(p, off[n_user], D, (tid >> 5) - 1);
   const bool unsorted = (flags & kUnsorted) != 0;
   if (!unsorted && (flags & kGap)) {
     // sorted, with wide gaps between consecutive users: fill those now
@@ -542,6 +625,25 @@ __device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch, 
       }
     }
   }
+  return flags;
+}
+
+// A unit is (user, head, up to tiles_per_unit query tiles of the user's
+// candidates): 1 for this kernel, 2 for the two-tile kernel.
+__device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch, int D,
+                            int tiles_per_unit) {
+  const int flags = plan_group(p, ctl, scratch, D);
+  if (flags < 0) return;
+  const bool unsorted = (flags & kPlanUnsorted) != 0;
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int grid = gridDim.x, b = blockIdx.x;
+  const int n_cand = (int)p.n_cand, n_user = (int)p.n_user;
+  PlanScratch S(scratch, n_user, n_cand);
+  int32_t* const off = S.off;
+  int32_t* const cs = S.cs;
+  int32_t* const order = S.order;
+  int32_t* const ubefore = S.ubefore;
+  (void)n_cand;
   // Units (H x groups of query tiles of users with candidates and keys),
   // prefix-summed over the users in index order, or longest first (below).
   const int cpt = p.cands_per_tile * tiles_per_unit;   // candidates per unit
@@ -646,6 +748,7 @@ __device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch, 
     w.kv_len = off[u + 1] - off[u];
     w.unit = -1;
     w.unit_first = 0;
+    w.n_split = 1;
   };
   WorkItem* mine = p.cta_items + (size_t)b * p.max_cta_items;
   if (pair) {
@@ -803,7 +906,7 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
     if (p.exact_rows) return is_v ? (const void*)&vmap_tmpl : (const void*)&kmap_tmpl;
     const int T = ctl->total_keys;
     if (row + kBlockN <= T) return is_v ? (const void*)&vmap_tmpl : (const void*)&kmap_tmpl;
-    CUtensorMap* tail_k = p.map_slots + 2 * blockIdx.x;
+    CUtensorMap* tail_k = p.map_slots + (size_t)p.map_stride * blockIdx.x;
     CUtensorMap* tail_v = tail_k + 1;
     if (!tail_ready) {
 #pragma unroll
@@ -822,15 +925,32 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
     }
     return is_v ? (const void*)tail_v : (const void*)tail_k;
   };
-  // one K or V tile (128 keys x D of one head) into ring slot `slot`
-  auto issue_tile = [&](bool is_v, int head, int32_t row, uint32_t slot) {
-    const void* map = kv_map(is_v, row);
+  // The V map for the tile at `row` of the CTA's item k, whose keys end at
+  // row `end`: a user's partial last tile goes through the item's bounded
+  // copy (the TMA fills the other users' rows with zeros).
+  bool bm_ready = false;
+  auto v_map_for = [&](int32_t row, int32_t end, int k) -> const void* {
+    if (row + kBlockN <= end) return kv_map(true, row);
+    if (!bm_ready) {
+      if (!wait_bounded_maps(p, ctl)) return nullptr;
+      bm_ready = true;
+    }
+    CUtensorMap* m = p.map_slots + (size_t)p.map_stride * blockIdx.x + 2 + k;
+    ptx::tensormap_acquire(m);
+    return m;
+  };
+  // one K or V tile (128 keys x D of one head) into ring slot `slot`, of the
+  // CTA's item k, whose keys end at row `end`
+  auto issue_tile = [&](bool is_v, int head, int32_t row, uint32_t slot, int32_t end, int k) -> bool {
+    const void* map = is_v ? v_map_for(row, end, k) : kv_map(false, row);
+    if (!map) return false;
     const uint32_t bar = ptx::smem_addr(&ctl->kv_full[slot]);
     const uint32_t dst = ptx::smem_addr(kv_smem + slot * C::kKVBytes);
     ptx::mbar_arrive_expect_tx(bar, C::kKVBytes);
 #pragma unroll
     for (int cb = 0; cb < C::kCB; ++cb)
       ptx::tma_load_2d(dst + cb * kBlockN * 128, map, bar, head * D + cb * 64, row);
+    return true;
   };
   // the Q tile of item w into Q buffer qb
   auto issue_q = [&](const WorkItem& w, uint32_t qb) {
@@ -876,7 +996,10 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
       tile = a + (i - k0 - 2 * a);
     }
   };
-  if (threadIdx.x == 0) trace(p, 0, kTrCtaStart);
+  if (threadIdx.x == 0) {
+    trace(p, 0, kTrCtaStart);
+    ctl->bmaps_ready = 0;   // the planning's scan words are free now
+  }
   ptx::tc_fence_before();
   if (warp == 0) {
     // The plan is complete: warp 0 releases the other warps and only then
@@ -897,7 +1020,8 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
         bool is_v;
         int t;
         load_at(e, n, is_v, t);
-        issue_tile(is_v, w.head, w.kv_begin + t * kBlockN, (uint32_t)e);
+        if (!issue_tile(is_v, w.head, w.kv_begin + t * kBlockN, (uint32_t)e, w.kv_begin + w.kv_len, 0))
+          break;
       }
       ctl->early_loads = e;
     }
@@ -952,7 +1076,10 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
             ok = false;
             break;
           }
-          issue_tile(is_v, w.head, w.kv_begin + t * kBlockN, slot);
+          if (!issue_tile(is_v, w.head, w.kv_begin + t * kBlockN, slot, w.kv_begin + w.kv_len, k)) {
+            ok = false;
+            break;
+          }
           ++kv_it;
         }
         trace(p, k, kTrProdIssued);
@@ -1060,8 +1187,12 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
       W.drain(ptx::smem_addr(&ctl->drain), 0);
     }
     __syncwarp();
-  } else if ((warp == 2 || warp == 3) && p.fused && mode != kModeSkip) {
-    prefetch_v_late(p, ctl->total_keys, D);
+  } else if (warp == 2 || warp == 3) {
+    // V's L2 prefetch first: the first tiles' loads need it sooner than any
+    // bounded map is needed
+    if (p.fused && mode != kModeSkip) prefetch_v_late(p, ctl->total_keys, D);
+    if (warp == 2 && mode != kModeSkip)
+      write_bounded_maps(p, ctl, p.fused ? &vmap_tmpl : static_cast<const CUtensorMap*>(p.vmap), n_my, item_at);
   } else if (warp >= kSoftmaxWarp0 && mode != kModeSkip) {
     // ------------------------------------------- softmax / correction / epilogue
     constexpr int kCols = kBlockN / kSplit;                  // key columns of a tile per thread

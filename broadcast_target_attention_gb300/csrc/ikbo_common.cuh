@@ -33,8 +33,9 @@ struct WorkItem {
   int32_t unit;        // split-combine unit, or -1 when the item covers all keys
   int32_t unit_first;  // first item index of the unit (its n_split items are consecutive)
   int32_t q_row;       // self-attention tile: its first row of q_user / out_user; else -1
+  int32_t n_split;     // key-interleaved kernel: chunks of the unit (1 = the item covers all keys)
 };
-static_assert(sizeof(WorkItem) == 36, "WorkItem layout");
+static_assert(sizeof(WorkItem) == 40, "WorkItem layout");
 
 struct PlanHeader {
   int32_t n_items;       // work items written
@@ -117,7 +118,9 @@ struct AttnParams {
   WorkItem* cta_items;      // fused: [grid][max_cta_items] this CTA's items
   int32_t max_cta_items;
   int32_t* perm_ws;         // fused, unsorted input: grouped position -> candidate
-  CUtensorMap* map_slots;   // fused: [grid][2] K/V tensor maps with the row count set on the device
+  CUtensorMap* map_slots;   // [grid][map_stride] tensor maps written on the device: K and V with the
+                            // row count T (fused), then per work item a V copy bounded at its user's end
+  int32_t map_stride;       // map slots per CTA: 2 + the most work items a CTA takes
   // fused self + target attention (one-tile tcgen05 kernel, in-kernel planning)
   const uint16_t* q_user;   // bf16 [T, H, D] queries of the user sequence, or null (target only)
   uint16_t* out_user;       // bf16 [T, H, D]
@@ -127,6 +130,12 @@ struct AttnParams {
   // item's user is vendor_to_user[item_to_vendor[i]], looked up while planning; null otherwise
   const int32_t* vendor_to_user;
   int64_t n_vendor;
+  // key-interleaved kernel: a unit cut into key-range chunks on several CTAs
+  // is merged by its first chunk from the others' partial results
+  float4* ab_partial_o;     // [grid][D / 4][128] O / l of every chunk, 16-byte column groups row-minor
+  float* ab_partial_lse;    // [grid][128] log-sum-exp (base 2) of every chunk's rows
+  unsigned long long* ab_flags;   // [grid] a chunk's partial is complete: ab_marker
+  unsigned long long ab_marker;   // non-zero, unique to the call
 };
 
 // In-kernel timeline tracing (ikbo_set_trace): the first kTraceItems items of

@@ -317,6 +317,7 @@ ikbo_plan_kernel(const __grid_constant__ PlanParams p, const __grid_constant__ P
     const int64_t h = rest / nmt;
     WorkItem w;
     w.q_row = -1;
+    w.n_split = (int32_t)s;
     w.user = u;
     w.head = (int32_t)h;
     w.cand_begin = (int32_t)(cand_start[u] + mt * cpt);

@@ -31,8 +31,10 @@
  * by the library.  Device-pointer entry points are asynchronous on `stream`
  * (a cudaStream_t; NULL = legacy default stream) and never synchronise the
  * host unless stated.  The library owns its scratch space (schedule, split
- * partials, tensor maps) and takes it from the device's stream-ordered
- * memory pool on `stream`, releasing it on the same stream.
+ * partials, tensor maps) and takes it, in stream order on `stream`, from a
+ * stream-ordered memory pool of its own on the current device (made by the
+ * first call that allocates; it keeps freed memory for later calls until
+ * ikbo_shutdown).  The device's default pool is neither used nor changed.
  *
  * CUDA graphs: the device-pointer entry points (ikbo_attn_fwd and its
  * no-alloc, fused, multi-level and linear-compression variants) can be
@@ -47,9 +49,9 @@
  * [0, n_user), offsets that are not a jagged index) and bounded waits that
  * ran out can only be seen on the GPU: the kernels then skip all work (out
  * is left unchanged), never trap, and record the error in a per-device error
- * word that ikbo_get_device_error() returns.  k/v must be finite: a key tile
- * can read rows of the neighbouring user, which are masked out with weight
- * zero, and 0 * inf is NaN.
+ * word that ikbo_get_device_error() returns.  A user's result depends on its
+ * own rows of k/v only: rows of other users (which a key tile may reach)
+ * never enter it, whatever their values, inf and NaN included.
  */
 #ifndef IKBO_H
 #define IKBO_H
@@ -150,11 +152,10 @@ int ikbo_version(void);
 
 /*
  * Releases what the library holds on every device it has used.
- *   - Its events and second stream.
- *   - The pinned error-word copy.
- *   - The scratch that its calls returned to each device's stream-ordered
- *     memory pool. That pool keeps freed memory between calls; it is
- *     trimmed here.
+ *   - Its events.
+ *   - The pinned error-word copy of the host-buffer entry point.
+ *   - Its own stream-ordered memory pool on each device, which keeps the
+ *     scratch its calls freed: trimmed and destroyed here.
  * It first waits for each such device's work to finish.  No other library
  * call may run meanwhile.  A later call sets the device up again.  The
  * no-alloc entry point's fixed array is part of the library image and is
@@ -191,6 +192,16 @@ int ikbo_get_timing(float* plan_ms, float* attn_ms);
  * flags = 0 restores normal operation.
  */
 int ikbo_set_debug(int flags, uint64_t timeout_ns);
+
+/*
+ * Test hook: the library's own stream-ordered pool on the current device
+ * (see "Ownership" above).  Writes the bytes its allocations hold now and
+ * the most they held at once since the last reset (0 and 0 before the first
+ * allocating call); reset != 0 then restarts that high-water mark.  The
+ * no-alloc entry point leaves both unchanged.  IKBO_ERR_CUDA when a CUDA
+ * call fails.
+ */
+int ikbo_pool_usage(int reset, uint64_t* used_now, uint64_t* used_high);
 
 /*
  * In-kernel timeline tracing, for profiling.  With a non-NULL device buffer
@@ -344,13 +355,21 @@ int ikbo_ml_attn_fwd(const void* q, const void* k_user, const void* v_user,
  *   3  the tcgen05 kernel with two query tiles of the same user and head per
  *      work item, sharing each K/V tile between them (ping-pong of two
  *      softmax warpgroups); inputs beyond the in-kernel planning limits run
- *      on kernel 2.
+ *      on kernel 2;
+ *   4  the tcgen05 kernel with the key tiles of one query tile dealt to two
+ *      softmax warpgroups in turn (even and odd tiles) and merged in the
+ *      CTA, one unit per CTA when units are few; a unit far longer than the
+ *      balanced share is cut into up to 8 key ranges on as many CTAs and
+ *      merged by the first of them.  For batches of a few very long users
+ *      (tens of thousands of keys); never chosen automatically, since the
+ *      host cannot see the sequence lengths.  Inputs beyond the in-kernel
+ *      planning limits run on kernel 2, and so do fused self + target calls.
  * Any other value selects 0.
  */
 int ikbo_set_kernel(int which);
 
 /*
- * The kernel (1, 2 or 3 as above) that a call with these sizes would run
+ * The kernel (1 to 4 as above) that a call with these sizes would run
  * with this thread's current choice.  Host arithmetic only: it touches no
  * GPU.  Negative sizes, H < 1, or Lq outside [1, 128] return IKBO_ERR_SHAPE.
  */
@@ -378,22 +397,28 @@ int ikbo_launches_per_call(int64_t n_cand, int64_t n_user);
  * partials, tensor maps) from the stream-ordered pool on every call; this
  * variant takes it instead from one fixed array in device memory that is
  * part of the library (IKBO_NOALLOC_SCRATCH_BYTES = 40 MiB, held on every
- * GPU where the library is loaded until the process exits).  It never calls
- * cudaMalloc, cudaMallocAsync, cudaFree or any other allocating routine.
+ * GPU where the library is loaded until the process exits).  It allocates
+ * no device memory and no pinned host memory (no cudaMalloc, cudaMallocAsync,
+ * cudaMallocFromPoolAsync, cudaHostAlloc or cudaFree) and changes no memory
+ * pool, on any call, the first included.
  *
  * Arguments, layouts, results and errors are those of ikbo_attn_fwd.  In
  * addition it returns IKBO_ERR_SCRATCH, with nothing enqueued, when the call
  * would need more scratch than the array holds (the need grows with n_cand,
- * n_user, H and D; every configuration in workloads.py needs under 30 MiB).
+ * n_user, H and D; every configuration in workloads.py, with every kernel
+ * choice, needs under 30 MiB).
  *
- * The first call on a device looks up the array's device address (with that
- * device current); make that first call before any stream capture.  Every
- * call on a device uses the same array, and the planning kernel
- * re-initialises everything the attention kernel reads, so a call never
- * depends on what an earlier call left there.  Two calls whose kernels
- * overlap on the GPU (different streams, no ordering between them) race on
- * the array and give wrong results: order them on one stream, or use
- * ikbo_attn_fwd.
+ * The first call on a device sets the device up with that device current:
+ * it queries the device's attributes, looks up the array's and the error
+ * word's device addresses (cudaGetSymbolAddress) and sets the chosen
+ * kernel's shared-memory attribute; make that first call before any stream
+ * capture.  Every call on a device uses the same array.  What a call's
+ * kernels read there is written earlier in the same call, except the flags
+ * of units cut into key ranges, which carry a value unique to the call and
+ * are reset after use; so a call never depends on what an earlier call left
+ * there.  Two calls whose kernels overlap on the GPU (different streams, no
+ * ordering between them) race on the array and give wrong results: order
+ * them on one stream, or use ikbo_attn_fwd.
  */
 #define IKBO_NOALLOC_SCRATCH_BYTES (40u * 1024u * 1024u)
 int ikbo_attn_fwd_noalloc(const void* q, const void* k_user, const void* v_user,

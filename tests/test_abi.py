@@ -103,7 +103,7 @@ def test_python_binding_raises_on_bad_status(lib):
 def test_selected_kernel(lib):
     """Automatic choice: two query tiles per item when the users have on average at least
     two query tiles each, the batch makes at least 600 two-tile items and the inputs fit the
-    in-kernel planning limits."""
+    in-kernel planning limits; the key-interleaved kernel (4) only when chosen."""
     sel = lib.ikbo_selected_kernel
     assert sel(1024, 15, 4, 1) == 2         # 1024 candidates / 15 users, Lq 1: < 1 tile per user
     assert sel(8, 2, 2, 1) == 2
@@ -119,7 +119,7 @@ def test_selected_kernel(lib):
     assert sel(8, 2, 0, 1) == _lib.IKBO_ERR_SHAPE
     assert sel(8, 2, 1, 0) == _lib.IKBO_ERR_SHAPE
     assert sel(8, 2, 1, 129) == _lib.IKBO_ERR_SHAPE
-    for which, expect in ((1, 1), (2, 2), (3, 3), (7, 2)):
+    for which, expect in ((1, 1), (2, 2), (3, 3), (4, 4), (7, 2)):
         prev = lib.ikbo_set_kernel(which)
         try:
             assert sel(1024, 15, 4, 1) == expect

@@ -23,7 +23,7 @@ def limit_workload(n_cand, n_user, shuffle, seed):
 @pytest.mark.parametrize("n_cand,n_user,launches", [(20480, 1024, 1), (20481, 1024, 2),
                                                      (20480, 1025, 2)])
 @pytest.mark.parametrize("shuffle", [False, True])
-@pytest.mark.parametrize("kernel", [0, 3])
+@pytest.mark.parametrize("kernel", [0, 3, 4])
 def test_planning_limits(gpu_lib, n_cand, n_user, launches, shuffle, kernel):
     wl = limit_workload(n_cand, n_user, shuffle, seed=n_cand + n_user)
     assert gpu_lib.launches_per_call(n_cand, n_user) == launches

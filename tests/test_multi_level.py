@@ -122,7 +122,7 @@ def test_attention_configs(gpu_lib, name, n_sample):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("kernel", [1, 2, 3])
+@pytest.mark.parametrize("kernel", [1, 2, 3, 4])
 @pytest.mark.parametrize("Lq,D", [(1, 128), (4, 64), (8, 128)])
 def test_attention_shuffled_maps_every_kernel(gpu_lib, kernel, Lq, D):
     cfg = W.MlConfig(name="shuf", n_item=700, n_vendor=45, n_user=6, H=2, D=D, Lq=Lq, seed=60 + Lq,

@@ -5,9 +5,10 @@ odd and single-candidate groups, empty sequences, users without candidates,
 an unsorted candidate map, Lq from 1 to 128, D = 64 and 128, split-KV units.
 Tolerance: max-abs 2e-2 and mean-abs 2e-3 for bf16 inputs with fp32
 accumulation.  Every GPU kernel is checked: the SIMT kernel (1), the tcgen05
-kernel with one query tile per work item (2) and the one with two query tiles
-of one user and head per item (3); the full-size configurations also with the
-automatic choice (0).
+kernel with one query tile per work item (2), the one with two query tiles
+of one user and head per item (3) and the one with the key tiles of one query
+tile over two softmax warpgroups (4); the full-size configurations also with
+the automatic choice (0).
 """
 import numpy as np
 import pytest
@@ -19,8 +20,8 @@ from _helpers import assert_close, out_f64, to_device
 
 pytestmark = pytest.mark.gpu
 
-KERNELS = [1, 2, 3]
-CONFIG_KERNELS = [0, 1, 2, 3]
+KERNELS = [1, 2, 3, 4]
+CONFIG_KERNELS = [0, 1, 2, 3, 4]
 # (config, number of candidates checked against the oracle; None = all)
 CONFIG_SAMPLES = [
     ("tiny_8x2", None),
@@ -147,7 +148,7 @@ def test_scale_values(gpu_lib, scale, kernel):
 def test_kernels_agree_at_full_size(gpu_lib):
     wl = workload("odd_groups_2048x16")
     a = run(gpu_lib, wl, 1).float()
-    for kernel in (2, 3):
+    for kernel in (2, 3, 4):
         b = run(gpu_lib, wl, kernel).float()
         assert (a - b).abs().max().item() <= 2e-2, kernel
 
