@@ -41,20 +41,13 @@
 // level above.
 //
 // Clusters (M of at most 8 row tiles): the CTAs of a cluster take the row
-// tiles of one batch entry at a time, CTA r tile r, so they share every X
-// tile.  Each CTA loads its own W tile and multicasts its share of the X
-// tile's 64-column blocks to the whole cluster (this GPU's own memory); a
-// ring slot is free once all the cluster's MMAs have read it, so every MMA
-// warp's commit arrives on that slot's barrier in all of the cluster's CTAs.
-// An X tile is thus read once from L2 for all the row tiles (a 128 x 256
-// tile alone needs 48 KB from L2 per 64-wide K step, more than L2 can feed
-// 152 SMs at the tensor pipe's rate), and a cluster sits on one die, so it
-// comes from DRAM once.
+// tiles of one batch entry at a time, CTA r tile r.  A cluster runs on one
+// die, so the X tile that all its CTAs load comes from DRAM once and from
+// that die's L2 for the others.  The CTAs touch nothing of one another:
+// each loads its own W and X tiles into its own ring.
 // Teardown: every byte that reaches a CTA is counted on one of its own ring
-// barriers, which its producer drains, and no CTA leaves before the whole
-// cluster has; after an abort (a wait that ran out) a CTA also waits 1 ms,
-// bounded, so that a peer's copy already in flight lands first.
-// Every wait is bounded, as in the attention kernels.
+// barriers, which its producer drains.  Every wait is bounded, as in the
+// attention kernels.
 #pragma once
 
 #include "ikbo_attn_tc.cuh"
@@ -81,7 +74,7 @@ struct LceParams {
   int32_t add;                // 1: add a row of Y (after the grid above has completed)
   int32_t y_via_map2;         // add with map2: 1 = Y row map2[map[b]]; 0 = Y row map[b], map2 only checked
   int32_t has_dependent;      // 1: the level below is this grid's programmatic dependent
-  int32_t cluster_n;          // CTAs per cluster: the row tiles of M (<= 8), or 1
+  int32_t cluster_n;          // CTAs per cluster: the row tiles of M (<= 8), or 1 (co-scheduling only)
   int* err_word;
   uint64_t timeout_ns;
 };
@@ -126,7 +119,7 @@ ikbo_lce_kernel(const __grid_constant__ LceParams p, const __grid_constant__ CUt
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kStages; ++i) {
       ptx::mbar_init(ptx::smem_addr(&ctl->full[i]), 1);
-      ptx::mbar_init(ptx::smem_addr(&ctl->empty[i]), p.cluster_n);   // every MMA warp of the cluster
+      ptx::mbar_init(ptx::smem_addr(&ctl->empty[i]), 1);
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(ptx::smem_addr(&ctl->acc_full[i]), 1);
@@ -156,7 +149,6 @@ ikbo_lce_kernel(const __grid_constant__ LceParams p, const __grid_constant__ CUt
   // tile = rank; without, (batch entry, row tile) pairs
   const int cn = p.cluster_n;
   const int rank = cn > 1 ? int(ptx::cluster_ctarank()) : 0;
-  const uint16_t cmask = uint16_t((1u << cn) - 1u);
   const int64_t first = cn > 1 ? blockIdx.x / cn : blockIdx.x;
   const int64_t stride = cn > 1 ? gridDim.x / cn : gridDim.x;
   const int64_t n_units = cn > 1 ? p.n_batch : p.n_batch * mt_count;
@@ -169,8 +161,6 @@ ikbo_lce_kernel(const __grid_constant__ LceParams p, const __grid_constant__ CUt
       mt = int(unit % mt_count);
     }
   };
-  // every CTA's barriers exist before a peer's multicast or commit reaches them
-  if (cn > 1) ptx::cluster_sync();
 
   if (layout_ok && warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -191,16 +181,10 @@ ikbo_lce_kernel(const __grid_constant__ LceParams p, const __grid_constant__ CUt
           ptx::mbar_arrive_expect_tx(bar, C::kStageBytes);
           // W[mt*128 .. +128, k .. k+64] (rows past M and columns past K read as zeros)
           ptx::tma_load_2d(dst, &wmap, bar, ks * kLceKStep, mt * kTileM);
-          // X[b, k .. k+64, 64 c .. 64 c + 64] for each 64-column block c; in
-          // a cluster this CTA multicasts the blocks c = rank, rank + cn, ...
+          // X[b, k .. k+64, 64 c .. 64 c + 64] for each 64-column block c
 #pragma unroll
-          for (int c = 0; c < NB; ++c) {
-            const uint32_t xdst = dst + C::kABytes + c * kLceKStep * 128;
-            if (cn == 1)
-              ptx::tma_load_3d(xdst, &xmap, bar, c * 64, ks * kLceKStep, b);
-            else if (c % cn == rank)
-              ptx::tma_load_3d_mc(xdst, &xmap, bar, c * 64, ks * kLceKStep, b, cmask);
-          }
+          for (int c = 0; c < NB; ++c)
+            ptx::tma_load_3d(dst + C::kABytes + c * kLceKStep * 128, &xmap, bar, c * 64, ks * kLceKStep, b);
         }
       }
       // every armed phase must complete before the CTA exits
@@ -240,11 +224,7 @@ ikbo_lce_kernel(const __grid_constant__ LceParams p, const __grid_constant__ CUt
           const uint64_t bdesc = ptx::smem_desc_sw128(b_base + kk * 16 * 128, kLceKStep * 128, 1024);
           ptx::mma_ss_warp(d_tmem, adesc, bdesc, kIdesc, (ks > 0 || kk > 0) ? 1u : 0u);
         }
-        // the slot is free for the cluster once every CTA's MMAs have read it
-        if (cn == 1)
-          ptx::mma_commit_warp(ptx::smem_addr(&ctl->empty[slot]));
-        else
-          ptx::mma_commit_mc_warp(ptx::smem_addr(&ctl->empty[slot]), cmask);
+        ptx::mma_commit_warp(ptx::smem_addr(&ctl->empty[slot]));
       }
       if (!ok) break;
       ptx::mma_commit_warp(ptx::smem_addr(&ctl->acc_full[buf]));
@@ -345,16 +325,6 @@ ikbo_lce_kernel(const __grid_constant__ LceParams p, const __grid_constant__ CUt
   }
   ptx::tc_fence_before();
   __syncthreads();
-  if (cn > 1) {
-    // no CTA leaves while a peer's multicast or commit may still reach it
-    ptx::cluster_sync();
-    if (threadIdx.x == 0 && ctl->abort_flag) {
-      const uint64_t t_end = ptx::globaltimer() + 1000000ull;   // 1 ms
-      while (ptx::globaltimer() < t_end) {
-      }
-    }
-    __syncthreads();
-  }
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, 512);

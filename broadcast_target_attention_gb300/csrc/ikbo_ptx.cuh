@@ -188,16 +188,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, uint3
       "l"(map), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
-// The same box into the same shared-memory offset of every CTA in cta_mask
-// (this GPU's own memory), completing bytes on each CTA's mbarrier at `bar`.
-__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const void* map, uint32_t bar, int32_t c0,
-                                               int32_t c1, int32_t c2, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
-      "l"(map), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "h"(cta_mask)
-      : "memory");
-}
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* map, uint32_t bar, int32_t c0,
                                             int32_t c1, int32_t c2, int32_t c3) {
   asm volatile(
@@ -309,18 +299,6 @@ __device__ __forceinline__ void mma_commit_warp(uint32_t bar) {
       "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
       : "memory");
 }
-// Warp-wide commit that arrives once on the mbarrier at `bar` in every CTA of
-// cta_mask (the same shared-memory offset in each).
-__device__ __forceinline__ void mma_commit_mc_warp(uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;\n\t}" ::"r"(bar),
-      "h"(cta_mask)
-      : "memory");
-}
-
 // Warp-wide TMA issue: the whole warp calls, converged; the elected lane issues.
 __device__ __forceinline__ void mbar_arrive_expect_tx_warp(uint32_t bar, uint32_t bytes) {
   asm volatile(
