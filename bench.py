@@ -41,7 +41,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from broadcast_target_attention_gb300 import accounting as A  # noqa: E402
-from broadcast_target_attention_gb300 import replicas as R  # noqa: E402
+from broadcast_target_attention_gb300 import partition as P  # noqa: E402
 from broadcast_target_attention_gb300 import workloads as W  # noqa: E402
 
 METRIC = "IKBO target-attn BF16 TFLOP/s & candidates/s (1024 cand/15 users); % of peak"
@@ -58,8 +58,8 @@ def peaks():
     return dict(FALLBACK_PEAKS)
 
 
-def workload_for_rank(name: str, rank: int):
-    return W.generate(R.rank_config(name, rank))
+def workload_one_gpu(name: str):
+    return W.generate(W.CONFIGS[name])
 
 
 def config_block(wl, extra=None):
@@ -249,11 +249,11 @@ def kernel_traffic(kernel_name: str, workload: str):
 
 def run_reference(args):
     """The oracle, as it stands, on the host cores: bounded samples of the workload."""
-    ws, rank, _ = R.dist_env()
+    ws, rank, _ = P.dist_env()
     if rank != 0:
         return
     import oracle
-    wl = workload_for_rank(args.config, 0)
+    wl = workload_one_gpu(args.config)
     c = wl.cfg
     L = np.diff(wl.user_offsets.astype(np.int64))
     cores = oracle.num_threads()
@@ -323,17 +323,22 @@ def run_ikbo(args):
 
     import broadcast_target_attention_gb300 as ikbo
 
-    ws, rank, local = R.dist_env()
+    ws, rank, local = P.dist_env()
     if ws > 1:
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     ikbo.load()
     ikbo.set_kernel(args.kernel)
-    wl = workload_for_rank(args.config, rank)
-    c = wl.cfg
+    # One batch for the whole job: the named workload grown N-fold for N ranks, its users
+    # (with all their candidates) dealt to the ranks longest first; this rank runs its shard.
+    full = W.generate(P.grown_config(args.config, ws))
+    users = P.assign_users(P.user_work(full.user_offsets, full.cand_to_user), ws)[rank]
+    wl = P.shard(full, users)[0] if ws > 1 else full
+    c = full.cfg
     nums = A.workload_numbers(wl)
     flops, alg_bytes = nums["flops"], nums["alg_bytes"]
+    total_flops = A.workload_numbers(full)["flops"]
 
     def t(a, dt):
         return torch.from_numpy(np.ascontiguousarray(a)).view(dt).to(dev)
@@ -370,7 +375,7 @@ def run_ikbo(args):
             step()
         barrier()
         block_s = max(time.perf_counter() - t0, 1e-6)
-        repeats = R.max_over_ranks(float(max(1, int(np.ceil(args.min_timed_s / block_s)))), dev)
+        repeats = P.max_over_ranks(float(max(1, int(np.ceil(args.min_timed_s / block_s)))), dev)
         repeats = int(min(repeats, max(1, 20000 // max(args.steps, 1))))
         n_timed = repeats * args.steps
         starts = [torch.cuda.Event(enable_timing=True) for _ in range(n_timed)]
@@ -427,9 +432,8 @@ def run_ikbo(args):
     assert ikbo.get_device_error() == 0
     clocks = clk.summary()
 
-    ms = R.max_over_ranks(statistics.mean(step_ms), dev)
-    total_flops = flops * ws
-    value = R.job_throughput(flops, ws, ms) / 1e12
+    ms = P.max_over_ranks(statistics.mean(step_ms), dev)
+    value = P.job_throughput(total_flops, ms) / 1e12
     pk = peaks()
     attn = statistics.mean(attn_ms)
     achieved_gbs = alg_bytes / (attn * 1e-3) / 1e9
@@ -450,15 +454,19 @@ def run_ikbo(args):
                 "peak_source": pk["source"] + " (burst cuBLAS bf16)"}
     qb = wl.q.nbytes
     h2d = qb + wl.k.nbytes + wl.v.nbytes + wl.user_offsets.nbytes + wl.cand_to_user.nbytes
-    e2e = R.max_over_ranks(statistics.mean(e2e_ms), dev)
+    e2e = P.max_over_ranks(statistics.mean(e2e_ms), dev)
     bc = statistics.mean(bc_ms)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
         "repeats": repeats, "timed_steps": n_timed,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": config_block(wl, {"parallelism": f"{ws} independent replica(s), users sharded, no exchange"}),
-        "candidates_per_s": R.job_throughput(wl.n_cand, ws, ms),
+        "config": config_block(full, {"parallelism": (
+            "one GPU" if ws == 1 else
+            f"one batch of {full.n_user} users over {ws} GPUs, whole users with their candidates "
+            f"per GPU (longest first, balanced by candidates x keys), no exchange"),
+            "global_batch": full.n_cand}),
+        "candidates_per_s": P.job_throughput(full.n_cand, ms),
         "pct_of_peak": {"bf16_tensor": value / ws / pk["bf16_tflops"],
                         "hbm_roofline_attn_kernel": achieved_gbs / pk["hbm_gbs"]},
         "kernel_ms": {"plan": statistics.mean(plan_ms), "attn": attn,
@@ -490,14 +498,14 @@ def run_fused(args):
 
     import broadcast_target_attention_gb300 as ikbo
 
-    ws, rank, local = R.dist_env()
+    ws, rank, local = P.dist_env()
     if ws > 1:
         raise SystemExit("--with-self measures one GPU")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     ikbo.load()
     ikbo.set_kernel(args.kernel)
-    wl = workload_for_rank(args.config, rank)
+    wl = workload_one_gpu(args.config)
     c = wl.cfg
     lens = np.diff(wl.user_offsets.astype(np.int64))
     nums = A.workload_numbers(wl)
@@ -623,7 +631,7 @@ def run_lce(args):
 
     import broadcast_target_attention_gb300 as ikbo
 
-    ws, rank, local = R.dist_env()
+    ws, rank, local = P.dist_env()
     if ws > 1:
         raise SystemExit("--lce measures one GPU")
     torch.cuda.set_device(local)
@@ -780,7 +788,7 @@ def run_ml(args):
 
     import broadcast_target_attention_gb300 as ikbo
 
-    ws, rank, local = R.dist_env()
+    ws, rank, local = P.dist_env()
     if ws > 1:
         raise SystemExit("--ml measures one GPU")
     torch.cuda.set_device(local)
@@ -878,7 +886,7 @@ def run_ml_lce(args):
 
     import broadcast_target_attention_gb300 as ikbo
 
-    ws, rank, local = R.dist_env()
+    ws, rank, local = P.dist_env()
     if ws > 1:
         raise SystemExit("--lce-ml measures one GPU")
     torch.cuda.set_device(local)
@@ -975,7 +983,7 @@ def run_ratio_sweep(args):
 
     import broadcast_target_attention_gb300 as ikbo
 
-    ws, rank, local = R.dist_env()
+    ws, rank, local = P.dist_env()
     if ws > 1:
         raise SystemExit("--ratio-sweep measures one GPU")
     torch.cuda.set_device(local)
