@@ -1187,11 +1187,8 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
       W.drain(ptx::smem_addr(&ctl->drain), 0);
     }
     __syncwarp();
-  } else if (warp == 2 || warp == 3) {
-    // V's L2 prefetch first: the first tiles' loads need it sooner than any
-    // bounded map is needed
-    if (p.fused && mode != kModeSkip) prefetch_v_late(p, ctl->total_keys, D);
-    if (warp == 2 && mode != kModeSkip)
+  } else if (warp == 2) {
+    if (mode != kModeSkip)
       write_bounded_maps(p, ctl, p.fused ? &vmap_tmpl : static_cast<const CUtensorMap*>(p.vmap), n_my, item_at);
   } else if (warp >= kSoftmaxWarp0 && mode != kModeSkip) {
     // ------------------------------------------- softmax / correction / epilogue
