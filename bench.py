@@ -59,7 +59,7 @@ def peaks():
 
 
 def workload_one_gpu(name: str):
-    return W.generate(W.CONFIGS[name])
+    return W.generate(W.attention_config(name))
 
 
 def config_block(wl, extra=None):
@@ -1032,7 +1032,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ikbo", choices=["ikbo", "reference"])
-    ap.add_argument("--config", default=W.HEADLINE, choices=sorted(W.CONFIGS))
+    ap.add_argument("--config", default=W.HEADLINE, choices=sorted(W.CONFIGS) + sorted(W.LONG_CONFIGS))
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--kernel", type=int, default=0, choices=[0, 1, 2, 3, 4],
                     help="attention kernel (ikbo_set_kernel): 0 = the automatic choice")

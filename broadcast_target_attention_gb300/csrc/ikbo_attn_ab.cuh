@@ -390,14 +390,17 @@ ikbo_attn_ab_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
         }
         CUtensorMap* m = p.map_slots + (size_t)p.map_stride * blockIdx.x + 2 + cur_item;
         ptx::tensormap_acquire(m);
+        ptx::prefetch_tensormap(m);
         return m;
       };
       // the next ring load; the item's keys end at row `end`
       auto ring = [&](bool is_v, int head, int32_t row, int32_t end) -> bool {
         const uint32_t slot = kv_it % NS;
-        if (!W.conv_wait(ptx::smem_addr(&ctl->kv_empty[slot]), ((kv_it / NS) & 1u) ^ 1u)) return false;
+        // the map first: a bounded map's acquire and descriptor fetch then
+        // overlap the wait for the slot
         const void* map = is_v ? v_map_for(row, end) : kv_map(false, row);
         if (!map) return false;
+        if (!W.conv_wait(ptx::smem_addr(&ctl->kv_empty[slot]), ((kv_it / NS) & 1u) ^ 1u)) return false;
         const uint32_t bar = ptx::smem_addr(&ctl->kv_full[slot]);
         const uint32_t dst = ptx::smem_addr(kv_smem + slot * C::kKVBytes);
         ptx::mbar_arrive_expect_tx_warp(bar, C::kKVBytes);

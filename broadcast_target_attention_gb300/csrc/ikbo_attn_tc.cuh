@@ -937,12 +937,16 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
     }
     CUtensorMap* m = p.map_slots + (size_t)p.map_stride * blockIdx.x + 2 + k;
     ptx::tensormap_acquire(m);
+    ptx::prefetch_tensormap(m);
     return m;
   };
-  // one K or V tile (128 keys x D of one head) into ring slot `slot`, of the
-  // CTA's item k, whose keys end at row `end`
-  auto issue_tile = [&](bool is_v, int head, int32_t row, uint32_t slot, int32_t end, int k) -> bool {
-    const void* map = is_v ? v_map_for(row, end, k) : kv_map(false, row);
+  // the map of a K or V tile at `row` of the CTA's item k, whose keys end at
+  // row `end` (null after an abort)
+  auto map_for = [&](bool is_v, int32_t row, int32_t end, int k) -> const void* {
+    return is_v ? v_map_for(row, end, k) : kv_map(false, row);
+  };
+  // one K or V tile (128 keys x D of one head) into ring slot `slot` through `map`
+  auto issue_tile = [&](const void* map, int head, int32_t row, uint32_t slot) -> bool {
     if (!map) return false;
     const uint32_t bar = ptx::smem_addr(&ctl->kv_full[slot]);
     const uint32_t dst = ptx::smem_addr(kv_smem + slot * C::kKVBytes);
@@ -1020,8 +1024,8 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
         bool is_v;
         int t;
         load_at(e, n, is_v, t);
-        if (!issue_tile(is_v, w.head, w.kv_begin + t * kBlockN, (uint32_t)e, w.kv_begin + w.kv_len, 0))
-          break;
+        const int32_t row = w.kv_begin + t * kBlockN;
+        if (!issue_tile(map_for(is_v, row, w.kv_begin + w.kv_len, 0), w.head, row, (uint32_t)e)) break;
       }
       ctl->early_loads = e;
     }
@@ -1072,11 +1076,15 @@ ikbo_attn_tc_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
           int t;
           load_at(i, n, is_v, t);
           const uint32_t slot = kv_it % NS;
-          if (!W.wait(ptx::smem_addr(&ctl->kv_empty[slot]), ((kv_it / NS) & 1u) ^ 1u)) {
+          // the map first: a bounded map's acquire and descriptor fetch then
+          // overlap the wait for the slot
+          const int32_t row = w.kv_begin + t * kBlockN;
+          const void* map = map_for(is_v, row, w.kv_begin + w.kv_len, k);
+          if (!map || !W.wait(ptx::smem_addr(&ctl->kv_empty[slot]), ((kv_it / NS) & 1u) ^ 1u)) {
             ok = false;
             break;
           }
-          if (!issue_tile(is_v, w.head, w.kv_begin + t * kBlockN, slot, w.kv_begin + w.kv_len, k)) {
+          if (!issue_tile(map, w.head, row, slot)) {
             ok = false;
             break;
           }

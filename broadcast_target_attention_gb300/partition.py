@@ -87,7 +87,7 @@ def grown_config(name: str, world_size: int) -> W.Config:
     """The batch that `world_size` GPUs share: the named workload with world_size times its
     users and candidates, drawn the same way (one batch, so per-GPU work stays that of
     the named workload as the GPUs grow).  world_size 1 gives the workload itself."""
-    cfg = W.CONFIGS[name]
+    cfg = W.attention_config(name)
     if world_size == 1:
         return cfg
     if isinstance(cfg.counts, (tuple, list)) or isinstance(cfg.lens, (tuple, list)):

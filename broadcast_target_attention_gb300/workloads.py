@@ -513,5 +513,39 @@ for _D in (64, 128):
             counts="multinomial", lens="loguniform", len_lo=128, len_hi=8192,
             description=f"16384 candidates over 64 users, L log-uniform [128,8192], H=16 D={_D} Lq={_Lq}")
 
+# Batches of few users, beside the table above.  Three have fewer units (user, head,
+# query tile) than SMs and one unit much longer than the others, so that how a
+# unit's keys are spread over SMs decides the time (the key-interleaved kernel,
+# ikbo_set_kernel(4), is built for these); the fourth, one user with many
+# candidates and short keys, is their counterpart with many short units.
+# Explicit counts and lengths; values N(0, 1).
+LONG_CONFIGS = {
+    "long_user_5000": Config(
+        name="long_user_5000", n_cand=1, n_user=1, H=2, D=128, Lq=1, seed=3,
+        counts=(1,), lens=(5000,),
+        description="1 candidate of 1 user with 5000 keys, H=2 D=128 Lq=1"),
+    "long_user_65000": Config(
+        name="long_user_65000", n_cand=7, n_user=2, H=2, D=128, Lq=3, seed=77,
+        counts=(5, 2), lens=(65000, 300),
+        description="7 candidates over 2 users with 65000 and 300 keys, H=2 D=128 Lq=3"),
+    "one_user_10000x700": Config(
+        name="one_user_10000x700", n_cand=10000, n_user=1, H=4, D=128, Lq=1, seed=9,
+        counts=(10000,), lens=(700,),
+        description="10000 candidates of 1 user with 700 keys, H=4 D=128 Lq=1"),
+    "few_long_82x4": Config(
+        name="few_long_82x4", n_cand=82, n_user=4, H=4, D=128, Lq=1, seed=10,
+        counts=(20, 50, 3, 9), lens=(12000, 3000, 8000, 500),
+        description="82 candidates over 4 users with 12000, 3000, 8000 and 500 keys, "
+                    "H=4 D=128 Lq=1"),
+}
+
+
+def attention_config(name: str) -> Config:
+    """A target-attention configuration by name, from the table or the long-user set."""
+    if name in CONFIGS:
+        return CONFIGS[name]
+    return LONG_CONFIGS[name]
+
+
 # The configuration the headline metric is quoted on (1024 candidates / 15 users).
 HEADLINE = "ratio_1024x15"

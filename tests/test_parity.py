@@ -39,7 +39,7 @@ _cache = {}
 
 def workload(name):
     if name not in _cache:
-        wl = W.generate(W.CONFIGS[name])
+        wl = W.generate(W.attention_config(name))
         _cache.clear()
         _cache[name] = wl
     return _cache[name]
@@ -78,6 +78,19 @@ def test_config_matches_oracle(gpu_lib, name, n_sample, kernel):
     out = run(gpu_lib, wl, kernel)
     assert_close(out_f64(out, cands), ref, f"{name} kernel={kernel}")
     # properties that hold for every row, checked at full size
+    assert torch.isfinite(out.float()).all()
+
+
+# the long-user set (few units, one much longer than the rest): every kernel choice
+LONG_SAMPLES = [(n, 160 if W.LONG_CONFIGS[n].n_cand > 1024 else None) for n in sorted(W.LONG_CONFIGS)]
+
+
+@pytest.mark.parametrize("name,n_sample", LONG_SAMPLES)
+@pytest.mark.parametrize("kernel", CONFIG_KERNELS)
+def test_long_user_config_matches_oracle(gpu_lib, name, n_sample, kernel):
+    wl, cands, ref = config_reference(name, n_sample)
+    out = run(gpu_lib, wl, kernel)
+    assert_close(out_f64(out, cands), ref, f"{name} kernel={kernel}")
     assert torch.isfinite(out.float()).all()
 
 

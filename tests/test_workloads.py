@@ -53,6 +53,23 @@ def test_extreme_and_sweep_structure():
     assert counts.sum() == 16384 and lens.min() >= 128 and lens.max() <= 8192
 
 
+def test_long_user_structure():
+    """The long-user set: explicit counts and lengths, as stated; all but the one-user
+    counterpart have fewer units than SMs."""
+    for name, cfg in W.LONG_CONFIGS.items():
+        assert W.attention_config(name) is cfg and name not in W.CONFIGS
+        off = np.zeros(cfg.n_user + 1, dtype=np.int64)
+        np.cumsum(cfg.lens, out=off[1:])
+        c2u = np.repeat(np.arange(cfg.n_user), cfg.counts)
+        assert len(c2u) == cfg.n_cand and len(cfg.lens) == cfg.n_user
+        cpt = 128 // cfg.Lq
+        units = cfg.H * sum(-(-c // cpt) for c in cfg.counts)
+        assert (units < 152) == (name != "one_user_10000x700"), name
+    wl = W.generate(W.LONG_CONFIGS["few_long_82x4"])
+    assert list(np.diff(wl.user_offsets)) == [12000, 3000, 8000, 500]
+    assert list(np.bincount(wl.cand_to_user)) == [20, 50, 3, 9]
+
+
 def test_shuffled_mapping_is_a_permutation():
     wl = W.custom(n_user=3, counts=[4, 2, 5], lens=[3, 4, 5], H=1, D=8, Lq=1, shuffle=True, seed=3)
     assert sorted(wl.cand_to_user.tolist()) == [0] * 4 + [1] * 2 + [2] * 5

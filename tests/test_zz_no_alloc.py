@@ -123,12 +123,12 @@ def _minimal(n_cand, n_user, H, Lq, D):
     return dict(q=q, k=k, v=k.clone(), user_offsets=off, cand_to_user=c2u)
 
 
-@pytest.mark.parametrize("name", sorted(W.CONFIGS))
+@pytest.mark.parametrize("name", sorted(W.CONFIGS) + sorted(W.LONG_CONFIGS))
 def test_noalloc_fits_every_configuration_and_kernel(gpu_lib, name):
     """The fixed array holds the scratch of every configuration's sizes with every kernel
     choice (the need depends on the sizes and the kernel, not on the values)."""
     lib = _lib.lib()
-    cfg = W.CONFIGS[name]
+    cfg = W.attention_config(name)
     d = _minimal(cfg.n_cand, cfg.n_user, cfg.H, cfg.Lq, cfg.D)
     out = torch.empty_like(d["q"])
     wl = type("Sizes", (), {"n_user": cfg.n_user, "scale": cfg.D ** -0.5})
