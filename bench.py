@@ -222,6 +222,14 @@ KERNEL_SOURCES = {
 }
 
 
+def lce_kernel_name(M: int, N: int) -> str:
+    """The compression kernel a call of these sizes launches: CTA pairs (M = 256 MMAs) when M
+    spans two to eight row tiles of 128 and N is 128 or 256, else one CTA per row tile."""
+    mt = -(-M // 128)
+    pairs = (N // 64) % 2 == 0 and 2 <= mt <= 8
+    return f"ikbo_lce_kernel<{N // 64}, {'true' if pairs else 'false'}>"
+
+
 def kernel_source_sha256(kernel_name: str = "ikbo_attn_tc_kernel") -> str:
     src = os.path.join(ROOT, "broadcast_target_attention_gb300", "csrc")
     h = hashlib.sha256()
@@ -715,7 +723,7 @@ def run_lce(args):
     ai = flops / alg_bytes
     ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
     gbs = alg_bytes / (ms * 1e-3) / 1e9
-    kname = f"ikbo_lce_kernel<{c.N // 64}>"
+    kname = lce_kernel_name(c.M, c.N)
     # DRAM bytes of the candidate stage (the launch that moves all but ~2 % of the bytes)
     traffic = kernel_traffic(kname, c.name)
     if ai < ridge:
@@ -958,7 +966,7 @@ def run_ml_lce(args):
                    "K_vendor": c.K_vendor, "K_item": c.K_item, "N": c.N,
                    "l2": "flushed before every timed step (write of 2x L2 size)",
                    "ai_flop_per_byte": flops / alg_bytes},
-        "roofline": _roofline(flops, alg_bytes, ms, f"ikbo_lce_kernel<{c.N // 64}>"),
+        "roofline": _roofline(flops, alg_bytes, ms, lce_kernel_name(c.M, c.N)),
         "broadcast_path": {"ms_per_step": bc, "ikbo_speedup": bc / ms,
                            "what": "torch: X = cat(X_user[u], X_vendor[v], X_item); matmul(W, X)"},
         "e2e": {"value": flops / (e2e * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,

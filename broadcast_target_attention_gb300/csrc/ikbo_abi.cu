@@ -38,8 +38,8 @@ struct DeviceState {
   int pp_grid[2] = {0, 0};   // CTAs of the two-tile tcgen05 kernel, D = 64 / 128
   int ab_grid[2] = {0, 0};   // CTAs of the key-interleaved tcgen05 kernel, D = 64 / 128
   std::atomic<uint64_t>* calls = nullptr;   // calls so far: the key-interleaved kernel's marker
-  bool lce_ready[4] = {false, false, false, false};   // shared-memory attribute set, N = 64 .. 256
-  int lce_clusters[4][9] = {};   // co-resident clusters of the LCE kernel, by N / 64 and cluster size
+  bool lce_ready[2][4] = {};      // shared-memory attribute set: by CTA-pair form, N = 64 .. 256
+  int lce_clusters[2][4][9] = {};   // co-resident clusters of the LCE kernel, by form, N / 64 and cluster size
   int* err_host = nullptr;       // pinned copy of the error word, made by the host-buffer entry point
   std::mutex* host_call = nullptr;   // serialises that entry point's use of err_host
   // The library's own stream-ordered pool on this device, made by the first
@@ -983,19 +983,19 @@ int encode_lce_x_map(CUtensorMap* m, const void* X, int64_t B, int K, int N) {
 // Units of the batch: one per batch entry and row tile, or, with clusters, one
 // per batch entry (a cluster of cluster_n CTAs takes its row tiles).  Grid:
 // as many CTAs as there are units, at most as many as fit at once.
-template <int NB>
+template <int NB, bool kPair>
 cudaError_t launch_lce(DeviceState* ds, const LceParams& lp, const CUtensorMap& wm,
                        const CUtensorMap& xm, bool pdl, cudaStream_t st) {
-  if (!ds->lce_ready[NB - 1]) {
-    cudaError_t e = cudaFuncSetAttribute(ikbo_lce_kernel<NB>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kLceSmemBytes);
+  auto kern = ikbo_lce_kernel<NB, kPair>;
+  if (!ds->lce_ready[kPair][NB - 1]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kLceSmemBytes);
     if (e != cudaSuccess) return e;
-    ds->lce_ready[NB - 1] = true;
+    ds->lce_ready[kPair][NB - 1] = true;
   }
   const int cn = lp.cluster_n;
   int grid = 0;
   if (cn > 1) {
-    int& fit = ds->lce_clusters[NB - 1][cn];
+    int& fit = ds->lce_clusters[kPair][NB - 1][cn];
     if (!fit) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3((ds->num_sms / cn) * cn);
@@ -1008,7 +1008,7 @@ cudaError_t launch_lce(DeviceState* ds, const LceParams& lp, const CUtensorMap& 
       attr[0].val.clusterDim.z = 1;
       cfg.attrs = attr;
       cfg.numAttrs = 1;
-      if (cudaOccupancyMaxActiveClusters(&fit, ikbo_lce_kernel<NB>, &cfg) != cudaSuccess || fit <= 0) {
+      if (cudaOccupancyMaxActiveClusters(&fit, kern, &cfg) != cudaSuccess || fit <= 0) {
         cudaGetLastError();
         fit = ds->num_sms / cn;
       }
@@ -1019,17 +1019,35 @@ cudaError_t launch_lce(DeviceState* ds, const LceParams& lp, const CUtensorMap& 
     const int64_t units = lp.n_batch * ((lp.M + kTileM - 1) / kTileM);
     grid = int(units < ds->num_sms ? units : ds->num_sms);
   }
-  return launch_ex(ikbo_lce_kernel<NB>, dim3(grid), dim3(kLceThreads), kLceSmemBytes, st, pdl, cn, lp,
-                   wm, xm);
+  return launch_ex(kern, dim3(grid), dim3(kLceThreads), kLceSmemBytes, st, pdl, cn, lp, wm, xm);
+}
+
+// CTA pairs (M = 256 MMAs over two CTAs) when M spans two row tiles or more,
+// at most eight, and N is a whole number of 128-column halves
+bool lce_pairs(int M, int NB) {
+  const int mt = (M + kTileM - 1) / kTileM;
+  return NB % 2 == 0 && mt >= 2 && mt <= 8;
+}
+
+// CTAs per cluster: the row tiles of one batch entry (rounded up to whole
+// pairs with CTA pairs), or 1
+int lce_cluster_n(int M, int NB) {
+  const int mt = (M + kTileM - 1) / kTileM;
+  if (lce_pairs(M, NB)) return 2 * ((mt + 1) / 2);
+  return (mt > 1 && mt <= 8) ? mt : 1;
 }
 
 cudaError_t launch_lce_nb(DeviceState* ds, int NB, const LceParams& lp, const CUtensorMap& wm,
                           const CUtensorMap& xm, bool pdl, cudaStream_t st) {
+  if (lce_pairs(lp.M, NB)) {
+    if (NB == 2) return launch_lce<2, true>(ds, lp, wm, xm, pdl, st);
+    return launch_lce<4, true>(ds, lp, wm, xm, pdl, st);
+  }
   switch (NB) {
-    case 1: return launch_lce<1>(ds, lp, wm, xm, pdl, st);
-    case 2: return launch_lce<2>(ds, lp, wm, xm, pdl, st);
-    case 3: return launch_lce<3>(ds, lp, wm, xm, pdl, st);
-    default: return launch_lce<4>(ds, lp, wm, xm, pdl, st);
+    case 1: return launch_lce<1, false>(ds, lp, wm, xm, pdl, st);
+    case 2: return launch_lce<2, false>(ds, lp, wm, xm, pdl, st);
+    case 3: return launch_lce<3, false>(ds, lp, wm, xm, pdl, st);
+    default: return launch_lce<4, false>(ds, lp, wm, xm, pdl, st);
   }
 }
 
@@ -1072,7 +1090,6 @@ int ikbo_lce_fwd(const void* W_user, const void* W_cand, const void* X_user, con
   if (rc != IKBO_OK) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int NB = N / 64;
-  const int mt = (M + kTileM - 1) / kTileM;
   CUtensorMap wc_map, xc_map, wu_map, xu_map;
   std::memset(&wu_map, 0, sizeof wu_map);
   std::memset(&xu_map, 0, sizeof xu_map);
@@ -1092,8 +1109,8 @@ int ikbo_lce_fwd(const void* W_user, const void* W_cand, const void* X_user, con
   lp.N = N;
   lp.err_word = ds->err_word;
   lp.timeout_ns = g_timeout_ns;
-  // the row tiles of one batch entry share its X tiles through a cluster
-  lp.cluster_n = (mt > 1 && mt <= 8) ? mt : 1;
+  // the row tiles of one batch entry run as one cluster (CTA pairs when N allows)
+  lp.cluster_n = lce_cluster_n(M, NB);
   cudaError_t e = cudaSuccess;
   const bool timed = g_timing;
   if (timed && (rc = ensure_events(ds)) != IKBO_OK) {
@@ -1181,7 +1198,6 @@ int ikbo_ml_lce_fwd(const void* W_user, const void* W_vendor, const void* W_item
   if (g_timing && (rc = ensure_events(ds)) != IKBO_OK) return rc;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int NB = N / 64;
-  const int mt = (M + kTileM - 1) / kTileM;
   CUtensorMap wi_map, xi_map, wv_map, xv_map, wu_map, xu_map;
   std::memset(&wv_map, 0, sizeof wv_map);
   std::memset(&xv_map, 0, sizeof xv_map);
@@ -1210,7 +1226,7 @@ int ikbo_ml_lce_fwd(const void* W_user, const void* W_vendor, const void* W_item
   lp.N = N;
   lp.err_word = ds->err_word;
   lp.timeout_ns = g_timeout_ns;
-  lp.cluster_n = (mt > 1 && mt <= 8) ? mt : 1;
+  lp.cluster_n = lce_cluster_n(M, NB);
   cudaError_t e = cudaSuccess;
   if (g_timing) cudaEventRecord(ds->ev[0], st);
   if (has_u) {

@@ -27,9 +27,19 @@
 //     O_A as soon as it sees S_A(j+1);
 //   * warps 4-7: softmax, correction and epilogue of tile A, warps 8-11 of
 //     tile B, one thread per query row (all 128 key columns of a tile).
-// An item whose user has an odd number of query tiles left has no tile B:
-// warps 8-11 skip it.  In a fused self + target call an item may also be two
-// blocks of 128 rows of the user's own sequence (tile B the second block).  Every wait is bounded, as in the single-tile kernel.
+// An item whose user has an odd number of query tiles left has no tile B.
+// When that query tile is the user's only one (no other item streams the
+// same keys) and it has two key tiles or more, the planner marks it
+// (n_split = 2) and its keys are split over the two warpgroups ("key-split"
+// item): the query tile is loaded into both Q
+// buffers, A takes key tiles 0, 2, 4, ..., B takes 1, 3, 5, ..., and the two
+// partial results of every row are merged in the CTA with the log-sum-exp
+// rule of "Chapter 4", §4.6.4 (each warpgroup finishes half of the output
+// columns).  Its ring order is K0, K1, then per pair of key tiles (2i, 2i+1):
+// V_2i, K_2i+2, V_2i+1, K_2i+3.  An item with one key tile and no tile B runs
+// on warps 4-7 alone.  In a fused self + target call an item may also be two
+// blocks of 128 rows of the user's own sequence (tile B the second block).
+// Every wait is bounded, as in the single-tile kernel.
 #pragma once
 
 #include "ikbo_attn_tc.cuh"
@@ -87,6 +97,10 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
       ptx::mbar_init(ptx::smem_addr(&ctl->kv_empty[i]), 1);
     }
     ptx::mbar_init(ptx::smem_addr(&ctl->drain), 1);
+    // key-split items: both warpgroups published their row statistics, and
+    // both finished reading the two accumulators (one arrival per warp)
+    ptx::mbar_init(ptx::smem_addr(&ctl->pair_go), kPpGroups * kPpSoftmaxWarps);
+    ptx::mbar_init(ptx::smem_addr(&ctl->pair_recv), kPpGroups * kPpSoftmaxWarps);
     ctl->abort_flag = 0;
     ctl->flags = 0;
     ptx::fence_mbar_init();
@@ -147,6 +161,16 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
   auto tile_rows = [&](const WorkItem& w, int g) {
     return (kSelf && w.q_row >= 0) ? tile_cands(w, g) : tile_cands(w, g) * Lq;
   };
+  // the user's only query tile, two key tiles or more: the keys split over
+  // both warpgroups.  (A lone tile of a user with other tiles is not split:
+  // its sibling items stream the same keys at one tile per step, and a split
+  // item running ahead of them at two would fetch from DRAM what they then
+  // fetch again: the sweeps ran 10-37 % slower so.)  At D = 64 the split is
+  // not compiled: its code made every other item of the D = 64 sweeps 7 %
+  // slower, while at D = 128 the same code made them 1.5-4 % faster.
+  auto key_split = [&](const WorkItem& w) {
+    return D == 128 && w.n_split == 2 && tile_cands(w, 1) == 0 && ntiles(w) >= 2;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -202,15 +226,18 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
         }
         CUtensorMap* m = p.map_slots + (size_t)p.map_stride * blockIdx.x + 2 + cur_item;
         ptx::tensormap_acquire(m);
+        ptx::prefetch_tensormap(m);
         return m;
       };
       // the next ring load: one K or V tile (128 keys x D of one head); the
       // item's keys end at row `end`
       auto ring = [&](bool is_v, int head, int32_t row, int32_t end) -> bool {
         const uint32_t slot = kv_it % NS;
-        if (!W.conv_wait(ptx::smem_addr(&ctl->kv_empty[slot]), ((kv_it / NS) & 1u) ^ 1u)) return false;
+        // the map first: a bounded map's acquire and descriptor fetch then
+        // overlap the wait for the slot
         const void* map = is_v ? v_map_for(row, end) : kv_map(false, row);
         if (!map) return false;
+        if (!W.conv_wait(ptx::smem_addr(&ctl->kv_empty[slot]), ((kv_it / NS) & 1u) ^ 1u)) return false;
         const uint32_t bar = ptx::smem_addr(&ctl->kv_full[slot]);
         const uint32_t dst = ptx::smem_addr(kv_smem + slot * C::kKVBytes);
         ptx::mbar_arrive_expect_tx_warp(bar, C::kKVBytes);
@@ -220,13 +247,13 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
         ++kv_it;
         return true;
       };
-      // query tile g of item w into Q buffer g
-      auto load_q = [&](int g, const WorkItem& w) -> bool {
+      // query tile src of item w into Q buffer g
+      auto load_q = [&](int g, const WorkItem& w, int src) -> bool {
         if (!W.conv_wait(ptx::smem_addr(&ctl->q_empty[g]), (qn[g] & 1u) ^ 1u)) return false;
         ++qn[g];
         if (p.debug_flags & 1) return true;    // test hook: never arm the Q barrier
-        const int nc = tile_cands(w, g);
-        const int32_t c0 = w.cand_begin + g * cpt;
+        const int nc = tile_cands(w, src);
+        const int32_t c0 = w.cand_begin + src * cpt;
         const uint32_t qbar = ptx::smem_addr(&ctl->q_full[g]);
         const uint32_t qdst = ptx::smem_addr(q_smem + g * C::kQBytes);
         if (kSelf && w.q_row >= 0) {
@@ -234,7 +261,7 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
           ptx::mbar_arrive_expect_tx_warp(qbar, uint32_t(C::kCB * kTileM * 128));
           for (int cb = 0; cb < C::kCB; ++cb)
             ptx::tma_load_2d_warp(qdst + cb * kTileM * 128, &qumap, qbar, w.head * D + cb * 64,
-                                  w.q_row + g * kTileM);
+                                  w.q_row + src * kTileM);
         } else if (sorted) {
           const int nb = p.qbox;
           const int nbox = ceil_div(nc, nb);
@@ -262,10 +289,24 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
         // Q_A and K_0 first: S_A(0) needs only these
         const int32_t end = w.kv_begin + w.kv_len;
         cur_item = k;
-        ok = load_q(0, w) && ring(false, w.head, w.kv_begin, end) && (!has_b || load_q(1, w));
-        for (int j = 0; j < n && ok; ++j) {
-          ok = ring(true, w.head, w.kv_begin + j * kBlockN, end);
-          if (ok && j + 1 < n) ok = ring(false, w.head, w.kv_begin + (j + 1) * kBlockN, end);
+        if (!key_split(w)) {
+          ok = load_q(0, w, 0) && ring(false, w.head, w.kv_begin, end) && (!has_b || load_q(1, w, 1));
+          for (int j = 0; j < n && ok; ++j) {
+            ok = ring(true, w.head, w.kv_begin + j * kBlockN, end);
+            if (ok && j + 1 < n) ok = ring(false, w.head, w.kv_begin + (j + 1) * kBlockN, end);
+          }
+        } else {
+          // the same query tile into both buffers; K0 for A, K1 for B, then
+          // per pair of key tiles V_2i, K_2i+2, V_2i+1, K_2i+3 (the MMA order)
+          auto row_of = [&](int t) { return w.kv_begin + t * kBlockN; };
+          ok = load_q(0, w, 0) && ring(false, w.head, row_of(0), end) && load_q(1, w, 0) &&
+               ring(false, w.head, row_of(1), end);
+          for (int t = 0; t < n && ok; t += 2) {
+            ok = ring(true, w.head, row_of(t), end);
+            if (ok && t + 2 < n) ok = ring(false, w.head, row_of(t + 2), end);
+            if (ok && t + 1 < n) ok = ring(true, w.head, row_of(t + 1), end);
+            if (ok && t + 3 < n) ok = ring(false, w.head, row_of(t + 3), end);
+          }
         }
         if (lane == 0) trace(p, k, kTrProdIssued);
       }
@@ -341,10 +382,48 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
         const WorkItem w = item_at(k);
         const int n = ntiles(w);
         const bool has_b = tile_cands(w, 1) > 0;
+        const bool split = key_split(w);
         if (!W.conv_wait(ptx::smem_addr(&ctl->q_full[0]), qn[0] & 1u)) break;
-        if (has_b && !W.conv_wait(ptx::smem_addr(&ctl->q_full[1]), qn[1] & 1u)) break;
+        if ((has_b || split) && !W.conv_wait(ptx::smem_addr(&ctl->q_full[1]), qn[1] & 1u)) break;
         ptx::tc_fence_after();
         if (lane == 0) trace(p, k, kTrMmaQ);
+        if (split) {
+          // A on key tiles 0, 2, 4, ..., B on 1, 3, 5, ...: per pair of key
+          // tiles PV_A, S_A(next), PV_B, S_B(next), the ring consumed in order
+          const int na = (n + 1) / 2, nb = n / 2;
+          uint32_t ri = kv_base;
+          // S_g on the K tile at ring index ri; the last S_g of the item frees Q_g
+          auto s_at = [&](int g, bool last) -> bool {
+            if (!kv_ready(ri)) return false;
+            issue_s(g, ri % NS);
+            if (last) ptx::mma_commit_warp(ptx::smem_addr(&ctl->q_empty[g]));
+            ptx::mma_commit_warp(ptx::smem_addr(&ctl->kv_empty[ri % NS]));
+            ++ri;
+            return true;
+          };
+          // O_g += P_g V for the V tile at ring index ri; the last one marks O_g complete
+          auto pv_at = [&](int g, bool acc, bool last) -> bool {
+            if (!kv_ready(ri) || !issue_pv(g, ri % NS, acc)) return false;
+            if (last) ptx::mma_commit_warp(ptx::smem_addr(&ctl->pv_done[g]));
+            ptx::mma_commit_warp(ptx::smem_addr(&ctl->kv_empty[ri % NS]));
+            ++ri;
+            return true;
+          };
+          ok = s_at(0, na == 1) && s_at(1, nb == 1);
+          if (ok && lane == 0) trace(p, k, kTrMmaFirstS);
+          for (int j = 0; j < na && ok; ++j) {
+            ok = pv_at(0, j > 0, j + 1 == na);
+            if (ok && j + 1 < na) ok = s_at(0, j + 2 == na);
+            if (ok && j < nb) ok = pv_at(1, j > 0, j + 1 == nb);
+            if (ok && j + 1 < nb) ok = s_at(1, j + 2 == nb);
+          }
+          if (!ok) break;
+          if (lane == 0) trace(p, k, kTrMmaLastPV);
+          kv_base = ri;
+          ++qn[0];
+          ++qn[1];
+          continue;
+        }
         if (!kv_ready(kv_base)) break;
         {
           const uint32_t ks = kv_base % NS;
@@ -412,17 +491,21 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
     const uint32_t ocol = tmem + lane_off + C::kOCol(g);
     const float sl2 = p.scale_log2;
     uint32_t tn = 0, dn = 0;                                  // S tiles and items of this tile so far
+    uint32_t sp = 0;                                          // key-split items so far
     for (int k = 0; k < n_my; ++k) {
       const WorkItem w = item_at(k);
-      const int nc = tile_cands(w, g);
+      const bool split = key_split(w);
+      const int tg = split ? 0 : g;                           // the query tile whose rows these are
+      const int nc = tile_cands(w, tg);
       if (nc == 0) continue;
       const int n = ntiles(w);
+      const int ng = split ? (n - g + 1) / 2 : n;             // key tiles of this warpgroup
       // Rows past the tile's queries hold stale shared memory; their results
       // are never stored, and they are left out of every decision below.
-      const bool live = row < tile_rows(w, g);
+      const bool live = row < tile_rows(w, tg);
       float m = -INFINITY, l = 0.f;
       bool ok = true;
-      for (int j = 0; j < n; ++j, ++tn) {
+      for (int j = 0; j < ng; ++j, ++tn) {
         if (!W.warp_wait(ptx::smem_addr(&ctl->s_full[g]), tn & 1u)) {
           ok = false;
           break;
@@ -439,7 +522,7 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
         // sc = scale on full tiles for scale > 0 (their order is that of the
         // scaled ones), else scaled here with the keys past the user's
         // sequence at -inf (sc = 1).
-        const int valid = min(kBlockN, w.kv_len - j * kBlockN);
+        const int valid = min(kBlockN, w.kv_len - (split ? 2 * j + g : j) * kBlockN);
         float sc = sl2;
         if (valid < kBlockN || !(sl2 > 0.f)) {
 #pragma unroll
@@ -517,20 +600,69 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
       ++dn;
       ptx::tc_fence_after();
       if (row == 0 && g == 0) trace(p, k, kTrEpiO);
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      const float2 inv2 = make_float2(inv, inv);
       uint16_t* dst;
       if (kSelf && w.q_row >= 0) {
-        // a self-attention row: out_user[q_row + 128 g + row, head, :]
-        const int64_t srow = live ? (int64_t)w.q_row + g * kTileM + row : 0;
+        // a self-attention row: out_user[q_row + 128 tg + row, head, :]
+        const int64_t srow = live ? (int64_t)w.q_row + tg * kTileM + row : 0;
         dst = p.out_user + ((srow * p.H + w.head) * D);
       } else {
         const int ci = live ? row / Lq : 0;
         const int tq = live ? row - ci * Lq : 0;
-        const int32_t gpos = w.cand_begin + g * cpt + ci;
+        const int32_t gpos = w.cand_begin + tg * cpt + ci;
         const int64_t cidx = live ? (sorted ? gpos : perm[gpos]) : 0;
         dst = p.out + (((cidx * p.H + w.head) * (int64_t)Lq + tq) * D);
       }
+      if (split) {
+        // Merge the two warpgroups' partial results of this row ("Chapter 4",
+        // §4.6.4): with M = max(m_A, m_B), a = 2^(m_A - M), b = 2^(m_B - M),
+        // out = (a O_A + b O_B) / (a l_A + b l_B).  Each warpgroup finishes
+        // half of the columns, reading both accumulators.
+        ctl->ab_ml[g][row] = make_float2(m, l);
+        __syncwarp();
+        ptx::mbar_arrive_warp(ptx::smem_addr(&ctl->pair_go));
+        if (!W.warp_wait(ptx::smem_addr(&ctl->pair_go), sp & 1u)) break;
+        const float2 other = ctl->ab_ml[g ^ 1][row];
+        const float mm = fmaxf(m, other.x);
+        const float a = fast_exp2(m - mm), b = fast_exp2(other.x - mm);
+        const float den = a * l + b * other.y;
+        const float inv = den > 0.f ? 1.f / den : 0.f;
+        const float2 fa2 = make_float2(a * inv, a * inv), fb2 = make_float2(b * inv, b * inv);
+        const uint32_t own = ocol, oth = tmem + lane_off + C::kOCol(g ^ 1);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          const int col = g * (D / 2) + c * 32;
+          uint32_t oa[32], ob[32];
+          ptx::tmem_ld32(own + col, oa);
+          ptx::tmem_ld32(oth + col, ob);
+          ptx::tmem_ld_wait();
+          if (live) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + col);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              uint32_t pk[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int i = 8 * q4 + 2 * e;
+                const float2 x = ffma2(make_float2(__uint_as_float(oa[i]), __uint_as_float(oa[i + 1])), fa2,
+                                       fmul2(make_float2(__uint_as_float(ob[i]), __uint_as_float(ob[i + 1])), fb2));
+                pk[e] = pack_bf16(x.x, x.y);
+              }
+              d4[q4] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+          }
+        }
+        if (row == 0 && g == 0) trace(p, k, kTrEpiStored);
+        // both warpgroups are done with both accumulators (and with the row
+        // statistics) before either hands over the next item's first P
+        ptx::tc_fence_before();
+        __syncwarp();
+        ptx::mbar_arrive_warp(ptx::smem_addr(&ctl->pair_recv));
+        if (!W.warp_wait(ptx::smem_addr(&ctl->pair_recv), sp & 1u)) break;
+        ++sp;
+        continue;
+      }
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];

@@ -748,7 +748,9 @@ __device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch, 
     w.kv_len = off[u + 1] - off[u];
     w.unit = -1;
     w.unit_first = 0;
-    w.n_split = 1;
+    // two-tile kernel: a user's only query tile may have its keys split over
+    // the two warpgroups
+    w.n_split = (tiles_per_unit == 2 && mt < nmt && r <= p.cands_per_tile) ? 2 : 1;
   };
   WorkItem* mine = p.cta_items + (size_t)b * p.max_cta_items;
   if (pair) {

@@ -33,7 +33,9 @@ struct WorkItem {
   int32_t unit;        // split-combine unit, or -1 when the item covers all keys
   int32_t unit_first;  // first item index of the unit (its n_split items are consecutive)
   int32_t q_row;       // self-attention tile: its first row of q_user / out_user; else -1
-  int32_t n_split;     // key-interleaved kernel: chunks of the unit (1 = the item covers all keys)
+  int32_t n_split;     // parts the unit's keys are cut into: key-interleaved kernel, chunks on as many
+                       // CTAs (1 = the item covers all keys); two-tile kernel, 2 = a user's only query
+                       // tile, its keys interleaved over the two warpgroups
 };
 static_assert(sizeof(WorkItem) == 40, "WorkItem layout");
 

@@ -43,11 +43,28 @@
 // Clusters (M of at most 8 row tiles): the CTAs of a cluster take the row
 // tiles of one batch entry at a time, CTA r tile r.  A cluster runs on one
 // die, so the X tile that all its CTAs load comes from DRAM once and from
-// that die's L2 for the others.  The CTAs touch nothing of one another:
-// each loads its own W and X tiles into its own ring.
-// Teardown: every byte that reaches a CTA is counted on one of its own ring
-// barriers, which its producer drains.  Every wait is bounded, as in the
-// attention kernels.
+// that die's L2 for the others.
+//
+// Two forms:
+//   kPair = false  every CTA computes its 128 rows alone (M = 128 MMAs); the
+//                  CTAs touch nothing of one another, each loads its own W
+//                  and the whole X tile into its own ring;
+//   kPair = true   CTAs 2i and 2i + 1 of the cluster compute 256 rows
+//                  together with M = 256 MMAs over both tensor cores
+//                  (cta_group::2).  Each CTA loads its own 128 rows of W and
+//                  HALF of the X tile's columns (the even CTA the first N/2,
+//                  the odd one the rest): per K step a CTA takes in 32 KB
+//                  instead of 48 KB at N = 256, and its tensor core reads
+//                  8 KB of shared memory per MMA instead of 12.  The even CTA
+//                  issues every MMA; both CTAs' loads complete on the even
+//                  CTA's ring barrier; each MMA commit arrives on the ring,
+//                  accumulator and drain barriers of both CTAs; the odd CTA's
+//                  epilogue hands its accumulator back to the even CTA's
+//                  barrier.  Each CTA's epilogue reads its own 128 rows from
+//                  its own tensor memory.
+// Teardown: every byte that reaches a CTA is counted on a ring barrier that a
+// producer drains; with CTA pairs no CTA leaves before its cluster has.
+// Every wait is bounded, as in the attention kernels.
 #pragma once
 
 #include "ikbo_attn_tc.cuh"
@@ -79,11 +96,12 @@ struct LceParams {
   uint64_t timeout_ns;
 };
 
-template <int NB>
+template <int NB, bool kPair = false>
 struct LceConfig {
   static constexpr int N = NB * 64;
+  static constexpr int kXBlocks = kPair ? NB / 2 : NB;  // 64-column blocks of X this CTA loads
   static constexpr int kABytes = kTileM * 128;          // 128 rows x 64 bf16
-  static constexpr int kBBytes = NB * kLceKStep * 128;  // NB blocks of 64 rows x 64 bf16
+  static constexpr int kBBytes = kXBlocks * kLceKStep * 128;  // blocks of 64 rows x 64 bf16
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStages0 = (kLceSmemBytes - kLceCtrlBytes) / kStageBytes;
   static constexpr int kStages = kStages0 < kLceMaxStages ? kStages0 : kLceMaxStages;
@@ -91,6 +109,7 @@ struct LceConfig {
   static_assert(kStages >= 2, "ring");
   static_assert(kDataBytes + kLceCtrlBytes <= kLceSmemBytes, "shared memory");
   static_assert(2 * N <= 512, "two accumulators in tensor memory");
+  static_assert(!kPair || NB % 2 == 0, "CTA pairs split X into halves of whole 64-column blocks");
 };
 
 struct LceCtrl {
@@ -102,11 +121,11 @@ struct LceCtrl {
 };
 static_assert(sizeof(LceCtrl) <= kLceCtrlBytes, "control block");
 
-template <int NB>
+template <int NB, bool kPair>
 __global__ void __launch_bounds__(kLceThreads, 1)
 ikbo_lce_kernel(const __grid_constant__ LceParams p, const __grid_constant__ CUtensorMap wmap,
                 const __grid_constant__ CUtensorMap xmap) {
-  using C = LceConfig<NB>;
+  using C = LceConfig<NB, kPair>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* data = smem_raw;
   LceCtrl* ctl = reinterpret_cast<LceCtrl*>(smem_raw + C::kDataBytes);
@@ -123,7 +142,9 @@ ikbo_lce_kernel(const __grid_constant__ LceParams p, const __grid_constant__ CUt
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(ptx::smem_addr(&ctl->acc_full[i]), 1);
-      ptx::mbar_init(ptx::smem_addr(&ctl->acc_empty[i]), 4);   // the 4 epilogue warps
+      // the 4 epilogue warps (with CTA pairs, the even CTA's barrier also
+      // takes the odd CTA's 4)
+      ptx::mbar_init(ptx::smem_addr(&ctl->acc_empty[i]), kPair ? 8 : 4);
     }
     ptx::mbar_init(ptx::smem_addr(&ctl->drain), 1);
     ctl->abort_flag = 0;
@@ -131,15 +152,22 @@ ikbo_lce_kernel(const __grid_constant__ LceParams p, const __grid_constant__ CUt
     if (!layout_ok) atomicOr(p.err_word, kErrLayout);
   }
   if (warp == 1) {
-    ptx::tmem_alloc(ptx::smem_addr(&ctl->tmem_base), 512);
-    ptx::tmem_relinquish();
+    if constexpr (kPair) {
+      ptx::tmem_alloc_pair(ptx::smem_addr(&ctl->tmem_base), 512);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(ptx::smem_addr(&ctl->tmem_base), 512);
+      ptx::tmem_relinquish();
+    }
   }
   if (warp == 2 && lane == 0) {
     ptx::prefetch_tensormap(&wmap);
     ptx::prefetch_tensormap(&xmap);
   }
   ptx::tc_fence_before();
-  __syncthreads();
+  // with CTA pairs, the peer's barriers are initialised before any MMA
+  // commit or TMA byte reaches them
+  if constexpr (kPair) ptx::cluster_sync(); else __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
   const Waiter W{&ctl->abort_flag, p.err_word, p.timeout_ns};
@@ -149,6 +177,12 @@ ikbo_lce_kernel(const __grid_constant__ LceParams p, const __grid_constant__ CUt
   // tile = rank; without, (batch entry, row tile) pairs
   const int cn = p.cluster_n;
   const int rank = cn > 1 ? int(ptx::cluster_ctarank()) : 0;
+  // CTA pairs: the even CTA (the "leader") issues the MMAs; barrier
+  // addresses in both CTAs of the pair
+  const bool leader = !kPair || (rank & 1) == 0;
+  const uint32_t pair_lead = uint32_t(rank & ~1), pair_odd = uint32_t(rank | 1);
+  auto lead_bar = [&](uint64_t* b) { return ptx::map_to_cta(ptx::smem_addr(b), pair_lead); };
+  auto odd_bar = [&](uint64_t* b) { return ptx::map_to_cta(ptx::smem_addr(b), pair_odd); };
   const int64_t first = cn > 1 ? blockIdx.x / cn : blockIdx.x;
   const int64_t stride = cn > 1 ? gridDim.x / cn : gridDim.x;
   const int64_t n_units = cn > 1 ? p.n_batch : p.n_batch * mt_count;
@@ -176,28 +210,53 @@ ikbo_lce_kernel(const __grid_constant__ LceParams p, const __grid_constant__ CUt
             ok = false;
             break;
           }
-          const uint32_t bar = ptx::smem_addr(&ctl->full[slot]);
           const uint32_t dst = ptx::smem_addr(data + slot * C::kStageBytes);
-          ptx::mbar_arrive_expect_tx(bar, C::kStageBytes);
-          // W[mt*128 .. +128, k .. k+64] (rows past M and columns past K read as zeros)
-          ptx::tma_load_2d(dst, &wmap, bar, ks * kLceKStep, mt * kTileM);
-          // X[b, k .. k+64, 64 c .. 64 c + 64] for each 64-column block c
+          if constexpr (kPair) {
+            // both CTAs' bytes complete on the even CTA's barrier, which the
+            // even CTA's producer arms for both
+            const uint32_t bar = lead_bar(&ctl->full[slot]);
+            if (leader) ptx::mbar_arrive_expect_tx(ptx::smem_addr(&ctl->full[slot]), 2 * C::kStageBytes);
+            ptx::tma_load_2d_pair(dst, &wmap, bar, ks * kLceKStep, mt * kTileM);
+            const int c0 = (rank & 1) * C::kXBlocks;   // this CTA's half of the columns
 #pragma unroll
-          for (int c = 0; c < NB; ++c)
-            ptx::tma_load_3d(dst + C::kABytes + c * kLceKStep * 128, &xmap, bar, c * 64, ks * kLceKStep, b);
+            for (int c = 0; c < C::kXBlocks; ++c)
+              ptx::tma_load_3d_pair(dst + C::kABytes + c * kLceKStep * 128, &xmap, bar, (c0 + c) * 64,
+                                    ks * kLceKStep, b);
+          } else {
+            const uint32_t bar = ptx::smem_addr(&ctl->full[slot]);
+            ptx::mbar_arrive_expect_tx(bar, C::kStageBytes);
+            // W[mt*128 .. +128, k .. k+64] (rows past M and columns past K read as zeros)
+            ptx::tma_load_2d(dst, &wmap, bar, ks * kLceKStep, mt * kTileM);
+            // X[b, k .. k+64, 64 c .. 64 c + 64] for each 64-column block c
+#pragma unroll
+            for (int c = 0; c < NB; ++c)
+              ptx::tma_load_3d(dst + C::kABytes + c * kLceKStep * 128, &xmap, bar, c * 64, ks * kLceKStep, b);
+          }
         }
       }
-      // every armed phase must complete before the CTA exits
-      for (uint32_t s = 0; s < (uint32_t)C::kStages && s < it; ++s) {
-        const uint32_t uses = (it - s + C::kStages - 1) / C::kStages;
-        W.drain(ptx::smem_addr(&ctl->full[s]), (uses - 1) & 1u);
-      }
+      // every armed phase must complete before the CTA exits (with CTA
+      // pairs the even CTA's barriers count both CTAs' bytes; the odd CTA
+      // stays until the cluster's closing barrier)
+      if (leader)
+        for (uint32_t s = 0; s < (uint32_t)C::kStages && s < it; ++s) {
+          const uint32_t uses = (it - s + C::kStages - 1) / C::kStages;
+          W.drain(ptx::smem_addr(&ctl->full[s]), (uses - 1) & 1u);
+        }
     }
     __syncwarp();
-  } else if (layout_ok && warp == 1) {
+  } else if (layout_ok && warp == 1 && leader) {
     // -------------------------------------------------------------- MMA warp
     // converged; the elected lane issues every MMA and commit
-    constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kTileM, C::N, 1);
+    constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kPair ? 2 * kTileM : kTileM, C::N, 1);
+    // commit to this CTA's barrier and, with CTA pairs, to the odd CTA's too
+    auto commit = [&](uint64_t* b) {
+      if constexpr (kPair) {
+        ptx::mma_commit_pair_warp(ptx::smem_addr(b));
+        ptx::mma_commit_pair_warp(odd_bar(b));
+      } else {
+        ptx::mma_commit_warp(ptx::smem_addr(b));
+      }
+    };
     uint32_t it = 0, ui = 0;
     bool ok = true;
     for (int64_t unit = first; unit < n_units && ok; unit += stride, ++ui) {
@@ -222,14 +281,17 @@ ikbo_lce_kernel(const __grid_constant__ LceParams p, const __grid_constant__ CUt
           // B: N contiguous (MN-major): 16 K-rows per step, 64-column blocks
           // kLceKStep * 128 bytes apart, 8-row groups 1 KB apart
           const uint64_t bdesc = ptx::smem_desc_sw128(b_base + kk * 16 * 128, kLceKStep * 128, 1024);
-          ptx::mma_ss_warp(d_tmem, adesc, bdesc, kIdesc, (ks > 0 || kk > 0) ? 1u : 0u);
+          if constexpr (kPair)
+            ptx::mma_ss_pair_warp(d_tmem, adesc, bdesc, kIdesc, (ks > 0 || kk > 0) ? 1u : 0u);
+          else
+            ptx::mma_ss_warp(d_tmem, adesc, bdesc, kIdesc, (ks > 0 || kk > 0) ? 1u : 0u);
         }
-        ptx::mma_commit_warp(ptx::smem_addr(&ctl->empty[slot]));
+        commit(&ctl->empty[slot]);
       }
       if (!ok) break;
-      ptx::mma_commit_warp(ptx::smem_addr(&ctl->acc_full[buf]));
+      commit(&ctl->acc_full[buf]);
     }
-    ptx::mma_commit_warp(ptx::smem_addr(&ctl->drain));
+    commit(&ctl->drain);
     if (lane == 0) W.drain(ptx::smem_addr(&ctl->drain), 0);
     __syncwarp();
   } else if (layout_ok && warp >= kLceEpiWarp0) {
@@ -318,16 +380,35 @@ ikbo_lce_kernel(const __grid_constant__ LceParams p, const __grid_constant__ CUt
           }
         }
       }
-      // this accumulator may take the next unit's MMAs
+      // this accumulator may take the next unit's MMAs (with CTA pairs, the
+      // even CTA's barrier counts both CTAs' epilogue warps)
       ptx::tc_fence_before();
-      ptx::mbar_arrive_warp(ptx::smem_addr(&ctl->acc_empty[buf]));
+      if constexpr (kPair) {
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive_cluster(lead_bar(&ctl->acc_empty[buf]));
+      } else {
+        ptx::mbar_arrive_warp(ptx::smem_addr(&ctl->acc_empty[buf]));
+      }
     }
   }
   ptx::tc_fence_before();
-  __syncthreads();
+  if constexpr (kPair) {
+    // The even CTA's MMAs read the odd CTA's shared memory and write its
+    // tensor memory, and the odd CTA's loads complete on the even CTA's
+    // barriers: both leave together, after the even CTA has drained both.
+    // The odd CTA also takes the drain commit, once its own roles are done
+    // (then the last MMA has completed, or the call has failed), so that it
+    // sees the last MMA complete before it frees its tensor memory.
+    __syncthreads();
+    if (warp == 1 && !leader && layout_ok && lane == 0) W.drain(ptx::smem_addr(&ctl->drain), 0);
+    __syncwarp();
+    ptx::cluster_sync();
+  } else {
+    __syncthreads();
+  }
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, 512);
+    if constexpr (kPair) ptx::tmem_dealloc_pair(tmem, 512); else ptx::tmem_dealloc(tmem, 512);
   }
 }
 

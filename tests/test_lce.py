@@ -3,7 +3,9 @@
 CPU: host-side argument checks (nothing reaches the GPU).  GPU: the tcgen05 path against
 the fp64 oracle on the pages' configuration (sampled candidates) and on small cases that
 cover ragged M (a partial last row tile), K blocks that are not multiples of 64, every
-supported N, a call without a user block, one candidate per user, and a bad index.
+supported N (N = 128 and 256 with M over one row tile run on CTA pairs with M = 256
+MMAs, the others CTA by CTA), a call without a user block, one candidate per user, and
+a bad index.
 """
 import numpy as np
 import pytest
@@ -86,11 +88,13 @@ def test_shapes(gpu_lib, M, K_user, K_cand, N):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("M", [700, 1100])
-def test_many_row_tiles(gpu_lib, M):
-    """Clusters of six CTAs (M = 700: six row tiles) and no cluster (M = 1100: nine)."""
-    cfg = W.LceConfig(name="mt", n_cand=5, n_user=2, M=M, K_user=16, K_cand=80, N=64, seed=M)
-    check(gpu_lib, W.lce_generate(cfg), f"M={M}")
+@pytest.mark.parametrize("N", [64, 256])
+@pytest.mark.parametrize("M", [700, 1024, 1100])
+def test_many_row_tiles(gpu_lib, M, N):
+    """Clusters of six CTAs (M = 700: six row tiles) and eight (M = 1024: eight, the most a
+    cluster takes), as three and four CTA pairs at N = 256; no cluster (M = 1100: nine)."""
+    cfg = W.LceConfig(name="mt", n_cand=5, n_user=2, M=M, K_user=16, K_cand=80, N=N, seed=M + N)
+    check(gpu_lib, W.lce_generate(cfg), f"M={M} N={N}")
 
 
 @pytest.mark.gpu
