@@ -980,12 +980,28 @@ int encode_lce_x_map(CUtensorMap* m, const void* X, int64_t B, int K, int N) {
   return r == CUDA_SUCCESS ? IKBO_OK : IKBO_ERR_CUDA;
 }
 
+// out [B, M, N] (the output, or the term of the level below) as a 3-D map
+// {N, M, B}: the epilogue's store boxes of 64 columns x 32 rows of one entry
+// (rows past M are not written).
+int encode_lce_out_map(CUtensorMap* m, const void* out, int64_t B, int M, int N) {
+  cuuint64_t dims[3] = {cuuint64_t(N), cuuint64_t(M), cuuint64_t(B)};
+  cuuint64_t strides[2] = {cuuint64_t(N) * 2, cuuint64_t(M) * N * 2};
+  cuuint32_t box[3] = {64, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(out), dims, strides,
+                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? IKBO_OK : IKBO_ERR_CUDA;
+}
+
 // Units of the batch: one per batch entry and row tile, or, with clusters, one
 // per batch entry (a cluster of cluster_n CTAs takes its row tiles).  Grid:
 // as many CTAs as there are units, at most as many as fit at once.
 template <int NB, bool kPair>
 cudaError_t launch_lce(DeviceState* ds, const LceParams& lp, const CUtensorMap& wm,
                        const CUtensorMap& xm, bool pdl, cudaStream_t st) {
+  CUtensorMap om;
+  if (encode_lce_out_map(&om, lp.out, lp.n_batch, lp.M, lp.N) != IKBO_OK) return cudaErrorInvalidValue;
   auto kern = ikbo_lce_kernel<NB, kPair>;
   if (!ds->lce_ready[kPair][NB - 1]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kLceSmemBytes);
@@ -1019,7 +1035,7 @@ cudaError_t launch_lce(DeviceState* ds, const LceParams& lp, const CUtensorMap& 
     const int64_t units = lp.n_batch * ((lp.M + kTileM - 1) / kTileM);
     grid = int(units < ds->num_sms ? units : ds->num_sms);
   }
-  return launch_ex(kern, dim3(grid), dim3(kLceThreads), kLceSmemBytes, st, pdl, cn, lp, wm, xm);
+  return launch_ex(kern, dim3(grid), dim3(kLceThreads), kLceSmemBytes, st, pdl, cn, lp, wm, xm, om);
 }
 
 // CTA pairs (M = 256 MMAs over two CTAs) when M spans two row tiles or more,

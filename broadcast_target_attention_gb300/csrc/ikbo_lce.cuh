@@ -35,7 +35,11 @@
 //              two accumulators so that the epilogue of one unit overlaps the
 //              MMAs of the next;
 //   warps 4-7  epilogue: TMEM lane r = row r of the tile; 32 columns at a time,
-//              + Y of the level above, rounded to bf16 and stored.
+//              + Y of the level above, rounded to bf16 into a shared-memory
+//              staging box (each warp its 32 rows x 64 columns, two boxes in
+//              turn), which the warp's TMA store writes out: whole 128-byte
+//              lines, where one row per thread would write 16 bytes to each
+//              of 32 rows 512 bytes apart.
 // Each level is launched as a programmatic dependent of the one above; only
 // its epilogue waits for the Y it adds, so its loads and MMAs overlap the
 // level above.
@@ -76,6 +80,8 @@ constexpr int kLceEpiWarp0 = 4;
 constexpr int kLceKStep = 64;                  // K per ring stage (one 128-byte swizzle atom of bf16)
 constexpr int kLceSmemBytes = 232448;          // the per-CTA maximum
 constexpr int kLceCtrlBytes = 1024;
+constexpr int kLceEpiBoxBytes = 32 * 64 * 2;   // one epilogue warp's store box: 32 rows x 64 bf16
+constexpr int kLceEpiBytes = 4 * 2 * kLceEpiBoxBytes;   // 4 warps x 2 boxes
 constexpr int kLceMaxStages = 8;
 
 struct LceParams {
@@ -103,11 +109,12 @@ struct LceConfig {
   static constexpr int kABytes = kTileM * 128;          // 128 rows x 64 bf16
   static constexpr int kBBytes = kXBlocks * kLceKStep * 128;  // blocks of 64 rows x 64 bf16
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kStages0 = (kLceSmemBytes - kLceCtrlBytes) / kStageBytes;
+  static constexpr int kStages0 = (kLceSmemBytes - kLceCtrlBytes - kLceEpiBytes) / kStageBytes;
   static constexpr int kStages = kStages0 < kLceMaxStages ? kStages0 : kLceMaxStages;
-  static constexpr int kDataBytes = kStages * kStageBytes;
+  static constexpr int kDataBytes = kStages * kStageBytes;   // the ring, then the epilogue boxes
   static_assert(kStages >= 2, "ring");
-  static_assert(kDataBytes + kLceCtrlBytes <= kLceSmemBytes, "shared memory");
+  static_assert(kDataBytes % 1024 == 0, "epilogue boxes 1 KB aligned (128-byte swizzle)");
+  static_assert(kDataBytes + kLceEpiBytes + kLceCtrlBytes <= kLceSmemBytes, "shared memory");
   static_assert(2 * N <= 512, "two accumulators in tensor memory");
   static_assert(!kPair || NB % 2 == 0, "CTA pairs split X into halves of whole 64-column blocks");
 };
@@ -124,11 +131,12 @@ static_assert(sizeof(LceCtrl) <= kLceCtrlBytes, "control block");
 template <int NB, bool kPair>
 __global__ void __launch_bounds__(kLceThreads, 1)
 ikbo_lce_kernel(const __grid_constant__ LceParams p, const __grid_constant__ CUtensorMap wmap,
-                const __grid_constant__ CUtensorMap xmap) {
+                const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap omap) {
   using C = LceConfig<NB, kPair>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* data = smem_raw;
-  LceCtrl* ctl = reinterpret_cast<LceCtrl*>(smem_raw + C::kDataBytes);
+  uint8_t* epi_smem = smem_raw + C::kDataBytes;
+  LceCtrl* ctl = reinterpret_cast<LceCtrl*>(smem_raw + C::kDataBytes + kLceEpiBytes);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   // the level below may start at once (it waits for this level's Y only in
@@ -163,6 +171,7 @@ ikbo_lce_kernel(const __grid_constant__ LceParams p, const __grid_constant__ CUt
   if (warp == 2 && lane == 0) {
     ptx::prefetch_tensormap(&wmap);
     ptx::prefetch_tensormap(&xmap);
+    ptx::prefetch_tensormap(&omap);
   }
   ptx::tc_fence_before();
   // with CTA pairs, the peer's barriers are initialised before any MMA
@@ -299,6 +308,10 @@ ikbo_lce_kernel(const __grid_constant__ LceParams p, const __grid_constant__ CUt
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;                      // TMEM lane == tile row
     const uint32_t lane_off = uint32_t(quarter * 32) << 16;
+    // this warp's two store boxes (32 rows x 64 columns, 128-byte swizzle)
+    const uint32_t box0 = ptx::smem_addr(epi_smem + quarter * 2 * kLceEpiBoxBytes);
+    uint32_t nbox = 0;          // boxes staged so far (the buffer is nbox & 1)
+    bool prev_stored = false;   // the box before was stored (its group may still read)
     bool y_ready = !p.add;
     uint32_t ui = 0;
     for (int64_t unit = first; unit < n_units; unit += stride, ++ui) {
@@ -352,7 +365,16 @@ ikbo_lce_kernel(const __grid_constant__ LceParams p, const __grid_constant__ CUt
         uint32_t o[32];
         ptx::tmem_ld32(acc + c * 32, o);
         ptx::tmem_ld_wait();
-        if (live && !bad) {
+        const uint32_t box = box0 + (nbox & 1u) * kLceEpiBoxBytes;
+        if ((c & 1) == 0 && !bad && nbox >= 2) {
+          // the box's buffer was last stored two boxes ago: that store has
+          // read it once at most one group (the box before) is still reading
+          if (lane == 0) {
+            if (prev_stored) ptx::bulk_wait_read_1(); else ptx::bulk_wait_read_0();
+          }
+          __syncwarp();
+        }
+        if (!bad) {
           float x[32];
 #pragma unroll
           for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(o[e]);
@@ -368,15 +390,27 @@ ikbo_lce_kernel(const __grid_constant__ LceParams p, const __grid_constant__ CUt
               }
             }
           }
-          uint4* dst = reinterpret_cast<uint4*>(p.out + ((int64_t)b * p.M + m) * p.N + c * 32);
+          // row `lane` of the box: 16-byte chunk k of the row at k ^ (row % 8)
 #pragma unroll
           for (int q8 = 0; q8 < 4; ++q8) {
-            uint4 v;
-            v.x = pack_bf16(x[8 * q8], x[8 * q8 + 1]);
-            v.y = pack_bf16(x[8 * q8 + 2], x[8 * q8 + 3]);
-            v.z = pack_bf16(x[8 * q8 + 4], x[8 * q8 + 5]);
-            v.w = pack_bf16(x[8 * q8 + 6], x[8 * q8 + 7]);
-            dst[q8] = v;
+            const uint32_t k = uint32_t(((c & 1) * 4 + q8) ^ (lane & 7));
+            ptx::st_shared_v4(box + lane * 128 + k * 16, pack_bf16(x[8 * q8], x[8 * q8 + 1]),
+                              pack_bf16(x[8 * q8 + 2], x[8 * q8 + 3]), pack_bf16(x[8 * q8 + 4], x[8 * q8 + 5]),
+                              pack_bf16(x[8 * q8 + 6], x[8 * q8 + 7]));
+          }
+          if (c & 1) {
+            // the box is complete: the warp's TMA store writes it (rows past M
+            // are not written), in a bulk group of its own
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            const int y0 = mt * kTileM + quarter * 32;
+            const bool store = y0 < p.M;
+            if (lane == 0) {
+              if (store) ptx::tma_store_3d(&omap, box, (c >> 1) * 64, y0, b);
+              ptx::bulk_commit_group();
+            }
+            prev_stored = store;
+            ++nbox;
           }
         }
       }
@@ -390,6 +424,9 @@ ikbo_lce_kernel(const __grid_constant__ LceParams p, const __grid_constant__ CUt
         ptx::mbar_arrive_warp(ptx::smem_addr(&ctl->acc_empty[buf]));
       }
     }
+    // every store has written its box before the CTA leaves
+    if (lane == 0) ptx::bulk_wait_all();
+    __syncwarp();
   }
   ptx::tc_fence_before();
   if constexpr (kPair) {
