@@ -879,16 +879,10 @@ ikbo_attn_ab_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
             }
           }
         }
-        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+        uint32_t w[16];
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          uint4 v;
-          v.x = pack_bf16(x[8 * q4 + 0], x[8 * q4 + 1]);
-          v.y = pack_bf16(x[8 * q4 + 2], x[8 * q4 + 3]);
-          v.z = pack_bf16(x[8 * q4 + 4], x[8 * q4 + 5]);
-          v.w = pack_bf16(x[8 * q4 + 6], x[8 * q4 + 7]);
-          d4[q4] = v;
-        }
+        for (int e = 0; e < 16; ++e) w[e] = pack_bf16(x[2 * e], x[2 * e + 1]);
+        store_bf16x32(dst + c * 32, w);
       }
       if (partial && live && g == 0) p.ab_partial_lse[slot * kTileM + row] = lse;
       // The next item's first PVs overwrite O_A and O_B: both warpgroups are

@@ -636,19 +636,14 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
           ptx::tmem_ld32(oth + col, ob);
           ptx::tmem_ld_wait();
           if (live) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + col);
+            uint32_t w[16];
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              uint32_t pk[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int i = 8 * q4 + 2 * e;
-                const float2 x = ffma2(make_float2(__uint_as_float(oa[i]), __uint_as_float(oa[i + 1])), fa2,
-                                       fmul2(make_float2(__uint_as_float(ob[i]), __uint_as_float(ob[i + 1])), fb2));
-                pk[e] = pack_bf16(x.x, x.y);
-              }
-              d4[q4] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            for (int e = 0; e < 16; ++e) {
+              const float2 x = ffma2(make_float2(__uint_as_float(oa[2 * e]), __uint_as_float(oa[2 * e + 1])), fa2,
+                                     fmul2(make_float2(__uint_as_float(ob[2 * e]), __uint_as_float(ob[2 * e + 1])), fb2));
+              w[e] = pack_bf16(x.x, x.y);
             }
+            store_bf16x32(dst + col, w);
           }
         }
         if (row == 0 && g == 0) trace(p, k, kTrEpiStored);
@@ -669,20 +664,13 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
         ptx::tmem_ld32(ocol + c * 32, o);
         ptx::tmem_ld_wait();
         if (live) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+          uint32_t w[16];
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const float2 x0 = fmul2(make_float2(__uint_as_float(o[8 * q4 + 0]), __uint_as_float(o[8 * q4 + 1])), inv2);
-            const float2 x1 = fmul2(make_float2(__uint_as_float(o[8 * q4 + 2]), __uint_as_float(o[8 * q4 + 3])), inv2);
-            const float2 x2 = fmul2(make_float2(__uint_as_float(o[8 * q4 + 4]), __uint_as_float(o[8 * q4 + 5])), inv2);
-            const float2 x3 = fmul2(make_float2(__uint_as_float(o[8 * q4 + 6]), __uint_as_float(o[8 * q4 + 7])), inv2);
-            uint4 v;
-            v.x = pack_bf16(x0.x, x0.y);
-            v.y = pack_bf16(x1.x, x1.y);
-            v.z = pack_bf16(x2.x, x2.y);
-            v.w = pack_bf16(x3.x, x3.y);
-            d4[q4] = v;
+          for (int e = 0; e < 16; ++e) {
+            const float2 x = fmul2(make_float2(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1])), inv2);
+            w[e] = pack_bf16(x.x, x.y);
           }
+          store_bf16x32(dst + c * 32, w);
         }
       }
       if (row == 0 && g == 0) trace(p, k, kTrEpiStored);

@@ -128,6 +128,27 @@ def test_edge_cases(gpu_lib, case, Lq, D, kernel):
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("D", [64, 128])
+def test_output_16_byte_aligned_only(gpu_lib, D, kernel):
+    """The output may be 16-byte aligned only (the C ABI's requirement): the epilogues then
+    store 16 bytes at a time instead of 32.  Neighbouring bytes stay untouched."""
+    wl = W.custom(n_user=4, counts=[130, 3, 1, 140], lens=[200, 1, 300, 129], H=2, D=D, Lq=2, seed=21)
+    d = to_device(wl)
+    n = d["q"].numel()
+    buf = torch.full((n + 16,), 7.0, dtype=torch.bfloat16, device=d["q"].device)
+    assert buf.data_ptr() % 32 == 0
+    out = buf[8:8 + n].view(d["q"].shape)        # 16 bytes past a 32-byte boundary
+    prev = gpu_lib.set_kernel(kernel)
+    try:
+        gpu_lib.attn_fwd(d["q"], d["k"], d["v"], d["user_offsets"], d["cand_to_user"], wl.scale, out=out)
+        assert gpu_lib.get_device_error() == 0
+    finally:
+        gpu_lib.set_kernel(prev)
+    assert bool((buf[:8] == 7.0).all()) and bool((buf[8 + n:] == 7.0).all())
+    assert_close(out_f64(out), oracle.attention_wl(wl), f"16-byte aligned out D={D} kernel={kernel}")
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("Lq", [5, 64, 128])
 def test_large_query_groups(gpu_lib, Lq, kernel):
     wl = W.custom(n_user=3, counts=[5, 2, 9], lens=[140, 70, 390], H=3, D=128, Lq=Lq, seed=7)
