@@ -488,7 +488,7 @@ def run_ikbo(args):
         "broadcast_path": {"ms_per_step": bc, "value": flops / (bc * 1e-3) / 1e12, "unit": "TFLOP/s",
                            "ikbo_speedup": bc / ms,
                            "extra_bytes": nums["broadcast_extra_bytes"]},
-        "gpu_launches": ikbo.launches_per_call(wl.n_cand, wl.n_user) * args.steps,
+        "gpu_launches": ikbo.launches_per_call(wl.n_cand, wl.n_user) * n_timed,
         "clocks": clocks,
     }
     if rank == 0:

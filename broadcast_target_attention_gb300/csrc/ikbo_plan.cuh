@@ -84,6 +84,8 @@ ikbo_plan_kernel(const __grid_constant__ PlanParams p, const __grid_constant__ P
 
   __shared__ int s_err;
   __shared__ int s_unsorted;
+  // sequence lengths of up to kLptMaxUsers users, for the longest-first order
+  __shared__ int32_t s_len[kLptMaxUsers];
   __shared__ int64_t s_scan[32];
   __shared__ int64_t s_sum_units, s_sum_tiles;
   const int tid = threadIdx.x;
@@ -134,6 +136,12 @@ ikbo_plan_kernel(const __grid_constant__ PlanParams p, const __grid_constant__ P
     return;
   }
   const bool sorted = !s_unsorted;
+  // the sequence lengths, from shared memory in the steps below (up to
+  // kLptMaxUsers users; beyond, from the offsets)
+  const bool len_smem = n_user <= kLptMaxUsers;
+  if (len_smem)
+    for (int64_t u = tid; u < n_user; u += nt) s_len[u] = off[u + 1] - off[u];
+  auto len_of = [&](int64_t u) -> int32_t { return len_smem ? s_len[u] : off[u + 1] - off[u]; };
 
   // 2. group candidates by user ---------------------------------------------
   int32_t* cand_start = p.cand_start;
@@ -190,7 +198,7 @@ ikbo_plan_kernel(const __grid_constant__ PlanParams p, const __grid_constant__ P
     const int64_t row_elems = (int64_t)p.H * x.Lq * x.D;   // bf16 elements per candidate
     for (int64_t c = tid; c < n_cand; c += nt) {
       const int32_t uc = c2u[c];
-      if (off[uc + 1] == off[uc]) {
+      if (len_of(uc) == 0) {
         uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(x.out) + c * row_elems);
         for (int64_t i = 0; i < row_elems / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
       }
@@ -233,10 +241,10 @@ ikbo_plan_kernel(const __grid_constant__ PlanParams p, const __grid_constant__ P
   int32_t* order = p.scratch;
   if (n_user <= kLptMaxUsers) {
     for (int64_t u = tid; u < n_user; u += nt) {
-      const int32_t Lu = off[u + 1] - off[u];
+      const int32_t Lu = s_len[u];
       int64_t rank = 0;
       for (int64_t w = 0; w < n_user; ++w) {
-        const int32_t Lw = off[w + 1] - off[w];
+        const int32_t Lw = s_len[w];
         rank += (Lw > Lu) || (Lw == Lu && w < u);
       }
       order[rank] = (int32_t)u;
@@ -296,49 +304,73 @@ ikbo_plan_kernel(const __grid_constant__ PlanParams p, const __grid_constant__ P
     }
     return;
   }
-  for (int64_t i = tid; i < n_items; i += nt) {
-    // rank of the user owning item i: last rank with items_before[rank] <= i
-    int64_t lo = 0, hi = n_user - 1;
-    while (lo < hi) {
-      const int64_t mid = (lo + hi + 1) >> 1;
-      if (items_before[mid] <= i) lo = mid; else hi = mid - 1;
-    }
-    const int64_t rk = lo;
+  // One warp per user rank: the user's sizes are read once, then its items
+  // (consecutive in the list) are made 32 at a time, lane l the l-th, and
+  // written by the warp as one contiguous run of 8-byte words.  (Item by
+  // item, each thread searching and loading the user's sizes anew and
+  // storing its 40 bytes word by word, this step took ~20 us for 4600 items:
+  // one SM's store unit is the limit for scattered 4-byte stores.)
+  static_assert(sizeof(WorkItem) == 40, "five 8-byte words per item");
+  const int lane = tid & 31, nwarps = nt >> 5;
+  for (int64_t rk = tid >> 5; rk < n_user; rk += nwarps) {
+    const int64_t i0 = items_before[rk], i1 = items_before[rk + 1];
+    if (i1 == i0) continue;
     const int32_t u = order[rk];
     const int64_t r = cand_start[u + 1] - cand_start[u];
     const int64_t L = off[u + 1] - off[u];
     const int64_t nmt = ceil_div64(r, cpt);
     const int64_t kt = ceil_div64(L, bn);
     const int64_t s = split_tiles ? ceil_div64(kt, split_tiles) : 1;
-    const int64_t local = i - items_before[rk];
-    const int64_t split = local % s;
-    const int64_t rest = local / s;
-    const int64_t mt = rest % nmt;
-    const int64_t h = rest / nmt;
-    WorkItem w;
-    w.q_row = -1;
-    w.n_split = (int32_t)s;
-    w.user = u;
-    w.head = (int32_t)h;
-    w.cand_begin = (int32_t)(cand_start[u] + mt * cpt);
-    w.n_cand = (int32_t)min((int64_t)cpt, r - mt * cpt);
-    const int64_t kchunk = s > 1 ? split_tiles * bn : L;
-    w.kv_begin = (int32_t)(off[u] + split * kchunk);
-    w.kv_len = (int32_t)min(kchunk, L - split * kchunk);
-    if (s > 1) {
-      w.unit = (int32_t)(units_before[rk] + rest);
-      w.unit_first = (int32_t)(i - split);
-      if (split == 0) {
-        p.units[w.unit].n_split = (int32_t)s;
-        p.units[w.unit].arrived = 0;
+    for (int64_t ib = i0; ib < i1; ib += 32) {
+      const int cnt = int(i1 - ib < 32 ? i1 - ib : 32);
+      const int64_t i = ib + lane;
+      WorkItem w = {};
+      if (lane < cnt) {
+        const int64_t local = i - i0;
+        const int64_t split = local % s;
+        const int64_t rest = local / s;
+        const int64_t mt = rest % nmt;
+        const int64_t h = rest / nmt;
+        w.q_row = -1;
+        w.n_split = (int32_t)s;
+        w.user = u;
+        w.head = (int32_t)h;
+        w.cand_begin = (int32_t)(cand_start[u] + mt * cpt);
+        w.n_cand = (int32_t)min((int64_t)cpt, r - mt * cpt);
+        const int64_t kchunk = s > 1 ? split_tiles * bn : L;
+        w.kv_begin = (int32_t)(off[u] + split * kchunk);
+        w.kv_len = (int32_t)min(kchunk, L - split * kchunk);
+        if (s > 1) {
+          w.unit = (int32_t)(units_before[rk] + rest);
+          w.unit_first = (int32_t)(i - split);
+          if (split == 0) {
+            p.units[w.unit].n_split = (int32_t)s;
+            p.units[w.unit].arrived = 0;
+          }
+        } else {
+          w.unit = -1;
+          w.unit_first = (int32_t)i;
+        }
       }
-    } else {
-      w.unit = -1;
-      w.unit_first = (int32_t)i;
+      // word j of the run is word j % 5 of lane j / 5's item
+      uint32_t wv[10];
+      memcpy(wv, &w, sizeof w);
+      uint2* dst = reinterpret_cast<uint2*>(p.items + ib);   // 8-byte aligned: 40 * ib bytes in
+#pragma unroll
+      for (int t = 0; t < 5; ++t) {
+        const int j = lane + 32 * t;
+        const int src = j / 5, q = j % 5;
+        uint2 v = make_uint2(0u, 0u);
+#pragma unroll
+        for (int x = 0; x < 5; ++x) {
+          const uint32_t lo = __shfl_sync(0xffffffffu, wv[2 * x], src);
+          const uint32_t hi = __shfl_sync(0xffffffffu, wv[2 * x + 1], src);
+          if (q == x) v = make_uint2(lo, hi);
+        }
+        if (j < 5 * cnt) dst[j] = v;
+      }
     }
-    p.items[i] = w;
   }
-
   // 7. tensor maps and header ------------------------------------------------
   const int32_t T = off[n_user];
   if (x.patch_maps && tid < 2) {
