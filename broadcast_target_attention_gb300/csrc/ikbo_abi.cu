@@ -182,11 +182,26 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Layout of the per-call scratch space.
 struct Workspace {
   size_t header, kmap, vmap, items, units, perm, cand_start, scratch, partial_o, partial_ml,
-      cta_items, map_slots, item_user, ab_o, ab_lse, ab_flags, total;
+      cta_items, map_slots, item_user, ab_o, ab_lse, ab_flags, clc_slots, total;
   int max_items, max_split_items, max_units, max_cta_items, grid, map_stride;
+  int clc_slot_bytes, clc_map_offset;
   int kernel;   // kKernSimt, kKernTc or kKernPp
   bool fused;
+  bool clc;     // two-tile kernel with Cluster Launch Control (grid = a bound on the units)
 };
+
+// Target-only calls on the two-tile kernel with at most this many users run
+// with Cluster Launch Control: one CTA per unit of work (the grid a bound on
+// their number), CTAs that finish early taking over those not yet started;
+// each SM keeps a slot of the plan's user tables and one bounded V map per user.
+constexpr int64_t kClcMaxUsers = 256;
+
+// The grid of the two-tile kernel with Cluster Launch Control: at least one CTA
+// per unit (H x two-tile groups of candidates of every user).
+int64_t pp_units_bound(int64_t n_cand, int64_t n_user, int H, int Lq) {
+  const int64_t pair = 2 * cands_per_tile(Lq);
+  return int64_t(H) * ((n_cand + pair - 1) / pair + (n_user < n_cand ? n_user : n_cand));
+}
 
 bool fits_in_kernel_planning(int64_t n_cand, int64_t n_user) {
   return n_cand <= kFusedMaxCand && n_user <= kFusedMaxUser;
@@ -228,8 +243,10 @@ int effective_kernel(int64_t n_cand, int64_t n_user, int H, int Lq) {
 // multi_level: a user -> vendor -> item call; when the planning kernel plans
 // it, it writes every item's user to item_user first.
 Workspace plan_workspace(int64_t n_cand, int64_t n_user, int H, int Lq, int D, int num_sms,
-                         int grid, int kernel, int64_t extra_units = 0, bool multi_level = false) {
+                         int grid, int kernel, int64_t extra_units = 0, bool multi_level = false,
+                         bool clc = false) {
   Workspace w = {};
+  w.clc = clc;
   const int cpt = cands_per_tile(Lq);
   const int64_t units_bound =
       int64_t(H) * ((n_cand + cpt - 1) / cpt + (n_user < n_cand ? n_user : n_cand)) + extra_units;
@@ -253,6 +270,13 @@ Workspace plan_workspace(int64_t n_cand, int64_t n_user, int H, int Lq, int D, i
   const int64_t listed_per_cta = (int64_t(w.max_items) + grid - 1) / grid;
   w.map_stride = 2 + int(listed_per_cta > w.max_cta_items ? listed_per_cta : w.max_cta_items);
   w.map_slots = take(sizeof(CUtensorMap) * size_t(grid) * size_t(w.map_stride));
+  if (w.fused && w.clc) {
+    // per SM: offsets, first candidates, units before each rank, users by
+    // rank (n_user + 1 ints each), then one bounded V map per user
+    w.clc_map_offset = int(align_up(sizeof(int32_t) * 4 * size_t(n_user + 1), 128));
+    w.clc_slot_bytes = int(w.clc_map_offset + sizeof(CUtensorMap) * size_t(n_user));
+    w.clc_slots = take(size_t(kClcSlots) * size_t(w.clc_slot_bytes));
+  }
   if (w.fused) {
     w.cta_items = take(sizeof(WorkItem) * size_t(grid) * size_t(w.max_cta_items));
     if (kernel == kKernAb) {
@@ -541,6 +565,7 @@ int run_ikbo(DeviceState* ds, const void* q, const void* k, const void* v, const
   ap.qbox = qbox_cands(Lq);
   ap.debug_flags = g_debug_flags;
   ap.trace = g_trace;
+  ap.trace_ctas = ds->num_sms;
   ap.fused = L.fused ? 1 : 0;
   ap.cands_per_tile = pp.cands_per_tile;
   ap.user_offsets = off;
@@ -551,6 +576,12 @@ int run_ikbo(DeviceState* ds, const void* q, const void* k, const void* v, const
   ap.perm_ws = pp.perm;
   ap.map_slots = reinterpret_cast<CUtensorMap*>(ws + L.map_slots);
   ap.map_stride = L.map_stride;
+  if (L.clc) {
+    ap.clc = 1;
+    ap.clc_slots = reinterpret_cast<uint8_t*>(ws + L.clc_slots);
+    ap.clc_slot_bytes = L.clc_slot_bytes;
+    ap.clc_map_offset = L.clc_map_offset;
+  }
   if (kernel == kKernAb) {
     ap.ab_partial_o = reinterpret_cast<float4*>(ws + L.ab_o);
     ap.ab_partial_lse = reinterpret_cast<float*>(ws + L.ab_lse);
@@ -631,8 +662,13 @@ int call_workspace(DeviceState* ds, int64_t n_cand, int64_t n_user, int H, int L
   }
   // a self-attention tile per 128 rows of every user, at most T / 128 + n_user per head
   const int64_t extra = self_T > 0 ? int64_t(H) * ((self_T + kTileM - 1) / kTileM + n_user) : 0;
+  const bool clc = kernel == kKernPp && self_T < 0 && n_user <= kClcMaxUsers;
+  if (clc) {
+    const int64_t ub = pp_units_bound(n_cand, n_user, H, Lq);
+    grid = int(ub > 0 ? ub : 1);
+  }
   *out = plan_workspace(n_cand, n_user, H, Lq, D, ds->num_sms, grid > 0 ? grid : ds->num_sms,
-                        kernel, extra, multi_level);
+                        kernel, extra, multi_level, clc);
   return IKBO_OK;
 }
 

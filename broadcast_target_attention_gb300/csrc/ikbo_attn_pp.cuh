@@ -101,6 +101,13 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
     // both finished reading the two accumulators (one arrival per warp)
     ptx::mbar_init(ptx::smem_addr(&ctl->pair_go), kPpGroups * kPpSoftmaxWarps);
     ptx::mbar_init(ptx::smem_addr(&ctl->pair_recv), kPpGroups * kPpSoftmaxWarps);
+    // Cluster Launch Control: an answer arrived; the producer fills an item
+    // queue slot; the MMA warp and the 8 softmax warps each release it
+    ptx::mbar_init(ptx::smem_addr(&ctl->q.clc_bar), 1);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(ptx::smem_addr(&ctl->q.item_full[i]), 1);
+      ptx::mbar_init(ptx::smem_addr(&ctl->q.item_empty[i]), 1 + kPpGroups * kPpSoftmaxWarps);
+    }
     ctl->abort_flag = 0;
     ctl->flags = 0;
     ptx::fence_mbar_init();
@@ -115,9 +122,14 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
     ptx::prefetch_tensormap(&vmap_tmpl);
     if (kSelf && p.q_user) ptx::prefetch_tensormap(&qumap);
   }
+  // Cluster Launch Control: this SM's slot for the plan's tables and the
+  // users' bounded V maps (one CTA per SM)
+  const uint32_t sm = ptx::smid();
+  const bool clc = !kSelf && p.clc && sm < (uint32_t)kClcSlots;
+  uint8_t* slot = clc ? p.clc_slots + (size_t)sm * p.clc_slot_bytes : nullptr;
   if (p.fused && layout_ok) plan_load(p, data);
   __syncthreads();
-  if (!layout_ok || !p.fused) {
+  if (!layout_ok || !p.fused || (!kSelf && p.clc && !clc)) {
     // this kernel plans in-kernel only; the host never launches it otherwise
     if (threadIdx.x == 0) {
       ctl->mode = kModeSkip;
@@ -126,7 +138,7 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
       atomicOr(p.err_word, kErrLayout);
     }
   } else {
-    plan_in_cta(p, ctl, data, D, kPpGroups);
+    plan_in_cta(p, ctl, data, D, kPpGroups, reinterpret_cast<int32_t*>(slot));
     ptx::fence_proxy_async_smem();
   }
   if (threadIdx.x == 0) ctl->bmaps_ready = 0;   // the planning's scan words are free now
@@ -148,6 +160,31 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
   const Waiter W{&ctl->abort_flag, p.err_word, p.timeout_ns};
   auto item_at = [&](int k) -> WorkItem {
     return k < kCtlItems ? ctl->items[k] : p.cta_items[(size_t)blockIdx.x * p.max_cta_items + k];
+  };
+  // Cluster Launch Control (mode kModeClc): the producer finds the CTA's k-th
+  // unit and puts its item in queue slot k % 2 (ctl->items); the MMA and
+  // softmax warps take it from there and release the slot when they start
+  // item k + 1.  The plan's tables and the bounded V maps are in the SM's
+  // slot.
+  const bool dyn = mode == kModeClc;
+  const int n_user_i = (int)p.n_user;
+  const int32_t* tabs = reinterpret_cast<const int32_t*>(slot);
+  CUtensorMap* user_maps = clc ? reinterpret_cast<CUtensorMap*>(slot + p.clc_map_offset) : nullptr;
+  auto queue_release = [&](int k) {
+    if (dyn && k > 0) ptx::mbar_arrive_warp(ptx::smem_addr(&ctl->q.item_empty[(k - 1) & 1]));
+  };
+  // the k-th item of a role's loop (false: none left, or a wait gave up)
+  auto next_item = [&](int k, WorkItem& w, bool converged) -> bool {
+    if (!dyn) {
+      if (k >= n_my) return false;
+      w = item_at(k);
+      return true;
+    }
+    queue_release(k);
+    const uint32_t bar = ptx::smem_addr(&ctl->q.item_full[k & 1]);
+    if (!(converged ? W.conv_wait(bar, (k >> 1) & 1u) : W.warp_wait(bar, (k >> 1) & 1u))) return false;
+    w = ctl->items[k & 1];
+    return w.user >= 0;
   };
   auto ntiles = [](const WorkItem& w) { return ceil_div(w.kv_len, kBlockN); };
   // candidates of query tile g of an item (tile B holds those past the
@@ -211,11 +248,12 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
       };
       uint32_t kv_it = 0;
       uint32_t qn[kPpGroups] = {0, 0};
-      // A user's partial last V tile goes through the item's copy of the V
-      // map bounded at the user's end row (the TMA fills the other users'
-      // rows with zeros), written by warp 2 after planning.
+      // A user's partial last V tile goes through a copy of the V map bounded
+      // at the user's end row (the TMA fills the other users' rows with
+      // zeros), written by warp 2 after planning: one per item, or with
+      // Cluster Launch Control one per user.
       bool bm_ready = false;
-      int cur_item = 0;
+      int cur_item = 0, cur_user = 0;
       auto v_map_for = [&](int32_t row, int32_t end) -> const void* {
         if (row + kBlockN <= end) return kv_map(true, row);
         if (!bm_ready) {
@@ -224,7 +262,8 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
           if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) return nullptr;
           bm_ready = true;
         }
-        CUtensorMap* m = p.map_slots + (size_t)p.map_stride * blockIdx.x + 2 + cur_item;
+        CUtensorMap* m = dyn ? user_maps + cur_user
+                             : p.map_slots + (size_t)p.map_stride * blockIdx.x + 2 + cur_item;
         ptx::tensormap_acquire(m);
         ptx::prefetch_tensormap(m);
         return m;
@@ -280,15 +319,72 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
         }
         return true;
       };
+      // Cluster Launch Control: the CTA's first unit is its own index; each
+      // next one is the index of a CTA of the grid that has not started,
+      // which the hardware cancels at this CTA's request (asked one unit
+      // ahead, so the answer arrives while the current unit runs).  The grid
+      // is sized by a bound on the units: indices past the plan's count are
+      // taken over too, and skipped, until a request cancels nothing.
+      const int N = ctl->n_units;
+      const uint32_t clc_bar = ptx::smem_addr(&ctl->q.clc_bar), clc_resp = ptx::smem_addr(ctl->q.clc_resp);
+      uint32_t clc_phase = 0;
+      bool clc_pending = false;
+      auto clc_ask = [&]() {
+        if (lane == 0) {
+          ptx::mbar_arrive_expect_tx(clc_bar, 16);
+          ptx::clc_try_cancel(clc_resp, clc_bar);
+        }
+        clc_pending = true;
+      };
+      auto clc_next = [&](int k) -> int {
+        if (k == 0) {
+          if ((int)blockIdx.x >= N) return -1;   // no unit of its own, none after it either
+          clc_ask();
+          return (int)blockIdx.x;
+        }
+        while (clc_pending) {
+          if (!W.conv_wait(clc_bar, clc_phase & 1u)) return -1;   // (still pending: drained below)
+          ++clc_phase;
+          clc_pending = false;
+          uint32_t x = 0;
+          if (!ptx::clc_query(clc_resp, x)) return -1;   // nothing left to take over
+          clc_ask();
+          if ((int)x < N) return (int)x;
+        }
+        return -1;
+      };
       bool ok = true;
-      for (int k = 0; k < n_my && ok; ++k) {
-        const WorkItem w = item_at(k);
+      for (int k = 0; ok; ++k) {
+        WorkItem w;
+        if (dyn) {
+          // the next unit (once queue slot k % 2 is free), as the slot's item
+          if (k >= 2 && !W.conv_wait(ptx::smem_addr(&ctl->q.item_empty[k & 1]), ((k >> 1) - 1) & 1u)) break;
+          const int unit = clc_next(k);
+          if (lane == 0) {
+            WorkItem x;
+            if (unit >= 0) {
+              const int n1 = n_user_i + 1;
+              decode_unit(unit, tabs, tabs + n1, tabs + 2 * n1, tabs + 3 * n1, n_user_i, kPpGroups, cpt,
+                          false, x);
+            } else {
+              x.user = -1;   // no unit left: the roles stop
+            }
+            ctl->items[k & 1] = x;
+            ptx::mbar_arrive(ptx::smem_addr(&ctl->q.item_full[k & 1]));
+          }
+          __syncwarp();
+          w = ctl->items[k & 1];
+          if (w.user < 0) break;
+        } else if (!next_item(k, w, true)) {
+          break;
+        }
+        cur_item = k;
+        cur_user = w.user;
         const int n = ntiles(w);
         const bool has_b = tile_cands(w, 1) > 0;
         if (lane == 0) trace(p, k, kTrProdItem);
         // Q_A and K_0 first: S_A(0) needs only these
         const int32_t end = w.kv_begin + w.kv_len;
-        cur_item = k;
         if (!key_split(w)) {
           ok = load_q(0, w, 0) && ring(false, w.head, w.kv_begin, end) && (!has_b || load_q(1, w, 1));
           for (int j = 0; j < n && ok; ++j) {
@@ -310,7 +406,9 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
         }
         if (lane == 0) trace(p, k, kTrProdIssued);
       }
-      // Drain: every armed barrier phase must complete before the CTA exits.
+      // Drain: every armed barrier phase must complete before the CTA exits
+      // (a cancellation request still out after an abort included).
+      if (lane == 0 && clc_pending) W.drain(clc_bar, clc_phase & 1u);
       if (lane == 0)
       for (uint32_t s = 0; s < (uint32_t)NS && s < kv_it; ++s) {
         const uint32_t uses = (kv_it - s + NS - 1) / NS;
@@ -378,8 +476,9 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
         return true;
       };
       bool ok = true;
-      for (int k = 0; k < n_my && ok; ++k) {
-        const WorkItem w = item_at(k);
+      for (int k = 0; ok; ++k) {
+        WorkItem w;
+        if (!next_item(k, w, true)) break;
         const int n = ntiles(w);
         const bool has_b = tile_cands(w, 1) > 0;
         const bool split = key_split(w);
@@ -480,7 +579,12 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
     __syncwarp();
   } else if ((warp == 2 || warp == 3) && mode != kModeSkip) {
     prefetch_v_late(p, ctl->total_keys, D);
-    if (warp == 2) write_bounded_maps(p, ctl, &vmap_tmpl, n_my, item_at);
+    if (warp == 2) {
+      if (dyn)
+        write_user_maps(ctl, user_maps, &vmap_tmpl, tabs, tabs + n_user_i + 1, n_user_i);
+      else
+        write_bounded_maps(p, ctl, &vmap_tmpl, n_my, item_at);
+    }
   } else if (warp >= kSoftmaxWarp0 && mode != kModeSkip) {
     // ------------------------------------------- softmax / correction / epilogue
     const int g = (warp - kSoftmaxWarp0) / kPpSoftmaxWarps;   // query tile of this warp
@@ -492,8 +596,9 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
     const float sl2 = p.scale_log2;
     uint32_t tn = 0, dn = 0;                                  // S tiles and items of this tile so far
     uint32_t sp = 0;                                          // key-split items so far
-    for (int k = 0; k < n_my; ++k) {
-      const WorkItem w = item_at(k);
+    for (int k = 0;; ++k) {
+      WorkItem w;
+      if (!next_item(k, w, false)) break;
       const bool split = key_split(w);
       const int tg = split ? 0 : g;                           // the query tile whose rows these are
       const int nc = tile_cands(w, tg);

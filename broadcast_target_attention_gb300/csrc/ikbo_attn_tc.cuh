@@ -105,7 +105,9 @@ constexpr int kSortWarps = 8;
 // consecutive users wider than this are filled in a second pass.
 constexpr int kSmallGap = 64;
 
-enum TcMode { kModeSkip = -1, kModeListed = 0, kModeIndep = 1, kModePair = 2 };
+enum TcMode { kModeSkip = -1, kModeListed = 0, kModeIndep = 1, kModePair = 2, kModeClc = 3 };
+// SM slots of the Cluster Launch Control tables (indexed by %smid)
+constexpr int kClcSlots = 256;
 // S/P buffers in tensor memory: the MMA warp computes S two tiles ahead of
 // the softmax, so a tile's scores are ready when the softmax gets to it.
 constexpr int kSBufs = 3;
@@ -164,6 +166,13 @@ struct TcCtrl {
   union {
     alignas(16) float partner_lse[kTileM];   // one-tile kernel, pair mode
     uint64_t s_free[2];                      // key-interleaved kernel: S buffer read by the softmax
+    struct {                                 // two-tile kernel, Cluster Launch Control:
+      alignas(16) uint32_t clc_resp[4];      //   the answer to a cancellation request
+      uint64_t clc_bar;                      //   ... has arrived
+      uint64_t item_full[2];                 //   queue slot k % 2 holds the CTA's k-th item
+      uint64_t item_empty[2];                //   every role is done with it
+      int lpt;                               //   the tables list the users longest first
+    } q;
   };
   int ab_chunk_tiles;                   // key-interleaved kernel: chunk size of split units (0 = none)
   int ab_units;                         // key-interleaved kernel: units (or chunks) in all
@@ -258,7 +267,7 @@ struct Waiter {
 };
 
 __device__ __forceinline__ void trace(const AttnParams& p, int ord, int point) {
-  if (p.trace && ord < kTraceItems)
+  if (p.trace && ord < kTraceItems && (int)blockIdx.x < p.trace_ctas)
     p.trace[(size_t(blockIdx.x) * kTraceItems + ord) * kTracePoints + point] = ptx::globaltimer();
 }
 
@@ -337,6 +346,21 @@ __device__ __forceinline__ void write_bounded_maps(const AttnParams& p, TcCtrl* 
     const WorkItem w = item_at(k);
     if (needs_bounded_map(w)) write_bounded_map(base + k, vtmpl, w.kv_begin + w.kv_len);
   }
+  asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0)
+    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(ptx::smem_addr(&ctl->bmaps_ready)), "r"(1)
+                 : "memory");
+}
+
+// All threads of one warp (Cluster Launch Control): a bounded V map for every
+// user with candidates whose keys end inside a tile, at maps[user], from the
+// CTA's tables (offsets, then first candidates); release them, set
+// ctl->bmaps_ready.
+__device__ __forceinline__ void write_user_maps(TcCtrl* ctl, CUtensorMap* maps, const CUtensorMap* vtmpl,
+                                                const int32_t* off, const int32_t* cs, int n_user) {
+  for (int u = threadIdx.x & 31; u < n_user; u += 32)
+    if (cs[u + 1] > cs[u] && (off[u + 1] - off[u]) % 128 != 0) write_bounded_map(maps + u, vtmpl, off[u + 1]);
   asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
   __syncwarp();
   if ((threadIdx.x & 31) == 0)
@@ -650,8 +674,55 @@ __device__ int plan_group(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch, in
 
 // A unit is (user, head, up to tiles_per_unit query tiles of the user's
 // candidates): 1 for this kernel, 2 for the two-tile kernel.
+// Unit i of the plan as a work item: user rank lo, the last with
+// ubefore[lo] <= i (users by rank: order, or index order when null), then its
+// head and query tile.  The tables are the planning scratch in shared memory,
+// or a CTA's copy in global memory (Cluster Launch Control).
+__device__ __forceinline__ void decode_unit(int i, const int32_t* off, const int32_t* cs,
+                                            const int32_t* ubefore, const int32_t* order, int n_user,
+                                            int tiles_per_unit, int cands_per_tile, bool self_tiles,
+                                            WorkItem& w) {
+  const int cpt = cands_per_tile * tiles_per_unit;   // candidates per unit
+  const int srows = kTileM * tiles_per_unit;         // sequence rows per self-attention unit
+  int lo = 0, hi = n_user - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (ubefore[mid] <= i) lo = mid; else hi = mid - 1;
+  }
+  const int u = order ? order[lo] : lo;
+  const int r = cs[u + 1] - cs[u];
+  const int L = off[u + 1] - off[u];
+  const int nmt = r > 0 ? ceil_div(r, cpt) : 0;
+  const int per_head = nmt + (self_tiles ? ceil_div(L, srows) : 0);
+  const int local = i - ubefore[lo];
+  const int h = local / per_head, mt = local - h * per_head;
+  w.user = u;
+  w.head = h;
+  if (mt < nmt) {
+    w.cand_begin = cs[u] + mt * cpt;
+    w.n_cand = min(cpt, r - mt * cpt);
+    w.q_row = -1;
+  } else {
+    // tiles of the user's own sequence (self-attention): up to srows rows
+    const int t = mt - nmt;
+    w.cand_begin = 0;
+    w.n_cand = min(srows, L - t * srows);
+    w.q_row = off[u] + t * srows;
+  }
+  w.kv_begin = off[u];
+  w.kv_len = L;
+  w.unit = -1;
+  w.unit_first = 0;
+  // two-tile kernel: a user's only query tile may have its keys split over
+  // the two warpgroups
+  w.n_split = (tiles_per_unit == 2 && mt < nmt && r <= cands_per_tile) ? 2 : 1;
+}
+
+// clc_tables (two-tile kernel with Cluster Launch Control): the units are not
+// dealt; the plan's user tables go to this global slot instead, from which the
+// CTA decodes unit blockIdx.x and those of the CTAs it takes over.
 __device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch, int D,
-                            int tiles_per_unit) {
+                            int tiles_per_unit, int32_t* clc_tables = nullptr) {
   const int flags = plan_group(p, ctl, scratch, D);
   if (flags < 0) return;
   const bool unsorted = (flags & kPlanUnsorted) != 0;
@@ -737,40 +808,27 @@ __device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch, 
     prefix();
   }
   trace_pro(p, 6);
+  if (clc_tables) {
+    const int n1 = n_user + 1;
+    for (int j = tid; j < n1; j += nt) {
+      clc_tables[j] = off[j];
+      clc_tables[n1 + j] = cs[j];
+      clc_tables[2 * n1 + j] = ubefore[j];
+      clc_tables[3 * n1 + j] = (lpt && j < n_user) ? order[j] : j;
+    }
+    if (tid == 0) {
+      ctl->mode = kModeClc;
+      ctl->sorted = unsorted ? 0 : 1;
+      ctl->total_keys = off[n_user];
+      ctl->n_my_items = 0;
+      ctl->q.lpt = lpt ? 1 : 0;
+    }
+    return;
+  }
   // decode unit i into a work item
   auto decode = [&](int i, WorkItem& w) {
-    int lo = 0, hi = n_user - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (ubefore[mid] <= i) lo = mid; else hi = mid - 1;
-    }
-    const int u = user_at(lo);
-    const int r = cs[u + 1] - cs[u];
-    const int L = off[u + 1] - off[u];
-    const int nmt = r > 0 ? ceil_div(r, cpt) : 0;
-    const int per_head = nmt + (p.q_user ? ceil_div(L, srows) : 0);
-    const int local = i - ubefore[lo];
-    const int h = local / per_head, mt = local - h * per_head;
-    w.user = u;
-    w.head = h;
-    if (mt < nmt) {
-      w.cand_begin = cs[u] + mt * cpt;
-      w.n_cand = min(cpt, r - mt * cpt);
-      w.q_row = -1;
-    } else {
-      // tiles of the user's own sequence (self-attention): up to srows rows
-      const int t = mt - nmt;
-      w.cand_begin = 0;
-      w.n_cand = min(srows, L - t * srows);
-      w.q_row = off[u] + t * srows;
-    }
-    w.kv_begin = off[u];
-    w.kv_len = off[u + 1] - off[u];
-    w.unit = -1;
-    w.unit_first = 0;
-    // two-tile kernel: a user's only query tile may have its keys split over
-    // the two warpgroups
-    w.n_split = (tiles_per_unit == 2 && mt < nmt && r <= p.cands_per_tile) ? 2 : 1;
+    decode_unit(i, off, cs, ubefore, lpt ? order : nullptr, n_user, tiles_per_unit, p.cands_per_tile,
+                p.q_user != nullptr, w);
   };
   WorkItem* mine = p.cta_items + (size_t)b * p.max_cta_items;
   if (pair) {

@@ -110,7 +110,8 @@ struct AttnParams {
   uint64_t timeout_ns;      // bound of every wait on another warp or the TMA/MMA units
   int32_t qbox;             // candidates per Q box of the sorted-order tensor map
   int32_t debug_flags;      // test hook: 1 = never arm the Q barrier (exercises the timeout path)
-  uint64_t* trace;          // optional %globaltimer stamps [grid][kTraceItems][kTracePoints], or null
+  uint64_t* trace;          // optional %globaltimer stamps [trace_ctas][kTraceItems][kTracePoints], or null
+  int32_t trace_ctas;       // CTAs the trace buffer has room for (the SMs): CTAs past them are not traced
   // in-kernel planning (tcgen05 kernel, "fused" mode)
   int32_t fused;            // 1: every CTA plans from the index tensors itself; 0: read `items`
   int32_t cands_per_tile;
@@ -138,6 +139,15 @@ struct AttnParams {
   float* ab_partial_lse;    // [grid][128] log-sum-exp (base 2) of every chunk's rows
   unsigned long long* ab_flags;   // [grid] a chunk's partial is complete: ab_marker
   unsigned long long ab_marker;   // non-zero, unique to the call
+  // two-tile kernel with Cluster Launch Control (clc = 1): one CTA per unit of
+  // work; a running CTA takes over CTAs that have not started.  Per SM a slot
+  // of clc_slot_bytes: the plan's user tables (offsets, first candidates,
+  // units before each rank, users by rank; n_user + 1 ints each), then from
+  // clc_map_offset one bounded V map per user.
+  int32_t clc;
+  int32_t clc_slot_bytes;
+  int32_t clc_map_offset;
+  uint8_t* clc_slots;
 };
 
 // In-kernel timeline tracing (ikbo_set_trace): the first kTraceItems items of

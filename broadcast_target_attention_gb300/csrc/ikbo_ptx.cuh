@@ -259,6 +259,37 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
                : "memory");
 }
 
+// ---- Cluster Launch Control ---------------------------------------------------
+// Ask the hardware to cancel a CTA of this grid that has not started yet; the
+// 16-byte answer lands in shared memory at `resp` (16-byte aligned) and
+// completes 16 bytes on `bar` (armed with expect_tx 16 by the caller).  After
+// an answer that cancelled nothing, no further request may be made.
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
+  asm volatile("clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];"
+               ::"r"(resp), "r"(bar)
+               : "memory");
+}
+// The answer at `resp`: true and the cancelled CTA's x index, or false.
+__device__ __forceinline__ bool clc_query(uint32_t resp, uint32_t& ctaid_x) {
+  uint32_t ok, x;
+  asm volatile(
+      "{\n\t.reg .b128 h;\n\t.reg .pred p;\n\t"
+      "ld.shared.b128 h, [%2];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, h;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t"
+      "clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, h;\n\t}"
+      : "=r"(ok), "=r"(x)
+      : "r"(resp)
+      : "memory");
+  ctaid_x = x;
+  return ok != 0;
+}
+__device__ __forceinline__ uint32_t smid() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+  return r;
+}
+
 // ---- CTA pairs (cta_group::2): one MMA of M = 256 rows over the tensor cores
 // of two CTAs of a cluster (ranks 2i and 2i + 1).  Every tcgen05 instruction of
 // a kernel that uses them takes the same cta_group.

@@ -208,9 +208,11 @@ int ikbo_pool_usage(int reset, uint64_t* used_now, uint64_t* used_high);
  * of at least (number of SMs) x 4 x 16 uint64 entries, later calls of the
  * tcgen05 kernel write %globaltimer stamps (ns) into it: entry
  * [(cta * 4 + item) * 16 + point] for the first 4 work items of every CTA,
- * at the points listed in csrc/ikbo_common.cuh (TracePoint).  Entries that
- * are not reached keep their old contents.  NULL switches tracing off (the
- * default).  The caller owns the buffer.
+ * at the points listed in csrc/ikbo_common.cuh (TracePoint), for CTAs with
+ * an index below the number of SMs (the two-tile kernel with Cluster Launch
+ * Control has more CTAs; the others are not traced).  Entries that are not
+ * reached keep their old contents.  NULL switches tracing off (the default).
+ * The caller owns the buffer.
  */
 int ikbo_set_trace(uint64_t* device_buffer);
 
@@ -354,8 +356,10 @@ int ikbo_ml_attn_fwd(const void* q, const void* k_user, const void* v_user,
  *      a unit over the two CTAs of a cluster when units are few;
  *   3  the tcgen05 kernel with two query tiles of the same user and head per
  *      work item, sharing each K/V tile between them (ping-pong of two
- *      softmax warpgroups); inputs beyond the in-kernel planning limits run
- *      on kernel 2;
+ *      softmax warpgroups); with at most 256 users its grid is one CTA per
+ *      item (a bound on their number) and running CTAs take over the items
+ *      of CTAs not yet started (Cluster Launch Control), longest first;
+ *      inputs beyond the in-kernel planning limits run on kernel 2;
  *   4  the tcgen05 kernel with the key tiles of one query tile dealt to two
  *      softmax warpgroups in turn (even and odd tiles) and merged in the
  *      CTA, one unit per CTA when units are few; a unit far longer than the
