@@ -138,14 +138,14 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
       atomicOr(p.err_word, kErrLayout);
     }
   } else {
-    plan_in_cta(p, ctl, data, D, kPpGroups, reinterpret_cast<int32_t*>(slot));
+    plan_in_cta<!kSelf>(p, ctl, data, D, kPpGroups, reinterpret_cast<int32_t*>(slot));
     ptx::fence_proxy_async_smem();
   }
   if (threadIdx.x == 0) ctl->bmaps_ready = 0;   // the planning's scan words are free now
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
-  if (threadIdx.x == 0) trace(p, 0, kTrCtaStart);
+  if (threadIdx.x == 0) trace_bounded(p, 0, kTrCtaStart);
 
   const uint32_t tmem = ctl->tmem_base;
   const int mode = ctl->mode;
@@ -382,7 +382,7 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
         cur_user = w.user;
         const int n = ntiles(w);
         const bool has_b = tile_cands(w, 1) > 0;
-        if (lane == 0) trace(p, k, kTrProdItem);
+        if (lane == 0) trace_bounded(p, k, kTrProdItem);
         // Q_A and K_0 first: S_A(0) needs only these
         const int32_t end = w.kv_begin + w.kv_len;
         if (!key_split(w)) {
@@ -404,7 +404,7 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
             if (ok && t + 3 < n) ok = ring(false, w.head, row_of(t + 3), end);
           }
         }
-        if (lane == 0) trace(p, k, kTrProdIssued);
+        if (lane == 0) trace_bounded(p, k, kTrProdIssued);
       }
       // Drain: every armed barrier phase must complete before the CTA exits
       // (a cancellation request still out after an abort included).
@@ -485,7 +485,7 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
         if (!W.conv_wait(ptx::smem_addr(&ctl->q_full[0]), qn[0] & 1u)) break;
         if ((has_b || split) && !W.conv_wait(ptx::smem_addr(&ctl->q_full[1]), qn[1] & 1u)) break;
         ptx::tc_fence_after();
-        if (lane == 0) trace(p, k, kTrMmaQ);
+        if (lane == 0) trace_bounded(p, k, kTrMmaQ);
         if (split) {
           // A on key tiles 0, 2, 4, ..., B on 1, 3, 5, ...: per pair of key
           // tiles PV_A, S_A(next), PV_B, S_B(next), the ring consumed in order
@@ -509,7 +509,7 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
             return true;
           };
           ok = s_at(0, na == 1) && s_at(1, nb == 1);
-          if (ok && lane == 0) trace(p, k, kTrMmaFirstS);
+          if (ok && lane == 0) trace_bounded(p, k, kTrMmaFirstS);
           for (int j = 0; j < na && ok; ++j) {
             ok = pv_at(0, j > 0, j + 1 == na);
             if (ok && j + 1 < na) ok = s_at(0, j + 2 == na);
@@ -517,7 +517,7 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
             if (ok && j + 1 < nb) ok = s_at(1, j + 2 == nb);
           }
           if (!ok) break;
-          if (lane == 0) trace(p, k, kTrMmaLastPV);
+          if (lane == 0) trace_bounded(p, k, kTrMmaLastPV);
           kv_base = ri;
           ++qn[0];
           ++qn[1];
@@ -534,7 +534,7 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
           }
           ptx::mma_commit_warp(ptx::smem_addr(&ctl->kv_empty[ks]));
         }
-        if (lane == 0) trace(p, k, kTrMmaFirstS);
+        if (lane == 0) trace_bounded(p, k, kTrMmaFirstS);
         for (int j = 0; j < n; ++j) {
           const uint32_t vi = kv_base + 2 * j + 1, ki = vi + 1;
           const bool more = j + 1 < n;
@@ -567,7 +567,7 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
             ptx::mma_commit_warp(ptx::smem_addr(&ctl->kv_empty[ki % NS]));
           }
         }
-        if (lane == 0) trace(p, k, kTrMmaLastPV);
+        if (lane == 0) trace_bounded(p, k, kTrMmaLastPV);
         kv_base += 2 * n;
         ++qn[0];
         if (has_b) ++qn[1];
@@ -704,7 +704,7 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
       if (!W.warp_wait(ptx::smem_addr(&ctl->pv_done[g]), dn & 1u)) break;
       ++dn;
       ptx::tc_fence_after();
-      if (row == 0 && g == 0) trace(p, k, kTrEpiO);
+      if (row == 0 && g == 0) trace_bounded(p, k, kTrEpiO);
       uint16_t* dst;
       if (kSelf && w.q_row >= 0) {
         // a self-attention row: out_user[q_row + 128 tg + row, head, :]
@@ -751,7 +751,7 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
             store_bf16x32(dst + col, w);
           }
         }
-        if (row == 0 && g == 0) trace(p, k, kTrEpiStored);
+        if (row == 0 && g == 0) trace_bounded(p, k, kTrEpiStored);
         // both warpgroups are done with both accumulators (and with the row
         // statistics) before either hands over the next item's first P
         ptx::tc_fence_before();
@@ -778,7 +778,7 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
           store_bf16x32(dst + c * 32, w);
         }
       }
-      if (row == 0 && g == 0) trace(p, k, kTrEpiStored);
+      if (row == 0 && g == 0) trace_bounded(p, k, kTrEpiStored);
       // the next item's PV_g(0) overwrites O_g: it waits for that item's
       // first P of this tile, which these warps hand over only after the
       // reads above
@@ -788,7 +788,7 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
 
   ptx::tc_fence_before();
   __syncthreads();
-  if (threadIdx.x == 0) trace(p, 0, kTrCtaEnd);
+  if (threadIdx.x == 0) trace_bounded(p, 0, kTrCtaEnd);
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, C::kTmemCols);

@@ -267,8 +267,16 @@ struct Waiter {
 };
 
 __device__ __forceinline__ void trace(const AttnParams& p, int ord, int point) {
-  if (p.trace && ord < kTraceItems && (int)blockIdx.x < p.trace_ctas)
+  if (p.trace && ord < kTraceItems)
     p.trace[(size_t(blockIdx.x) * kTraceItems + ord) * kTracePoints + point] = ptx::globaltimer();
+}
+
+// The same for a kernel whose grid may exceed the buffer's CTAs (the two-tile
+// kernel with Cluster Launch Control).  (A separate function: the extra test in
+// every call site of trace() cost the one-tile kernel ~1 us of its ~22 us
+// launches, which instruction fetch bounds.)
+__device__ __forceinline__ void trace_bounded(const AttnParams& p, int ord, int point) {
+  if ((int)blockIdx.x < p.trace_ctas) trace(p, ord, point);
 }
 
 // Prologue timeline (debug_flags bit 4): item slot 3, points 0..10.
@@ -718,9 +726,12 @@ __device__ __forceinline__ void decode_unit(int i, const int32_t* off, const int
   w.n_split = (tiles_per_unit == 2 && mt < nmt && r <= cands_per_tile) ? 2 : 1;
 }
 
-// clc_tables (two-tile kernel with Cluster Launch Control): the units are not
-// dealt; the plan's user tables go to this global slot instead, from which the
-// CTA decodes unit blockIdx.x and those of the CTAs it takes over.
+// kClc (two-tile kernel with Cluster Launch Control, clc_tables non-null):
+// the units are not dealt; the plan's user tables go to this global slot
+// instead, from which the CTA decodes unit blockIdx.x and those of the CTAs it
+// takes over.  (A template parameter, so that the one-tile kernel, whose
+// short launches are bound by instruction fetch, carries none of that code.)
+template <bool kClc = false>
 __device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch, int D,
                             int tiles_per_unit, int32_t* clc_tables = nullptr) {
   const int flags = plan_group(p, ctl, scratch, D);
@@ -808,7 +819,7 @@ __device__ void plan_in_cta(const AttnParams& p, TcCtrl* ctl, uint8_t* scratch, 
     prefix();
   }
   trace_pro(p, 6);
-  if (clc_tables) {
+  if (kClc && clc_tables) {
     const int n1 = n_user + 1;
     for (int j = tid; j < n1; j += nt) {
       clc_tables[j] = off[j];
