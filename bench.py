@@ -398,8 +398,11 @@ def run_ikbo(args):
         barrier()
         clk.mark_end()
         step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-        # 1b. the same steps with no flush between them (inputs L2-resident), for reference
+        # 1b. the same steps with no flush between them (inputs L2-resident), for reference.
+        # A GPU-side pause (touching no memory) before each keeps the host's enqueue ahead
+        # of the GPU, so that no step's events take in the host's launch time.
         for i in range(min(args.steps, 200)):
+            torch.cuda._sleep(100_000)
             starts[i].record()
             step()
             ends[i].record()
