@@ -448,7 +448,7 @@ def run_ikbo(args):
     pk = peaks()
     attn = statistics.mean(attn_ms)
     achieved_gbs = alg_bytes / (attn * 1e-3) / 1e9
-    kname = f"{ikbo.KERNEL_NAMES[ikbo.selected_kernel(wl.n_cand, wl.n_user, c.H, c.Lq)]}<{c.D}>"
+    kname = f"{ikbo.KERNEL_NAMES[ikbo.selected_kernel(wl.n_cand, wl.n_user, c.H, c.Lq, c.D)]}<{c.D}>"
     traffic = kernel_traffic(kname, c.name)
     ai = flops / alg_bytes
     ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
@@ -594,9 +594,8 @@ def run_fused(args):
     pk = peaks()
     ai = flops / alg_bytes
     ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
-    # the SIMT choice runs fused calls on the one-tile kernel
-    choice = ikbo.selected_kernel(wl.n_cand, wl.n_user, c.H, c.Lq)
-    kname = f"{ikbo.KERNEL_NAMES[ikbo.KERNEL_TC if choice == ikbo.KERNEL_SIMT else choice]}<{c.D}>"
+    choice = ikbo.selected_kernel(wl.n_cand, wl.n_user, c.H, c.Lq, c.D, int(wl.user_offsets[-1]))
+    kname = f"{ikbo.KERNEL_NAMES[choice]}<{c.D}>"
     if choice == ikbo.KERNEL_TC2:
         kname = kname[:-1] + ", true>"          # the fused instantiation of the two-tile kernel
     traffic = kernel_traffic(kname, c.name)
@@ -866,7 +865,7 @@ def run_ml(args):
     assert ikbo.get_device_error() == 0
     ms = statistics.mean(ms_list)
     kms = statistics.mean(kern)
-    kname = f"{ikbo.KERNEL_NAMES[ikbo.selected_kernel(wl.n_cand, wl.n_user, c.H, c.Lq)]}<{c.D}>"
+    kname = f"{ikbo.KERNEL_NAMES[ikbo.selected_kernel(wl.n_cand, wl.n_user, c.H, c.Lq, c.D)]}<{c.D}>"
     h2d = sum(x.nbytes for x in (wl.q, wl.k, wl.v, wl.user_offsets, m.item_to_vendor, m.vendor_to_user))
     e2e = statistics.mean(e2e_ms)
     line = {
@@ -1022,7 +1021,7 @@ def run_ratio_sweep(args):
         assert ikbo.get_device_error() == 0
         ms = statistics.mean(_timed(ikbo_step, args.steps, flush, dev))
         bc = statistics.mean(_timed(bc_step, min(args.steps, 10), flush, dev))
-        kname = f"{ikbo.KERNEL_NAMES[ikbo.selected_kernel(n_cand, n_user, 4, 1)]}<128>"
+        kname = f"{ikbo.KERNEL_NAMES[ikbo.selected_kernel(n_cand, n_user, 4, 1, 128)]}<128>"
         line = {
             "metric": METRIC + " -- candidate-to-user ratio sweep",
             "value": nums["flops"] / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "n_gpus": 1,

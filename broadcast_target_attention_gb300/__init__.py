@@ -322,9 +322,11 @@ def set_kernel(which: int) -> int:
     return int(_lib.lib().ikbo_set_kernel(int(which)))
 
 
-def selected_kernel(n_cand: int, n_user: int, H: int, Lq: int) -> int:
-    """The kernel (1 to 4) a call of these sizes runs with this thread's choice."""
-    n = int(_lib.lib().ikbo_selected_kernel(int(n_cand), int(n_user), int(H), int(Lq)))
+def selected_kernel(n_cand: int, n_user: int, H: int, Lq: int, D: int, self_rows: int = -1) -> int:
+    """The kernel (1 to 4) that attn_fwd (self_rows < 0) or fused_attn_fwd over self_rows
+    sequence rows runs with these sizes and this thread's choice."""
+    n = int(_lib.lib().ikbo_selected_kernel(int(n_cand), int(n_user), int(H), int(Lq), int(D),
+                                            int(self_rows)))
     _check(min(n, 0), "selected_kernel")
     return n
 

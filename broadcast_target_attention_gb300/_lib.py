@@ -39,7 +39,7 @@ SIGNATURES = {
     "ikbo_set_trace": (ctypes.c_int, [_P]),
     "ikbo_pool_usage": (ctypes.c_int, [ctypes.c_int, _P, _P]),
     "ikbo_launches_per_call": (ctypes.c_int, [_I64, _I64]),
-    "ikbo_selected_kernel": (ctypes.c_int, [_I64, _I64, ctypes.c_int32, ctypes.c_int32]),
+    "ikbo_selected_kernel": (ctypes.c_int, [_I64, _I64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _I64]),
     "ikbo_fused_attn_fwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _I32,
                                             _I32, _F, _P, _P, _P]),
     "ikbo_ml_attn_fwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _I32, _I32,

@@ -211,15 +211,20 @@ bool fits_in_kernel_planning(int64_t n_cand, int64_t n_user) {
 // average at least two query tiles each and the batch makes at least this
 // many two-tile items (about four per SM of a GB300).  Measured on one GB300
 // it is 3-19 % faster than the one-tile kernel on such batches (2 to 64
-// tiles per user, 1024 to 4096 items), and 12 % slower on a batch of ~260
-// items of very unequal cost (Zipf-distributed candidates, 64 to 4096 keys),
-// which it cannot spread evenly over the SMs.
+// tiles per user, 1024 to 4096 items).
 constexpr int64_t kPpMinItems = 600;
+// ... or at least this many where it deals by Cluster Launch Control and asks
+// for each next unit only once the current one's loads are issued (target
+// attention alone, at most kClcMaxUsers users, D = 128): there it is 6 %
+// faster than the one-tile kernel on ~260 items of very unequal cost
+// (Zipf-distributed candidates, 64 to 4096 keys); the two are even on 160
+// items of one user.
+constexpr int64_t kPpMinItemsClc = 200;
 
-// The kernel a call runs with the thread's choice.  The two-tile and the
-// key-interleaved kernels plan in-kernel only, so inputs beyond those limits
-// take the one-tile kernel.
-int effective_kernel(int64_t n_cand, int64_t n_user, int H, int Lq) {
+// The kernel the thread's choice gives.  The two-tile and the key-interleaved
+// kernels plan in-kernel only, so inputs beyond those limits take the
+// one-tile kernel.  target_only: not a fused self + target call.
+int kernel_choice(int64_t n_cand, int64_t n_user, int H, int Lq, int D, bool target_only) {
   if (t_kernel == kKernSimt) return kKernSimt;
   if (t_kernel == kKernTc || !fits_in_kernel_planning(n_cand, n_user)) return kKernTc;
   if (t_kernel == kKernPp) return kKernPp;
@@ -231,7 +236,15 @@ int effective_kernel(int64_t n_cand, int64_t n_user, int H, int Lq) {
   const int64_t pair = 2 * cpt;        // candidates of a two-tile item
   const bool two_tiles = n_cand >= pair * n_user;
   const int64_t items = int64_t(H) * ((n_cand + pair - 1) / pair);
-  return (two_tiles && items >= kPpMinItems) ? kKernPp : kKernTc;
+  const bool late_clc = target_only && D == 128 && n_user <= kClcMaxUsers;
+  return (two_tiles && items >= (late_clc ? kPpMinItemsClc : kPpMinItems)) ? kKernPp : kKernTc;
+}
+
+// The kernel a call runs.  self_T >= 0: a fused self + target call, which
+// runs on the one- or two-tile kernel.
+int effective_kernel(int64_t n_cand, int64_t n_user, int H, int Lq, int D, int64_t self_T) {
+  const int k = kernel_choice(n_cand, n_user, H, Lq, D, self_T < 0);
+  return (self_T >= 0 && (k == kKernSimt || k == kKernAb)) ? kKernTc : k;
 }
 
 // kernel: kKernTc (plans in-kernel when the inputs fit its shared memory,
@@ -647,9 +660,7 @@ int run_ikbo(DeviceState* ds, const void* q, const void* k, const void* v, const
 int call_workspace(DeviceState* ds, int64_t n_cand, int64_t n_user, int H, int Lq, int D,
                    Workspace* out, int64_t self_T = -1, bool multi_level = false) {
   int grid = 0;
-  int kernel = effective_kernel(n_cand, n_user, H, Lq);
-  // fused self + target calls run on the one- or two-tile kernel
-  if (self_T >= 0 && (kernel == kKernSimt || kernel == kKernAb)) kernel = kKernTc;
+  const int kernel = effective_kernel(n_cand, n_user, H, Lq, D, self_T);
   if (kernel == kKernAb) {
     grid = D == 64 ? ab_grid<64>(ds) : ab_grid<128>(ds);
     if (grid <= 0) return IKBO_ERR_CUDA;
@@ -1466,9 +1477,11 @@ int ikbo_set_kernel(int which) {
   return prev;
 }
 
-int ikbo_selected_kernel(int64_t n_cand, int64_t n_user, int32_t H, int32_t Lq) {
-  if (n_cand < 0 || n_user < 0 || H < 1 || Lq < 1 || Lq > kTileM) return IKBO_ERR_SHAPE;
-  return effective_kernel(n_cand, n_user, H, Lq);
+int ikbo_selected_kernel(int64_t n_cand, int64_t n_user, int32_t H, int32_t Lq, int32_t D,
+                         int64_t self_rows) {
+  if (n_cand < 0 || n_user < 0 || H < 1 || Lq < 1 || Lq > kTileM || (D != 64 && D != 128))
+    return IKBO_ERR_SHAPE;
+  return effective_kernel(n_cand, n_user, H, Lq, D, self_rows < 0 ? -1 : self_rows);
 }
 
 int ikbo_launches_per_call(int64_t n_cand, int64_t n_user) {

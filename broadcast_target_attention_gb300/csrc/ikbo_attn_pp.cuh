@@ -321,10 +321,19 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
       };
       // Cluster Launch Control: the CTA's first unit is its own index; each
       // next one is the index of a CTA of the grid that has not started,
-      // which the hardware cancels at this CTA's request (asked one unit
-      // ahead, so the answer arrives while the current unit runs).  The grid
-      // is sized by a bound on the units: indices past the plan's count are
-      // taken over too, and skipped, until a request cancels nothing.
+      // which the hardware cancels at this CTA's request.  At D = 128 the
+      // request goes out once the current unit's loads are all issued: its
+      // answer still arrives while the unit's last key tiles are computed,
+      // and the unit taken is the next in the list when this CTA is nearly
+      // free.  (Asked at the start of the current unit, the CTAs that
+      // started the longest units took the next-longest at once: on
+      // odd_groups_2048x16 the busiest CTA ran 30 % above the mean.)  At
+      // D = 64, whose units are short, the late request made every unit
+      // slower (2 % on the sweeps), so there it goes out as the unit starts.
+      // The grid is sized by a bound on the units: indices past the plan's
+      // count are taken over too, and skipped, until a request cancels
+      // nothing.
+      constexpr bool kLateAsk = D == 128;
       const int N = ctl->n_units;
       const uint32_t clc_bar = ptx::smem_addr(&ctl->q.clc_bar), clc_resp = ptx::smem_addr(ctl->q.clc_resp);
       uint32_t clc_phase = 0;
@@ -339,7 +348,7 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
       auto clc_next = [&](int k) -> int {
         if (k == 0) {
           if ((int)blockIdx.x >= N) return -1;   // no unit of its own, none after it either
-          clc_ask();
+          if (!kLateAsk) clc_ask();
           return (int)blockIdx.x;
         }
         while (clc_pending) {
@@ -348,7 +357,7 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
           clc_pending = false;
           uint32_t x = 0;
           if (!ptx::clc_query(clc_resp, x)) return -1;   // nothing left to take over
-          clc_ask();
+          if (!kLateAsk || (int)x >= N) clc_ask();
           if ((int)x < N) return (int)x;
         }
         return -1;
@@ -405,6 +414,7 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
           }
         }
         if (lane == 0) trace_bounded(p, k, kTrProdIssued);
+        if (kLateAsk && dyn && ok) clc_ask();   // the next unit
       }
       // Drain: every armed barrier phase must complete before the CTA exits
       // (a cancellation request still out after an abort included).

@@ -348,8 +348,11 @@ int ikbo_ml_attn_fwd(const void* q, const void* k_user, const void* v_user,
  *   0  automatic (the default): 3 when the users have on average at least
  *      two query tiles each (n_cand >= 2 * c * n_user, c = floor(128 / Lq)),
  *      the batch makes at least 600 two-tile items
- *      (H * ceil(n_cand / (2 * c)) >= 600) and the inputs fit the in-kernel
- *      planning limits (n_cand <= 20480, n_user <= 1024); else 2;
+ *      (H * ceil(n_cand / (2 * c)) >= 600), or at least 200 for target
+ *      attention alone with D = 128 and at most 256 users (the case that
+ *      kernel 3 deals by Cluster Launch Control, each next item asked for
+ *      late), and the inputs fit the in-kernel planning limits
+ *      (n_cand <= 20480, n_user <= 1024); else 2;
  *   1  the SIMT kernel, kept as an independent GPU cross-check;
  *   2  the tcgen05/TMEM/TMA kernel with one query tile (up to 128 rows of one
  *      user's candidates) per work item, whose pair mode splits the keys of
@@ -373,11 +376,15 @@ int ikbo_ml_attn_fwd(const void* q, const void* k_user, const void* v_user,
 int ikbo_set_kernel(int which);
 
 /*
- * The kernel (1 to 4 as above) that a call with these sizes would run
- * with this thread's current choice.  Host arithmetic only: it touches no
- * GPU.  Negative sizes, H < 1, or Lq outside [1, 128] return IKBO_ERR_SHAPE.
+ * The kernel (1 to 4 as above) that a call with these sizes would run with
+ * this thread's current choice: ikbo_attn_fwd when self_rows < 0, else
+ * ikbo_fused_attn_fwd over self_rows sequence rows (a fused call runs on
+ * kernel 2 or 3).  Host arithmetic only: it touches no GPU.  Negative sizes,
+ * H < 1, Lq outside [1, 128] or D other than 64 and 128 return
+ * IKBO_ERR_SHAPE.
  */
-int ikbo_selected_kernel(int64_t n_cand, int64_t n_user, int32_t H, int32_t Lq);
+int ikbo_selected_kernel(int64_t n_cand, int64_t n_user, int32_t H, int32_t Lq, int32_t D,
+                         int64_t self_rows);
 
 /*
  * Number of kernel launches that ikbo_attn_fwd (and ikbo_attn_fwd_host,

@@ -102,28 +102,40 @@ def test_python_binding_raises_on_bad_status(lib):
 
 def test_selected_kernel(lib):
     """Automatic choice: two query tiles per item when the users have on average at least
-    two query tiles each, the batch makes at least 600 two-tile items and the inputs fit the
-    in-kernel planning limits; the key-interleaved kernel (4) only when chosen."""
+    two query tiles each, the batch makes at least 600 two-tile items (200 for target
+    attention alone at D = 128 with at most 256 users) and the inputs fit the in-kernel
+    planning limits; the key-interleaved kernel (4) only when chosen; a fused call on the
+    one- or two-tile kernel."""
     sel = lib.ikbo_selected_kernel
-    assert sel(1024, 15, 4, 1) == 2         # 1024 candidates / 15 users, Lq 1: < 1 tile per user
-    assert sel(8, 2, 2, 1) == 2
-    assert sel(2048, 16, 8, 4) == 2         # 4 tiles per user, but only 256 items
-    assert sel(4096, 4, 8, 8) == 3          # 64 tiles per user, 1024 items
-    assert sel(16384, 64, 16, 1) == 3       # exactly two tiles per user, 1024 items
-    assert sel(16383, 64, 16, 1) == 2
-    assert sel(16384, 64, 16, 4) == 3
-    assert sel(16384, 64, 2, 1) == 2        # 128 items
-    assert sel(20481, 4, 8, 8) == 2         # beyond the in-kernel planning limits
-    assert sel(4096, 1025, 8, 1) == 2
-    assert sel(-1, 2, 1, 1) == _lib.IKBO_ERR_SHAPE
-    assert sel(8, 2, 0, 1) == _lib.IKBO_ERR_SHAPE
-    assert sel(8, 2, 1, 0) == _lib.IKBO_ERR_SHAPE
-    assert sel(8, 2, 1, 129) == _lib.IKBO_ERR_SHAPE
-    for which, expect in ((1, 1), (2, 2), (3, 3), (4, 4), (7, 2)):
+    assert sel(1024, 15, 4, 1, 128, -1) == 2      # 1024 candidates / 15 users, Lq 1: < 1 tile per user
+    assert sel(8, 2, 2, 1, 64, -1) == 2
+    assert sel(2048, 16, 8, 4, 128, -1) == 3      # 4 tiles per user, 256 items, D 128
+    assert sel(2048, 16, 8, 4, 64, -1) == 2       # the same at D 64
+    assert sel(2048, 16, 8, 4, 128, 34855) == 2   # the same, fused with self-attention
+    assert sel(1600, 16, 8, 4, 128, -1) == 3      # exactly 200 items
+    assert sel(1000, 16, 16, 4, 128, -1) == 2     # 256 items, fewer than two tiles per user
+    assert sel(8192, 256, 1, 8, 128, -1) == 3     # 256 items of 256 users
+    assert sel(8224, 257, 1, 8, 128, -1) == 2     # 257 items of 257 users
+    assert sel(6336, 99, 1, 8, 128, -1) == 2      # 198 items
+    assert sel(4096, 4, 8, 8, 128, -1) == 3       # 64 tiles per user, 1024 items
+    assert sel(4096, 4, 8, 8, 64, 20000) == 3     # ... fused too
+    assert sel(16384, 64, 16, 1, 64, -1) == 3     # exactly two tiles per user, 1024 items
+    assert sel(16383, 64, 16, 1, 64, -1) == 2
+    assert sel(16384, 64, 16, 4, 128, -1) == 3
+    assert sel(16384, 64, 2, 1, 128, -1) == 2     # 128 items
+    assert sel(20481, 4, 8, 8, 128, -1) == 2      # beyond the in-kernel planning limits
+    assert sel(4096, 1025, 8, 1, 128, -1) == 2
+    assert sel(-1, 2, 1, 1, 64, -1) == _lib.IKBO_ERR_SHAPE
+    assert sel(8, 2, 0, 1, 64, -1) == _lib.IKBO_ERR_SHAPE
+    assert sel(8, 2, 1, 0, 64, -1) == _lib.IKBO_ERR_SHAPE
+    assert sel(8, 2, 1, 129, 64, -1) == _lib.IKBO_ERR_SHAPE
+    assert sel(8, 2, 1, 1, 96, -1) == _lib.IKBO_ERR_SHAPE
+    for which, expect, fused in ((1, 1, 2), (2, 2, 2), (3, 3, 3), (4, 4, 2), (7, 2, 2)):
         prev = lib.ikbo_set_kernel(which)
         try:
-            assert sel(1024, 15, 4, 1) == expect
-            assert sel(20481, 4, 8, 8) == (1 if which == 1 else 2)   # two tiles: in-kernel planning only
+            assert sel(1024, 15, 4, 1, 128, -1) == expect
+            assert sel(1024, 15, 4, 1, 128, 9000) == fused
+            assert sel(20481, 4, 8, 8, 128, -1) == (1 if which == 1 else 2)   # two tiles: in-kernel planning only
             assert lib.ikbo_launches_per_call(1024, 15) == (2 if which == 1 else 1)
         finally:
             lib.ikbo_set_kernel(prev)
