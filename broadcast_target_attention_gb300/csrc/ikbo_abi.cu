@@ -591,6 +591,9 @@ int run_ikbo(DeviceState* ds, const void* q, const void* k, const void* v, const
   ap.map_stride = L.map_stride;
   if (L.clc) {
     ap.clc = 1;
+    // the prologue stamps (flag 4) of every CTA are not bounded by the trace
+    // buffer's CTAs, and this grid has more CTAs than SMs
+    ap.debug_flags &= ~4;
     ap.clc_slots = reinterpret_cast<uint8_t*>(ws + L.clc_slots);
     ap.clc_slot_bytes = L.clc_slot_bytes;
     ap.clc_map_offset = L.clc_map_offset;

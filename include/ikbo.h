@@ -181,10 +181,11 @@ int ikbo_get_timing(float* plan_ms, float* attn_ms);
  * bound runs out: the kernel then records IKBO_ERR_TIMEOUT, skips all work
  * and exits normally (nothing traps, the context stays usable).
  * flags = 4, with a trace buffer set (ikbo_set_trace), also stamps the
- * prologue of every CTA into item slot 3: 0 entry, 1 barriers and tensor
- * memory ready, 2 index tensors loaded, 3 tensor maps set, 4 validated,
- * 5 grouped, 6 units counted, 7 planned, 8 cluster ready, 9 work done,
- * 10 exit.  flags = 2 stamps the first item's tiles instead of items 1
+ * prologue of every CTA into item slot 3 (not on the two-tile kernel with
+ * Cluster Launch Control, whose grid has more CTAs than the buffer holds):
+ * 0 entry, 1 barriers and tensor memory ready, 2 index tensors loaded,
+ * 3 tensor maps set, 4 validated, 5 grouped, 6 units counted, 7 planned,
+ * 8 cluster ready, 9 work done, 10 exit.  flags = 2 stamps the first item's tiles instead of items 1
  * and 2: softmax tiles 0-3 in slot 1 (points 4j .. 4j+3: scores seen,
  * row maximum done, maxima exchanged, P handed over) and MMA tiles 0-7 in
  * slot 2 (points 2j, 2j+1: S and PV issued).  The bits combine.
