@@ -127,7 +127,7 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
   const uint32_t sm = ptx::smid();
   const bool clc = !kSelf && p.clc && sm < (uint32_t)kClcSlots;
   uint8_t* slot = clc ? p.clc_slots + (size_t)sm * p.clc_slot_bytes : nullptr;
-  if (p.fused && layout_ok) plan_load(p, data);
+  if (p.fused && layout_ok) plan_load<16>(p, data);
   __syncthreads();
   if (!layout_ok || !p.fused || (!kSelf && p.clc && !clc)) {
     // this kernel plans in-kernel only; the host never launches it otherwise

@@ -484,10 +484,15 @@ struct PlanScratch {
   }
 };
 
+// kInFlight: loads of each thread in flight at once.  Each round waits for
+// its loads (from DRAM when L2 holds no copy), so a large batch of
+// candidates wants many: 16384 entries over 384 threads are 11 rounds of 4
+// but 3 of 16.  (The one-tile kernel keeps 4: its launches are short and
+// bound by instruction fetch, and its batches small.)
+template <int kInFlight = 4>
 __device__ __forceinline__ void plan_load(const AttnParams& p, uint8_t* scratch) {
   const int n_cand = (int)p.n_cand, n_user = (int)p.n_user;
   PlanScratch S(scratch, n_user, n_cand);
-  // up to four loads of each thread in flight at once
   for (int base = 0; base <= n_user; base += 4 * blockDim.x) {
     int v[4];
 #pragma unroll
@@ -501,10 +506,10 @@ __device__ __forceinline__ void plan_load(const AttnParams& p, uint8_t* scratch)
       if (u <= n_user) S.off[u] = v[i];
     }
   }
-  for (int base = 0; base < n_cand; base += 4 * blockDim.x) {
-    int v[4];
+  for (int base = 0; base < n_cand; base += kInFlight * blockDim.x) {
+    int v[kInFlight];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < kInFlight; ++i) {
       const int c = base + i * blockDim.x + threadIdx.x;
       v[i] = c < n_cand ? p.cand_to_user[c] : 0;
     }
@@ -512,11 +517,11 @@ __device__ __forceinline__ void plan_load(const AttnParams& p, uint8_t* scratch)
       // a multi-level call: the loaded values are vendors; an out-of-range
       // one becomes -1, which the validation reports as a bad index
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < kInFlight; ++i)
         v[i] = (v[i] >= 0 && int64_t(v[i]) < p.n_vendor) ? p.vendor_to_user[v[i]] : -1;
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < kInFlight; ++i) {
       const int c = base + i * blockDim.x + threadIdx.x;
       if (c < n_cand) S.c2u[c] = v[i];
     }
