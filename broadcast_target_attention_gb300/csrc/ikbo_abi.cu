@@ -22,8 +22,11 @@
 
 namespace ikbo {
 
-// Per-device error word (bits kErrIndex, kErrOffsets, kErrTimeout).
-__device__ int g_ikbo_error_word;
+// Error words (bits kErrIndex, kErrOffsets, kErrTimeout), one per stream:
+// word i > 0 belongs to the i-th stream of the device that made a call, in
+// order of first use; word 0 is shared by the streams past kErrSlots - 1.
+constexpr int kErrSlots = 64;
+__device__ int g_ikbo_error_word[kErrSlots];
 
 namespace {
 
@@ -46,7 +49,9 @@ struct DeviceState {
   // call that allocates: it keeps freed scratch between calls (the device's
   // default pool, which other code may use, is left as it is).
   cudaMemPool_t pool = nullptr;
-  int* err_word = nullptr;
+  int* err_word = nullptr;                       // the device's g_ikbo_error_word
+  cudaStream_t err_stream[kErrSlots] = {};       // stream of each word (1 .. err_streams)
+  int err_streams = 0;
   cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
   bool ev_ready = false;
 };
@@ -109,6 +114,20 @@ int device_state(DeviceState** out) {
   *out = &s;
   return IKBO_OK;
 }
+
+// The error word of stream `st`: the stream's own once it has one, a new one
+// on its first call, the shared word 0 once all are taken.  (A call captured
+// in a graph records into the word of the stream it was captured on.)
+int error_slot(DeviceState* ds, cudaStream_t st, bool take) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  for (int i = 1; i <= ds->err_streams; ++i)
+    if (ds->err_stream[i] == st) return i;
+  if (!take || ds->err_streams + 1 >= kErrSlots) return 0;
+  ds->err_stream[++ds->err_streams] = st;
+  return ds->err_streams;
+}
+
+int* error_word(DeviceState* ds, cudaStream_t st) { return ds->err_word + error_slot(ds, st, true); }
 
 // `bytes` of scratch from the library's pool on the current device, in
 // stream order on `st` (made on first use; freed memory stays in the pool).
@@ -520,7 +539,7 @@ int run_ikbo(DeviceState* ds, const void* q, const void* k, const void* v, const
   pp.perm = reinterpret_cast<int32_t*>(ws + L.perm);
   pp.cand_start = reinterpret_cast<int32_t*>(ws + L.cand_start);
   pp.scratch = reinterpret_cast<int32_t*>(ws + L.scratch);
-  pp.err_word = ds->err_word;
+  pp.err_word = error_word(ds, st);
   if (vendor) {
     pp.vendor_to_user = vendor->vendor_to_user;
     pp.n_vendor = vendor->n_vendor;
@@ -571,7 +590,7 @@ int run_ikbo(DeviceState* ds, const void* q, const void* k, const void* v, const
   ap.perm = pp.perm;
   ap.partial_o = L.max_split_items ? reinterpret_cast<float*>(ws + L.partial_o) : nullptr;
   ap.partial_ml = L.max_split_items ? reinterpret_cast<float2*>(ws + L.partial_ml) : nullptr;
-  ap.err_word = ds->err_word;
+  ap.err_word = error_word(ds, st);
   ap.kmap = px.kmap_dst;
   ap.vmap = px.vmap_dst;
   ap.timeout_ns = g_timeout_ns;
@@ -784,14 +803,15 @@ int ikbo_attn_fwd_host(const void* q, const void* k_user, const void* v_user,
     }
     ds->err_host = static_cast<int*>(h);
   }
+  int* const word_dev = error_word(ds, st);
   if (e == cudaSuccess && rc == IKBO_OK)
-    e = cudaMemcpyAsync(ds->err_host, ds->err_word, sizeof(int), cudaMemcpyDeviceToHost, st);
+    e = cudaMemcpyAsync(ds->err_host, word_dev, sizeof(int), cudaMemcpyDeviceToHost, st);
   if (cudaStreamSynchronize(st) != cudaSuccess || e != cudaSuccess) return IKBO_ERR_CUDA;
   if (rc != IKBO_OK) return rc;
   const int word = *ds->err_host;
   if (word) {
     // clear it, as ikbo_get_device_error does
-    if (cudaMemsetAsync(ds->err_word, 0, sizeof(int), st) != cudaSuccess ||
+    if (cudaMemsetAsync(word_dev, 0, sizeof(int), st) != cudaSuccess ||
         cudaStreamSynchronize(st) != cudaSuccess)
       return IKBO_ERR_CUDA;
   }
@@ -1173,7 +1193,7 @@ int ikbo_lce_fwd(const void* W_user, const void* W_cand, const void* X_user, con
   LceParams lp = {};
   lp.M = M;
   lp.N = N;
-  lp.err_word = ds->err_word;
+  lp.err_word = error_word(ds, st);
   lp.timeout_ns = g_timeout_ns;
   // the row tiles of one batch entry run as one cluster (CTA pairs when N allows)
   lp.cluster_n = lce_cluster_n(M, NB);
@@ -1290,7 +1310,7 @@ int ikbo_ml_lce_fwd(const void* W_user, const void* W_vendor, const void* W_item
   LceParams lp = {};
   lp.M = M;
   lp.N = N;
-  lp.err_word = ds->err_word;
+  lp.err_word = error_word(ds, st);
   lp.timeout_ns = g_timeout_ns;
   lp.cluster_n = lce_cluster_n(M, NB);
   cudaError_t e = cudaSuccess;
@@ -1359,13 +1379,14 @@ int ikbo_get_device_error(ikbo_stream_t stream) {
   DeviceState* ds = nullptr;
   int rc = device_state(&ds);
   if (rc != IKBO_OK) return rc;
-  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return IKBO_ERR_CUDA;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return IKBO_ERR_CUDA;
+  const size_t at = sizeof(int) * size_t(error_slot(ds, st, false));
   int word = 0;
-  if (cudaMemcpyFromSymbol(&word, g_ikbo_error_word, sizeof word) != cudaSuccess)
+  if (cudaMemcpyFromSymbol(&word, g_ikbo_error_word, sizeof word, at) != cudaSuccess)
     return IKBO_ERR_CUDA;
   const int zero = 0;
-  if (word && cudaMemcpyToSymbol(g_ikbo_error_word, &zero, sizeof zero) != cudaSuccess)
+  if (word && cudaMemcpyToSymbol(g_ikbo_error_word, &zero, sizeof zero, at) != cudaSuccess)
     return IKBO_ERR_CUDA;
   return status_of_error_word(word);
 }

@@ -48,8 +48,12 @@
  * _DEVICE).  Bad contents of the index tensors (a candidate mapped outside
  * [0, n_user), offsets that are not a jagged index) and bounded waits that
  * ran out can only be seen on the GPU: the kernels then skip all work (out
- * is left unchanged), never trap, and record the error in a per-device error
- * word that ikbo_get_device_error() returns.  A user's result depends on its
+ * is left unchanged), never trap, and record the error in the error word of
+ * the call's stream, which ikbo_get_device_error(stream) returns: each of
+ * the first 63 streams of a device that make a call gets a word of its own
+ * (later streams share one), so callers on different streams see only their
+ * own errors.  A call captured in a CUDA graph records into the word of the
+ * stream it was captured on.  A user's result depends on its
  * own rows of k/v only: rows of other users (which a key tile may reach)
  * never enter it, whatever their values, inf and NaN included.
  */
@@ -137,10 +141,12 @@ int ikbo_attn_fwd_host(const void* q, const void* k_user, const void* v_user,
                        float scale, void* out, ikbo_stream_t stream);
 
 /*
- * Synchronises `stream`, then returns and clears the current device's error
- * word: IKBO_OK, or IKBO_ERR_INDEX / _OFFSETS / _TIMEOUT for the first kind
- * of error recorded since the last call.  The word is shared by all streams
- * of the device.
+ * Synchronises `stream`, then returns and clears the error word of `stream`
+ * on the current device (see "Errors" above): IKBO_OK, or IKBO_ERR_INDEX /
+ * _OFFSETS / _TIMEOUT for the first kind of error that calls on `stream`
+ * recorded since the word was last cleared.  Errors of calls on other
+ * streams are not seen (except between streams past the first 63, which
+ * share one word).
  */
 int ikbo_get_device_error(ikbo_stream_t stream);
 

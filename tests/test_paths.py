@@ -91,6 +91,28 @@ def test_bad_candidate_index_is_reported_not_trapped(gpu_lib, kernel):
     assert gpu_lib.get_device_error() == 0   # the word was cleared
 
 
+def test_errors_are_kept_per_stream(gpu_lib):
+    """An index error of a call on one stream is reported on that stream only: a caller on
+    another stream sees its own clean calls, before and after, and the word is cleared."""
+    wl = W.custom(n_user=2, counts=[2, 2], lens=[10, 20], H=2, D=64, Lq=1)
+    d = to_device(wl)
+    bad = torch.tensor([0, 1, 2, 1], dtype=torch.int32, device="cuda")
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    out_a = torch.full_like(d["q"], 7.0)
+    with torch.cuda.stream(sa):
+        gpu_lib.attn_fwd(d["q"], d["k"], d["v"], d["user_offsets"], bad, wl.scale, out=out_a)
+    with torch.cuda.stream(sb):
+        out_b = gpu_lib.attn_fwd(d["q"], d["k"], d["v"], d["user_offsets"], d["cand_to_user"], wl.scale)
+    assert gpu_lib.get_device_error(sb) == 0
+    assert gpu_lib.get_device_error(sa) == _lib.IKBO_ERR_INDEX
+    assert gpu_lib.get_device_error(sa) == 0
+    assert bool((out_a == 7.0).all())
+    assert_close(out_f64(out_b), oracle.attention_wl(wl), "clean call on the other stream")
+    # the legacy default stream keeps its own word too
+    assert gpu_lib.get_device_error(torch.cuda.default_stream()) == 0
+
+
 def test_bad_offsets_are_reported(gpu_lib):
     wl = W.custom(n_user=2, counts=[2, 2], lens=[10, 20], H=2, D=64, Lq=1)
     rc, out = _sentinel_call(gpu_lib, wl, off=[0, 25, 20])
