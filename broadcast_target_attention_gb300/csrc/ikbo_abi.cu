@@ -1403,6 +1403,9 @@ int ikbo_shutdown(void) {
     DeviceState& s = g_dev[d];
     if (!s.ready) continue;
     if (cudaSetDevice(d) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) rc = IKBO_ERR_CUDA;
+    // the streams' words start clean for whichever streams call next
+    static const int zeros[kErrSlots] = {};
+    if (cudaMemcpyToSymbol(g_ikbo_error_word, zeros, sizeof zeros) != cudaSuccess) rc = IKBO_ERR_CUDA;
     for (auto& e : s.ev)
       if (e) cudaEventDestroy(e);
     if (s.err_host) cudaFreeHost(s.err_host);

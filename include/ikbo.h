@@ -162,6 +162,7 @@ int ikbo_version(void);
  *   - The pinned error-word copy of the host-buffer entry point.
  *   - Its own stream-ordered memory pool on each device, which keeps the
  *     scratch its calls freed: trimmed and destroyed here.
+ *   - The streams' error words: cleared, and the streams forgotten.
  * It first waits for each such device's work to finish.  No other library
  * call may run meanwhile.  A later call sets the device up again.  The
  * no-alloc entry point's fixed array is part of the library image and is
