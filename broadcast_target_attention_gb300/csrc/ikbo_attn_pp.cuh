@@ -328,8 +328,9 @@ ikbo_attn_pp_kernel(const __grid_constant__ AttnParams p, const __grid_constant_
       // free.  (Asked at the start of the current unit, the CTAs that
       // started the longest units took the next-longest at once: on
       // odd_groups_2048x16 the busiest CTA ran 30 % above the mean.)  At
-      // D = 64, whose units are short, the late request made every unit
-      // slower (2 % on the sweeps), so there it goes out as the unit starts.
+      // D = 64 the late request made every unit slower (2 % on the sweeps;
+      // asking a few loads earlier did not help either), so there it goes
+      // out as the unit starts.
       // The grid is sized by a bound on the units: indices past the plan's
       // count are taken over too, and skipped, until a request cancels
       // nothing.
